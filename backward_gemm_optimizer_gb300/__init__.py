@@ -1,0 +1,10 @@
+"""FORGE fused weight-gradient + optimizer step for one GB300 (sm_103a).
+
+The compute lives in ``libforge.so`` (hand-written CUDA kernels behind the
+C ABI in ``include/forge.h``); this package is its thin Python binding.
+"""
+
+from ._lib import (  # noqa: F401
+    BF16, EXPORTED, F32, FLAG_TEST_FORCE_TIMEOUT, FLAG_TILE_N_64, FLAG_TILE_N_128, FLAG_TILE_N_AUTO,
+    I8B128, LIB_PATH, ForgeError, dgrad, lib, sync_status, tensor_desc, version, wgrad_step_adamw,
+    wgrad_step_lion, wgrad_step_sgdm, workspace_bytes)

@@ -1,0 +1,173 @@
+"""ctypes binding of ``libforge.so`` (argument marshalling only).
+
+Every function here fills the C descriptors of ``include/forge.h`` from
+torch tensors and calls the library; all arithmetic runs in the library's
+CUDA kernels. If the library has not been built the import fails loudly:
+there is no CPU fallback.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch  # loads the CUDA runtime the library links against
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libforge.so")
+
+F32, BF16, I8B128 = 0, 1, 2
+FLAG_TILE_N_AUTO, FLAG_TILE_N_128, FLAG_TILE_N_64 = 0, 1, 2
+FLAG_TEST_FORCE_TIMEOUT = 0x100
+
+STATUS_NAMES = {0: "FORGE_OK", 1: "FORGE_ERR_INVALID_ARG", 2: "FORGE_ERR_UNSUPPORTED",
+                3: "FORGE_ERR_ALIGNMENT", 4: "FORGE_ERR_CUDA", 5: "FORGE_ERR_TIMEOUT"}
+
+EXPORTED = ("forge_wgrad_step_adamw", "forge_wgrad_step_sgdm", "forge_wgrad_step_lion",
+            "forge_dgrad", "forge_sync_status", "forge_last_error", "forge_version",
+            "forge_workspace_bytes")
+
+
+class ForgeTensor(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("rows", ctypes.c_int64),
+                ("cols", ctypes.c_int64), ("ld", ctypes.c_int64), ("scale", ctypes.c_void_p)]
+
+
+class ForgeHyper(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_double), ("beta1", ctypes.c_double), ("beta2", ctypes.c_double),
+                ("eps", ctypes.c_double), ("weight_decay", ctypes.c_double),
+                ("sr_w", ctypes.c_int32), ("sr_moments", ctypes.c_int32), ("flags", ctypes.c_uint32)]
+
+
+class ForgeError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is missing: build the CUDA library first "
+            "(python -c 'import __graft_entry__ as g; g.build()'). There is no CPU fallback.")
+    lib = ctypes.CDLL(LIB_PATH)
+    P = ctypes.POINTER
+    T, H = ForgeTensor, ForgeHyper
+    vp, i64, u64 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint64
+    lib.forge_wgrad_step_adamw.argtypes = [P(T), P(T), P(T), P(T), P(T), P(H), i64, u64, vp]
+    lib.forge_wgrad_step_sgdm.argtypes = [P(T), P(T), P(T), P(T), P(H), i64, u64, vp]
+    lib.forge_wgrad_step_lion.argtypes = [P(T), P(T), P(T), P(T), P(H), i64, u64, vp]
+    lib.forge_dgrad.argtypes = [P(T), P(T), P(T), vp]
+    lib.forge_sync_status.argtypes = [vp]
+    for f in ("forge_wgrad_step_adamw", "forge_wgrad_step_sgdm", "forge_wgrad_step_lion",
+              "forge_dgrad", "forge_sync_status"):
+        getattr(lib, f).restype = ctypes.c_int
+    lib.forge_last_error.restype = ctypes.c_char_p
+    lib.forge_version.restype = ctypes.c_char_p
+    lib.forge_workspace_bytes.argtypes = [i64, i64, i64]
+    lib.forge_workspace_bytes.restype = ctypes.c_size_t
+    return lib
+
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        _lib = _load()
+    return _lib
+
+
+def _check(status: int):
+    if status != 0:
+        raise ForgeError(status, lib().forge_last_error().decode())
+
+
+def _dtype_code(t: torch.Tensor, scale: Optional[torch.Tensor]) -> int:
+    if t.dtype == torch.float32:
+        return F32
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype in (torch.int8, torch.uint8):
+        if scale is None:
+            raise ValueError("8-bit moment codes need their fp32 scale tensor [D_in/128, D_out]")
+        return I8B128
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def tensor_desc(t: torch.Tensor, scale: Optional[torch.Tensor] = None) -> ForgeTensor:
+    """Descriptor of a 2-D tensor with unit column stride (rows may be padded)."""
+    if t.dim() != 2:
+        raise ValueError("expected a 2-D tensor")
+    if t.numel() > 0 and t.stride(1) != 1:
+        raise ValueError("columns must be contiguous (stride(1) == 1)")
+    if scale is not None and (scale.dtype != torch.float32 or not scale.is_contiguous()):
+        raise ValueError("scale must be a contiguous float32 tensor")
+    ld = t.stride(0) if t.shape[0] > 1 else max(t.shape[1], t.stride(0))
+    return ForgeTensor(ctypes.c_void_p(t.data_ptr() if t.numel() else 0), _dtype_code(t, scale),
+                       t.shape[0], t.shape[1], max(ld, t.shape[1]),
+                       ctypes.c_void_p(scale.data_ptr() if scale is not None else 0))
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _hyper(lr, beta1, beta2, eps, weight_decay, sr_w, sr_moments, flags) -> ForgeHyper:
+    return ForgeHyper(float(lr), float(beta1), float(beta2), float(eps), float(weight_decay),
+                      int(bool(sr_w)), int(bool(sr_moments)), int(flags))
+
+
+def wgrad_step_adamw(X, dY, W, m, v, *, lr, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0,
+                     step, seed=0, sr_w=False, sr_moments=False, m_scale=None, v_scale=None,
+                     flags=0, stream=None):
+    """Fused G = dY^T X and AdamW step on W, m, v in place (forge_wgrad_step_adamw)."""
+    tX, tdY, tW = tensor_desc(X), tensor_desc(dY), tensor_desc(W)
+    tm, tv = tensor_desc(m, m_scale), tensor_desc(v, v_scale)
+    h = _hyper(lr, beta1, beta2, eps, weight_decay, sr_w, sr_moments, flags)
+    _check(lib().forge_wgrad_step_adamw(ctypes.byref(tX), ctypes.byref(tdY), ctypes.byref(tW),
+                                        ctypes.byref(tm), ctypes.byref(tv), ctypes.byref(h),
+                                        int(step), int(seed) & 0xFFFFFFFFFFFFFFFF, _stream(stream)))
+
+
+def wgrad_step_sgdm(X, dY, W, m, *, lr, momentum=0.9, weight_decay=0.0, step, seed=0,
+                    sr_w=False, sr_moments=False, m_scale=None, flags=0, stream=None):
+    """Fused G = dY^T X and SGD-momentum step on W, m in place (forge_wgrad_step_sgdm)."""
+    tX, tdY, tW, tm = tensor_desc(X), tensor_desc(dY), tensor_desc(W), tensor_desc(m, m_scale)
+    h = _hyper(lr, momentum, 0.0, 0.0, weight_decay, sr_w, sr_moments, flags)
+    _check(lib().forge_wgrad_step_sgdm(ctypes.byref(tX), ctypes.byref(tdY), ctypes.byref(tW),
+                                       ctypes.byref(tm), ctypes.byref(h), int(step),
+                                       int(seed) & 0xFFFFFFFFFFFFFFFF, _stream(stream)))
+
+
+def wgrad_step_lion(X, dY, W, m, *, lr, beta1=0.9, beta2=0.99, weight_decay=0.0, step, seed=0,
+                    sr_w=False, sr_moments=False, m_scale=None, flags=0, stream=None):
+    """Fused G = dY^T X and Lion step on W, m in place (forge_wgrad_step_lion)."""
+    tX, tdY, tW, tm = tensor_desc(X), tensor_desc(dY), tensor_desc(W), tensor_desc(m, m_scale)
+    h = _hyper(lr, beta1, beta2, 0.0, weight_decay, sr_w, sr_moments, flags)
+    _check(lib().forge_wgrad_step_lion(ctypes.byref(tX), ctypes.byref(tdY), ctypes.byref(tW),
+                                       ctypes.byref(tm), ctypes.byref(h), int(step),
+                                       int(seed) & 0xFFFFFFFFFFFFFFFF, _stream(stream)))
+
+
+def dgrad(dY, W_old, dX, *, stream=None):
+    """dX = dY W_old (forge_dgrad); enqueue before the step that overwrites W."""
+    tdY, tW, tdX = tensor_desc(dY), tensor_desc(W_old), tensor_desc(dX)
+    _check(lib().forge_dgrad(ctypes.byref(tdY), ctypes.byref(tW), ctypes.byref(tdX), _stream(stream)))
+
+
+def sync_status(stream=None):
+    """Synchronise the stream and raise ForgeError if a kernel's bounded wait gave up."""
+    _check(lib().forge_sync_status(_stream(stream)))
+
+
+def version() -> str:
+    return lib().forge_version().decode()
+
+
+def workspace_bytes(d_out: int, d_in: int, bt: int) -> int:
+    return int(lib().forge_workspace_bytes(d_out, d_in, bt))

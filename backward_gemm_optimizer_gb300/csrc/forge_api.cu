@@ -1,0 +1,439 @@
+// forge_api.cu -- the C ABI declared in include/forge.h: argument
+// validation, tensor-map encoding, the tile-scheduler / tile-shape policy,
+// host folding of the per-step scalars, launch, and the device status word.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "../../include/forge.h"
+#include "forge_params.h"
+
+using namespace forge;
+
+// Device status word (per device): 0, or the code of the first bounded wait
+// that gave up since it was last read.
+__device__ unsigned int forge_device_status[4];
+
+namespace {
+
+thread_local std::string g_last_error;
+
+forge_status fail(forge_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+forge_status ok() {
+  g_last_error.clear();
+  return FORGE_OK;
+}
+
+// ------------------------------------------------------------------ driver entry points
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+struct DeviceInfo {
+  int sms = 0;
+  unsigned int* status = nullptr;
+};
+
+constexpr int kMaxDevices = 64;
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+forge_status device_info(DeviceInfo** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(FORGE_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return fail(FORGE_ERR_CUDA, "device id %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (d.status == nullptr) {
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (major != 10 || minor != 3)
+      return fail(FORGE_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a only", dev,
+                  major, minor);
+    e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return fail(FORGE_ERR_CUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, forge_device_status);
+    if (e != cudaSuccess) return fail(FORGE_ERR_CUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+    d.status = static_cast<unsigned int*>(p);
+  }
+  *out = &d;
+  return FORGE_OK;
+}
+
+// ------------------------------------------------------------------ validation
+
+const char* dtype_name(int dt) {
+  switch (dt) {
+    case FORGE_F32: return "f32";
+    case FORGE_BF16: return "bf16";
+    case FORGE_I8B128: return "i8b128";
+    default: return "?";
+  }
+}
+
+int elem_bytes(int dt) { return dt == FORGE_F32 ? 4 : dt == FORGE_BF16 ? 2 : 1; }
+
+forge_status check_tensor(const forge_tensor* t, const char* name, int64_t rows, int64_t cols, bool needs_tma) {
+  if (t == nullptr) return fail(FORGE_ERR_INVALID_ARG, "%s: null descriptor", name);
+  if (t->dtype != FORGE_F32 && t->dtype != FORGE_BF16 && t->dtype != FORGE_I8B128)
+    return fail(FORGE_ERR_INVALID_ARG, "%s: unknown dtype %d", name, t->dtype);
+  if (t->rows != rows || t->cols != cols)
+    return fail(FORGE_ERR_INVALID_ARG, "%s: shape %lld x %lld, expected %lld x %lld", name, (long long)t->rows,
+                (long long)t->cols, (long long)rows, (long long)cols);
+  if (t->ld < t->cols) return fail(FORGE_ERR_INVALID_ARG, "%s: ld %lld < cols %lld", name, (long long)t->ld,
+                                   (long long)t->cols);
+  if (rows > 0 && cols > 0 && t->data == nullptr) return fail(FORGE_ERR_INVALID_ARG, "%s: null data", name);
+  if (t->dtype == FORGE_I8B128 && t->scale == nullptr && rows > 0 && cols > 0)
+    return fail(FORGE_ERR_INVALID_ARG, "%s: 8-bit block state needs its scale array", name);
+  if (needs_tma) {
+    if (reinterpret_cast<uintptr_t>(t->data) % 16 != 0)
+      return fail(FORGE_ERR_ALIGNMENT, "%s: base address not 16-byte aligned", name);
+    if ((t->ld * elem_bytes(t->dtype)) % 16 != 0)
+      return fail(FORGE_ERR_ALIGNMENT, "%s: row pitch %lld bytes is not a multiple of 16", name,
+                  (long long)(t->ld * elem_bytes(t->dtype)));
+  }
+  if (t->dtype == FORGE_I8B128 && reinterpret_cast<uintptr_t>(t->scale) % 16 != 0)
+    return fail(FORGE_ERR_ALIGNMENT, "%s: scale array not 16-byte aligned", name);
+  return FORGE_OK;
+}
+
+bool finite(double x) { return std::isfinite(x); }
+
+// ------------------------------------------------------------------ tensor maps
+
+forge_status encode_2d(CUtensorMap* map, const forge_tensor* t, CUtensorMapDataType dt, int esize, uint32_t box_x,
+                       uint32_t box_y, CUtensorMapSwizzle swz, const char* name) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return fail(FORGE_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(t->cols), static_cast<cuuint64_t>(t->rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(t->ld) * esize};
+  const cuuint32_t box[2] = {box_x, box_y};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, dt, 2, t->data, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(FORGE_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed: %d", name, (int)r);
+  return FORGE_OK;
+}
+
+// Chunk maps of the W / m / v tiles: 32 columns x 128 rows, swizzle = row bytes.
+forge_status encode_state(CUtensorMap* map, const forge_tensor* t, const char* name) {
+  CUtensorMapDataType dt;
+  CUtensorMapSwizzle swz;
+  int es;
+  if (t->dtype == FORGE_F32) { dt = CU_TENSOR_MAP_DATA_TYPE_FLOAT32; es = 4; swz = CU_TENSOR_MAP_SWIZZLE_128B; }
+  else if (t->dtype == FORGE_BF16) { dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16; es = 2; swz = CU_TENSOR_MAP_SWIZZLE_64B; }
+  else { dt = CU_TENSOR_MAP_DATA_TYPE_UINT8; es = 1; swz = CU_TENSOR_MAP_SWIZZLE_32B; }
+  return encode_2d(map, t, dt, es, 32, 128, swz, name);
+}
+
+// ------------------------------------------------------------------ scalars
+
+StepScalars fold(int opt, const forge_hyper* h, int64_t t) {
+  StepScalars s{};
+  const double td = static_cast<double>(t);
+  s.b1 = static_cast<float>(h->beta1);
+  s.omb1 = static_cast<float>(1.0 - h->beta1);
+  s.b2 = static_cast<float>(h->beta2);
+  s.omb2 = static_cast<float>(1.0 - h->beta2);
+  s.decay = static_cast<float>(1.0 - h->lr * h->weight_decay);
+  s.eps = static_cast<float>(h->eps);
+  s.wd = static_cast<float>(h->weight_decay);
+  if (opt == OPT_ADAMW) {
+    s.step_size = static_cast<float>(h->lr / (1.0 - std::pow(h->beta1, td)));
+    s.inv_sqrt_bc2 = static_cast<float>(1.0 / std::sqrt(1.0 - std::pow(h->beta2, td)));
+  } else {
+    s.step_size = static_cast<float>(h->lr);
+    s.inv_sqrt_bc2 = 1.0f;
+  }
+  return s;
+}
+
+int mkind(int dt) { return dt == FORGE_F32 ? M_F32 : dt == FORGE_BF16 ? M_BF16 : M_Q8; }
+
+constexpr uint64_t kTimeoutNs = 4000000000ull;  // 4 s: far beyond any healthy wait
+
+// ------------------------------------------------------------------ the fused step
+
+forge_status wgrad_step(int opt, const forge_tensor* X, const forge_tensor* dY, forge_tensor* W, forge_tensor* m,
+                        forge_tensor* v, const forge_hyper* h, int64_t step, uint64_t seed, forge_stream_t stream) {
+  const char* oname = opt == OPT_ADAMW ? "adamw" : opt == OPT_SGDM ? "sgdm" : "lion";
+  if (X == nullptr || dY == nullptr || W == nullptr || m == nullptr || h == nullptr)
+    return fail(FORGE_ERR_INVALID_ARG, "%s: null argument", oname);
+  if (opt == OPT_ADAMW && v == nullptr) return fail(FORGE_ERR_INVALID_ARG, "adamw: null v");
+  if (step < 1) return fail(FORGE_ERR_INVALID_ARG, "%s: step must be >= 1 (got %lld)", oname, (long long)step);
+  if (step > 0xFFFFFFFFll) return fail(FORGE_ERR_INVALID_ARG, "%s: step exceeds 2^32 - 1", oname);
+  if (!finite(h->lr) || !finite(h->beta1) || !finite(h->beta2) || !finite(h->eps) || !finite(h->weight_decay))
+    return fail(FORGE_ERR_INVALID_ARG, "%s: non-finite hyper-parameter", oname);
+  if (opt == OPT_ADAMW && (h->beta1 >= 1.0 || h->beta2 >= 1.0 || h->beta1 < 0.0 || h->beta2 < 0.0))
+    return fail(FORGE_ERR_INVALID_ARG, "adamw: betas must lie in [0, 1)");
+  if (h->flags & ~(FORGE_FLAG_TILE_N_MASK | FORGE_FLAG_TEST_FORCE_TIMEOUT))
+    return fail(FORGE_ERR_INVALID_ARG, "%s: unknown flags 0x%x", oname, h->flags);
+
+  const int64_t bt = X->rows, d_in = X->cols, d_out = dY->cols;
+  if (bt < 0 || d_in < 0 || d_out < 0) return fail(FORGE_ERR_INVALID_ARG, "%s: negative size", oname);
+  if (X->dtype != dY->dtype || (X->dtype != FORGE_BF16 && X->dtype != FORGE_F32))
+    return fail(FORGE_ERR_UNSUPPORTED, "%s: X and dY must both be bf16 or both f32 (got %s, %s)", oname,
+                dtype_name(X->dtype), dtype_name(dY->dtype));
+  const bool tc = X->dtype == FORGE_BF16;
+  forge_status st;
+  if ((st = check_tensor(X, "X", bt, d_in, true)) != FORGE_OK) return st;
+  if ((st = check_tensor(dY, "dY", bt, d_out, true)) != FORGE_OK) return st;
+  if ((st = check_tensor(W, "W", d_out, d_in, true)) != FORGE_OK) return st;
+  if ((st = check_tensor(m, "m", d_out, d_in, true)) != FORGE_OK) return st;
+  if (opt == OPT_ADAMW && (st = check_tensor(v, "v", d_out, d_in, true)) != FORGE_OK) return st;
+  if (W->dtype == FORGE_I8B128) return fail(FORGE_ERR_UNSUPPORTED, "%s: W must be f32 or bf16", oname);
+  if (opt == OPT_ADAMW && v->dtype != m->dtype)
+    return fail(FORGE_ERR_UNSUPPORTED, "adamw: m and v must share a dtype (got %s, %s)", dtype_name(m->dtype),
+                dtype_name(v->dtype));
+  if (d_in % 8 != 0 || d_out % 8 != 0)
+    return fail(FORGE_ERR_UNSUPPORTED, "%s: D_in (%lld) and D_out (%lld) must be multiples of 8", oname,
+                (long long)d_in, (long long)d_out);
+  if (m->dtype == FORGE_I8B128 && d_in % 128 != 0)
+    return fail(FORGE_ERR_UNSUPPORTED, "%s: 8-bit block moments need D_in %% 128 == 0 (got %lld)", oname,
+                (long long)d_in);
+  if (h->sr_w && W->dtype != FORGE_BF16)
+    return fail(FORGE_ERR_INVALID_ARG, "%s: sr_w requires bf16 W", oname);
+  if (h->sr_moments && m->dtype != FORGE_BF16)
+    return fail(FORGE_ERR_INVALID_ARG, "%s: sr_moments requires bf16 moments", oname);
+  if (bt > 0x7FFFFFFF || d_in > 0x7FFFFFFF || d_out > 0x7FFFFFFF)
+    return fail(FORGE_ERR_INVALID_ARG, "%s: dimension exceeds 2^31 - 1", oname);
+  if (d_in == 0 || d_out == 0) return ok();
+
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != FORGE_OK) return st;
+  const StepScalars sc = fold(opt, h, step);
+  const int wk = W->dtype == FORGE_F32 ? W_F32 : W_BF16;
+  const int mk = mkind(m->dtype);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+  if (!tc) {
+    if (h->flags & FORGE_FLAG_TEST_FORCE_TIMEOUT)
+      return fail(FORGE_ERR_UNSUPPORTED, "%s: the timeout test hook exists on the tensor-core path only", oname);
+    WgradSimtParams p{};
+    p.X = static_cast<const float*>(X->data);
+    p.dY = static_cast<const float*>(dY->data);
+    p.W = W->data;
+    p.m = m->data;
+    p.v = opt == OPT_ADAMW ? v->data : nullptr;
+    p.m_scale = static_cast<float*>(m->scale);
+    p.v_scale = opt == OPT_ADAMW ? static_cast<float*>(v->scale) : nullptr;
+    p.ld_x = X->ld; p.ld_dy = dY->ld; p.ld_w = W->ld; p.ld_m = m->ld; p.ld_v = opt == OPT_ADAMW ? v->ld : 0;
+    p.d_out = static_cast<int>(d_out); p.d_in = static_cast<int>(d_in); p.bt = static_cast<int>(bt);
+    p.sc = sc;
+    p.step = static_cast<uint32_t>(step);
+    p.seed_lo = static_cast<uint32_t>(seed); p.seed_hi = static_cast<uint32_t>(seed >> 32);
+    p.sr_w = h->sr_w ? 1 : 0; p.sr_m = h->sr_moments ? 1 : 0;
+    cudaError_t e = launch_wgrad_simt(p, opt, wk, mk, s);
+    if (e != cudaSuccess) return fail(FORGE_ERR_CUDA, "%s (fp32 path) launch: %s", oname, cudaGetErrorString(e));
+    return ok();
+  }
+
+  // ---- tensor-core path: tile-shape / scheduler policy
+  const int tiles_m = static_cast<int>((d_out + 127) / 128);
+  int bn = 128;
+  const uint32_t force = h->flags & FORGE_FLAG_TILE_N_MASK;
+  if (force == FORGE_FLAG_TILE_N_64) bn = 64;
+  else if (force == FORGE_FLAG_TILE_N_128) bn = 128;
+  else if (force != FORGE_FLAG_TILE_N_AUTO) return fail(FORGE_ERR_INVALID_ARG, "%s: bad tile flag", oname);
+  else if (mk != M_Q8 && tiles_m * ((d_in + 127) / 128) < dev->sms) bn = 64;  // too few tiles for one wave
+  if (mk == M_Q8 && bn != 128)
+    return fail(FORGE_ERR_UNSUPPORTED, "%s: 8-bit block moments need 128-column tiles", oname);
+  const int deep = (bt >= 1024 && bn == 128) ? 1 : 0;
+  const int tiles_n = static_cast<int>((d_in + bn - 1) / bn);
+
+  WgradTcParams p;
+  std::memset(&p, 0, sizeof(p));
+  if (bt > 0) {  // with BT = 0 the kernel issues no operand loads and needs no operand maps
+    if ((st = encode_2d(&p.tm_dy, dY, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B,
+                        "dY")) != FORGE_OK)
+      return st;
+    if ((st = encode_2d(&p.tm_x, X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B, "X")) !=
+        FORGE_OK)
+      return st;
+  }
+  if ((st = encode_state(&p.tm_w, W, "W")) != FORGE_OK) return st;
+  if ((st = encode_state(&p.tm_m, m, "m")) != FORGE_OK) return st;
+  if (opt == OPT_ADAMW) {
+    if ((st = encode_state(&p.tm_v, v, "v")) != FORGE_OK) return st;
+  } else {
+    p.tm_v = p.tm_m;  // unused
+  }
+  p.sc = sc;
+  p.m_scale = static_cast<float*>(m->scale);
+  p.v_scale = opt == OPT_ADAMW ? static_cast<float*>(v->scale) : nullptr;
+  p.status = dev->status;
+  p.d_out = static_cast<int>(d_out);
+  p.d_in = static_cast<int>(d_in);
+  p.bt = static_cast<int>(bt);
+  p.tiles_m = tiles_m;
+  p.tiles_n = tiles_n;
+  p.num_tiles = tiles_m * tiles_n;
+  p.num_kb = static_cast<int>((bt + 63) / 64);
+  p.group_m = 8;
+  p.step = static_cast<uint32_t>(step);
+  p.seed_lo = static_cast<uint32_t>(seed);
+  p.seed_hi = static_cast<uint32_t>(seed >> 32);
+  p.sr_w = h->sr_w ? 1 : 0;
+  p.sr_m = h->sr_moments ? 1 : 0;
+  p.flags = h->flags;
+  p.timeout_ns = kTimeoutNs;
+
+  TcLaunch l{};
+  l.opt = opt; l.wk = wk; l.mk = mk; l.bn = bn; l.deep = deep;
+  l.grid = p.num_tiles < dev->sms ? p.num_tiles : dev->sms;
+  l.stream = s;
+  cudaError_t e = opt == OPT_ADAMW ? launch_wgrad_tc_adamw(p, l)
+                  : opt == OPT_SGDM ? launch_wgrad_tc_sgdm(p, l)
+                                    : launch_wgrad_tc_lion(p, l);
+  if (e != cudaSuccess) return fail(FORGE_ERR_CUDA, "%s launch: %s", oname, cudaGetErrorString(e));
+  return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+forge_status forge_wgrad_step_adamw(const forge_tensor* X, const forge_tensor* dY, forge_tensor* W, forge_tensor* m,
+                                    forge_tensor* v, const forge_hyper* h, int64_t step, uint64_t seed,
+                                    forge_stream_t stream) {
+  return wgrad_step(OPT_ADAMW, X, dY, W, m, v, h, step, seed, stream);
+}
+
+forge_status forge_wgrad_step_sgdm(const forge_tensor* X, const forge_tensor* dY, forge_tensor* W, forge_tensor* m,
+                                   const forge_hyper* h, int64_t step, uint64_t seed, forge_stream_t stream) {
+  return wgrad_step(OPT_SGDM, X, dY, W, m, nullptr, h, step, seed, stream);
+}
+
+forge_status forge_wgrad_step_lion(const forge_tensor* X, const forge_tensor* dY, forge_tensor* W, forge_tensor* m,
+                                   const forge_hyper* h, int64_t step, uint64_t seed, forge_stream_t stream) {
+  return wgrad_step(OPT_LION, X, dY, W, m, nullptr, h, step, seed, stream);
+}
+
+forge_status forge_dgrad(const forge_tensor* dY, const forge_tensor* W_old, forge_tensor* dX, forge_stream_t stream) {
+  if (dY == nullptr || W_old == nullptr || dX == nullptr) return fail(FORGE_ERR_INVALID_ARG, "dgrad: null argument");
+  const int64_t bt = dY->rows, d_out = dY->cols, d_in = W_old->cols;
+  if (bt < 0 || d_out < 0 || d_in < 0) return fail(FORGE_ERR_INVALID_ARG, "dgrad: negative size");
+  if (dY->dtype != FORGE_BF16) return fail(FORGE_ERR_UNSUPPORTED, "dgrad: dY must be bf16");
+  if (W_old->dtype != FORGE_BF16 && W_old->dtype != FORGE_F32)
+    return fail(FORGE_ERR_UNSUPPORTED, "dgrad: W must be bf16 or f32");
+  if (dX->dtype != FORGE_BF16 && dX->dtype != FORGE_F32)
+    return fail(FORGE_ERR_UNSUPPORTED, "dgrad: dX must be bf16 or f32");
+  forge_status st;
+  if ((st = check_tensor(dY, "dY", bt, d_out, true)) != FORGE_OK) return st;
+  if ((st = check_tensor(W_old, "W", d_out, d_in, true)) != FORGE_OK) return st;
+  if ((st = check_tensor(dX, "dX", bt, d_in, true)) != FORGE_OK) return st;
+  if (d_in % 8 != 0 || d_out % 8 != 0)
+    return fail(FORGE_ERR_UNSUPPORTED, "dgrad: D_in (%lld) and D_out (%lld) must be multiples of 8",
+                (long long)d_in, (long long)d_out);
+  if (bt > 0x7FFFFFFF || d_in > 0x7FFFFFFF || d_out > 0x7FFFFFFF)
+    return fail(FORGE_ERR_INVALID_ARG, "dgrad: dimension exceeds 2^31 - 1");
+  if (bt == 0 || d_in == 0) return ok();
+
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != FORGE_OK) return st;
+  DgradParams p;
+  std::memset(&p, 0, sizeof(p));
+  if ((st = encode_2d(&p.tm_dy, dY, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, "dY")) !=
+      FORGE_OK)
+    return st;
+  if (W_old->dtype == FORGE_BF16) {
+    if ((st = encode_2d(&p.tm_w, W_old, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B,
+                        "W")) != FORGE_OK)
+      return st;
+    p.w_f32 = nullptr;
+  } else {
+    if ((st = encode_2d(&p.tm_w, W_old, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 32, 64, CU_TENSOR_MAP_SWIZZLE_128B,
+                        "W")) != FORGE_OK)
+      return st;
+    p.w_f32 = static_cast<const float*>(W_old->data);
+    p.ld_w32 = W_old->ld;
+  }
+  p.dX = dX->data;
+  p.ld_dx = dX->ld;
+  p.dx_bf16 = dX->dtype == FORGE_BF16 ? 1 : 0;
+  p.status = dev->status;
+  p.bt = static_cast<int>(bt);
+  p.d_out = static_cast<int>(d_out);
+  p.d_in = static_cast<int>(d_in);
+  p.tiles_m = static_cast<int>((bt + 127) / 128);
+  p.tiles_n = static_cast<int>((d_in + 127) / 128);
+  p.num_tiles = p.tiles_m * p.tiles_n;
+  p.num_kb = static_cast<int>((d_out + 63) / 64);
+  p.group_m = 8;
+  p.timeout_ns = kTimeoutNs;
+  const int grid = p.num_tiles < dev->sms ? p.num_tiles : dev->sms;
+  cudaError_t e = launch_dgrad_tc(p, grid, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(FORGE_ERR_CUDA, "dgrad launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+forge_status forge_sync_status(forge_stream_t stream) {
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(FORGE_ERR_CUDA, "cudaStreamSynchronize: %s", cudaGetErrorString(e));
+  unsigned int host[4] = {0, 0, 0, 0};
+  e = cudaMemcpyFromSymbol(host, forge_device_status, sizeof(host));
+  if (e != cudaSuccess) return fail(FORGE_ERR_CUDA, "reading the status word: %s", cudaGetErrorString(e));
+  if (host[0] != 0) {
+    const unsigned int zero[4] = {0, 0, 0, 0};
+    e = cudaMemcpyToSymbol(forge_device_status, zero, sizeof(zero));
+    if (e != cudaSuccess) return fail(FORGE_ERR_CUDA, "clearing the status word: %s", cudaGetErrorString(e));
+    const char* what = "unknown wait";
+    switch (host[0]) {
+      case WAIT_OP_EMPTY: what = "operand producer waiting for a free stage"; break;
+      case WAIT_OP_FULL: what = "MMA issuer waiting for an operand stage"; break;
+      case WAIT_TMEM_EMPTY: what = "MMA issuer waiting for a drained accumulator"; break;
+      case WAIT_ST_EMPTY: what = "state producer waiting for a free slot"; break;
+      case WAIT_ST_WRITTEN: what = "state storer waiting for the epilogue"; break;
+      case WAIT_TMEM_FULL: what = "epilogue waiting for an accumulator"; break;
+      case WAIT_ST_FULL: what = "epilogue waiting for a state slot"; break;
+      case WAIT_RED: what = "epilogue waiting for the block absmax exchange"; break;
+      case WAIT_TEST_HOOK: what = "forced-timeout test hook"; break;
+      case WAIT_MMA_DRAIN: what = "MMA issuer draining after an abort"; break;
+      case WAIT_DRAIN: what = "producer draining after an abort"; break;
+      default: break;
+    }
+    return fail(FORGE_ERR_TIMEOUT, "device wait gave up: %s (code 0x%x)", what, host[0]);
+  }
+  return ok();
+}
+
+const char* forge_last_error(void) { return g_last_error.c_str(); }
+
+const char* forge_version(void) { return "0.1.0"; }
+
+size_t forge_workspace_bytes(int64_t, int64_t, int64_t) { return 0; }
+
+}  // extern "C"

@@ -1,0 +1,106 @@
+// forge_params.h -- kernel parameter blocks and launcher declarations
+// shared between the C-ABI translation unit and the kernel translation
+// units. Host and device code both include it.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "forge_math.cuh"
+
+namespace forge {
+
+// Device status word codes (first failure wins). The low byte names the
+// wait that gave up.
+enum : uint32_t {
+  STATUS_OK = 0,
+  WAIT_OP_EMPTY = 0xF001,     // operand producer: free operand stage
+  WAIT_OP_FULL = 0xF002,      // MMA issuer: operand stage landed
+  WAIT_TMEM_EMPTY = 0xF003,   // MMA issuer: accumulator buffer drained
+  WAIT_ST_EMPTY = 0xF004,     // state producer: free state slot
+  WAIT_ST_WRITTEN = 0xF005,   // state storer: epilogue finished a slot
+  WAIT_TMEM_FULL = 0xF006,    // epilogue: accumulator ready
+  WAIT_ST_FULL = 0xF007,      // epilogue: state slot landed
+  WAIT_RED = 0xF008,          // epilogue: 8-bit block absmax exchange
+  WAIT_TEST_HOOK = 0xF009,    // epilogue: the forced-timeout test barrier
+  WAIT_MMA_DRAIN = 0xF00A,    // MMA issuer: in-flight MMAs after an abort
+  WAIT_DRAIN = 0xF00B,        // a producer's in-flight loads after an abort
+};
+
+constexpr uint32_t FLAG_TILE_N_MASK = 7u;
+constexpr uint32_t FLAG_TEST_FORCE_TIMEOUT = 0x100u;
+
+// Tensor-core fused step (bf16 X / dY).
+struct alignas(128) WgradTcParams {
+  CUtensorMap tm_dy;  // dY  [BT][D_out] bf16, box 64 x 64, 128-byte swizzle
+  CUtensorMap tm_x;   // X   [BT][D_in]  bf16, box 64 x 64, 128-byte swizzle
+  CUtensorMap tm_w;   // W   [D_out][D_in], box 32 cols x 128 rows
+  CUtensorMap tm_m;   // m   (values or 8-bit codes), box 32 x 128
+  CUtensorMap tm_v;   // v   (AdamW only)
+  StepScalars sc;
+  float* m_scale;     // 8-bit state: [D_in/128][D_out]
+  float* v_scale;
+  unsigned int* status;
+  int d_out, d_in, bt;
+  int tiles_m, tiles_n, num_tiles, num_kb;
+  int group_m;
+  uint32_t step, seed_lo, seed_hi;
+  int sr_w, sr_m;
+  uint32_t flags;
+  uint64_t timeout_ns;
+};
+
+// fp32 fused step (fp32 X / dY), plain CUDA cores.
+struct WgradSimtParams {
+  const float* X;
+  const float* dY;
+  void* W;
+  void* m;
+  void* v;
+  float* m_scale;
+  float* v_scale;
+  int64_t ld_x, ld_dy, ld_w, ld_m, ld_v;
+  int d_out, d_in, bt;
+  StepScalars sc;
+  uint32_t step, seed_lo, seed_hi;
+  int sr_w, sr_m;
+};
+
+// Input gradient dX = dY W (tensor cores).
+struct alignas(128) DgradParams {
+  CUtensorMap tm_dy;  // dY [BT][D_out] bf16, box 64 (K) x 128 (M rows), 128-byte swizzle
+  CUtensorMap tm_w;   // W bf16 [D_out][D_in], box 64 (N) x 64 (K), 128-byte swizzle
+  const float* w_f32; // W fp32 (staged and rounded to bf16 by the kernel) or null
+  int64_t ld_w32;
+  void* dX;           // [BT][D_in]
+  int64_t ld_dx;
+  int dx_bf16;
+  unsigned int* status;
+  int bt, d_out, d_in;
+  int tiles_m, tiles_n, num_tiles, num_kb;
+  int group_m;
+  uint32_t flags;
+  uint64_t timeout_ns;
+};
+
+struct TcLaunch {
+  int opt, wk, mk;
+  int bn;       // tile width (64 or 128)
+  int deep;     // 1: deeper operand pipeline for long token axes
+  int grid;
+  cudaStream_t stream;
+};
+
+// Defined in the kernel translation units.
+cudaError_t launch_wgrad_tc_adamw(const WgradTcParams& p, const TcLaunch& l);
+cudaError_t launch_wgrad_tc_sgdm(const WgradTcParams& p, const TcLaunch& l);
+cudaError_t launch_wgrad_tc_lion(const WgradTcParams& p, const TcLaunch& l);
+cudaError_t launch_wgrad_simt(const WgradSimtParams& p, int opt, int wk, int mk, cudaStream_t stream);
+cudaError_t launch_dgrad_tc(const DgradParams& p, int grid, cudaStream_t stream);
+
+// Whether a (opt, wk, mk, bn, deep) variant has a tensor-core kernel.
+bool wgrad_tc_supported(int opt, int wk, int mk, int bn, int deep);
+
+}  // namespace forge

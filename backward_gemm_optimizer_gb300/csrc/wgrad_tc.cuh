@@ -1,0 +1,628 @@
+// wgrad_tc.cuh -- the fused weight-gradient + optimizer-step kernel for
+// sm_103a (FORGE, Algorithm 1, re-designed for tcgen05 tensor cores).
+//
+// One persistent CTA per SM walks a grouped raster of 128 x BN gradient
+// tiles G_ij = sum_k dY_k,i^T X_k,j (Eq. 5). Warp roles (384 threads):
+//
+//   warp 0      operand producer: TMA loads of the 64-token slabs of dY and
+//               X into a STAGES-deep shared-memory ring;
+//   warp 1      MMA issuer: one thread issues tcgen05.mma (M = 128, N = BN,
+//               K = 16) into a double-buffered fp32 TMEM accumulator; the
+//               warp also owns the TMEM allocation;
+//   warp 2      state producer: TMA loads of the W / m / v tiles, in
+//               32-column chunks, into an NBUF-deep slot ring;
+//   warp 3      state storer: TMA stores of each finished chunk;
+//   warps 4-11  epilogue: warp w reads TMEM lane quadrant w % 4 (row p of
+//               the tile = TMEM lane) and column half (w - 4) / 4 of each
+//               chunk, applies the optimizer element-wise in fp32 and writes
+//               the new W / m / v back into the slot (Algorithm 1 phase 2-3).
+//
+// The accumulator never leaves TMEM / registers: no gradient tile is ever
+// written to global memory (Proposition 3). Both operands are token-major
+// in memory, so A = dY^T and B = X are fed to the tensor cores as MN-major
+// shared-memory matrices (no transpose is materialised).
+//
+// Every wait is bounded: a wait that gives up records a status code, sets
+// a shared abort flag seen by every other role, and the CTA drains what it
+// has in flight and exits; it never traps and never waits forever.
+#pragma once
+
+#include <cstdint>
+
+#include "forge_math.cuh"
+#include "forge_params.h"
+#include "forge_ptx.cuh"
+
+namespace forge {
+
+template <int OPT, int WK, int MK, int BN_, int STAGES_, int NBUF_>
+struct TcCfg {
+  static constexpr int BM = 128;       // tile rows (D_out), one per TMEM lane
+  static constexpr int BN = BN_;       // tile columns (D_in)
+  static constexpr int BK = 64;        // tokens per operand stage
+  static constexpr int CW = 32;        // state chunk width (columns)
+  static constexpr int STAGES = STAGES_;
+  static constexpr int NBUF = NBUF_;
+  static constexpr int NCH = BN / CW;  // chunks per tile
+  static constexpr bool TWO = (OPT == OPT_ADAMW);  // second moment present
+  static constexpr bool Q8 = (MK == M_Q8);
+  static constexpr int WE = (WK == W_F32) ? 4 : 2;
+  static constexpr int ME = (MK == M_F32) ? 4 : (MK == M_BF16 ? 2 : 1);
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int W_CH = BM * CW * WE;
+  static constexpr int M_CH = BM * CW * ME;
+  static constexpr int V_CH = TWO ? M_CH : 0;
+  static constexpr int SLOT_BYTES = ((W_CH + M_CH + V_CH + 1023) / 1024) * 1024;
+  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NBUF * SLOT_BYTES;
+  static constexpr int TMEM_COLS = (2 * BN <= 128) ? 128 : (2 * BN <= 256 ? 256 : 512);
+  static constexpr int NUM_THREADS = 384;
+  static constexpr int EPI_WARPS = 8;
+  static constexpr int EPI_THREADS = EPI_WARPS * 32;
+  static constexpr uint32_t IDESC = make_idesc_bf16(BM, BN, 1, 1);
+
+};
+
+// Byte offset of 16-byte chunk `c` of row `r` in a TMA tile whose rows are
+// 32 * E bytes, written with the matching swizzle (128, 64 or 32 bytes):
+// the chunk index is XOR-ed with address bits 7.. of the row start.
+template <int E>
+__device__ __forceinline__ uint32_t swz(int r, int c) {
+  constexpr int RB = 32 * E;
+  const int x = (RB == 128) ? (r & 7) : (RB == 64 ? ((r >> 1) & 3) : ((r >> 2) & 1));
+  return static_cast<uint32_t>(r * RB + ((c ^ x) << 4));
+}
+
+// 16 consecutive values of row r, columns [16h, 16h + 16) of a chunk.
+template <int KIND>  // 0: f32, 1: bf16
+__device__ __forceinline__ void ld16(const uint8_t* base, int r, int h, float (&o)[16]) {
+  if constexpr (KIND == 0) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float4 t = *reinterpret_cast<const float4*>(base + swz<4>(r, 4 * h + k));
+      o[4 * k + 0] = t.x; o[4 * k + 1] = t.y; o[4 * k + 2] = t.z; o[4 * k + 3] = t.w;
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const uint4 t = *reinterpret_cast<const uint4*>(base + swz<2>(r, 2 * h + k));
+      const uint32_t wv[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        o[8 * k + 2 * i + 0] = bf16_bits_to_f32(wv[i] & 0xFFFFu);
+        o[8 * k + 2 * i + 1] = bf16_bits_to_f32(wv[i] >> 16);
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void st16_f32(uint8_t* base, int r, int h, const float (&o)[16]) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    *reinterpret_cast<float4*>(base + swz<4>(r, 4 * h + k)) =
+        make_float4(o[4 * k + 0], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+}
+
+__device__ __forceinline__ void st16_bf16(uint8_t* base, int r, int h, const uint32_t (&b)[16]) {
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    uint4 t;
+    t.x = b[8 * k + 0] | (b[8 * k + 1] << 16);
+    t.y = b[8 * k + 2] | (b[8 * k + 3] << 16);
+    t.z = b[8 * k + 4] | (b[8 * k + 5] << 16);
+    t.w = b[8 * k + 6] | (b[8 * k + 7] << 16);
+    *reinterpret_cast<uint4*>(base + swz<2>(r, 2 * h + k)) = t;
+  }
+}
+
+__device__ __forceinline__ void ld16_codes(const uint8_t* base, int r, int h, uint32_t (&c)[16]) {
+  const uint4 t = *reinterpret_cast<const uint4*>(base + swz<1>(r, h));
+  const uint32_t wv[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+  for (int i = 0; i < 16; ++i) c[i] = (wv[i >> 2] >> (8 * (i & 3))) & 0xFFu;
+}
+
+__device__ __forceinline__ void st16_codes(uint8_t* base, int r, int h, const uint32_t (&c)[16]) {
+  uint32_t wv[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+  for (int i = 0; i < 16; ++i) wv[i >> 2] |= (c[i] & 0xFFu) << (8 * (i & 3));
+  *reinterpret_cast<uint4*>(base + swz<1>(r, h)) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+}
+
+__device__ __forceinline__ int32_t sext8(uint32_t b) { return static_cast<int32_t>(static_cast<int8_t>(b & 0xFFu)); }
+
+__device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, int group_m, int& tm, int& tn) {
+  const int per_group = group_m * tiles_n;
+  const int g = tile / per_group;
+  const int first_m = g * group_m;
+  const int rem = tiles_m - first_m;
+  const int gsize = rem < group_m ? rem : group_m;
+  const int in_g = tile - g * per_group;
+  tm = first_m + in_g % gsize;
+  tn = in_g / gsize;
+}
+
+// Bounded wait on an mbarrier phase. Returns false if the CTA is aborting
+// (another role gave up) or if this wait exceeded `limit_ns`, in which case
+// it raises the abort flag and records `code` in the device status word.
+__device__ __forceinline__ bool bwait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                      unsigned int* status, uint32_t code, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((n & 7u) == 0u) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > limit_ns) {
+        *abort_flag = 1;
+        atomicCAS(status, 0u, code);
+        return false;
+      }
+    }
+  }
+}
+
+// After an abort: wait (bounded) for the last fills a producer issued on a
+// ring of barriers, so that no TMA write lands after the CTA has exited.
+__device__ __forceinline__ void drain_ring(uint64_t* full, int ring, uint32_t issued, unsigned int* status) {
+  const uint32_t first = issued > static_cast<uint32_t>(ring) ? issued - ring : 0u;
+  for (uint32_t k = first; k < issued; ++k) {
+    const int s = static_cast<int>(k % ring);
+    const uint32_t ph = (k / ring) & 1u;
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(&full[s], ph)) {
+      if (globaltimer_ns() - t0 > 200000000ull) {  // 0.2 s: a load never takes this long
+        atomicCAS(status, 0u, WAIT_DRAIN);
+        break;
+      }
+    }
+  }
+}
+
+template <int OPT, int WK, int MK, int BN, int STAGES, int NBUF>
+__global__ void __launch_bounds__(384, 1) wgrad_step_tc_kernel(const __grid_constant__ WgradTcParams p) {
+  using C = TcCfg<OPT, WK, MK, BN, STAGES, NBUF>;
+  static_assert(BN == 64 || BN == 128, "tile width");
+  static_assert(!C::Q8 || BN == 128, "8-bit blocks span one 128-column tile row");
+  static_assert(!C::Q8 || NBUF >= C::NCH, "8-bit moments hold a whole tile of slots");
+  static_assert(NBUF >= 2 && STAGES >= 2, "pipelines");
+  static_assert(C::SMEM_BYTES <= 227 * 1024, "shared memory");
+
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t op_full[STAGES], op_empty[STAGES];
+  __shared__ __align__(8) uint64_t st_full[NBUF], st_empty[NBUF], st_written[NBUF];
+  __shared__ __align__(8) uint64_t tm_full[2], tm_empty[2];
+  __shared__ __align__(8) uint64_t red_bar[2];
+  __shared__ __align__(8) uint64_t never_bar, mma_drain_bar;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+  __shared__ float red_sh[2][2][2][128];  // [tile parity][m | sqrt v][half][row]
+
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* op_base = smem;
+  uint8_t* st_base = smem + STAGES * C::STAGE_BYTES;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  volatile int* abort_flag = &abort_sh;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) { mbar_init(&op_full[s], 1); mbar_init(&op_empty[s], 1); }
+    for (int s = 0; s < NBUF; ++s) {
+      mbar_init(&st_full[s], 1);
+      mbar_init(&st_empty[s], 1);
+      mbar_init(&st_written[s], C::EPI_THREADS);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tm_full[b], 1);
+      mbar_init(&tm_empty[b], C::EPI_WARPS);
+      mbar_init(&red_bar[b], C::EPI_THREADS);
+    }
+    mbar_init(&never_bar, 1);
+    mbar_init(&mma_drain_bar, 1);
+    abort_sh = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    if (p.num_kb > 0) { prefetch_tmap(&p.tm_dy); prefetch_tmap(&p.tm_x); }
+    prefetch_tmap(&p.tm_w); prefetch_tmap(&p.tm_m);
+    if constexpr (C::TWO) prefetch_tmap(&p.tm_v);
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base_sh, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = tmem_base_sh;
+  const uint64_t lim = p.timeout_ns;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ operand producer
+    if (lane == 0) {
+      uint32_t kseq = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+        int tm, tn;
+        tile_coords(tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+        for (int kb = 0; kb < p.num_kb; ++kb, ++kseq) {
+          const int s = static_cast<int>(kseq % STAGES);
+          const uint32_t ph = (kseq / STAGES) & 1u;
+          if (!bwait(&op_empty[s], ph ^ 1u, abort_flag, p.status, WAIT_OP_EMPTY, lim)) { ok = false; break; }
+          uint8_t* a = op_base + s * C::STAGE_BYTES;
+          uint8_t* b = a + C::A_BYTES;
+          mbar_arrive_expect_tx(&op_full[s], C::STAGE_BYTES);
+          tma_load_2d(a, &p.tm_dy, &op_full[s], tm * C::BM, kb * C::BK);
+          tma_load_2d(a + 8192, &p.tm_dy, &op_full[s], tm * C::BM + 64, kb * C::BK);
+#pragma unroll
+          for (int bb = 0; bb < BN / 64; ++bb)
+            tma_load_2d(b + bb * 8192, &p.tm_x, &op_full[s], tn * BN + bb * 64, kb * C::BK);
+        }
+      }
+      if (!ok) drain_ring(op_full, STAGES, kseq, p.status);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t kseq = 0;
+      bool ok = true;
+      int it = 0;
+      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++it) {
+        const int buf = it & 1;
+        const uint32_t eph = ((it >> 1) & 1) ^ 1u;
+        if (!bwait(&tm_empty[buf], eph, abort_flag, p.status, WAIT_TMEM_EMPTY, lim)) { ok = false; break; }
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
+        for (int kb = 0; kb < p.num_kb; ++kb, ++kseq) {
+          const int s = static_cast<int>(kseq % STAGES);
+          const uint32_t ph = (kseq / STAGES) & 1u;
+          if (!bwait(&op_full[s], ph, abort_flag, p.status, WAIT_OP_FULL, lim)) { ok = false; break; }
+          tc_fence_after_sync();
+          const uint32_t a0 = smem_u32(op_base + s * C::STAGE_BYTES);
+          const uint32_t b0 = a0 + C::A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < C::BK / 16; ++kk) {
+            // 16 tokens = two 8-row K groups of 1024 bytes; MN atoms 8192 bytes apart.
+            const uint64_t ad = make_smem_desc(a0 + kk * 2048, 8192, 1024, 2);
+            const uint64_t bd = make_smem_desc(b0 + kk * 2048, 8192, 1024, 2);
+            umma_f16(d_tmem, ad, bd, C::IDESC, (kb > 0 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(&op_empty[s]);
+        }
+        if (!ok) break;
+        umma_commit(&tm_full[buf]);
+      }
+      if (!ok) {
+        // Let every MMA already issued finish before TMEM is released.
+        umma_commit(&mma_drain_bar);
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(&mma_drain_bar, 0)) {
+          if (globaltimer_ns() - t0 > 200000000ull) { atomicCAS(p.status, 0u, WAIT_MMA_DRAIN); break; }
+        }
+      }
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ state producer
+    if (lane == 0) {
+      uint32_t cseq = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+        int tm, tn;
+        tile_coords(tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+        for (int c = 0; c < C::NCH; ++c, ++cseq) {
+          const int s = static_cast<int>(cseq % NBUF);
+          const uint32_t ph = (cseq / NBUF) & 1u;
+          if (!bwait(&st_empty[s], ph ^ 1u, abort_flag, p.status, WAIT_ST_EMPTY, lim)) { ok = false; break; }
+          uint8_t* slot = st_base + s * C::SLOT_BYTES;
+          const int x = tn * BN + c * C::CW, y = tm * C::BM;
+          mbar_arrive_expect_tx(&st_full[s], C::W_CH + C::M_CH + C::V_CH);
+          tma_load_2d(slot, &p.tm_w, &st_full[s], x, y);
+          tma_load_2d(slot + C::W_CH, &p.tm_m, &st_full[s], x, y);
+          if constexpr (C::TWO) tma_load_2d(slot + C::W_CH + C::M_CH, &p.tm_v, &st_full[s], x, y);
+        }
+      }
+      if (!ok) drain_ring(st_full, NBUF, cseq, p.status);
+    }
+  } else if (warp == 3) {
+    // ------------------------------------------------------------ state storer
+    if (lane == 0) {
+      uint32_t cseq = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+        int tm, tn;
+        tile_coords(tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+        for (int c = 0; c < C::NCH; ++c, ++cseq) {
+          const int s = static_cast<int>(cseq % NBUF);
+          const uint32_t ph = (cseq / NBUF) & 1u;
+          if (!bwait(&st_written[s], ph, abort_flag, p.status, WAIT_ST_WRITTEN, lim)) { ok = false; break; }
+          const uint8_t* slot = st_base + s * C::SLOT_BYTES;
+          const int x = tn * BN + c * C::CW, y = tm * C::BM;
+          tma_store_2d(&p.tm_w, slot, x, y);
+          tma_store_2d(&p.tm_m, slot + C::W_CH, x, y);
+          if constexpr (C::TWO) tma_store_2d(&p.tm_v, slot + C::W_CH + C::M_CH, x, y);
+          bulk_commit_group();
+          bulk_wait_group_read0();
+          mbar_arrive(&st_empty[s]);
+        }
+      }
+      bulk_wait_group0();
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (warps 4..11)
+    const int q = warp & 3;          // TMEM lane quadrant this warp may access
+    const int h = (warp - 4) >> 2;   // column half of each 32-column chunk
+    const int r = q * 32 + lane;     // tile row == TMEM lane
+    const StepScalars sc = p.sc;
+    uint32_t cseq = 0;
+    int it = 0;
+    bool ok = true;
+
+    if (p.flags & FLAG_TEST_FORCE_TIMEOUT) {
+      // Test hook: a barrier nothing signals, with a short bound.
+      ok = bwait(&never_bar, 0, abort_flag, p.status, WAIT_TEST_HOOK, 1000000ull);
+      ok = __all_sync(0xFFFFFFFFu, ok);
+    }
+
+    for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++it) {
+      int tm, tn;
+      tile_coords(tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+      const int buf = it & 1;
+      ok = bwait(&tm_full[buf], (it >> 1) & 1, abort_flag, p.status, WAIT_TMEM_FULL, lim);
+      ok = __all_sync(0xFFFFFFFFu, ok);
+      if (!ok) break;
+      tc_fence_after_sync();
+      const int row = tm * C::BM + r;
+      const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * BN);
+
+      if constexpr (!C::Q8) {
+        for (int c = 0; c < C::NCH; ++c, ++cseq) {
+          const int s = static_cast<int>(cseq % NBUF);
+          ok = bwait(&st_full[s], (cseq / NBUF) & 1u, abort_flag, p.status, WAIT_ST_FULL, lim);
+          ok = __all_sync(0xFFFFFFFFu, ok);
+          if (!ok) break;
+          uint32_t gr[16];
+          if (p.num_kb > 0) {
+            tmem_ld_32x32b_x16(t_lane + c * C::CW + h * 16, gr);
+            tmem_ld_wait();
+          } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) gr[j] = 0u;
+          }
+          uint8_t* slot = st_base + s * C::SLOT_BYTES;
+          uint8_t* sw = slot;
+          uint8_t* sm = slot + C::W_CH;
+          uint8_t* sv = slot + C::W_CH + C::M_CH;
+          float w[16], m[16], v[16];
+          ld16<WK == W_F32 ? 0 : 1>(sw, r, h, w);
+          ld16<MK == M_F32 ? 0 : 1>(sm, r, h, m);
+          if constexpr (C::TWO) ld16<MK == M_F32 ? 0 : 1>(sv, r, h, v);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float g = __uint_as_float(gr[j]);
+            float w1, m1, v1 = 0.0f;
+            if constexpr (OPT == OPT_ADAMW) adamw_elem(g, w[j], m[j], v[j], sc, w1, m1, v1);
+            else if constexpr (OPT == OPT_SGDM) sgdm_elem(g, w[j], m[j], sc, w1, m1);
+            else lion_elem(g, w[j], m[j], sc, w1, m1);
+            w[j] = w1; m[j] = m1;
+            if constexpr (C::TWO) v[j] = v1;
+          }
+          const int q0 = tn * BN + c * C::CW + h * 16;   // first column of this thread's 16
+          const uint64_t idx0 = static_cast<uint64_t>(row) * static_cast<uint64_t>(p.d_in) + q0;
+          if constexpr (WK == W_F32) {
+            st16_f32(sw, r, h, w);
+          } else {
+            uint32_t b[16];
+            if (p.sr_w) {
+#pragma unroll
+              for (int k = 0; k < 2; ++k) {
+                const U4 rr = sr_block((idx0 >> 3) + k, p.step, 0u, p.seed_lo, p.seed_hi);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) b[8 * k + j] = f32_to_bf16_sr(w[8 * k + j], sr_lane(rr, j));
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) b[j] = f32_to_bf16_rne(w[j]);
+            }
+            st16_bf16(sw, r, h, b);
+          }
+          if constexpr (MK == M_F32) {
+            st16_f32(sm, r, h, m);
+            if constexpr (C::TWO) st16_f32(sv, r, h, v);
+          } else {
+            uint32_t b[16];
+            if (p.sr_m) {
+#pragma unroll
+              for (int k = 0; k < 2; ++k) {
+                const U4 rr = sr_block((idx0 >> 3) + k, p.step, 1u, p.seed_lo, p.seed_hi);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) b[8 * k + j] = f32_to_bf16_sr(m[8 * k + j], sr_lane(rr, j));
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) b[j] = f32_to_bf16_rne(m[j]);
+            }
+            st16_bf16(sm, r, h, b);
+            if constexpr (C::TWO) {
+              if (p.sr_m) {
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                  const U4 rr = sr_block((idx0 >> 3) + k, p.step, 2u, p.seed_lo, p.seed_hi);
+#pragma unroll
+                  for (int j = 0; j < 8; ++j) b[8 * k + j] = f32_to_bf16_sr(v[8 * k + j], sr_lane(rr, j));
+                }
+              } else {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) b[j] = f32_to_bf16_rne(v[j]);
+              }
+              st16_bf16(sv, r, h, b);
+            }
+          }
+          fence_proxy_async_smem();
+          mbar_arrive(&st_written[s]);
+        }
+        if (!ok) break;
+      } else {
+        // -------------------------------------------------- 8-bit block moments
+        // The 128 columns of this tile row are one quantisation block, so the
+        // new block absmax needs every chunk: pass 1 forms the new moments
+        // and their absmax, pass 2 recomputes them, steps W and quantises.
+        const int jb = tn;  // block column (BN == 128)
+        float sm_old = 0.0f, sv_old = 0.0f;
+        if (row < p.d_out) {
+          sm_old = p.m_scale[static_cast<int64_t>(jb) * p.d_out + row];
+          if constexpr (C::TWO) sv_old = p.v_scale[static_cast<int64_t>(jb) * p.d_out + row];
+        }
+        float am = 0.0f, au = 0.0f;
+        for (int c = 0; c < C::NCH; ++c) {
+          const uint32_t k = cseq + c;
+          const int s = static_cast<int>(k % NBUF);
+          ok = bwait(&st_full[s], (k / NBUF) & 1u, abort_flag, p.status, WAIT_ST_FULL, lim);
+          ok = __all_sync(0xFFFFFFFFu, ok);
+          if (!ok) break;
+          uint32_t gr[16];
+          if (p.num_kb > 0) {
+            tmem_ld_32x32b_x16(t_lane + c * C::CW + h * 16, gr);
+            tmem_ld_wait();
+          } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) gr[j] = 0u;
+          }
+          const uint8_t* slot = st_base + s * C::SLOT_BYTES;
+          uint32_t cm[16], cv[16];
+          float w[16];
+          ld16_codes(slot + C::W_CH, r, h, cm);
+          if constexpr (C::TWO) ld16_codes(slot + C::W_CH + C::M_CH, r, h, cv);
+          if constexpr (OPT == OPT_SGDM) ld16<WK == W_F32 ? 0 : 1>(slot, r, h, w);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float g = __uint_as_float(gr[j]);
+            const float m0 = dequant_m(sext8(cm[j]), sm_old);
+            float m1;
+            if constexpr (OPT == OPT_ADAMW) {
+              float v1;
+              adamw_moments(g, m0, dequant_v(cv[j], sv_old), sc, m1, v1);
+              au = fmaxf(au, __fsqrt_rn(v1));
+            } else if constexpr (OPT == OPT_SGDM) {
+              m1 = __fadd_rn(__fmul_rn(sc.b1, m0), __fadd_rn(g, __fmul_rn(sc.wd, w[j])));
+            } else {
+              m1 = __fadd_rn(__fmul_rn(sc.b2, m0), __fmul_rn(sc.omb2, g));
+            }
+            am = fmaxf(am, fabsf(m1));
+          }
+        }
+        if (!ok) break;
+        // Combine the two column halves of each row (bounded, abort-aware).
+        red_sh[it & 1][0][h][r] = am;
+        red_sh[it & 1][1][h][r] = au;
+        mbar_arrive(&red_bar[it & 1]);
+        ok = bwait(&red_bar[it & 1], (it >> 1) & 1, abort_flag, p.status, WAIT_RED, lim);
+        ok = __all_sync(0xFFFFFFFFu, ok);
+        if (!ok) break;
+        am = fmaxf(am, red_sh[it & 1][0][h ^ 1][r]);
+        au = fmaxf(au, red_sh[it & 1][1][h ^ 1][r]);
+        const float sm_new = __fdiv_rn(am, 127.0f);
+        const float sv_new = __fdiv_rn(au, 255.0f);
+        if (h == 0 && row < p.d_out) {
+          p.m_scale[static_cast<int64_t>(jb) * p.d_out + row] = sm_new;
+          if constexpr (C::TWO) p.v_scale[static_cast<int64_t>(jb) * p.d_out + row] = sv_new;
+        }
+        for (int c = 0; c < C::NCH; ++c, ++cseq) {
+          const int s = static_cast<int>(cseq % NBUF);
+          uint32_t gr[16];
+          if (p.num_kb > 0) {
+            tmem_ld_32x32b_x16(t_lane + c * C::CW + h * 16, gr);
+            tmem_ld_wait();
+          } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) gr[j] = 0u;
+          }
+          uint8_t* slot = st_base + s * C::SLOT_BYTES;
+          uint8_t* sw = slot;
+          uint8_t* smc = slot + C::W_CH;
+          uint8_t* svc = slot + C::W_CH + C::M_CH;
+          uint32_t cm[16], cv[16];
+          float w[16];
+          ld16<WK == W_F32 ? 0 : 1>(sw, r, h, w);
+          ld16_codes(smc, r, h, cm);
+          if constexpr (C::TWO) ld16_codes(svc, r, h, cv);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float g = __uint_as_float(gr[j]);
+            const float m0 = dequant_m(sext8(cm[j]), sm_old);
+            float w1, m1;
+            if constexpr (OPT == OPT_ADAMW) {
+              float v1;
+              adamw_elem(g, w[j], m0, dequant_v(cv[j], sv_old), sc, w1, m1, v1);
+              cv[j] = quant_v(v1, __fsqrt_rn(v1), sv_new);
+            } else if constexpr (OPT == OPT_SGDM) {
+              sgdm_elem(g, w[j], m0, sc, w1, m1);
+            } else {
+              lion_elem(g, w[j], m0, sc, w1, m1);
+            }
+            w[j] = w1;
+            cm[j] = static_cast<uint32_t>(quant_m(m1, sm_new)) & 0xFFu;
+          }
+          if constexpr (WK == W_F32) {
+            st16_f32(sw, r, h, w);
+          } else {
+            uint32_t b[16];
+            const int q0 = tn * BN + c * C::CW + h * 16;
+            const uint64_t idx0 = static_cast<uint64_t>(row) * static_cast<uint64_t>(p.d_in) + q0;
+            if (p.sr_w) {
+#pragma unroll
+              for (int k = 0; k < 2; ++k) {
+                const U4 rr = sr_block((idx0 >> 3) + k, p.step, 0u, p.seed_lo, p.seed_hi);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) b[8 * k + j] = f32_to_bf16_sr(w[8 * k + j], sr_lane(rr, j));
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) b[j] = f32_to_bf16_rne(w[j]);
+            }
+            st16_bf16(sw, r, h, b);
+          }
+          st16_codes(smc, r, h, cm);
+          if constexpr (C::TWO) st16_codes(svc, r, h, cv);
+          fence_proxy_async_smem();
+          mbar_arrive(&st_written[s]);
+        }
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tm_empty[buf]);
+    }
+  }
+
+  // ------------------------------------------------------------ teardown
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+template <int OPT, int WK, int MK, int BN, int STAGES, int NBUF>
+cudaError_t launch_tc_variant(const WgradTcParams& p, int grid, cudaStream_t stream) {
+  using C = TcCfg<OPT, WK, MK, BN, STAGES, NBUF>;
+  auto kern = wgrad_step_tc_kernel<OPT, WK, MK, BN, STAGES, NBUF>;
+  // The opt-in shared-memory size is a per-device function attribute: set
+  // it once per device (bit d of the mask) before the first launch there.
+  static unsigned long long attr_mask = 0ull;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (!(__atomic_load_n(&attr_mask, __ATOMIC_ACQUIRE) & bit)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    __atomic_fetch_or(&attr_mask, bit, __ATOMIC_ACQ_REL);
+  }
+  kern<<<grid, C::NUM_THREADS, C::SMEM_BYTES, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace forge

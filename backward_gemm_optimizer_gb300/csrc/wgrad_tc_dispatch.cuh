@@ -1,0 +1,69 @@
+// wgrad_tc_dispatch.cuh -- compile-time choice of pipeline depths and the
+// runtime dispatch over (weight dtype, moment dtype, tile width, depth) for
+// one optimizer. Included once per optimizer translation unit.
+#pragma once
+
+#include "wgrad_tc.cuh"
+
+namespace forge {
+
+// Shared memory available to the dynamic ring after the kernel's static
+// shared memory (barriers + the 4 KB absmax exchange) is accounted for.
+constexpr int kDynSmemBudget = 227 * 1024 - 5 * 1024;
+
+template <int OPT, int WK, int MK, int BN, int STAGES>
+constexpr int slots_that_fit() {
+  using C = TcCfg<OPT, WK, MK, BN, STAGES, 2>;
+  const int avail = kDynSmemBudget - 1024 - STAGES * C::STAGE_BYTES;
+  const int n = avail / C::SLOT_BYTES;
+  return n > 8 ? 8 : n;
+}
+
+// Operand stages: 2 for short token axes (the step is bound by the state
+// stream), 4 (or 3 when the state slots would not fit) for long ones.
+template <int OPT, int WK, int MK, int BN, int DEEP>
+constexpr int pick_stages() {
+  if (!DEEP) return 2;
+  constexpr int need = (MK == M_Q8) ? 4 : 2;
+  return slots_that_fit<OPT, WK, MK, BN, 4>() >= need ? 4 : 3;
+}
+
+template <int OPT, int WK, int MK, int BN, int DEEP>
+cudaError_t launch_one(const WgradTcParams& p, int grid, cudaStream_t stream) {
+  constexpr int S = pick_stages<OPT, WK, MK, BN, DEEP>();
+  constexpr int N = slots_that_fit<OPT, WK, MK, BN, S>();
+  static_assert(N >= ((MK == M_Q8) ? 4 : 2), "state ring does not fit");
+  return launch_tc_variant<OPT, WK, MK, BN, S, N>(p, grid, stream);
+}
+
+template <int OPT, int WK, int MK>
+cudaError_t launch_mk(const WgradTcParams& p, const TcLaunch& l) {
+  if constexpr (MK == M_Q8) {
+    if (l.bn != 128) return cudaErrorInvalidValue;
+    return l.deep ? launch_one<OPT, WK, MK, 128, 1>(p, l.grid, l.stream)
+                  : launch_one<OPT, WK, MK, 128, 0>(p, l.grid, l.stream);
+  } else {
+    if (l.bn == 64) {
+      if (l.deep) return cudaErrorInvalidValue;
+      return launch_one<OPT, WK, MK, 64, 0>(p, l.grid, l.stream);
+    }
+    return l.deep ? launch_one<OPT, WK, MK, 128, 1>(p, l.grid, l.stream)
+                  : launch_one<OPT, WK, MK, 128, 0>(p, l.grid, l.stream);
+  }
+}
+
+template <int OPT>
+cudaError_t launch_opt(const WgradTcParams& p, const TcLaunch& l) {
+  if (l.wk == W_F32) {
+    if (l.mk == M_F32) return launch_mk<OPT, W_F32, M_F32>(p, l);
+    if (l.mk == M_BF16) return launch_mk<OPT, W_F32, M_BF16>(p, l);
+    if (l.mk == M_Q8) return launch_mk<OPT, W_F32, M_Q8>(p, l);
+  } else {
+    if (l.mk == M_F32) return launch_mk<OPT, W_BF16, M_F32>(p, l);
+    if (l.mk == M_BF16) return launch_mk<OPT, W_BF16, M_BF16>(p, l);
+    if (l.mk == M_Q8) return launch_mk<OPT, W_BF16, M_Q8>(p, l);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace forge

@@ -1,0 +1,358 @@
+"""Benchmark of the FORGE hot path on one GB300: input gradient + fused
+weight-gradient / optimizer step of one Llama-3.1-8B linear layer.
+
+Default workload (the headline configuration): the MLP up-projection,
+W 14336 x 4096 fp32 master weights with fp32 AdamW moments, BT = 512
+tokens of bf16 activations X and upstream gradients dY. One step =
+forge_dgrad (dX = dY W_old) followed by forge_wgrad_step_adamw (G = dY^T X
+and the AdamW step, fused). The state (1.4 GB) is far larger than L2 and
+L2 is also flushed between timed steps.
+
+Prints one JSON line (see the keys below). ``--impl reference`` times the
+CPU oracle instead (a bounded row sample, extrapolated).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "fused wgrad+AdamW µs/step, GB/s & % roofline at Llama-8B linear shapes"
+UNIT = "us/step"
+
+WORKLOADS = {
+    # name: (D_out, D_in, BT, W storage, moment storage)
+    "llama31_8b_up_proj_bt512_f32state": (14336, 4096, 512, "f32", "f32"),
+    "llama31_8b_up_proj_bt512_bf16state_sr": (14336, 4096, 512, "bf16", "bf16"),
+    "llama31_8b_up_proj_bt2048_bf16state_sr": (14336, 4096, 2048, "bf16", "bf16"),
+    "llama31_8b_up_proj_bt8192_bf16state_sr": (14336, 4096, 8192, "bf16", "bf16"),
+    "llama31_8b_up_proj_bt512_q8state": (14336, 4096, 512, "f32", "q8"),
+}
+DEFAULT = "llama31_8b_up_proj_bt512_f32state"
+HYPER = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01)
+
+
+def state_bytes_per_param(w, st):
+    wb = 4 if w == "f32" else 2
+    mb = {"f32": 4, "bf16": 2, "q8": 1 + 4 / 128}[st]
+    return 2 * wb + 2 * 2 * mb   # W read + write, m and v read + write
+
+
+def algorithmic_bytes(d_out, d_in, bt, w, st):
+    """State read + written once, X and dY read once (no re-reads, no G)."""
+    return int(round(d_out * d_in * state_bytes_per_param(w, st))) + 2 * bt * (d_in + d_out)
+
+
+def dgrad_algorithmic_bytes(d_out, d_in, bt, w):
+    return d_out * d_in * (4 if w == "f32" else 2) + 2 * bt * d_out + 2 * bt * d_in
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d.get("hbm_gbs", 6800.0), d.get("bf16_tflops", 1900.0), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms in the background."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.f = None
+
+    def start(self):
+        try:
+            self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.flush()
+        self.f.seek(0)
+        rows = [r.split(",") for r in self.f.read().strip().splitlines() if r.strip()]
+        os.unlink(self.f.name)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1])); mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- CPU oracle arm
+
+
+def cpu_oracle_step_us(d_out, d_in, bt, w, st, rows):
+    """Time the CPU oracle (dgrad + step) on a row sample of W, extrapolated."""
+    from backward_gemm_optimizer_gb300 import synthetic as S
+    import oracle.forge_oracle as O
+
+    prob = S.linear_problem(rows, d_in, bt, seed=0, x_dtype="bf16", w_dtype=w, state=st)
+    Xn = prob.X.float().numpy(); dYn = prob.dY.float().numpy()
+    def tonp(t):
+        if t is None:
+            return None
+        import torch
+        return t.view(torch.int16).numpy().view(np.uint16) if t.dtype == torch.bfloat16 else t.numpy()
+    state = O.State(W=tonp(prob.W), m=tonp(prob.m), v=tonp(prob.v), m_scale=tonp(prob.m_scale),
+                    v_scale=tonp(prob.v_scale), w_dtype=w, state=st)
+    h = O.Hyper(**HYPER)
+    t0 = time.perf_counter()
+    O.dgrad_f64(dYn, O.load_w(state))            # this row block's share of dX
+    O.step("adamw", Xn, dYn, state, h, 1, seed=1234, sr_w=(w == "bf16"))
+    dt = time.perf_counter() - t0
+    return dt * 1e6 * (d_out / rows), dt
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    d_out, d_in, bt, w, st = WORKLOADS[args.workload]
+    rows = args.cpu_rows
+    vals = []
+    t_start = time.perf_counter()
+    for i in range(args.warmup + args.steps):
+        us, _ = cpu_oracle_step_us(d_out, d_in, bt, w, st, rows)
+        if i >= args.warmup:
+            vals.append(us)
+        if time.perf_counter() - t_start > args.cpu_budget_s:
+            break
+    v = statistics.median(vals) if vals else us
+    cores = os.cpu_count()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(v, 1), "unit": UNIT, "n_gpus": world,
+        "steps": len(vals), "warmup": args.warmup, "ms_per_step": round(v / 1000, 3), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "d_out": d_out, "d_in": d_in, "bt": bt, "w": w, "state": st},
+        "cpu_baseline": {"value": round(v, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"rows 0..{rows} of W ({rows}/{d_out} of the layer), dgrad share + step, "
+                                   f"float64 numpy, extrapolated x{d_out / rows:.2f}"},
+        "e2e": {"value": round(v, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------- GPU arm
+
+
+def make_state(d_out, d_in, bt, w, st, dev, seed=0):
+    import torch
+    from backward_gemm_optimizer_gb300 import synthetic as S
+    prob = S.linear_problem(d_out, d_in, bt, seed=seed, x_dtype="bf16", w_dtype=w, state=st)
+    out = {k: t.to(dev) for k, t in prob.tensors().items()}
+    out["dX"] = torch.empty((bt, d_in), dtype=torch.bfloat16, device=dev)
+    host = {"X": prob.X.pin_memory(), "dY": prob.dY.pin_memory(),
+            "dX": torch.empty((bt, d_in), dtype=torch.bfloat16).pin_memory()}
+    return out, host
+
+
+def one_step(F, s, w, st, t, stream):
+    F.dgrad(s["dY"], s["W"], s["dX"], stream=stream)
+    F.wgrad_step_adamw(s["X"], s["dY"], s["W"], s["m"], s["v"], m_scale=s.get("m_scale"),
+                       v_scale=s.get("v_scale"), step=t, seed=1234, sr_w=(w == "bf16"), stream=stream, **HYPER)
+
+
+def run_gpu(args, rank, world, local_rank):
+    import torch
+    import backward_gemm_optimizer_gb300 as F
+
+    dev = torch.device(f"cuda:{local_rank}")
+    torch.cuda.set_device(dev)
+    d_out, d_in, bt, w, st = WORKLOADS[args.workload]
+    s, host = make_state(d_out, d_in, bt, w, st, dev, seed=rank)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)   # 256 MB > L2
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    t = 1
+    for _ in range(args.warmup):
+        one_step(F, s, w, st, t, stream); t += 1
+    F.sync_status(stream)
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    sampler = ClockSampler(local_rank)
+    barrier()
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    time.sleep(0.3)
+    wall0 = time.perf_counter()
+    for i in range(K):
+        flush.fill_(float(i))                      # evict L2 between steps (not timed)
+        ev[i][0].record(stream)
+        F.dgrad(s["dY"], s["W"], s["dX"], stream=stream)
+        ev[i][1].record(stream)
+        F.wgrad_step_adamw(s["X"], s["dY"], s["W"], s["m"], s["v"], m_scale=s.get("m_scale"),
+                           v_scale=s.get("v_scale"), step=t, seed=1234, sr_w=(w == "bf16"), stream=stream,
+                           **HYPER)
+        ev[i][2].record(stream)
+        t += 1
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - wall0
+    barrier()
+    clocks = sampler.stop()
+    F.sync_status(stream)
+    step_ms = [ev[i][0].elapsed_time(ev[i][2]) for i in range(K)]
+    dgrad_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    fused_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    total_ms = sum(step_ms)
+    if world > 1:
+        tt = torch.tensor([total_ms], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(tt.item())
+
+    # ---- end to end through the public API, host buffers, copies timed
+    KE = max(1, min(args.e2e_steps, K))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for i in range(KE):
+        s["X"].copy_(host["X"], non_blocking=True)
+        s["dY"].copy_(host["dY"], non_blocking=True)
+        one_step(F, s, w, st, t, stream); t += 1
+        host["dX"].copy_(s["dX"], non_blocking=True)
+        F.sync_status(stream)                       # reads the status word back each step
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / KE
+    h2d = host["X"].numel() * 2 + host["dY"].numel() * 2
+    d2h = host["dX"].numel() * 2 + 16
+
+    if rank != 0:
+        return
+    hbm, tflops, peak_src = load_peaks()
+    us = total_ms * 1000.0 / K
+    fused_us = statistics.mean(fused_ms) * 1000.0
+    fused_med = statistics.median(fused_ms) * 1000.0
+    dgrad_us = statistics.mean(dgrad_ms) * 1000.0
+    abytes = algorithmic_bytes(d_out, d_in, bt, w, st)
+    achieved = abytes / (fused_us * 1e-6) / 1e9
+    flops = 2.0 * bt * d_out * d_in
+    t_roof = max(abytes / (hbm * 1e9), flops / (tflops * 1e12)) * 1e6
+    bound = "hbm" if abytes / (hbm * 1e9) >= flops / (tflops * 1e12) else "tensor"
+    traffic = None
+    tr_path = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tr_path):
+        with open(tr_path) as f:
+            traffic = json.load(f).get(args.workload)
+    line = {
+        "metric": METRIC, "value": round(us, 2), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(us / 1000.0, 4), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "d_out": d_out, "d_in": d_in, "bt": bt, "w_storage": w,
+                   "moment_storage": st, "optimizer": "adamw", "step": "forge_dgrad + forge_wgrad_step_adamw",
+                   "l2": "flushed between steps (256 MB write) and state 1.4 GB > L2",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "fused_kernel_us": round(fused_us, 2), "fused_kernel_median_us": round(fused_med, 2),
+        "dgrad_kernel_us": round(dgrad_us, 2),
+        "fused_GBps": round(achieved, 1), "fused_TFLOPs": round(flops / (fused_us * 1e-6) / 1e12, 1),
+        "fused_roofline_us": round(t_roof, 2), "fused_frac_of_roofline": round(t_roof / fused_us, 4),
+        "roofline": {"bound": bound, "achieved": round(achieved, 1) if bound == "hbm" else
+                     round(flops / (fused_us * 1e-6) / 1e12, 1),
+                     "peak": hbm if bound == "hbm" else tflops, "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
+                     "frac": round((achieved / hbm) if bound == "hbm" else
+                                   (flops / (fused_us * 1e-6) / 1e12) / tflops, 4),
+                     "traffic": traffic, "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_src == "measured" else peak_src,
+                     "algorithmic_bytes": abytes, "kernel": "wgrad_step_tc_kernel"},
+        "e2e": {"value": round(e2e_ms * 1000.0, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": 2 * K,
+        "clocks": clocks,
+        "wall_s_timed": round(wall, 3),
+    }
+    if not args.no_cpu_baseline:
+        try:
+            rows = min(args.cpu_rows, d_out)
+            vals, spent = [], 0.0
+            while spent < args.cpu_min_s or not vals:     # repeat to ~10 s of CPU work
+                v, dt = cpu_oracle_step_us(d_out, d_in, bt, w, st, rows)
+                vals.append(v); spent += dt
+            line["cpu_baseline"] = {"value": round(statistics.median(vals), 1), "unit": UNIT,
+                                    "cores": os.cpu_count(), "kind": "oracle",
+                                    "sample": f"rows 0..{rows} of W (x{d_out / rows:.2f} to the layer), dgrad share "
+                                              f"+ AdamW step, float64 numpy, median of {len(vals)} runs, "
+                                              f"{spent:.1f} s of CPU work"}
+        except Exception as e:  # report, do not fail the GPU line
+            line["cpu_baseline"] = {"value": None, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                                    "sample": f"failed: {e}"}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="forge", choices=["forge", "reference"])
+    ap.add_argument("--workload", default=DEFAULT, choices=sorted(WORKLOADS))
+    ap.add_argument("--e2e-steps", type=int, default=100)
+    ap.add_argument("--cpu-rows", type=int, default=14336)
+    ap.add_argument("--cpu-min-s", type=float, default=10.0)
+    ap.add_argument("--cpu-budget-s", type=float, default=120.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    try:
+        run_gpu(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,212 @@
+/*
+ * forge.h -- C ABI of the fused weight-gradient + optimizer-step library
+ * for one NVIDIA GB300 GPU (sm_103a).
+ *
+ * What it computes (FORGE, "Fused On-Register Gradient Elimination for
+ * Memory-Efficient LLM Training", arXiv 2606.22932):
+ *
+ *   For a linear layer Y = X W^T (section 2.1, Eq. 2) with
+ *     X  : BT x D_in   (saved input),
+ *     dY : BT x D_out  (upstream gradient),
+ *     W  : D_out x D_in,
+ *   the weight gradient G = dY^T X (Eq. 3) is formed one 128-row tile at a
+ *   time, accumulated over the token axis in fp32 (Eq. 5, Algorithm 1
+ *   phase 1), and each accumulator tile is consumed at once by an
+ *   element-wise optimizer step (Algorithm 1 phase 2). Only the updated
+ *   weight and moment tiles are written (Algorithm 1 phase 3); G is never
+ *   stored and no gradient-sized buffer is ever allocated (Proposition 3).
+ *   Proposition 1 (Appendix A) makes the result equal to "materialise G,
+ *   then step" up to the summation order of G (Corollary 1).
+ *
+ * Conventions shared by every entry point
+ *   - All tensors are row-major 2-D views described by forge_tensor.
+ *     "ld" is the distance in elements between consecutive rows
+ *     (ld >= cols). The caller allocates and owns every buffer; the
+ *     library never allocates device memory on these calls.
+ *   - Device tensors: base address 16-byte aligned and ld * element size
+ *     a multiple of 16 bytes (the tensor-memory-accelerator rule); the
+ *     column counts D_in and D_out must be multiples of 8. BT may be any
+ *     value >= 0 (BT = 0 is a step with a zero gradient).
+ *   - Every call is enqueued on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream) and returns without synchronising. Argument
+ *     and launch errors are returned as a forge_status; the message is
+ *     available from forge_last_error() on the calling thread. No C++
+ *     exception crosses this interface.
+ *   - Device-side failures (a bounded wait inside a kernel that gave up)
+ *     are recorded in a per-device status word and reported by
+ *     forge_sync_status(). Kernels never trap and never wait unboundedly.
+ *   - There is no CPU fallback: a variant without a GPU kernel returns
+ *     FORGE_ERR_UNSUPPORTED.
+ */
+#ifndef FORGE_H_
+#define FORGE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Compatible with cudaStream_t (a pointer to the runtime's opaque stream). */
+struct CUstream_st;
+typedef struct CUstream_st* forge_stream_t;
+
+typedef enum {
+  FORGE_OK = 0,
+  FORGE_ERR_INVALID_ARG = 1, /* null pointer, bad shape, bad step, bad hyper-parameter */
+  FORGE_ERR_UNSUPPORTED = 2, /* a dtype / option combination with no kernel */
+  FORGE_ERR_ALIGNMENT = 3,   /* base address or row pitch breaks the 16-byte rule */
+  FORGE_ERR_CUDA = 4,        /* a CUDA runtime or driver call failed */
+  FORGE_ERR_TIMEOUT = 5      /* a kernel's bounded wait gave up (forge_sync_status) */
+} forge_status;
+
+typedef enum {
+  FORGE_F32 = 0,
+  FORGE_BF16 = 1,
+  /* 8-bit block-quantised moment (section 2.3; Appendix B), one fp32 scale
+   * s per 128 consecutive elements of a row (D_in must be a multiple of
+   * 128). First moment: int8 codes, m = code * s, s = absmax(m) / 127.
+   * Second moment: uint8 codes of sqrt(v), v = (code * s)^2,
+   * s = absmax(sqrt(v)) / 255. Code 0 is reserved for an exactly zero
+   * moment. `scale` points to fp32 scales laid out [D_in/128][D_out]
+   * (contiguous; block column major), so one 128-row tile reads 512
+   * contiguous bytes. */
+  FORGE_I8B128 = 2
+} forge_dtype;
+
+typedef struct {
+  void* data;        /* device pointer to element (0, 0) */
+  int32_t dtype;     /* forge_dtype */
+  int64_t rows;
+  int64_t cols;
+  int64_t ld;        /* elements between rows (codes for FORGE_I8B128) */
+  void* scale;       /* FORGE_I8B128 only: fp32 scales [cols/128][rows]; else NULL */
+} forge_tensor;
+
+/* Flags (forge_hyper.flags). */
+#define FORGE_FLAG_TILE_N_AUTO 0u   /* tile width chosen by the scheduler policy */
+#define FORGE_FLAG_TILE_N_128 1u    /* force 128 x 128 gradient tiles */
+#define FORGE_FLAG_TILE_N_64 2u     /* force 128 x 64 gradient tiles */
+#define FORGE_FLAG_TILE_N_MASK 7u
+/* Test hook for the device-side failure path: the epilogue waits on a
+ * barrier that nothing signals, with a ~1 ms bound, gives up, and the
+ * step returns without touching W or its moments; forge_sync_status() then
+ * reports FORGE_ERR_TIMEOUT. */
+#define FORGE_FLAG_TEST_FORCE_TIMEOUT 0x100u
+
+typedef struct {
+  double lr;            /* eta */
+  double beta1;         /* AdamW / Lion beta1; SGD-momentum: momentum mu */
+  double beta2;         /* AdamW beta2; Lion: decay of the stored moment */
+  double eps;           /* AdamW epsilon (added outside the square root) */
+  double weight_decay;  /* lambda: decoupled for AdamW and Lion, L2 for SGD-momentum */
+  int32_t sr_w;         /* bf16 W only: 1 = stochastic rounding, 0 = round-to-nearest-even */
+  int32_t sr_moments;   /* bf16 moments only: 1 = stochastic rounding, 0 = RNE */
+  uint32_t flags;       /* FORGE_FLAG_* */
+} forge_hyper;
+
+/*
+ * forge_wgrad_step_adamw -- fused G = dY^T X and AdamW step, in place.
+ *
+ * Computes, per element (p, q), with t = step (Algorithm 1, lines 11-14):
+ *   m' = b1 m + (1 - b1) g
+ *   v' = b2 v + (1 - b2) g^2
+ *   W' = (1 - lr wd) W - lr (m' / (1 - b1^t)) / (sqrt(v' / (1 - b2^t)) + eps)
+ * where g = G[p][q]. The arithmetic is fp32: the scalars 1 - b1, 1 - b2,
+ * 1 - lr wd, lr / (1 - b1^t) and 1 / sqrt(1 - b2^t) are folded in double on
+ * the host and rounded to float once; each element then evaluates
+ *   m' = b1*m + (1-b1)*g;  v' = b2*v + (1-b2)*(g*g);
+ *   d = sqrt(v')*(1/sqrt(1-b2^t)) + eps;  W' = (1-lr wd)*W - (lr/(1-b1^t))*(m'/d)
+ * with every operation correctly rounded and no fused multiply-add.
+ * The new moments used by the update are the unrounded fp32 values;
+ * storage rounding applies to what is written.
+ *
+ * X, dY: both FORGE_BF16 (tensor-core path) or both FORGE_F32 (an fp32
+ *   path for small problems). X is BT x D_in, dY is BT x D_out.
+ * W: FORGE_F32 (master weights) or FORGE_BF16, D_out x D_in, updated in place.
+ *   bf16 W is written with stochastic rounding when h->sr_w (Appendix C,
+ *   Proposition 5): the 16-bit draw of element idx = p * D_in + q is half
+ *   (idx % 2) of word (idx % 8) / 2 of Philox4x32-10 with key
+ *   (seed lo, seed hi) and counter (idx / 8 lo, idx / 8 hi, step, site),
+ *   site 0 for W, 1 for m, 2 for v.
+ * m, v: both FORGE_F32, both FORGE_BF16 or both FORGE_I8B128, D_out x D_in,
+ *   updated in place (scales too).
+ * step: t >= 1 (FORGE_ERR_INVALID_ARG otherwise).
+ * Precondition (Remark 1): W is overwritten, so the input gradient
+ *   dX = dY W must already have been enqueued (forge_dgrad) on the same
+ *   stream, and W must have no other gradient consumer in this step.
+ * W, m and v must not overlap X, dY or each other.
+ */
+forge_status forge_wgrad_step_adamw(const forge_tensor* X, const forge_tensor* dY,
+                                    forge_tensor* W, forge_tensor* m, forge_tensor* v,
+                                    const forge_hyper* h, int64_t step, uint64_t seed,
+                                    forge_stream_t stream);
+
+/*
+ * forge_wgrad_step_sgdm -- fused G = dY^T X and SGD with momentum, in place.
+ *
+ * The paper lists SGD-momentum among the fully fused element-wise rules
+ * (Appendix N (i), item 8: "single moment") without printing it; this
+ * library implements the common rule with coupled L2 decay, no dampening
+ * and no Nesterov term, mu = h->beta1:
+ *   g~ = g + wd*W;  m' = mu*m + g~;  W' = W - lr*m'     (fp32, no FMA).
+ * Arguments as for forge_wgrad_step_adamw without v (m: F32, BF16 or
+ * I8B128 with the first-moment code rule). h->beta2 and h->eps are unused.
+ */
+forge_status forge_wgrad_step_sgdm(const forge_tensor* X, const forge_tensor* dY,
+                                   forge_tensor* W, forge_tensor* m,
+                                   const forge_hyper* h, int64_t step, uint64_t seed,
+                                   forge_stream_t stream);
+
+/*
+ * forge_wgrad_step_lion -- fused G = dY^T X and Lion, in place.
+ *
+ * Appendix N (i), item 4 ("sign-of-momentum update with a single moment
+ * buffer"), following Chen et al. 2023, sign(0) = 0:
+ *   c = b1*m + (1-b1)*g;  W' = (1-lr wd)*W - lr*sign(c);  m' = b2*m + (1-b2)*g.
+ * Arguments as for forge_wgrad_step_sgdm; h->eps is unused.
+ */
+forge_status forge_wgrad_step_lion(const forge_tensor* X, const forge_tensor* dY,
+                                   forge_tensor* W, forge_tensor* m,
+                                   const forge_hyper* h, int64_t step, uint64_t seed,
+                                   forge_stream_t stream);
+
+/*
+ * forge_dgrad -- input gradient dX = dY W_old (Remark 1, Appendix A).
+ *
+ * Must be enqueued before the step that overwrites W, on the same stream,
+ * so that it reads the pre-update weights. dY: FORGE_BF16, BT x D_out.
+ * W_old: FORGE_BF16 or FORGE_F32 (fp32 master weights are rounded to bf16
+ * as they are staged for the tensor cores), D_out x D_in. dX: FORGE_BF16
+ * or FORGE_F32, BT x D_in (fp32 accumulation, one rounding at the store).
+ */
+forge_status forge_dgrad(const forge_tensor* dY, const forge_tensor* W_old, forge_tensor* dX,
+                         forge_stream_t stream);
+
+/*
+ * forge_sync_status -- synchronise `stream`, then read and clear the
+ * device status word of the current device. Returns FORGE_ERR_TIMEOUT if
+ * a kernel's bounded wait gave up since the last call (the message names
+ * the wait), FORGE_ERR_CUDA if synchronisation failed, else FORGE_OK.
+ */
+forge_status forge_sync_status(forge_stream_t stream);
+
+/* Message of the last failed call on this thread ("" if none). */
+const char* forge_last_error(void);
+
+/* Library version, e.g. "0.1.0". */
+const char* forge_version(void);
+
+/*
+ * forge_workspace_bytes -- device scratch the steps need beyond their
+ * arguments. It is 0: the persistent scheduler keeps its state on chip,
+ * and the gradient never leaves the tensor-memory accumulators.
+ */
+size_t forge_workspace_bytes(int64_t d_out, int64_t d_in, int64_t bt);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FORGE_H_ */

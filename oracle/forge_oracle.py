@@ -136,7 +136,8 @@ def lion_f64(W, m, G, h: Hyper, t: int):
     assert t >= 1
     W = np.asarray(W, np.float64); m = np.asarray(m, np.float64); G = np.asarray(G, np.float64)
     c = h.beta1 * m + (1.0 - h.beta1) * G
-    W1 = (1.0 - h.lr * h.weight_decay) * W - h.lr * np.sign(c)
+    sg = np.where(c > 0, 1.0, np.where(c < 0, -1.0, 0.0))
+    W1 = (1.0 - h.lr * h.weight_decay) * W - h.lr * sg
     m1 = h.beta2 * m + (1.0 - h.beta2) * G
     return W1, m1
 
@@ -207,7 +208,8 @@ def lion_f32(W, m, G, s: dict):
     m' = b2*m + omb2*g."""
     W, m, G = _f32(W), _f32(m), _f32(G)
     c = s["b1"] * m + s["omb1"] * G
-    sg = np.sign(c).astype(np.float32)
+    # sign with sign(+-0) = +0
+    sg = np.where(c > 0, F32(1.0), np.where(c < 0, F32(-1.0), F32(0.0))).astype(np.float32)
     W1 = s["decay"] * W - s["lr"] * sg
     m1 = s["b2"] * m + s["omb2"] * G
     return W1, m1

@@ -1,0 +1,153 @@
+"""Helpers shared by the GPU parity tests: run the CUDA path through the C
+ABI on seeded inputs, run the CPU oracle on the same inputs, compare."""
+
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import backward_gemm_optimizer_gb300 as F
+from backward_gemm_optimizer_gb300 import synthetic as S
+import oracle.forge_oracle as O
+import oracle.tolerance as T
+
+HYPER = {
+    "adamw": dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01),
+    "sgdm": dict(lr=2e-5, beta1=0.9, beta2=0.0, eps=0.0, weight_decay=1e-2),
+    "lion": dict(lr=3e-6, beta1=0.9, beta2=0.99, eps=0.0, weight_decay=1.0),
+}
+
+# (W storage, moment storage) combinations with a kernel.
+VARIANTS = [("f32", "f32"), ("f32", "bf16"), ("bf16", "bf16"), ("f32", "q8"), ("bf16", "q8"), ("bf16", "f32")]
+
+
+def to_np(t: torch.Tensor) -> np.ndarray:
+    t = t.detach().cpu()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16).copy()
+    return t.numpy().copy()
+
+
+def oracle_state(prob: S.LinearProblem, w_dtype: str, state: str) -> O.State:
+    return O.State(W=to_np(prob.W), m=to_np(prob.m), v=to_np(prob.v) if prob.v is not None else None,
+                   m_scale=to_np(prob.m_scale) if prob.m_scale is not None else None,
+                   v_scale=to_np(prob.v_scale) if prob.v_scale is not None else None,
+                   w_dtype=w_dtype, state=state)
+
+
+def gpu_step(opt: str, prob: S.LinearProblem, t: int, *, seed: int = 0, sr_w=False, sr_moments=False,
+             flags=0, dev="cuda:0", hyper=None):
+    """Copy the problem to the GPU, run one fused step, return the new state (CPU numpy)."""
+    hp = dict(HYPER[opt] if hyper is None else hyper)
+    X, dY, W = prob.X.to(dev), prob.dY.to(dev), prob.W.to(dev)
+    m = prob.m.to(dev)
+    ms = prob.m_scale.to(dev) if prob.m_scale is not None else None
+    common = dict(step=t, seed=seed, sr_w=sr_w, sr_moments=sr_moments, flags=flags)
+    if opt == "adamw":
+        v = prob.v.to(dev)
+        vs = prob.v_scale.to(dev) if prob.v_scale is not None else None
+        F.wgrad_step_adamw(X, dY, W, m, v, m_scale=ms, v_scale=vs, **hp, **common)
+    elif opt == "sgdm":
+        v = vs = None
+        F.wgrad_step_sgdm(X, dY, W, m, lr=hp["lr"], momentum=hp["beta1"], weight_decay=hp["weight_decay"],
+                          m_scale=ms, **common)
+    else:
+        v = vs = None
+        F.wgrad_step_lion(X, dY, W, m, lr=hp["lr"], beta1=hp["beta1"], beta2=hp["beta2"],
+                          weight_decay=hp["weight_decay"], m_scale=ms, **common)
+    F.sync_status()
+    return O.State(W=to_np(W), m=to_np(m), v=to_np(v) if v is not None else None,
+                   m_scale=to_np(ms) if ms is not None else None, v_scale=to_np(vs) if vs is not None else None)
+
+
+def oracle_step(opt, prob, w_dtype, state, t, *, seed=0, sr_w=False, sr_moments=False, mode="f64", hyper=None):
+    hp = dict(HYPER[opt] if hyper is None else hyper)
+    st = oracle_state(prob, w_dtype, state)
+    Xn = prob.X.float().numpy()
+    dYn = prob.dY.float().numpy()
+    return O.step(opt, Xn, dYn, st, O.Hyper(**hp), t, seed=seed, sr_w=sr_w, sr_moments=sr_moments, mode=mode)
+
+
+def assert_bit_exact(got: O.State, ref: O.State, opt: str):
+    def eq(a, b, name):
+        a = np.asarray(a); b = np.asarray(b)
+        assert a.shape == b.shape, (name, a.shape, b.shape)
+        if a.dtype == np.float32:
+            a = a.view(np.uint32); b = np.asarray(b, np.float32).view(np.uint32)
+        nbad = int(np.sum(a != b))
+        assert nbad == 0, f"{name}: {nbad} of {a.size} elements differ; first at {np.argwhere(a != b)[:3].tolist()}"
+    eq(got.W, ref.W, "W")
+    eq(got.m, ref.m, "m")
+    if ref.m_scale is not None:
+        eq(got.m_scale, ref.m_scale, "m_scale")
+    if opt == "adamw":
+        eq(got.v, ref.v, "v")
+        if ref.v_scale is not None:
+            eq(got.v_scale, ref.v_scale, "v_scale")
+
+
+def _vals(x, kind):
+    if kind == "bf16":
+        return O.bf16_bits_to_f32(x).astype(np.float64)
+    return np.asarray(x, np.float64)
+
+
+def check_tolerance(opt, prob, w_dtype, state, t, got: O.State, *, seed=0, sr_w=False, sr_moments=False,
+                    hyper=None, rtol=1e-5):
+    """Compare a random-input GPU step with the float64 oracle; returns a report dict."""
+    hp = dict(HYPER[opt] if hyper is None else hyper)
+    h = O.Hyper(**hp)
+    st = oracle_state(prob, w_dtype, state)
+    Xn = prob.X.float().numpy(); dYn = prob.dY.float().numpy()
+    G = O.wgrad_f64(dYn, Xn)
+    A = O.abs_wgrad_f64(dYn, Xn)
+    ref = O.step(opt, None, None, st, h, t, seed=seed, sr_w=sr_w, sr_moments=sr_moments, G=G)
+    W0, m0 = O.load_w(st), O.load_m(st)
+    if opt == "adamw":
+        tw, tm, tv = T.adamw_tol(W0, m0, O.load_v(st), G, A, h, t, rtol)
+    elif opt == "sgdm":
+        (tw, tm), tv = T.sgdm_tol(W0, m0, G, A, h, t, rtol), None
+    else:
+        (tw, tm), tv = T.lion_tol(W0, m0, G, A, h, t, rtol), None
+    rep = {}
+
+    def cmp(name, g, r, tol, kind):
+        if kind == "f32":
+            rep[name] = T.rel_violation(g, r, tol)
+            assert rep[name] <= 1.0, f"{name}: {rep[name]:.3f} of the tolerance"
+        elif kind == "bf16":
+            # The stored bf16 value is the fp32 result rounded once: within the
+            # fp32 tolerance plus one bf16 ulp (where there is no cancellation
+            # the tolerance is far below an ulp, so that is "within 1 ulp").
+            gv = O.bf16_bits_to_f32(g).astype(np.float64)
+            rv = O.bf16_bits_to_f32(r).astype(np.float64)
+            ulp = np.maximum(T.bf16_ulp(g), T.bf16_ulp(r))
+            rep[name] = T.rel_violation(gv, rv, tol + ulp)
+            d = T.bf16_ulp_distance(g, r)
+            rep[name + "_max_ulp"] = int(d.max()) if d.size else 0
+            rep[name + "_mismatch"] = float(np.mean(d != 0)) if d.size else 0.0
+            rep[name + "_beyond_1ulp"] = float(np.mean(d > 1)) if d.size else 0.0
+            assert rep[name] <= 1.0, f"{name}: {rep[name]:.3f} of (tolerance + 1 ulp)"
+            assert rep[name + "_beyond_1ulp"] <= 1e-3, rep
+            assert rep[name + "_mismatch"] <= 1e-2, rep
+
+    cmp("W", got.W, ref.W, tw, w_dtype)
+    if state in ("f32", "bf16"):
+        cmp("m", got.m, ref.m, tm, state)
+        if opt == "adamw":
+            cmp("v", got.v, ref.v, tv, state)
+    else:
+        # 8-bit: codes within one step of the oracle's, rare differences.
+        dm = np.abs(got.m.astype(np.int32) - ref.m.astype(np.int32))
+        rep["m_code_max"] = int(dm.max()); rep["m_code_mismatch"] = float(np.mean(dm != 0))
+        assert rep["m_code_max"] <= 1 and rep["m_code_mismatch"] <= 1e-2, rep
+        np.testing.assert_allclose(got.m_scale, ref.m_scale, rtol=1e-4, atol=1e-30)
+        if opt == "adamw":
+            dv = np.abs(got.v.astype(np.int32) - ref.v.astype(np.int32))
+            rep["v_code_max"] = int(dv.max()); rep["v_code_mismatch"] = float(np.mean(dv != 0))
+            assert rep["v_code_max"] <= 1 and rep["v_code_mismatch"] <= 1e-2, rep
+            np.testing.assert_allclose(got.v_scale, ref.v_scale, rtol=1e-4, atol=1e-30)
+            # the reserved zero code: exactly the zero moments
+            assert np.array_equal(got.v == 0, ref.v == 0)
+        assert np.array_equal(got.m == 0, ref.m == 0)
+    return rep

@@ -1,0 +1,308 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Exact-gradient cases (integer-valued inputs, so G is exact in fp32 in any
+summation order) must match the oracle's float32 op-sequence mode bit for
+bit in every variant, including stochastic-rounding decisions and 8-bit
+codes. Random-input cases are held to the element-wise tolerance of
+oracle/tolerance.py (a 1e-5 relative perturbation of the step's inputs,
+the gradient's scaled by |dY|^T |X|) for fp32 outputs, one bf16 ulp for
+bf16 outputs, and one code for 8-bit codes.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import backward_gemm_optimizer_gb300 as F
+from backward_gemm_optimizer_gb300 import synthetic as S
+import oracle.forge_oracle as O
+
+from forge_cases import HYPER, VARIANTS, assert_bit_exact, check_tolerance, gpu_step, oracle_step, to_np
+
+pytestmark = pytest.mark.gpu
+
+OPTS = ["adamw", "sgdm", "lion"]
+# (D_out, D_in, BT): several tiles and a ragged token tail; ragged D; one tile.
+SHAPES = [(256, 384, 200), (136, 200, 70), (128, 128, 64)]
+
+
+def _prob(shape, seed, x_dtype, w, st, exact, fresh=False, zero_rows=0.0):
+    d_out, d_in, bt = shape
+    return S.linear_problem(d_out, d_in, bt, seed=seed, x_dtype=x_dtype, w_dtype=w, state=st, exact=exact,
+                            fresh_moments=fresh, zero_row_fraction=zero_rows)
+
+
+def _ok_shape(shape, st):
+    return st != "q8" or shape[1] % 128 == 0
+
+
+# ---------------------------------------------------------------------------
+# Bit-exact against the float32 op-sequence oracle (exact gradients)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("opt", OPTS)
+@pytest.mark.parametrize("variant", VARIANTS, ids=lambda v: f"W{v[0]}-m{v[1]}")
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_exact_gradient_bit_exact(opt, variant, shape):
+    w, st = variant
+    if not _ok_shape(shape, st):
+        pytest.skip("8-bit blocks need D_in % 128 == 0")
+    sr = w == "bf16"
+    srm = st == "bf16"
+    prob = _prob(shape, 11, "bf16", w, st, exact=True)
+    for t in (1, 7):
+        got = gpu_step(opt, prob, t, seed=1234, sr_w=sr, sr_moments=srm)
+        ref = oracle_step(opt, prob, w, st, t, seed=1234, sr_w=sr, sr_moments=srm, mode="f32emu")
+        assert_bit_exact(got, ref, opt)
+
+
+@pytest.mark.parametrize("opt", OPTS)
+@pytest.mark.parametrize("variant", [("bf16", "bf16"), ("f32", "q8")], ids=lambda v: f"W{v[0]}-m{v[1]}")
+def test_exact_gradient_rne_stores(opt, variant):
+    # Round-to-nearest-even stores of bf16 W / moments (no stochastic rounding).
+    w, st = variant
+    prob = _prob((256, 384, 130), 5, "bf16", w, st, exact=True)
+    got = gpu_step(opt, prob, 3, seed=9)
+    ref = oracle_step(opt, prob, w, st, 3, seed=9, mode="f32emu")
+    assert_bit_exact(got, ref, opt)
+
+
+# ---------------------------------------------------------------------------
+# Random inputs against the float64 oracle within the stated tolerance
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("opt", OPTS)
+@pytest.mark.parametrize("variant", VARIANTS, ids=lambda v: f"W{v[0]}-m{v[1]}")
+@pytest.mark.parametrize("shape", SHAPES[:2], ids=lambda s: "x".join(map(str, s)))
+def test_random_inputs_within_tolerance(opt, variant, shape):
+    w, st = variant
+    if not _ok_shape(shape, st):
+        pytest.skip("8-bit blocks need D_in % 128 == 0")
+    sr = w == "bf16"
+    prob = _prob(shape, 21, "bf16", w, st, exact=False)
+    got = gpu_step(opt, prob, 2, seed=77, sr_w=sr)
+    rep = check_tolerance(opt, prob, w, st, 2, got, seed=77, sr_w=sr)
+    print(opt, w, st, shape, rep)
+
+
+def test_adamw_tolerance_at_paper_verification_shape():
+    # D_in = D_out = 512, BT = 256 (the paper's per-family numerical check, Appendix N).
+    prob = _prob((512, 512, 256), 31, "bf16", "f32", "f32", exact=False)
+    got = gpu_step("adamw", prob, 1)
+    rep = check_tolerance("adamw", prob, "f32", "f32", 1, got)
+    assert rep["W"] <= 1.0 and rep["m"] <= 1.0 and rep["v"] <= 1.0
+
+
+# ---------------------------------------------------------------------------
+# fp32 inputs (CUDA-core path): the 3-step fp32 AdamW problem
+# ---------------------------------------------------------------------------
+
+def test_fp32_three_steps_fresh_inputs():
+    # W 256x256 ~N(0, 0.02), X and dY 128 x 256 ~N(0, 1) drawn fresh each step,
+    # m = v = 0, AdamW lr 1e-3, betas (0.9, 0.999), eps 1e-8, wd 0.01, seed 0.
+    d_out = d_in = 256
+    bt = 128
+    dev = "cuda:0"
+    W0 = S.normal((d_out, d_in), 0.02, 0, S.STREAM_W, "f32")
+    W = W0.clone().to(dev)
+    m = torch.zeros_like(W); v = torch.zeros_like(W)
+    st = O.State(W=W0.numpy().copy(), m=np.zeros((d_out, d_in), np.float32), v=np.zeros((d_out, d_in), np.float32))
+    h = O.Hyper(**HYPER["adamw"])
+    worst = 0.0
+    from oracle import tolerance as T
+    for t in (1, 2, 3):
+        X, dY = S.step_inputs(d_out, d_in, bt, 0, t, "f32")
+        F.wgrad_step_adamw(X.to(dev), dY.to(dev), W, m, v, step=t, **HYPER["adamw"])
+        F.sync_status()
+        Xn, dYn = X.numpy(), dY.numpy()
+        G = O.wgrad_f64(dYn, Xn); A = O.abs_wgrad_f64(dYn, Xn)
+        tw, tm, tv = T.adamw_tol(st.W, st.m, st.v, G, A, h, t)
+        ref = O.step("adamw", Xn, dYn, st, h, t)
+        for name, g, r, tol in (("W", W, ref.W, tw), ("m", m, ref.m, tm), ("v", v, ref.v, tv)):
+            viol = T.rel_violation(to_np(g), r, tol)
+            worst = max(worst, viol)
+            assert viol <= 1.0, (t, name, viol)
+        # continue the trajectory from the GPU's own state (the oracle is
+        # held to one step at a time)
+        st = O.State(W=to_np(W), m=to_np(m), v=to_np(v))
+    print("fp32 3-step worst tolerance use", worst)
+
+
+@pytest.mark.parametrize("opt", OPTS)
+@pytest.mark.parametrize("variant", VARIANTS, ids=lambda v: f"W{v[0]}-m{v[1]}")
+def test_fp32_inputs_exact_bit_exact(opt, variant):
+    w, st = variant
+    prob = _prob((64, 256, 40), 4, "f32", w, st, exact=True)
+    got = gpu_step(opt, prob, 2, seed=5, sr_w=w == "bf16", sr_moments=st == "bf16")
+    ref = oracle_step(opt, prob, w, st, 2, seed=5, sr_w=w == "bf16", sr_moments=st == "bf16", mode="f32emu")
+    assert_bit_exact(got, ref, opt)
+
+
+# ---------------------------------------------------------------------------
+# Edge cases
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("opt", OPTS)
+@pytest.mark.parametrize("x_dtype", ["bf16", "f32"])
+def test_empty_token_axis_is_a_zero_gradient_step(opt, x_dtype):
+    prob = _prob((136, 256, 0), 2, x_dtype, "f32", "f32", exact=True)
+    got = gpu_step(opt, prob, 4)
+    ref = oracle_step(opt, prob, "f32", "f32", 4, mode="f32emu")
+    assert_bit_exact(got, ref, opt)
+
+
+@pytest.mark.parametrize("shape", [(8, 8, 1), (8, 128, 3), (264, 8, 65), (1000, 1024, 1)])
+def test_degenerate_and_minimum_shapes(shape):
+    prob = _prob(shape, 8, "bf16", "f32", "f32", exact=True)
+    got = gpu_step("adamw", prob, 1)
+    ref = oracle_step("adamw", prob, "f32", "f32", 1, mode="f32emu")
+    assert_bit_exact(got, ref, "adamw")
+
+
+def test_q8_zero_gradient_rows_keep_reserved_zero_codes():
+    # 30% of W rows get an exactly zero gradient and start from zero moments.
+    prob = _prob((512, 512, 256), 3, "bf16", "f32", "q8", exact=False, zero_rows=0.3)
+    got = gpu_step("adamw", prob, 1)
+    zr = prob.zero_rows
+    assert np.all(got.m[zr] == 0) and np.all(got.v[zr] == 0)
+    assert np.all(got.m_scale[:, zr] == 0) and np.all(got.v_scale[:, zr] == 0)
+    decay = np.float32(1.0 - HYPER["adamw"]["lr"] * HYPER["adamw"]["weight_decay"])
+    assert np.array_equal(got.W[zr], (decay * to_np(prob.W)[zr]).astype(np.float32))
+    assert np.all(got.v[~zr] != 0)       # nonzero second moments never take code 0
+    check_tolerance("adamw", prob, "f32", "q8", 1, got)
+
+
+def test_sr_weight_store_is_unbiased_on_gpu():
+    # The quarter-ulp example: lr chosen so every update is ~1/4 bf16 ulp.
+    d_out, d_in = 256, 512
+    dev = "cuda:0"
+    X = torch.zeros((1, d_in), dtype=torch.bfloat16, device=dev)
+    dY = torch.zeros((1, d_out), dtype=torch.bfloat16, device=dev)
+    W = torch.full((d_out, d_in), 0.75, dtype=torch.bfloat16, device=dev)
+    m = torch.full((d_out, d_in), 1.0, dtype=torch.float32, device=dev)   # SGDM with mu = 1, g = 0
+    W_rne = W.clone(); m_rne = m.clone()
+    for t in range(1, 101):
+        F.wgrad_step_sgdm(X, dY, W, m, lr=1e-3, momentum=1.0, weight_decay=0.0, step=t, seed=1234, sr_w=True)
+        F.wgrad_step_sgdm(X, dY, W_rne, m_rne, lr=1e-3, momentum=1.0, weight_decay=0.0, step=t)
+    F.sync_status()
+    assert torch.all(W_rne == 0.75)
+    mean_change = float(W.float().mean() - 0.75)
+    se = 10 * 2 ** -8 / 2 / np.sqrt(d_out * d_in)
+    assert abs(mean_change - (-0.1)) < 5 * se, mean_change
+
+
+# ---------------------------------------------------------------------------
+# Invariances
+# ---------------------------------------------------------------------------
+
+def test_run_to_run_determinism():
+    prob = _prob((512, 1024, 512), 9, "bf16", "bf16", "bf16", exact=False)
+    a = gpu_step("adamw", prob, 3, seed=1, sr_w=True)
+    b = gpu_step("adamw", prob, 3, seed=1, sr_w=True)
+    assert_bit_exact(a, b, "adamw")
+
+
+def test_row_shard_invariance():
+    # A row block of W stepped on its own (the tensor-parallel shard of
+    # Proposition 2 (i)) equals the same rows of the full step, bit for bit.
+    dev = "cuda:0"
+    prob = _prob((512, 384, 300), 12, "bf16", "f32", "f32", exact=False)
+    full = gpu_step("adamw", prob, 2)
+    X, dY = prob.X.to(dev), prob.dY.to(dev)
+    W, m, v = prob.W.to(dev), prob.m.to(dev), prob.v.to(dev)
+    for r0, r1 in ((0, 128), (128, 384), (384, 512)):
+        F.wgrad_step_adamw(X, dY[:, r0:r1], W[r0:r1], m[r0:r1], v[r0:r1], step=2, **HYPER["adamw"])
+    F.sync_status()
+    assert np.array_equal(to_np(W).view(np.uint32), full.W.view(np.uint32))
+    assert np.array_equal(to_np(m).view(np.uint32), full.m.view(np.uint32))
+    assert np.array_equal(to_np(v).view(np.uint32), full.v.view(np.uint32))
+
+
+@pytest.mark.parametrize("exact", [True, False])
+def test_tile_width_invariance(exact):
+    prob = _prob((256, 512, 192), 13, "bf16", "f32", "f32", exact=exact)
+    a = gpu_step("adamw", prob, 1, flags=F.FLAG_TILE_N_128)
+    b = gpu_step("adamw", prob, 1, flags=F.FLAG_TILE_N_64)
+    assert_bit_exact(a, b, "adamw")
+
+
+def test_checkpoint_resume_bit_identical():
+    # 3 steps == 2 steps, copy the state out and back (a checkpoint), 1 step.
+    dev = "cuda:0"
+    prob = _prob((256, 384, 128), 14, "bf16", "bf16", "q8", exact=False)
+    def run(n, state=None):
+        W = prob.W.to(dev).clone(); m = prob.m.to(dev).clone(); v = prob.v.to(dev).clone()
+        ms = prob.m_scale.to(dev).clone(); vs = prob.v_scale.to(dev).clone()
+        if state is not None:
+            for dst, src in zip((W, m, v, ms, vs), state):
+                dst.copy_(src.to(dev))
+        for t in n:
+            F.wgrad_step_adamw(prob.X.to(dev), prob.dY.to(dev), W, m, v, m_scale=ms, v_scale=vs, step=t,
+                               seed=42, sr_w=True, **HYPER["adamw"])
+        F.sync_status()
+        return [x.cpu() for x in (W, m, v, ms, vs)]
+    a = run([1, 2, 3])
+    ck = run([1, 2])
+    b = run([3], state=ck)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+
+
+# ---------------------------------------------------------------------------
+# Failure path: a bounded device wait that gives up (no fault, no hang)
+# ---------------------------------------------------------------------------
+
+def test_forced_device_timeout_reports_and_leaves_state():
+    dev = "cuda:0"
+    prob = _prob((256, 256, 64), 15, "bf16", "f32", "f32", exact=False)
+    X, dY = prob.X.to(dev), prob.dY.to(dev)
+    W, m, v = prob.W.to(dev), prob.m.to(dev), prob.v.to(dev)
+    F.wgrad_step_adamw(X, dY, W, m, v, step=1, flags=F.FLAG_TEST_FORCE_TIMEOUT, **HYPER["adamw"])
+    with pytest.raises(F.ForgeError) as ei:
+        F.sync_status()
+    assert ei.value.status == 5 and "test hook" in str(ei.value)
+    assert torch.equal(W.cpu(), prob.W) and torch.equal(m.cpu(), prob.m) and torch.equal(v.cpu(), prob.v)
+    # the context is healthy: the next call runs normally
+    F.wgrad_step_adamw(X, dY, W, m, v, step=1, **HYPER["adamw"])
+    F.sync_status()
+    assert not torch.equal(W.cpu(), prob.W)
+
+
+# ---------------------------------------------------------------------------
+# Input gradient (Remark 1)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("w_dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dx_dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("shape", [(256, 384, 200), (136, 200, 70), (1024, 512, 512)])
+def test_dgrad_exact(w_dtype, dx_dtype, shape):
+    d_out, d_in, bt = shape
+    dev = "cuda:0"
+    dY = S.small_integers((bt, d_out), -3, 3, 1, S.STREAM_DY, "bf16")
+    W = S.small_integers((d_out, d_in), -3, 3, 1, S.STREAM_W, w_dtype)
+    dX = torch.empty((bt, d_in), dtype=torch.bfloat16 if dx_dtype == "bf16" else torch.float32, device=dev)
+    F.dgrad(dY.to(dev), W.to(dev), dX)
+    F.sync_status()
+    ref = O.dgrad_f64(dY.float().numpy(), W.float().numpy())
+    got = dX.float().cpu().numpy()
+    if dx_dtype == "bf16":
+        ref = O.bf16_bits_to_f32(O.f64_to_bf16_rne(ref))
+    assert np.array_equal(got, ref.astype(np.float32))
+
+
+def test_dgrad_random_reads_pre_update_weights():
+    d_out, d_in, bt = 1024, 512, 256
+    dev = "cuda:0"
+    prob = S.linear_problem(d_out, d_in, bt, seed=16, x_dtype="bf16", w_dtype="f32", state="f32",
+                            w_bf16_representable=False)
+    X, dY = prob.X.to(dev), prob.dY.to(dev)
+    W, m, v = prob.W.to(dev), prob.m.to(dev), prob.v.to(dev)
+    dX = torch.empty((bt, d_in), dtype=torch.float32, device=dev)
+    F.dgrad(dY, W, dX)                                   # enqueued first (Remark 1)
+    F.wgrad_step_adamw(X, dY, W, m, v, step=1, **HYPER["adamw"])
+    F.sync_status()
+    w16 = O.bf16_bits_to_f32(O.f32_to_bf16_rne(prob.W.numpy())).astype(np.float64)
+    dYn = prob.dY.float().numpy()
+    ref = dYn @ w16
+    tol = 1e-5 * (np.abs(dYn) @ np.abs(w16))
+    assert np.all(np.abs(dX.cpu().numpy() - ref) <= tol)
