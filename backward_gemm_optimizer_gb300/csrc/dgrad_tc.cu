@@ -9,9 +9,9 @@
 // bf16 (round-to-nearest-even) into the swizzled operand layout before the
 // MMA consumes them.
 //
-// Warp roles (384 threads): 0 TMA producer, 1 MMA issuer + TMEM owner,
-// 4-7 epilogue (TMEM lane quadrant = warp % 4, thread = token row),
-// 8-11 converters (fp32 weights only). All waits are bounded.
+// Warp roles (512 threads): 0 dY producer, 1 MMA issuer + TMEM owner,
+// 2 W producer, 4-7 epilogue (TMEM lane quadrant = warp % 4, thread =
+// token row), 8-15 converters (fp32 weights only). All waits are bounded.
 #include <cstdint>
 
 #include "forge_math.cuh"
@@ -23,17 +23,27 @@ namespace forge {
 namespace {
 
 constexpr int BM = 128, BN = 128, BK = 64;
-constexpr int A_BYTES = BM * BK * 2;       // 16 KB
-constexpr int B_BYTES = BK * BN * 2;       // 16 KB
+constexpr int A_BYTES = BM * BK * 2;       // 16 KB: dY tile, K-major
+constexpr int B_BYTES = BK * BN * 2;       // 16 KB: bf16 W tile, MN-major
 constexpr int STG_BYTES = BK * BN * 4;     // 32 KB: fp32 W tile as four 32-column swizzled boxes
 constexpr int TMEM_COLS = 256;
+constexpr int NUM_THREADS = 512;
+constexpr int CONV_THREADS = 256;          // warps 8-15
 constexpr uint32_t IDESC = make_idesc_bf16(BM, BN, 0, 1);
 
+// Three rings, each released by its own consumer, so that a load is never
+// held back by an unrelated stage: dY tiles (released by the MMA), fp32
+// staging tiles (released by the converters once read) and bf16 W tiles
+// (filled by TMA or by the converters, released by the MMA).
 template <bool F32W>
 struct DCfg {
-  static constexpr int STAGES = F32W ? 3 : 4;
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + (F32W ? STG_BYTES : 0);
-  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES;
+  static constexpr int SA = F32W ? 3 : 6;
+  static constexpr int SB = F32W ? 2 : 6;
+  static constexpr int SS = F32W ? 4 : 0;
+  static constexpr int A_OFF = 0;
+  static constexpr int B_OFF = SA * A_BYTES;
+  static constexpr int S_OFF = B_OFF + SB * B_BYTES;
+  static constexpr int SMEM_BYTES = 1024 + S_OFF + SS * STG_BYTES;
 };
 
 __device__ __forceinline__ bool dwait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
@@ -53,6 +63,16 @@ __device__ __forceinline__ bool dwait(uint64_t* bar, uint32_t parity, volatile i
   }
 }
 
+// After an abort: wait (bounded) for the last fills issued on a ring.
+__device__ __forceinline__ void ddrain(uint64_t* full, int ring, uint32_t issued, unsigned int* status) {
+  const uint32_t first = issued > static_cast<uint32_t>(ring) ? issued - ring : 0u;
+  for (uint32_t k = first; k < issued; ++k) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(&full[k % ring], (k / ring) & 1u))
+      if (globaltimer_ns() - t0 > 200000000ull) { atomicCAS(status, 0u, WAIT_DRAIN); break; }
+  }
+}
+
 __device__ __forceinline__ void dtile(int tile, int tiles_m, int tiles_n, int group_m, int& tm, int& tn) {
   const int per_group = group_m * tiles_n;
   const int g = tile / per_group;
@@ -65,26 +85,27 @@ __device__ __forceinline__ void dtile(int tile, int tiles_m, int tiles_n, int gr
 }
 
 template <bool F32W>
-__global__ void __launch_bounds__(384, 1) dgrad_tc_kernel(const __grid_constant__ DgradParams p) {
+__global__ void __launch_bounds__(NUM_THREADS, 1) dgrad_tc_kernel(const __grid_constant__ DgradParams p) {
   using C = DCfg<F32W>;
-  constexpr int S = C::STAGES;
+  constexpr int SA = C::SA, SB = C::SB, SS = C::SS > 0 ? C::SS : 1;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t full[S], conv[S], empty[S];
+  __shared__ __align__(8) uint64_t a_full[SA], a_empty[SA], b_full[SB], b_empty[SB], s_full[SS], s_empty[SS];
   __shared__ __align__(8) uint64_t tm_full[2], tm_empty[2], drain_bar;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* a_ring = smem + C::A_OFF;
+  uint8_t* b_ring = smem + C::B_OFF;
+  uint8_t* s_ring = smem + C::S_OFF;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int* abort_flag = &abort_sh;
   const uint64_t lim = p.timeout_ns;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&conv[s], 128);
-      mbar_init(&empty[s], 1);
-    }
+    for (int s = 0; s < SA; ++s) { mbar_init(&a_full[s], 1); mbar_init(&a_empty[s], 1); }
+    for (int s = 0; s < SB; ++s) { mbar_init(&b_full[s], F32W ? CONV_THREADS : 1); mbar_init(&b_empty[s], 1); }
+    for (int s = 0; s < SS; ++s) { mbar_init(&s_full[s], 1); mbar_init(&s_empty[s], CONV_THREADS); }
     for (int b = 0; b < 2; ++b) { mbar_init(&tm_full[b], 1); mbar_init(&tm_empty[b], 4); }
     mbar_init(&drain_bar, 1);
     abort_sh = 0;
@@ -98,46 +119,66 @@ __global__ void __launch_bounds__(384, 1) dgrad_tc_kernel(const __grid_constant_
   const uint32_t tmem_base = tmem_base_sh;
 
   if (warp == 0) {
+    // ------------------------------------------------------------ dY producer
     if (lane == 0) {
-      uint32_t kseq = 0;
+      uint32_t k = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
         int tm, tn;
         dtile(tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
-        for (int kb = 0; kb < p.num_kb; ++kb, ++kseq) {
-          const int s = static_cast<int>(kseq % S);
-          if (!dwait(&empty[s], ((kseq / S) & 1u) ^ 1u, abort_flag, p.status, WAIT_OP_EMPTY, lim)) {
+        for (int kb = 0; kb < p.num_kb; ++kb, ++k) {
+          const int s = static_cast<int>(k % SA);
+          if (!dwait(&a_empty[s], ((k / SA) & 1u) ^ 1u, abort_flag, p.status, WAIT_OP_EMPTY, lim)) {
             ok = false;
             break;
           }
-          uint8_t* a = smem + s * C::STAGE_BYTES;
-          uint8_t* b = a + A_BYTES;
+          mbar_arrive_expect_tx(&a_full[s], A_BYTES);
+          tma_load_2d(a_ring + s * A_BYTES, &p.tm_dy, &a_full[s], kb * BK, tm * BM);
+        }
+      }
+      if (!ok) ddrain(a_full, SA, k, p.status);
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ W producer
+    if (lane == 0) {
+      uint32_t k = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+        int tm, tn;
+        dtile(tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+        for (int kb = 0; kb < p.num_kb; ++kb, ++k) {
           if constexpr (F32W) {
-            uint8_t* stg = b + B_BYTES;
-            mbar_arrive_expect_tx(&full[s], A_BYTES + STG_BYTES);
-            tma_load_2d(a, &p.tm_dy, &full[s], kb * BK, tm * BM);
+            const int s = static_cast<int>(k % SS);
+            if (!dwait(&s_empty[s], ((k / SS) & 1u) ^ 1u, abort_flag, p.status, WAIT_OP_EMPTY, lim)) {
+              ok = false;
+              break;
+            }
+            uint8_t* stg = s_ring + s * STG_BYTES;
+            mbar_arrive_expect_tx(&s_full[s], STG_BYTES);
 #pragma unroll
-            for (int bb = 0; bb < 4; ++bb) tma_load_2d(stg + bb * 8192, &p.tm_w, &full[s], tn * BN + bb * 32, kb * BK);
+            for (int bb = 0; bb < 4; ++bb) tma_load_2d(stg + bb * 8192, &p.tm_w, &s_full[s], tn * BN + bb * 32, kb * BK);
           } else {
-            mbar_arrive_expect_tx(&full[s], A_BYTES + B_BYTES);
-            tma_load_2d(a, &p.tm_dy, &full[s], kb * BK, tm * BM);
-            tma_load_2d(b, &p.tm_w, &full[s], tn * BN, kb * BK);
-            tma_load_2d(b + 8192, &p.tm_w, &full[s], tn * BN + 64, kb * BK);
+            const int s = static_cast<int>(k % SB);
+            if (!dwait(&b_empty[s], ((k / SB) & 1u) ^ 1u, abort_flag, p.status, WAIT_OP_EMPTY, lim)) {
+              ok = false;
+              break;
+            }
+            uint8_t* b = b_ring + s * B_BYTES;
+            mbar_arrive_expect_tx(&b_full[s], B_BYTES);
+            tma_load_2d(b, &p.tm_w, &b_full[s], tn * BN, kb * BK);
+            tma_load_2d(b + 8192, &p.tm_w, &b_full[s], tn * BN + 64, kb * BK);
           }
         }
       }
       if (!ok) {
-        const uint32_t first = kseq > static_cast<uint32_t>(S) ? kseq - S : 0u;
-        for (uint32_t k = first; k < kseq; ++k) {
-          const uint64_t t0 = globaltimer_ns();
-          while (!mbar_try_wait(&full[k % S], (k / S) & 1u))
-            if (globaltimer_ns() - t0 > 200000000ull) { atomicCAS(p.status, 0u, WAIT_DRAIN); break; }
-        }
+        if constexpr (F32W) ddrain(s_full, SS, k, p.status);
+        else ddrain(b_full, SB, k, p.status);
       }
     }
   } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      uint32_t kseq = 0;
+      uint32_t k = 0;
       bool ok = true;
       int it = 0;
       for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++it) {
@@ -148,14 +189,16 @@ __global__ void __launch_bounds__(384, 1) dgrad_tc_kernel(const __grid_constant_
         }
         tc_fence_after_sync();
         const uint32_t d = tmem_base + static_cast<uint32_t>(buf * BN);
-        for (int kb = 0; kb < p.num_kb; ++kb, ++kseq) {
-          const int s = static_cast<int>(kseq % S);
-          const uint32_t ph = (kseq / S) & 1u;
-          uint64_t* ready = F32W ? &conv[s] : &full[s];
-          if (!dwait(ready, ph, abort_flag, p.status, WAIT_OP_FULL, lim)) { ok = false; break; }
+        for (int kb = 0; kb < p.num_kb; ++kb, ++k) {
+          const int sa = static_cast<int>(k % SA), sb = static_cast<int>(k % SB);
+          if (!dwait(&a_full[sa], (k / SA) & 1u, abort_flag, p.status, WAIT_OP_FULL, lim) ||
+              !dwait(&b_full[sb], (k / SB) & 1u, abort_flag, p.status, WAIT_OP_FULL, lim)) {
+            ok = false;
+            break;
+          }
           tc_fence_after_sync();
-          const uint32_t a0 = smem_u32(smem + s * C::STAGE_BYTES);
-          const uint32_t b0 = a0 + A_BYTES;
+          const uint32_t a0 = smem_u32(a_ring + sa * A_BYTES);
+          const uint32_t b0 = smem_u32(b_ring + sb * B_BYTES);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             // A: K-major, 128-byte swizzle, 8-row groups 1024 bytes apart; a
@@ -165,7 +208,8 @@ __global__ void __launch_bounds__(384, 1) dgrad_tc_kernel(const __grid_constant_
             const uint64_t bd = make_smem_desc(b0 + kk * 2048, 8192, 1024, 2);
             umma_f16(d, ad, bd, IDESC, (kb > 0 || kk > 0) ? 1u : 0u);
           }
-          umma_commit(&empty[s]);
+          umma_commit(&a_empty[sa]);
+          umma_commit(&b_empty[sb]);
         }
         if (!ok) break;
         umma_commit(&tm_full[buf]);
@@ -211,9 +255,7 @@ __global__ void __launch_bounds__(384, 1) dgrad_tc_kernel(const __grid_constant_
           if (full_chunk) {
             uint32_t b[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-              b[j] = f32_to_bf16_rne(__uint_as_float(acc[2 * j])) |
-                     (f32_to_bf16_rne(__uint_as_float(acc[2 * j + 1])) << 16);
+            for (int j = 0; j < 8; ++j) b[j] = pack_bf16x2_rn(__uint_as_float(acc[2 * j]), __uint_as_float(acc[2 * j + 1]));
             reinterpret_cast<uint4*>(out)[0] = make_uint4(b[0], b[1], b[2], b[3]);
             reinterpret_cast<uint4*>(out)[1] = make_uint4(b[4], b[5], b[6], b[7]);
           } else {
@@ -245,38 +287,43 @@ __global__ void __launch_bounds__(384, 1) dgrad_tc_kernel(const __grid_constant_
     // MN-major swizzled operand. Consecutive threads take consecutive K
     // rows, so both the reads and the writes are bank-conflict free.
     const int ct = threadIdx.x - 256;
-    uint32_t kseq = 0;
+    uint32_t k = 0;
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-      for (int kb = 0; kb < p.num_kb; ++kb, ++kseq) {
-        const int s = static_cast<int>(kseq % S);
-        const uint32_t ph = (kseq / S) & 1u;
-        ok = dwait(&full[s], ph, abort_flag, p.status, WAIT_OP_FULL, lim);
+      for (int kb = 0; kb < p.num_kb; ++kb, ++k) {
+        const int ss = static_cast<int>(k % SS), sb = static_cast<int>(k % SB);
+        ok = dwait(&s_full[ss], (k / SS) & 1u, abort_flag, p.status, WAIT_OP_FULL, lim) &&
+             dwait(&b_empty[sb], ((k / SB) & 1u) ^ 1u, abort_flag, p.status, WAIT_OP_EMPTY, lim);
         ok = __all_sync(0xFFFFFFFFu, ok);
         if (!ok) break;
-        uint8_t* b = smem + s * C::STAGE_BYTES + A_BYTES;
-        const uint8_t* stg = b + B_BYTES;
+        uint8_t* b = b_ring + sb * B_BYTES;
+        const uint8_t* stg = s_ring + ss * STG_BYTES;
+        uint4 o[4];
+        int dst[4];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int i = ct + 128 * j;
-          const int k = i & 63;              // K row
+        for (int j = 0; j < 4; ++j) {
+          const int i = ct + CONV_THREADS * j;
+          const int kr = i & 63;             // K row
           const int hh = (i >> 6) & 3;       // 8-column group within the 32-column box
           const int bb = i >> 8;             // box (32 columns)
-          const uint8_t* src = stg + bb * 8192 + k * 128;
-          const float4 u0 = *reinterpret_cast<const float4*>(src + (((2 * hh) ^ (k & 7)) << 4));
-          const float4 u1 = *reinterpret_cast<const float4*>(src + (((2 * hh + 1) ^ (k & 7)) << 4));
-          uint4 o;
-          o.x = f32_to_bf16_rne(u0.x) | (f32_to_bf16_rne(u0.y) << 16);
-          o.y = f32_to_bf16_rne(u0.z) | (f32_to_bf16_rne(u0.w) << 16);
-          o.z = f32_to_bf16_rne(u1.x) | (f32_to_bf16_rne(u1.y) << 16);
-          o.w = f32_to_bf16_rne(u1.z) | (f32_to_bf16_rne(u1.w) << 16);
+          const uint8_t* src = stg + bb * 8192 + kr * 128;
+          const float4 u0 = *reinterpret_cast<const float4*>(src + (((2 * hh) ^ (kr & 7)) << 4));
+          const float4 u1 = *reinterpret_cast<const float4*>(src + (((2 * hh + 1) ^ (kr & 7)) << 4));
+          o[j].x = pack_bf16x2_rn(u0.x, u0.y);
+          o[j].y = pack_bf16x2_rn(u0.z, u0.w);
+          o[j].z = pack_bf16x2_rn(u1.x, u1.y);
+          o[j].w = pack_bf16x2_rn(u1.z, u1.w);
           const int n = bb * 32 + hh * 8;    // column within the 128-wide tile
-          const int atom = n >> 6;
-          const int chunk = ((n & 63) >> 3) ^ (k & 7);
-          *reinterpret_cast<uint4*>(b + atom * 8192 + k * 128 + (chunk << 4)) = o;
+          dst[j] = (n >> 6) * 8192 + kr * 128 + ((((n & 63) >> 3) ^ (kr & 7)) << 4);
         }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) *reinterpret_cast<uint4*>(b + dst[j]) = o[j];
         fence_proxy_async_smem();
-        mbar_arrive(&conv[s]);
+        mbar_arrive(&b_full[sb]);
+        // Release the staging slot only now: the stores above consume every
+        // value loaded from it, so those loads have returned before the next
+        // TMA fill may overwrite the slot.
+        mbar_arrive(&s_empty[ss]);
       }
     }
   }
@@ -303,7 +350,7 @@ cudaError_t launch_d(const DgradParams& p, int grid, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     __atomic_fetch_or(&attr_mask, bit, __ATOMIC_ACQ_REL);
   }
-  kern<<<grid, 384, DCfg<F32W>::SMEM_BYTES, stream>>>(p);
+  kern<<<grid, NUM_THREADS, DCfg<F32W>::SMEM_BYTES, stream>>>(p);
   return cudaGetLastError();
 }
 

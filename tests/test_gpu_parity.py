@@ -306,3 +306,22 @@ def test_dgrad_random_reads_pre_update_weights():
     ref = dYn @ w16
     tol = 1e-5 * (np.abs(dYn) @ np.abs(w16))
     assert np.all(np.abs(dX.cpu().numpy() - ref) <= tol)
+
+
+@pytest.mark.parametrize("shape", [(4096, 512, 256), (14336, 4096, 512), (2048, 4096, 512)])
+def test_dgrad_f32_and_bf16_weights_agree_bit_for_bit(shape):
+    # fp32 master weights that are bf16-representable must give exactly the
+    # dX of the same weights stored as bf16 (the staging conversion is exact),
+    # on every repetition (no stale staging data).
+    d_out, d_in, bt = shape
+    dev = "cuda:0"
+    W16 = S.normal((d_out, d_in), 0.02, 2, S.STREAM_W, "bf16").to(dev)
+    W32 = W16.float()
+    dY = S.normal((bt, d_out), 1.0, 2, S.STREAM_DY, "bf16").to(dev)
+    ref = torch.empty((bt, d_in), dtype=torch.float32, device=dev)
+    F.dgrad(dY, W16, ref)
+    for _ in range(4):
+        out = torch.empty_like(ref)
+        F.dgrad(dY, W32, out)
+        F.sync_status()
+        assert torch.equal(out, ref), int((out != ref).sum())
