@@ -58,6 +58,33 @@ def dgrad_algorithmic_bytes(d_out, d_in, bt, w):
     return d_out * d_in * (4 if w == "f32" else 2) + 2 * bt * d_out + 2 * bt * d_in
 
 
+KERNEL_SOURCES = ["wgrad_tc.cuh", "wgrad_tc_dispatch.cuh", "wgrad_tc_adamw.cu", "forge_math.cuh", "forge_ptx.cuh",
+                  "forge_params.h"]
+
+
+def kernel_source_hash() -> str:
+    """Hash of the sources that define the fused kernel (ties an ncu capture to this code)."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "backward_gemm_optimizer_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic(workload: str):
+    """DRAM bytes per launch of the fused kernel from the committed ncu capture, if it
+    was taken on the current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None, None
+    with open(p) as f:
+        d = json.load(f).get(workload)
+    if not d or d.get("kernel_source_hash") != kernel_source_hash():
+        return None, None
+    return d.get("dram_bytes_per_launch"), d.get("units_scale", 1.0)
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -170,6 +197,30 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+# --------------------------------------------------------------------------- ranks (replicas)
+
+
+def replica_seed(rank: int) -> int:
+    """Each rank steps its own, independently drawn layer (replicas; no data-path collective)."""
+    return rank
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch
+        torch.distributed.barrier()
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The job's time is the slowest rank's (max over ranks)."""
+    if world <= 1:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
 # --------------------------------------------------------------------------- GPU arm
 
 
@@ -197,13 +248,9 @@ def run_gpu(args, rank, world, local_rank):
     dev = torch.device(f"cuda:{local_rank}")
     torch.cuda.set_device(dev)
     d_out, d_in, bt, w, st = WORKLOADS[args.workload]
-    s, host = make_state(d_out, d_in, bt, w, st, dev, seed=rank)
+    s, host = make_state(d_out, d_in, bt, w, st, dev, seed=replica_seed(rank))
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)   # 256 MB > L2
-
-    def barrier():
-        if world > 1:
-            torch.distributed.barrier()
 
     t = 1
     for _ in range(args.warmup):
@@ -213,7 +260,7 @@ def run_gpu(args, rank, world, local_rank):
     K = args.steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
     sampler = ClockSampler(local_rank)
-    barrier()
+    barrier(world)
     torch.cuda.synchronize(dev)
     sampler.start()
     time.sleep(0.3)
@@ -230,22 +277,18 @@ def run_gpu(args, rank, world, local_rank):
         t += 1
     torch.cuda.synchronize(dev)
     wall = time.perf_counter() - wall0
-    barrier()
+    barrier(world)
     clocks = sampler.stop()
     F.sync_status(stream)
     step_ms = [ev[i][0].elapsed_time(ev[i][2]) for i in range(K)]
     dgrad_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
     fused_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
-    total_ms = sum(step_ms)
-    if world > 1:
-        tt = torch.tensor([total_ms], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(sum(step_ms), world, dev)
 
     # ---- end to end through the public API, host buffers, copies timed
     KE = max(1, min(args.e2e_steps, K))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier()
+    barrier(world)
     torch.cuda.synchronize(dev)
     e0.record(stream)
     for i in range(KE):
@@ -272,11 +315,7 @@ def run_gpu(args, rank, world, local_rank):
     flops = 2.0 * bt * d_out * d_in
     t_roof = max(abytes / (hbm * 1e9), flops / (tflops * 1e12)) * 1e6
     bound = "hbm" if abytes / (hbm * 1e9) >= flops / (tflops * 1e12) else "tensor"
-    traffic = None
-    tr_path = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tr_path):
-        with open(tr_path) as f:
-            traffic = json.load(f).get(args.workload)
+    traffic, _ = load_traffic(args.workload)
     line = {
         "metric": METRIC, "value": round(us, 2), "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(us / 1000.0, 4), "higher_is_better": False,
@@ -296,7 +335,8 @@ def run_gpu(args, rank, world, local_rank):
                                    (flops / (fused_us * 1e-6) / 1e12) / tflops, 4),
                      "traffic": traffic, "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_src == "measured" else peak_src,
-                     "algorithmic_bytes": abytes, "kernel": "wgrad_step_tc_kernel"},
+                     "algorithmic_bytes": abytes, "kernel": "wgrad_step_tc_kernel",
+                     "kernel_source_hash": kernel_source_hash()},
         "e2e": {"value": round(e2e_ms * 1000.0, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": 2 * K,
