@@ -101,7 +101,7 @@ __global__ void __launch_bounds__(128) wgrad_step_simt_kernel(const WgradSimtPar
 #pragma unroll
     for (int i = 0; i < SR; ++i) {
       float am = fabsf(m1[i]);
-      float au = TWO ? __fsqrt_rn(v1[i]) : 0.0f;
+      float au = TWO ? v1[i] : 0.0f;     // max v'; sqrt(max v') = max sqrt(v')
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
         am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, o));
@@ -115,7 +115,7 @@ __global__ void __launch_bounds__(128) wgrad_step_simt_kernel(const WgradSimtPar
       const float am = fmaxf(fmaxf(red[0][0][i], red[0][1][i]), fmaxf(red[0][2][i], red[0][3][i]));
       const float au = fmaxf(fmaxf(red[1][0][i], red[1][1][i]), fmaxf(red[1][2][i], red[1][3][i]));
       sm_new[i] = __fdiv_rn(am, 127.0f);
-      sv_new[i] = __fdiv_rn(au, 255.0f);
+      sv_new[i] = __fdiv_rn(__fsqrt_rn(au), 255.0f);
     }
     __syncthreads();  // every thread has read the old scales and the reduction
     if (t == 0) {
@@ -155,10 +155,10 @@ __global__ void __launch_bounds__(128) wgrad_step_simt_kernel(const WgradSimtPar
       }
     } else {
       static_cast<int8_t*>(p.m)[static_cast<int64_t>(row) * p.ld_m + q] =
-          static_cast<int8_t>(quant_m(m1[i], sm_new[i]));
+          static_cast<int8_t>(quant_m(m1[i], sm_new[i], block_inv(sm_new[i])));
       if constexpr (TWO)
         static_cast<uint8_t*>(p.v)[static_cast<int64_t>(row) * p.ld_v + q] =
-            static_cast<uint8_t>(quant_v(v1[i], __fsqrt_rn(v1[i]), sv_new[i]));
+            static_cast<uint8_t>(quant_v(v1[i], __fsqrt_rn(v1[i]), sv_new[i], block_inv(sv_new[i])));
     }
   }
 }

@@ -2,7 +2,7 @@
 // sm_103a (FORGE, Algorithm 1, re-designed for tcgen05 tensor cores).
 //
 // One persistent CTA per SM walks a grouped raster of 128 x BN gradient
-// tiles G_ij = sum_k dY_k,i^T X_k,j (Eq. 5). Warp roles (384 threads):
+// tiles G_ij = sum_k dY_k,i^T X_k,j (Eq. 5). Warp roles (640 threads):
 //
 //   warp 0      operand producer: TMA loads of the 64-token slabs of dY and
 //               X into a STAGES-deep shared-memory ring;
@@ -12,10 +12,13 @@
 //   warp 2      state producer: TMA loads of the W / m / v tiles, in
 //               32-column chunks, into an NBUF-deep slot ring;
 //   warp 3      state storer: TMA stores of each finished chunk;
-//   warps 4-11  epilogue: warp w reads TMEM lane quadrant w % 4 (row p of
-//               the tile = TMEM lane) and column half (w - 4) / 4 of each
-//               chunk, applies the optimizer element-wise in fp32 and writes
-//               the new W / m / v back into the slot (Algorithm 1 phase 2-3).
+//   warps 4-19  epilogue: warp w reads TMEM lane quadrant w % 4 (row p of
+//               the tile = TMEM lane) and 8-column quarter (w - 4) / 4 of each
+//               32-column chunk, applies the optimizer element-wise in fp32
+//               and writes the new W / m / v back into the slot (Algorithm 1
+//               phase 2-3). Four epilogue warps per scheduler hide the
+//               latency of the per-element arithmetic (divide, square root,
+//               Philox rounds).
 //
 // The accumulator never leaves TMEM / registers: no gradient tile is ever
 // written to global memory (Proposition 3). Both operands are token-major
@@ -57,9 +60,10 @@ struct TcCfg {
   static constexpr int SLOT_BYTES = ((W_CH + M_CH + V_CH + 1023) / 1024) * 1024;
   static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NBUF * SLOT_BYTES;
   static constexpr int TMEM_COLS = (2 * BN <= 128) ? 128 : (2 * BN <= 256 ? 256 : 512);
-  static constexpr int NUM_THREADS = 384;
-  static constexpr int EPI_WARPS = 8;
+  static constexpr int EPI_WARPS = 16;
   static constexpr int EPI_THREADS = EPI_WARPS * 32;
+  static constexpr int NUM_THREADS = 128 + EPI_THREADS;
+  static constexpr int QCOLS = 8;                // columns per epilogue thread per chunk
   static constexpr uint32_t IDESC = make_idesc_bf16(BM, BN, 1, 1);
 
 };
@@ -74,60 +78,68 @@ __device__ __forceinline__ uint32_t swz(int r, int c) {
   return static_cast<uint32_t>(r * RB + ((c ^ x) << 4));
 }
 
-// 16 consecutive values of row r, columns [16h, 16h + 16) of a chunk.
+// 8 consecutive values of row r, columns [8h, 8h + 8) of a 32-column chunk.
 template <int KIND>  // 0: f32, 1: bf16
-__device__ __forceinline__ void ld16(const uint8_t* base, int r, int h, float (&o)[16]) {
+__device__ __forceinline__ void ld8(const uint8_t* base, int r, int h, float (&o)[8]) {
   if constexpr (KIND == 0) {
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float4 t = *reinterpret_cast<const float4*>(base + swz<4>(r, 4 * h + k));
+    for (int k = 0; k < 2; ++k) {
+      const float4 t = *reinterpret_cast<const float4*>(base + swz<4>(r, 2 * h + k));
       o[4 * k + 0] = t.x; o[4 * k + 1] = t.y; o[4 * k + 2] = t.z; o[4 * k + 3] = t.w;
     }
   } else {
+    const uint4 t = *reinterpret_cast<const uint4*>(base + swz<2>(r, h));
+    const uint32_t wv[4] = {t.x, t.y, t.z, t.w};
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const uint4 t = *reinterpret_cast<const uint4*>(base + swz<2>(r, 2 * h + k));
-      const uint32_t wv[4] = {t.x, t.y, t.z, t.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        o[8 * k + 2 * i + 0] = bf16_bits_to_f32(wv[i] & 0xFFFFu);
-        o[8 * k + 2 * i + 1] = bf16_bits_to_f32(wv[i] >> 16);
-      }
+    for (int i = 0; i < 4; ++i) {
+      o[2 * i + 0] = bf16_bits_to_f32(wv[i] & 0xFFFFu);
+      o[2 * i + 1] = bf16_bits_to_f32(wv[i] >> 16);
     }
   }
 }
 
-__device__ __forceinline__ void st16_f32(uint8_t* base, int r, int h, const float (&o)[16]) {
+__device__ __forceinline__ void st8_f32(uint8_t* base, int r, int h, const float (&o)[8]) {
 #pragma unroll
-  for (int k = 0; k < 4; ++k)
-    *reinterpret_cast<float4*>(base + swz<4>(r, 4 * h + k)) =
+  for (int k = 0; k < 2; ++k)
+    *reinterpret_cast<float4*>(base + swz<4>(r, 2 * h + k)) =
         make_float4(o[4 * k + 0], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
 }
 
-__device__ __forceinline__ void st16_bf16(uint8_t* base, int r, int h, const uint32_t (&b)[16]) {
+__device__ __forceinline__ void st8_bf16(uint8_t* base, int r, int h, const uint4& t) {
+  *reinterpret_cast<uint4*>(base + swz<2>(r, h)) = t;
+}
+
+// 8 codes of row r, columns [8h, 8h + 8): half (h % 2) of 16-byte chunk h / 2.
+__device__ __forceinline__ void ld8_codes(const uint8_t* base, int r, int h, uint32_t (&c)[8]) {
+  const uint2 t = *reinterpret_cast<const uint2*>(base + swz<1>(r, h >> 1) + (h & 1) * 8);
 #pragma unroll
-  for (int k = 0; k < 2; ++k) {
-    uint4 t;
-    t.x = b[8 * k + 0] | (b[8 * k + 1] << 16);
-    t.y = b[8 * k + 2] | (b[8 * k + 3] << 16);
-    t.z = b[8 * k + 4] | (b[8 * k + 5] << 16);
-    t.w = b[8 * k + 6] | (b[8 * k + 7] << 16);
-    *reinterpret_cast<uint4*>(base + swz<2>(r, 2 * h + k)) = t;
+  for (int i = 0; i < 8; ++i) c[i] = ((i < 4 ? t.x : t.y) >> (8 * (i & 3))) & 0xFFu;
+}
+
+__device__ __forceinline__ void st8_codes(uint8_t* base, int r, int h, const uint32_t (&c)[8]) {
+  uint2 t = make_uint2(0u, 0u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) t.x |= (c[i] & 0xFFu) << (8 * i);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) t.y |= (c[4 + i] & 0xFFu) << (8 * i);
+  *reinterpret_cast<uint2*>(base + swz<1>(r, h >> 1) + (h & 1) * 8) = t;
+}
+
+// Eight bf16 stores of `x` packed in four words: stochastic rounding with
+// the Philox block of elements idx8 * 8 .. idx8 * 8 + 7 at `site`, or
+// round-to-nearest-even.
+__device__ __forceinline__ void to_bf16x8(const float (&x)[8], bool sr, uint64_t idx8, uint32_t site,
+                                          const WgradTcParams& p, uint4& o) {
+  if (sr) {
+    const U4 rr = sr_block(idx8, p.step, site, p.seed_lo, p.seed_hi);
+    uint32_t b[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) b[j] = f32_to_bf16_sr(x[j], sr_lane(rr, j));
+    o = make_uint4(b[0] | (b[1] << 16), b[2] | (b[3] << 16), b[4] | (b[5] << 16), b[6] | (b[7] << 16));
+  } else {
+    o = make_uint4(pack_bf16x2_rn(x[0], x[1]), pack_bf16x2_rn(x[2], x[3]), pack_bf16x2_rn(x[4], x[5]),
+                   pack_bf16x2_rn(x[6], x[7]));
   }
-}
-
-__device__ __forceinline__ void ld16_codes(const uint8_t* base, int r, int h, uint32_t (&c)[16]) {
-  const uint4 t = *reinterpret_cast<const uint4*>(base + swz<1>(r, h));
-  const uint32_t wv[4] = {t.x, t.y, t.z, t.w};
-#pragma unroll
-  for (int i = 0; i < 16; ++i) c[i] = (wv[i >> 2] >> (8 * (i & 3))) & 0xFFu;
-}
-
-__device__ __forceinline__ void st16_codes(uint8_t* base, int r, int h, const uint32_t (&c)[16]) {
-  uint32_t wv[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-  for (int i = 0; i < 16; ++i) wv[i >> 2] |= (c[i] & 0xFFu) << (8 * (i & 3));
-  *reinterpret_cast<uint4*>(base + swz<1>(r, h)) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
 }
 
 __device__ __forceinline__ int32_t sext8(uint32_t b) { return static_cast<int32_t>(static_cast<int8_t>(b & 0xFFu)); }
@@ -181,7 +193,7 @@ __device__ __forceinline__ void drain_ring(uint64_t* full, int ring, uint32_t is
 }
 
 template <int OPT, int WK, int MK, int BN, int STAGES, int NBUF>
-__global__ void __launch_bounds__(384, 1) wgrad_step_tc_kernel(const __grid_constant__ WgradTcParams p) {
+__global__ void __launch_bounds__(128 + 512, 1) wgrad_step_tc_kernel(const __grid_constant__ WgradTcParams p) {
   using C = TcCfg<OPT, WK, MK, BN, STAGES, NBUF>;
   static_assert(BN == 64 || BN == 128, "tile width");
   static_assert(!C::Q8 || BN == 128, "8-bit blocks span one 128-column tile row");
@@ -197,7 +209,7 @@ __global__ void __launch_bounds__(384, 1) wgrad_step_tc_kernel(const __grid_cons
   __shared__ __align__(8) uint64_t never_bar, mma_drain_bar;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
-  __shared__ float red_sh[2][2][2][128];  // [tile parity][m | sqrt v][half][row]
+  __shared__ float red_sh[2][2][4][128];  // [tile parity][|m'| | v'][column quarter][row]
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* op_base = smem;
@@ -350,9 +362,9 @@ __global__ void __launch_bounds__(384, 1) wgrad_step_tc_kernel(const __grid_cons
       bulk_wait_group0();
     }
   } else {
-    // ------------------------------------------------------------ epilogue (warps 4..11)
+    // ------------------------------------------------------------ epilogue (warps 4..19)
     const int q = warp & 3;          // TMEM lane quadrant this warp may access
-    const int h = (warp - 4) >> 2;   // column half of each 32-column chunk
+    const int h = (warp - 4) >> 2;   // 8-column quarter of each 32-column chunk
     const int r = q * 32 + lane;     // tile row == TMEM lane
     const StepScalars sc = p.sc;
     uint32_t cseq = 0;
@@ -382,24 +394,24 @@ __global__ void __launch_bounds__(384, 1) wgrad_step_tc_kernel(const __grid_cons
           ok = bwait(&st_full[s], (cseq / NBUF) & 1u, abort_flag, p.status, WAIT_ST_FULL, lim);
           ok = __all_sync(0xFFFFFFFFu, ok);
           if (!ok) break;
-          uint32_t gr[16];
+          uint32_t gr[8];
           if (p.num_kb > 0) {
-            tmem_ld_32x32b_x16(t_lane + c * C::CW + h * 16, gr);
+            tmem_ld_32x32b_x8(t_lane + c * C::CW + h * 8, gr);
             tmem_ld_wait();
           } else {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) gr[j] = 0u;
+            for (int j = 0; j < 8; ++j) gr[j] = 0u;
           }
           uint8_t* slot = st_base + s * C::SLOT_BYTES;
           uint8_t* sw = slot;
           uint8_t* sm = slot + C::W_CH;
           uint8_t* sv = slot + C::W_CH + C::M_CH;
-          float w[16], m[16], v[16];
-          ld16<WK == W_F32 ? 0 : 1>(sw, r, h, w);
-          ld16<MK == M_F32 ? 0 : 1>(sm, r, h, m);
-          if constexpr (C::TWO) ld16<MK == M_F32 ? 0 : 1>(sv, r, h, v);
+          float w[8], m[8], v[8];
+          ld8<WK == W_F32 ? 0 : 1>(sw, r, h, w);
+          ld8<MK == M_F32 ? 0 : 1>(sm, r, h, m);
+          if constexpr (C::TWO) ld8<MK == M_F32 ? 0 : 1>(sv, r, h, v);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
+          for (int j = 0; j < 8; ++j) {
             const float g = __uint_as_float(gr[j]);
             float w1, m1, v1 = 0.0f;
             if constexpr (OPT == OPT_ADAMW) adamw_elem(g, w[j], m[j], v[j], sc, w1, m1, v1);
@@ -408,55 +420,26 @@ __global__ void __launch_bounds__(384, 1) wgrad_step_tc_kernel(const __grid_cons
             w[j] = w1; m[j] = m1;
             if constexpr (C::TWO) v[j] = v1;
           }
-          const int q0 = tn * BN + c * C::CW + h * 16;   // first column of this thread's 16
-          const uint64_t idx0 = static_cast<uint64_t>(row) * static_cast<uint64_t>(p.d_in) + q0;
+          // Element index of this thread's first column; 8-aligned (D_in % 8 == 0).
+          const uint64_t idx8 =
+              (static_cast<uint64_t>(row) * static_cast<uint64_t>(p.d_in) + (tn * BN + c * C::CW + h * 8)) >> 3;
           if constexpr (WK == W_F32) {
-            st16_f32(sw, r, h, w);
+            st8_f32(sw, r, h, w);
           } else {
-            uint32_t b[16];
-            if (p.sr_w) {
-#pragma unroll
-              for (int k = 0; k < 2; ++k) {
-                const U4 rr = sr_block((idx0 >> 3) + k, p.step, 0u, p.seed_lo, p.seed_hi);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) b[8 * k + j] = f32_to_bf16_sr(w[8 * k + j], sr_lane(rr, j));
-              }
-            } else {
-#pragma unroll
-              for (int j = 0; j < 16; ++j) b[j] = f32_to_bf16_rne(w[j]);
-            }
-            st16_bf16(sw, r, h, b);
+            uint4 b;
+            to_bf16x8(w, p.sr_w != 0, idx8, 0u, p, b);
+            st8_bf16(sw, r, h, b);
           }
           if constexpr (MK == M_F32) {
-            st16_f32(sm, r, h, m);
-            if constexpr (C::TWO) st16_f32(sv, r, h, v);
+            st8_f32(sm, r, h, m);
+            if constexpr (C::TWO) st8_f32(sv, r, h, v);
           } else {
-            uint32_t b[16];
-            if (p.sr_m) {
-#pragma unroll
-              for (int k = 0; k < 2; ++k) {
-                const U4 rr = sr_block((idx0 >> 3) + k, p.step, 1u, p.seed_lo, p.seed_hi);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) b[8 * k + j] = f32_to_bf16_sr(m[8 * k + j], sr_lane(rr, j));
-              }
-            } else {
-#pragma unroll
-              for (int j = 0; j < 16; ++j) b[j] = f32_to_bf16_rne(m[j]);
-            }
-            st16_bf16(sm, r, h, b);
+            uint4 b;
+            to_bf16x8(m, p.sr_m != 0, idx8, 1u, p, b);
+            st8_bf16(sm, r, h, b);
             if constexpr (C::TWO) {
-              if (p.sr_m) {
-#pragma unroll
-                for (int k = 0; k < 2; ++k) {
-                  const U4 rr = sr_block((idx0 >> 3) + k, p.step, 2u, p.seed_lo, p.seed_hi);
-#pragma unroll
-                  for (int j = 0; j < 8; ++j) b[8 * k + j] = f32_to_bf16_sr(v[8 * k + j], sr_lane(rr, j));
-                }
-              } else {
-#pragma unroll
-                for (int j = 0; j < 16; ++j) b[j] = f32_to_bf16_rne(v[j]);
-              }
-              st16_bf16(sv, r, h, b);
+              to_bf16x8(v, p.sr_m != 0, idx8, 2u, p, b);
+              st8_bf16(sv, r, h, b);
             }
           }
           fence_proxy_async_smem();
@@ -481,29 +464,29 @@ __global__ void __launch_bounds__(384, 1) wgrad_step_tc_kernel(const __grid_cons
           ok = bwait(&st_full[s], (k / NBUF) & 1u, abort_flag, p.status, WAIT_ST_FULL, lim);
           ok = __all_sync(0xFFFFFFFFu, ok);
           if (!ok) break;
-          uint32_t gr[16];
+          uint32_t gr[8];
           if (p.num_kb > 0) {
-            tmem_ld_32x32b_x16(t_lane + c * C::CW + h * 16, gr);
+            tmem_ld_32x32b_x8(t_lane + c * C::CW + h * 8, gr);
             tmem_ld_wait();
           } else {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) gr[j] = 0u;
+            for (int j = 0; j < 8; ++j) gr[j] = 0u;
           }
           const uint8_t* slot = st_base + s * C::SLOT_BYTES;
-          uint32_t cm[16], cv[16];
-          float w[16];
-          ld16_codes(slot + C::W_CH, r, h, cm);
-          if constexpr (C::TWO) ld16_codes(slot + C::W_CH + C::M_CH, r, h, cv);
-          if constexpr (OPT == OPT_SGDM) ld16<WK == W_F32 ? 0 : 1>(slot, r, h, w);
+          uint32_t cm[8], cv[8];
+          float w[8];
+          ld8_codes(slot + C::W_CH, r, h, cm);
+          if constexpr (C::TWO) ld8_codes(slot + C::W_CH + C::M_CH, r, h, cv);
+          if constexpr (OPT == OPT_SGDM) ld8<WK == W_F32 ? 0 : 1>(slot, r, h, w);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
+          for (int j = 0; j < 8; ++j) {
             const float g = __uint_as_float(gr[j]);
             const float m0 = dequant_m(sext8(cm[j]), sm_old);
             float m1;
             if constexpr (OPT == OPT_ADAMW) {
               float v1;
               adamw_moments(g, m0, dequant_v(cv[j], sv_old), sc, m1, v1);
-              au = fmaxf(au, __fsqrt_rn(v1));
+              au = fmaxf(au, v1);     // max v'; sqrt is taken once per row below
             } else if constexpr (OPT == OPT_SGDM) {
               m1 = __fadd_rn(__fmul_rn(sc.b1, m0), __fadd_rn(g, __fmul_rn(sc.wd, w[j])));
             } else {
@@ -513,78 +496,73 @@ __global__ void __launch_bounds__(384, 1) wgrad_step_tc_kernel(const __grid_cons
           }
         }
         if (!ok) break;
-        // Combine the two column halves of each row (bounded, abort-aware).
+        // Combine the four column quarters of each row (bounded, abort-aware).
         red_sh[it & 1][0][h][r] = am;
         red_sh[it & 1][1][h][r] = au;
         mbar_arrive(&red_bar[it & 1]);
         ok = bwait(&red_bar[it & 1], (it >> 1) & 1, abort_flag, p.status, WAIT_RED, lim);
         ok = __all_sync(0xFFFFFFFFu, ok);
         if (!ok) break;
-        am = fmaxf(am, red_sh[it & 1][0][h ^ 1][r]);
-        au = fmaxf(au, red_sh[it & 1][1][h ^ 1][r]);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          am = fmaxf(am, red_sh[it & 1][0][k][r]);
+          au = fmaxf(au, red_sh[it & 1][1][k][r]);
+        }
+        // sqrt is monotonic and correctly rounded: max sqrt(v') = sqrt(max v').
         const float sm_new = __fdiv_rn(am, 127.0f);
-        const float sv_new = __fdiv_rn(au, 255.0f);
+        const float sv_new = __fdiv_rn(__fsqrt_rn(au), 255.0f);
+        const float im_new = block_inv(sm_new), iv_new = block_inv(sv_new);
         if (h == 0 && row < p.d_out) {
           p.m_scale[static_cast<int64_t>(jb) * p.d_out + row] = sm_new;
           if constexpr (C::TWO) p.v_scale[static_cast<int64_t>(jb) * p.d_out + row] = sv_new;
         }
         for (int c = 0; c < C::NCH; ++c, ++cseq) {
           const int s = static_cast<int>(cseq % NBUF);
-          uint32_t gr[16];
+          uint32_t gr[8];
           if (p.num_kb > 0) {
-            tmem_ld_32x32b_x16(t_lane + c * C::CW + h * 16, gr);
+            tmem_ld_32x32b_x8(t_lane + c * C::CW + h * 8, gr);
             tmem_ld_wait();
           } else {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) gr[j] = 0u;
+            for (int j = 0; j < 8; ++j) gr[j] = 0u;
           }
           uint8_t* slot = st_base + s * C::SLOT_BYTES;
           uint8_t* sw = slot;
           uint8_t* smc = slot + C::W_CH;
           uint8_t* svc = slot + C::W_CH + C::M_CH;
-          uint32_t cm[16], cv[16];
-          float w[16];
-          ld16<WK == W_F32 ? 0 : 1>(sw, r, h, w);
-          ld16_codes(smc, r, h, cm);
-          if constexpr (C::TWO) ld16_codes(svc, r, h, cv);
+          uint32_t cm[8], cv[8];
+          float w[8];
+          ld8<WK == W_F32 ? 0 : 1>(sw, r, h, w);
+          ld8_codes(smc, r, h, cm);
+          if constexpr (C::TWO) ld8_codes(svc, r, h, cv);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
+          for (int j = 0; j < 8; ++j) {
             const float g = __uint_as_float(gr[j]);
             const float m0 = dequant_m(sext8(cm[j]), sm_old);
             float w1, m1;
             if constexpr (OPT == OPT_ADAMW) {
-              float v1;
-              adamw_elem(g, w[j], m0, dequant_v(cv[j], sv_old), sc, w1, m1, v1);
-              cv[j] = quant_v(v1, __fsqrt_rn(v1), sv_new);
+              float v1, sq1;
+              adamw_elem(g, w[j], m0, dequant_v(cv[j], sv_old), sc, w1, m1, v1, sq1);
+              cv[j] = quant_v(v1, sq1, sv_new, iv_new);
             } else if constexpr (OPT == OPT_SGDM) {
               sgdm_elem(g, w[j], m0, sc, w1, m1);
             } else {
               lion_elem(g, w[j], m0, sc, w1, m1);
             }
             w[j] = w1;
-            cm[j] = static_cast<uint32_t>(quant_m(m1, sm_new)) & 0xFFu;
+            cm[j] = static_cast<uint32_t>(quant_m(m1, sm_new, im_new)) & 0xFFu;
           }
           if constexpr (WK == W_F32) {
-            st16_f32(sw, r, h, w);
+            st8_f32(sw, r, h, w);
           } else {
-            uint32_t b[16];
-            const int q0 = tn * BN + c * C::CW + h * 16;
-            const uint64_t idx0 = static_cast<uint64_t>(row) * static_cast<uint64_t>(p.d_in) + q0;
-            if (p.sr_w) {
-#pragma unroll
-              for (int k = 0; k < 2; ++k) {
-                const U4 rr = sr_block((idx0 >> 3) + k, p.step, 0u, p.seed_lo, p.seed_hi);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) b[8 * k + j] = f32_to_bf16_sr(w[8 * k + j], sr_lane(rr, j));
-              }
-            } else {
-#pragma unroll
-              for (int j = 0; j < 16; ++j) b[j] = f32_to_bf16_rne(w[j]);
-            }
-            st16_bf16(sw, r, h, b);
+            uint4 b;
+            const uint64_t idx8 =
+                (static_cast<uint64_t>(row) * static_cast<uint64_t>(p.d_in) + (tn * BN + c * C::CW + h * 8)) >> 3;
+            to_bf16x8(w, p.sr_w != 0, idx8, 0u, p, b);
+            st8_bf16(sw, r, h, b);
           }
-          st16_codes(smc, r, h, cm);
-          if constexpr (C::TWO) st16_codes(svc, r, h, cv);
+          st8_codes(smc, r, h, cm);
+          if constexpr (C::TWO) st8_codes(svc, r, h, cv);
           fence_proxy_async_smem();
           mbar_arrive(&st_written[s]);
         }

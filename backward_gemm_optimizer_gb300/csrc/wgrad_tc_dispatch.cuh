@@ -8,8 +8,8 @@
 namespace forge {
 
 // Shared memory available to the dynamic ring after the kernel's static
-// shared memory (barriers + the 4 KB absmax exchange) is accounted for.
-constexpr int kDynSmemBudget = 227 * 1024 - 5 * 1024;
+// shared memory (barriers + the 8 KB absmax exchange) is accounted for.
+constexpr int kDynSmemBudget = 227 * 1024 - 9 * 1024;
 
 template <int OPT, int WK, int MK, int BN, int STAGES>
 constexpr int slots_that_fit() {

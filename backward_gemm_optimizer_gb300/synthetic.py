@@ -212,3 +212,20 @@ def step_inputs(d_out: int, d_in: int, bt: int, seed: int, step: int, x_dtype: s
     X = normal((bt, d_in), 1.0, seed * 1000003 + step, STREAM_X, x_dtype)
     dY = normal((bt, d_out), 1.0, seed * 1000003 + step, STREAM_DY, x_dtype)
     return X, dY
+
+
+def device_normal_(t: torch.Tensor, std: float, seed: int, stream_id: int, absolute: bool = False) -> torch.Tensor:
+    """Fill a device tensor with N(0, std) (or |N(0, std)|) from torch's seeded
+    device generator keyed on (seed, stream_id). Used where host generation
+    would be too slow (the 7-billion-parameter linear stack)."""
+    g = torch.Generator(device=t.device)
+    g.manual_seed(int(seed) * 1000003 + int(stream_id))
+    if t.dtype == torch.float32:
+        t.normal_(0.0, std, generator=g)
+    else:
+        tmp = torch.empty(t.shape, dtype=torch.float32, device=t.device)
+        tmp.normal_(0.0, std, generator=g)
+        t.copy_(tmp)
+    if absolute:
+        t.abs_()
+    return t

@@ -40,6 +40,11 @@ WORKLOADS = {
     "llama31_8b_up_proj_bt512_q8state": (14336, 4096, 512, "f32", "q8"),
 }
 DEFAULT = "llama31_8b_up_proj_bt512_f32state"
+# The full Llama-3.1-8B linear stack (32 layers x 7 linears, BT = 512).
+STACKS = {f"llama31_8b_stack_{o}_{st}": (o, st) for o in ("adamw", "lion", "sgdm") for st in ("f32state", "bf16state")}
+STACK_HYPER = {"adamw": dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01),
+               "lion": dict(lr=3e-6, beta1=0.9, beta2=0.99, eps=0.0, weight_decay=1.0),
+               "sgdm": dict(lr=2e-5, beta1=0.9, beta2=0.0, eps=0.0, weight_decay=1e-2)}
 HYPER = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01)
 
 
@@ -361,13 +366,172 @@ def run_gpu(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+def run_stack(args, rank, world, local_rank):
+    """One step = backward over the 224 linears of Llama-3.1-8B (layer 31 .. 0,
+    down, up, gate, o, v, k, q): forge_dgrad then the fused step, per linear."""
+    import torch
+    import backward_gemm_optimizer_gb300 as F
+    from backward_gemm_optimizer_gb300 import synthetic as S
+
+    opt, stname = STACKS[args.workload]
+    wdt = torch.float32 if stname == "f32state" else torch.bfloat16
+    mdt = wdt
+    two = opt == "adamw"
+    bt = 512
+    dev = torch.device(f"cuda:{local_rank}")
+    torch.cuda.set_device(dev)
+    hp = STACK_HYPER[opt]
+    order = [x for x in reversed(S.LLAMA31_8B_LINEARS)]
+    layers = []
+    sid = 0
+    for layer in range(S.LLAMA31_8B_LAYERS):
+        lin = {}
+        for name, d_out, d_in in order:
+            sid += 1
+            L = {"name": name, "d_out": d_out, "d_in": d_in}
+            L["W"] = S.device_normal_(torch.empty((d_out, d_in), dtype=wdt, device=dev), 0.02, replica_seed(rank), 16 * sid)
+            L["m"] = S.device_normal_(torch.empty((d_out, d_in), dtype=mdt, device=dev), 1e-3, replica_seed(rank), 16 * sid + 1)
+            if two:
+                L["v"] = S.device_normal_(torch.empty((d_out, d_in), dtype=mdt, device=dev), 1e-6, replica_seed(rank),
+                                          16 * sid + 2, absolute=True)
+            L["X"] = S.device_normal_(torch.empty((bt, d_in), dtype=torch.bfloat16, device=dev), 1.0, replica_seed(rank),
+                                      16 * sid + 3)
+            L["dY"] = S.device_normal_(torch.empty((bt, d_out), dtype=torch.bfloat16, device=dev), 1.0,
+                                       replica_seed(rank), 16 * sid + 4)
+            lin[name] = L
+        layers.append(lin)
+    dX = {d_in: torch.empty((bt, d_in), dtype=torch.bfloat16, device=dev) for _, _, d_in in order}
+    stream = torch.cuda.current_stream(dev)
+    sr = stname == "bf16state"
+
+    def stack_step(t, events=None):
+        i = 0
+        for layer in reversed(range(len(layers))):
+            for name, _, _ in order:
+                L = layers[layer][name]
+                if events is not None:
+                    events[i][0].record(stream)
+                F.dgrad(L["dY"], L["W"], dX[L["d_in"]], stream=stream)
+                if events is not None:
+                    events[i][1].record(stream)
+                launch_step_only(L, t)
+                if events is not None:
+                    events[i][2].record(stream)
+                i += 1
+
+    def launch_step_only(L, t):
+        if opt == "adamw":
+            F.wgrad_step_adamw(L["X"], L["dY"], L["W"], L["m"], L["v"], step=t, seed=1234, sr_w=sr, stream=stream, **hp)
+        elif opt == "lion":
+            F.wgrad_step_lion(L["X"], L["dY"], L["W"], L["m"], lr=hp["lr"], beta1=hp["beta1"], beta2=hp["beta2"],
+                              weight_decay=hp["weight_decay"], step=t, seed=1234, sr_w=sr, stream=stream)
+        else:
+            F.wgrad_step_sgdm(L["X"], L["dY"], L["W"], L["m"], lr=hp["lr"], momentum=hp["beta1"],
+                              weight_decay=hp["weight_decay"], step=t, seed=1234, sr_w=sr, stream=stream)
+
+    t = 1
+    for _ in range(args.warmup):
+        stack_step(t); t += 1
+    F.sync_status(stream)
+    n_lin = len(layers) * len(order)
+    K = args.steps
+    # per-linear events for one instrumented pass (per-shape breakdown)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_lin)]
+    torch.cuda.synchronize(dev)
+    stack_step(t, ev); t += 1
+    torch.cuda.synchronize(dev)
+    per_shape = {}
+    i = 0
+    for layer in reversed(range(len(layers))):
+        for name, d_out, d_in in order:
+            a = per_shape.setdefault(name, {"d_out": d_out, "d_in": d_in, "dgrad_us": 0.0, "step_us": 0.0, "n": 0})
+            a["dgrad_us"] += ev[i][0].elapsed_time(ev[i][1]) * 1000.0
+            a["step_us"] += ev[i][1].elapsed_time(ev[i][2]) * 1000.0
+            a["n"] += 1
+            i += 1
+    hbm, tflops, _ = load_peaks()
+    for name, a in per_shape.items():
+        a["dgrad_us"] = round(a["dgrad_us"] / a["n"], 2)
+        a["step_us"] = round(a["step_us"] / a["n"], 2)
+        eb = 4 if stname == "f32state" else 2
+        sb = 2 * eb * (3 if two else 2)     # W and each moment read + written once
+        ab = a["d_out"] * a["d_in"] * sb + 2 * bt * (a["d_out"] + a["d_in"])
+        a["step_GBps"] = round(ab / (a["step_us"] * 1e-6) / 1e9, 1)
+        a["step_frac_of_hbm"] = round(a["step_GBps"] / hbm, 4)
+    # timed: plain launches, then the same step replayed as a CUDA graph
+    sampler = ClockSampler(local_rank)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    time.sleep(0.2)
+    e0.record(stream)
+    for _ in range(K):
+        stack_step(t); t += 1
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    F.sync_status(stream)
+    eager_ms = max_over_ranks(e0.elapsed_time(e1) / K, world, dev)
+    graph_ms = None
+    if args.graph:
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        # capture on a side stream: the library launches on the stream it is given
+        tg = t
+        with torch.cuda.graph(g, stream=side):
+            cap = torch.cuda.current_stream(dev)
+            for layer in reversed(range(len(layers))):
+                for name, _, _ in order:
+                    L = layers[layer][name]
+                    F.dgrad(L["dY"], L["W"], dX[L["d_in"]], stream=cap)
+                    if opt == "adamw":
+                        F.wgrad_step_adamw(L["X"], L["dY"], L["W"], L["m"], L["v"], step=tg, seed=1234, sr_w=sr,
+                                           stream=cap, **hp)
+                    elif opt == "lion":
+                        F.wgrad_step_lion(L["X"], L["dY"], L["W"], L["m"], lr=hp["lr"], beta1=hp["beta1"],
+                                          beta2=hp["beta2"], weight_decay=hp["weight_decay"], step=tg, seed=1234,
+                                          sr_w=sr, stream=cap)
+                    else:
+                        F.wgrad_step_sgdm(L["X"], L["dY"], L["W"], L["m"], lr=hp["lr"], momentum=hp["beta1"],
+                                          weight_decay=hp["weight_decay"], step=tg, seed=1234, sr_w=sr, stream=cap)
+        torch.cuda.synchronize(dev)
+        g.replay(); torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(K):
+            g.replay()     # the same step index each replay (graph parameters are fixed)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        F.sync_status(stream)
+        graph_ms = max_over_ranks(e0.elapsed_time(e1) / K, world, dev)
+    if rank != 0:
+        return
+    params = sum(a["d_out"] * a["d_in"] * a["n"] for a in per_shape.values())
+    step_total_us = sum(a["step_us"] * a["n"] for a in per_shape.values())
+    dgrad_total_us = sum(a["dgrad_us"] * a["n"] for a in per_shape.values())
+    line = {
+        "metric": METRIC, "value": round(eager_ms * 1000.0, 1), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(eager_ms, 3), "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "linears": n_lin, "params": params, "bt": bt, "optimizer": opt,
+                   "state": stname, "step": "224 x (forge_dgrad + fused step), layer 31..0",
+                   "l2": "state 84 GB (fp32) / 42 GB (bf16) >> L2"},
+        "graph_ms_per_step": round(graph_ms, 3) if graph_ms is not None else None,
+        "fused_steps_us_total": round(step_total_us, 1), "dgrads_us_total": round(dgrad_total_us, 1),
+        "per_shape": per_shape, "gpu_launches": 2 * n_lin * K, "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="forge", choices=["forge", "reference"])
-    ap.add_argument("--workload", default=DEFAULT, choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default=DEFAULT, choices=sorted(WORKLOADS) + sorted(STACKS))
+    ap.add_argument("--graph", action="store_true", help="stack workloads: also replay the step as a CUDA graph")
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--cpu-rows", type=int, default=14336)
     ap.add_argument("--cpu-min-s", type=float, default=10.0)
@@ -387,7 +551,10 @@ def main():
         torch.cuda.set_device(local_rank)
         torch.distributed.init_process_group("nccl")
     try:
-        run_gpu(args, rank, world, local_rank)
+        if args.workload in STACKS:
+            run_stack(args, rank, world, local_rank)
+        else:
+            run_gpu(args, rank, world, local_rank)
     finally:
         if world > 1:
             import torch

@@ -51,7 +51,9 @@ design notes of this library):
   u = sqrt(v), s = absmax(u) / 255, code = clamp(rint(u / s), 1, 255)
   for v != 0 and 0 for v == 0; an all-zero block has scale 0. The stored
   scale is s. Dequantisation: m = code * s, v = (code * s)^2. The code
-  decisions are taken in float32, the kernel's precision.
+  decisions are taken in float32, the kernel's precision, with x / s
+  evaluated as x * fl(1/s) (one correctly rounded reciprocal per block);
+* a NaN stored as bf16 with round-to-nearest-even becomes 0x7FFF.
 """
 
 from __future__ import annotations
@@ -227,14 +229,14 @@ def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
 
 
 def f32_to_bf16_rne(x) -> np.ndarray:
-    """float32 -> bf16 bits, round to nearest, ties to even; NaN -> quiet NaN."""
+    """float32 -> bf16 bits, round to nearest, ties to even; NaN -> 0x7FFF."""
     x = np.ascontiguousarray(x, dtype=np.float32)
     b = x.view(np.uint32).astype(np.uint64)
     lsb = (b >> np.uint64(16)) & np.uint64(1)
     r = ((b + np.uint64(0x7FFF) + lsb) >> np.uint64(16)) & np.uint64(0xFFFF)
     nan = np.isnan(x)
     if nan.any():
-        r[nan] = ((b[nan] >> np.uint64(16)) | np.uint64(0x0040)) & np.uint64(0xFFFF)
+        r[nan] = np.uint64(0x7FFF)
     return r.astype(np.uint16)
 
 
@@ -270,7 +272,7 @@ def f64_to_bf16_rne(x) -> np.ndarray:
     sign = np.where(np.signbit(flat_x), np.uint32(0x8000), np.uint32(0))
     res = (mag | sign).astype(np.uint32)
     nan = np.isnan(flat_x)
-    res[nan] = np.uint32(0x7FC0)
+    res[nan] = np.uint32(0x7FFF)
     inf = np.isinf(flat_x)
     res[inf] = np.where(np.signbit(flat_x[inf]), np.uint32(0xFF80), np.uint32(0x7F80))
     flat_o[:] = res.astype(np.uint16)
@@ -375,18 +377,24 @@ def _blocks(a: np.ndarray) -> np.ndarray:
     return a.reshape(rows, cols // QBLOCK, QBLOCK)
 
 
+def _inv(s: np.ndarray) -> np.ndarray:
+    """1/s correctly rounded in float32 (1 where s == 0; those blocks are all zero)."""
+    safe = np.where(s > 0, s, F32(1.0)).astype(np.float32)
+    return (F32(1.0) / safe).astype(np.float32)
+
+
 def quant_m(m1) -> Tuple[np.ndarray, np.ndarray]:
     """First moment -> (int8 codes [rows, cols], scales [cols/128, rows]).
 
-    s = absmax / 127 (float32 division); code = clamp(rint(m / s), -127, 127);
-    a nonzero m whose code rounds to 0 gets sign(m); all-zero block: s = 0.
+    s = absmax / 127 (float32 division); code = clamp(rint(m * (1/s)), -127, 127)
+    with the float32 reciprocal 1/s taken once per block; a nonzero m whose
+    code rounds to 0 gets sign(m); all-zero block: s = 0.
     """
     m1 = _f32(m1)
     b = _blocks(m1)
     amax = np.max(np.abs(b), axis=2)                    # [rows, nb] f32
     s = (amax / F32(127.0)).astype(np.float32)
-    safe = np.where(s > 0, s, F32(1.0)).astype(np.float32)
-    q = np.rint(b / safe[:, :, None])
+    q = np.rint((b * _inv(s)[:, :, None]).astype(np.float32))
     q = np.clip(q, -127, 127)
     bump = (b != 0) & (q == 0)
     q = np.where(bump, np.sign(b), q)
@@ -399,7 +407,7 @@ def quant_v(v1) -> Tuple[np.ndarray, np.ndarray]:
     """Second moment -> (uint8 codes of sqrt(v), scales [cols/128, rows]).
 
     u = sqrt(v) (float32); s = absmax(u) / 255; code = 0 for v == 0 and
-    clamp(rint(u / s), 1, 255) otherwise (zero code only for exact zero,
+    clamp(rint(u * (1/s)), 1, 255) otherwise (zero code only for exact zero,
     which floors a nonzero v away from zero).
     """
     v1 = _f32(v1)
@@ -407,8 +415,7 @@ def quant_v(v1) -> Tuple[np.ndarray, np.ndarray]:
     b = _blocks(u)
     amax = np.max(b, axis=2)
     s = (amax / F32(255.0)).astype(np.float32)
-    safe = np.where(s > 0, s, F32(1.0)).astype(np.float32)
-    q = np.clip(np.rint(b / safe[:, :, None]), 1, 255)
+    q = np.clip(np.rint((b * _inv(s)[:, :, None]).astype(np.float32)), 1, 255)
     q = np.where(_blocks(v1) == 0, 0, q)
     q = np.where((s > 0)[:, :, None], q, 0)
     codes = q.astype(np.uint8).reshape(v1.shape)

@@ -274,7 +274,8 @@ def test_forced_device_timeout_reports_and_leaves_state():
 
 @pytest.mark.parametrize("w_dtype", ["bf16", "f32"])
 @pytest.mark.parametrize("dx_dtype", ["bf16", "f32"])
-@pytest.mark.parametrize("shape", [(256, 384, 200), (136, 200, 70), (1024, 512, 512)])
+@pytest.mark.parametrize("shape", [(256, 384, 200), (136, 200, 70), (1024, 512, 512), (2048, 1024, 64),
+                                   (1024, 512, 640)])
 def test_dgrad_exact(w_dtype, dx_dtype, shape):
     d_out, d_in, bt = shape
     dev = "cuda:0"
@@ -308,7 +309,7 @@ def test_dgrad_random_reads_pre_update_weights():
     assert np.all(np.abs(dX.cpu().numpy() - ref) <= tol)
 
 
-@pytest.mark.parametrize("shape", [(4096, 512, 256), (14336, 4096, 512), (2048, 4096, 512)])
+@pytest.mark.parametrize("shape", [(4096, 512, 256), (14336, 4096, 512), (2048, 4096, 512), (4096, 14336, 512)])
 def test_dgrad_f32_and_bf16_weights_agree_bit_for_bit(shape):
     # fp32 master weights that are bf16-representable must give exactly the
     # dX of the same weights stored as bf16 (the staging conversion is exact),
