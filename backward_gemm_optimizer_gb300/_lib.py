@@ -25,6 +25,8 @@ STATUS_NAMES = {0: "FORGE_OK", 1: "FORGE_ERR_INVALID_ARG", 2: "FORGE_ERR_UNSUPPO
                 3: "FORGE_ERR_ALIGNMENT", 4: "FORGE_ERR_CUDA", 5: "FORGE_ERR_TIMEOUT"}
 
 EXPORTED = ("forge_wgrad_step_adamw", "forge_wgrad_step_sgdm", "forge_wgrad_step_lion",
+            "forge_wgrad_step_sgd", "forge_wgrad_step_rmsprop", "forge_wgrad_step_adagrad",
+            "forge_wgrad_step_nadam", "forge_wgrad_step_radam",
             "forge_dgrad", "forge_sync_status", "forge_last_error", "forge_version",
             "forge_workspace_bytes")
 
@@ -37,7 +39,8 @@ class ForgeTensor(ctypes.Structure):
 class ForgeHyper(ctypes.Structure):
     _fields_ = [("lr", ctypes.c_double), ("beta1", ctypes.c_double), ("beta2", ctypes.c_double),
                 ("eps", ctypes.c_double), ("weight_decay", ctypes.c_double),
-                ("sr_w", ctypes.c_int32), ("sr_moments", ctypes.c_int32), ("flags", ctypes.c_uint32)]
+                ("sr_w", ctypes.c_int32), ("sr_moments", ctypes.c_int32), ("flags", ctypes.c_uint32),
+                ("momentum_decay", ctypes.c_double)]
 
 
 class ForgeError(RuntimeError):
@@ -58,10 +61,16 @@ def _load() -> ctypes.CDLL:
     lib.forge_wgrad_step_adamw.argtypes = [P(T), P(T), P(T), P(T), P(T), P(H), i64, u64, vp]
     lib.forge_wgrad_step_sgdm.argtypes = [P(T), P(T), P(T), P(T), P(H), i64, u64, vp]
     lib.forge_wgrad_step_lion.argtypes = [P(T), P(T), P(T), P(T), P(H), i64, u64, vp]
+    lib.forge_wgrad_step_sgd.argtypes = [P(T), P(T), P(T), P(H), i64, u64, vp]
+    lib.forge_wgrad_step_rmsprop.argtypes = [P(T), P(T), P(T), P(T), P(H), i64, u64, vp]
+    lib.forge_wgrad_step_adagrad.argtypes = [P(T), P(T), P(T), P(T), P(H), i64, u64, vp]
+    lib.forge_wgrad_step_nadam.argtypes = [P(T), P(T), P(T), P(T), P(T), P(H), i64, u64, vp]
+    lib.forge_wgrad_step_radam.argtypes = [P(T), P(T), P(T), P(T), P(T), P(H), i64, u64, vp]
     lib.forge_dgrad.argtypes = [P(T), P(T), P(T), vp]
     lib.forge_sync_status.argtypes = [vp]
     for f in ("forge_wgrad_step_adamw", "forge_wgrad_step_sgdm", "forge_wgrad_step_lion",
-              "forge_dgrad", "forge_sync_status"):
+              "forge_wgrad_step_sgd", "forge_wgrad_step_rmsprop", "forge_wgrad_step_adagrad",
+              "forge_wgrad_step_nadam", "forge_wgrad_step_radam", "forge_dgrad", "forge_sync_status"):
         getattr(lib, f).restype = ctypes.c_int
     lib.forge_last_error.restype = ctypes.c_char_p
     lib.forge_version.restype = ctypes.c_char_p
@@ -117,9 +126,9 @@ def _stream(stream) -> ctypes.c_void_p:
     return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
 
 
-def _hyper(lr, beta1, beta2, eps, weight_decay, sr_w, sr_moments, flags) -> ForgeHyper:
+def _hyper(lr, beta1, beta2, eps, weight_decay, sr_w, sr_moments, flags, momentum_decay=0.0) -> ForgeHyper:
     return ForgeHyper(float(lr), float(beta1), float(beta2), float(eps), float(weight_decay),
-                      int(bool(sr_w)), int(bool(sr_moments)), int(flags))
+                      int(bool(sr_w)), int(bool(sr_moments)), int(flags), float(momentum_decay))
 
 
 def wgrad_step_adamw(X, dY, W, m, v, *, lr, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0,
@@ -152,6 +161,54 @@ def wgrad_step_lion(X, dY, W, m, *, lr, beta1=0.9, beta2=0.99, weight_decay=0.0,
     _check(lib().forge_wgrad_step_lion(ctypes.byref(tX), ctypes.byref(tdY), ctypes.byref(tW),
                                        ctypes.byref(tm), ctypes.byref(h), int(step),
                                        int(seed) & 0xFFFFFFFFFFFFFFFF, _stream(stream)))
+
+
+def _seed(seed):
+    return int(seed) & 0xFFFFFFFFFFFFFFFF
+
+
+def wgrad_step_sgd(X, dY, W, *, lr, weight_decay=0.0, step, seed=0, sr_w=False, flags=0, stream=None):
+    """Fused G = dY^T X and plain SGD step on W in place (forge_wgrad_step_sgd)."""
+    tX, tdY, tW = tensor_desc(X), tensor_desc(dY), tensor_desc(W)
+    h = _hyper(lr, 0.0, 0.0, 0.0, weight_decay, sr_w, False, flags)
+    _check(lib().forge_wgrad_step_sgd(ctypes.byref(tX), ctypes.byref(tdY), ctypes.byref(tW), ctypes.byref(h),
+                                      int(step), _seed(seed), _stream(stream)))
+
+
+def wgrad_step_rmsprop(X, dY, W, v, *, lr, alpha=0.99, eps=1e-8, weight_decay=0.0, step, seed=0, sr_w=False,
+                       sr_moments=False, flags=0, stream=None):
+    """Fused G = dY^T X and RMSprop step on W, v in place (forge_wgrad_step_rmsprop)."""
+    tX, tdY, tW, tv = tensor_desc(X), tensor_desc(dY), tensor_desc(W), tensor_desc(v)
+    h = _hyper(lr, 0.0, alpha, eps, weight_decay, sr_w, sr_moments, flags)
+    _check(lib().forge_wgrad_step_rmsprop(ctypes.byref(tX), ctypes.byref(tdY), ctypes.byref(tW), ctypes.byref(tv),
+                                          ctypes.byref(h), int(step), _seed(seed), _stream(stream)))
+
+
+def wgrad_step_adagrad(X, dY, W, v, *, lr, eps=1e-10, weight_decay=0.0, step, seed=0, sr_w=False,
+                       sr_moments=False, flags=0, stream=None):
+    """Fused G = dY^T X and AdaGrad step on W, v in place (forge_wgrad_step_adagrad)."""
+    tX, tdY, tW, tv = tensor_desc(X), tensor_desc(dY), tensor_desc(W), tensor_desc(v)
+    h = _hyper(lr, 0.0, 0.0, eps, weight_decay, sr_w, sr_moments, flags)
+    _check(lib().forge_wgrad_step_adagrad(ctypes.byref(tX), ctypes.byref(tdY), ctypes.byref(tW), ctypes.byref(tv),
+                                          ctypes.byref(h), int(step), _seed(seed), _stream(stream)))
+
+
+def wgrad_step_nadam(X, dY, W, m, v, *, lr, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0,
+                     momentum_decay=4e-3, step, seed=0, sr_w=False, sr_moments=False, flags=0, stream=None):
+    """Fused G = dY^T X and NAdam step on W, m, v in place (forge_wgrad_step_nadam)."""
+    tX, tdY, tW, tm, tv = tensor_desc(X), tensor_desc(dY), tensor_desc(W), tensor_desc(m), tensor_desc(v)
+    h = _hyper(lr, beta1, beta2, eps, weight_decay, sr_w, sr_moments, flags, momentum_decay)
+    _check(lib().forge_wgrad_step_nadam(ctypes.byref(tX), ctypes.byref(tdY), ctypes.byref(tW), ctypes.byref(tm),
+                                        ctypes.byref(tv), ctypes.byref(h), int(step), _seed(seed), _stream(stream)))
+
+
+def wgrad_step_radam(X, dY, W, m, v, *, lr, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0, step, seed=0,
+                     sr_w=False, sr_moments=False, flags=0, stream=None):
+    """Fused G = dY^T X and RAdam step on W, m, v in place (forge_wgrad_step_radam)."""
+    tX, tdY, tW, tm, tv = tensor_desc(X), tensor_desc(dY), tensor_desc(W), tensor_desc(m), tensor_desc(v)
+    h = _hyper(lr, beta1, beta2, eps, weight_decay, sr_w, sr_moments, flags)
+    _check(lib().forge_wgrad_step_radam(ctypes.byref(tX), ctypes.byref(tdY), ctypes.byref(tW), ctypes.byref(tm),
+                                        ctypes.byref(tv), ctypes.byref(h), int(step), _seed(seed), _stream(stream)))
 
 
 def dgrad(dY, W_old, dX, *, stream=None):

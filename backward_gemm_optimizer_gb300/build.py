@@ -25,6 +25,11 @@ SOURCES = [
     "wgrad_tc_adamw.cu",
     "wgrad_tc_sgdm.cu",
     "wgrad_tc_lion.cu",
+    "wgrad_tc_sgd.cu",
+    "wgrad_tc_rmsprop.cu",
+    "wgrad_tc_adagrad.cu",
+    "wgrad_tc_nadam.cu",
+    "wgrad_tc_radam.cu",
     "wgrad_simt.cu",
     "dgrad_tc.cu",
 ]

@@ -161,6 +161,20 @@ forge_status encode_state(CUtensorMap* map, const forge_tensor* t, const char* n
 
 // ------------------------------------------------------------------ scalars
 
+// NAdam's momentum schedule mu_i = b1 (1 - 0.5 * 0.96^(i psi)) and its running
+// product prod_{i<=t} mu_i. The product is extended from the last value this
+// thread computed when the step advances (O(1) per step in a training loop).
+double nadam_mu(double b1, double psi, double i) { return b1 * (1.0 - 0.5 * std::pow(0.96, i * psi)); }
+
+double nadam_mu_product(double b1, double psi, int64_t t) {
+  thread_local double c_b1 = -1.0, c_psi = -1.0, c_prod = 1.0;
+  thread_local int64_t c_t = 0;
+  if (c_b1 != b1 || c_psi != psi || t < c_t) { c_b1 = b1; c_psi = psi; c_t = 0; c_prod = 1.0; }
+  for (int64_t i = c_t + 1; i <= t; ++i) c_prod *= nadam_mu(b1, psi, static_cast<double>(i));
+  c_t = t;
+  return c_prod;
+}
+
 StepScalars fold(int opt, const forge_hyper* h, int64_t t) {
   StepScalars s{};
   const double td = static_cast<double>(t);
@@ -171,14 +185,46 @@ StepScalars fold(int opt, const forge_hyper* h, int64_t t) {
   s.decay = static_cast<float>(1.0 - h->lr * h->weight_decay);
   s.eps = static_cast<float>(h->eps);
   s.wd = static_cast<float>(h->weight_decay);
+  s.step_size = static_cast<float>(h->lr);
+  s.inv_sqrt_bc2 = 1.0f;
+  s.c2 = 0.0f;
+  s.rect = 0;
+  const double bc1 = 1.0 - std::pow(h->beta1, td), bc2 = 1.0 - std::pow(h->beta2, td);
   if (opt == OPT_ADAMW) {
-    s.step_size = static_cast<float>(h->lr / (1.0 - std::pow(h->beta1, td)));
-    s.inv_sqrt_bc2 = static_cast<float>(1.0 / std::sqrt(1.0 - std::pow(h->beta2, td)));
-  } else {
-    s.step_size = static_cast<float>(h->lr);
-    s.inv_sqrt_bc2 = 1.0f;
+    s.step_size = static_cast<float>(h->lr / bc1);
+    s.inv_sqrt_bc2 = static_cast<float>(1.0 / std::sqrt(bc2));
+  } else if (opt == OPT_NADAM) {
+    const double mu_t = nadam_mu(h->beta1, h->momentum_decay, td);
+    const double mu_n = nadam_mu(h->beta1, h->momentum_decay, td + 1.0);
+    const double prod = nadam_mu_product(h->beta1, h->momentum_decay, t);
+    s.step_size = static_cast<float>(h->lr * (1.0 - mu_t) / (1.0 - prod));
+    s.c2 = static_cast<float>(h->lr * mu_n / (1.0 - prod * mu_n));
+    s.inv_sqrt_bc2 = static_cast<float>(1.0 / std::sqrt(bc2));
+  } else if (opt == OPT_RADAM) {
+    const double rho_inf = 2.0 / (1.0 - h->beta2) - 1.0;
+    const double rho_t = rho_inf - 2.0 * td * std::pow(h->beta2, td) / bc2;
+    if (rho_t > 5.0) {
+      const double r = std::sqrt((rho_t - 4.0) * (rho_t - 2.0) * rho_inf / ((rho_inf - 4.0) * (rho_inf - 2.0) * rho_t));
+      s.rect = 1;
+      s.step_size = static_cast<float>(h->lr * r * std::sqrt(bc2) / bc1);
+    } else {
+      s.step_size = static_cast<float>(h->lr / bc1);
+    }
   }
   return s;
+}
+
+const char* opt_name(int opt) {
+  switch (opt) {
+    case OPT_ADAMW: return "adamw";
+    case OPT_SGDM: return "sgdm";
+    case OPT_LION: return "lion";
+    case OPT_SGD: return "sgd";
+    case OPT_RMSPROP: return "rmsprop";
+    case OPT_ADAGRAD: return "adagrad";
+    case OPT_NADAM: return "nadam";
+    default: return "radam";
+  }
 }
 
 int mkind(int dt) { return dt == FORGE_F32 ? M_F32 : dt == FORGE_BF16 ? M_BF16 : M_Q8; }
@@ -189,16 +235,22 @@ constexpr uint64_t kTimeoutNs = 4000000000ull;  // 4 s: far beyond any healthy w
 
 forge_status wgrad_step(int opt, const forge_tensor* X, const forge_tensor* dY, forge_tensor* W, forge_tensor* m,
                         forge_tensor* v, const forge_hyper* h, int64_t step, uint64_t seed, forge_stream_t stream) {
-  const char* oname = opt == OPT_ADAMW ? "adamw" : opt == OPT_SGDM ? "sgdm" : "lion";
-  if (X == nullptr || dY == nullptr || W == nullptr || m == nullptr || h == nullptr)
+  const char* oname = opt_name(opt);
+  const int nst = opt_nstate(opt);
+  if (X == nullptr || dY == nullptr || W == nullptr || h == nullptr || (nst >= 1 && m == nullptr))
     return fail(FORGE_ERR_INVALID_ARG, "%s: null argument", oname);
-  if (opt == OPT_ADAMW && v == nullptr) return fail(FORGE_ERR_INVALID_ARG, "adamw: null v");
+  if (nst == 2 && v == nullptr) return fail(FORGE_ERR_INVALID_ARG, "%s: null v", oname);
+  const bool two_betas = opt == OPT_ADAMW || opt == OPT_NADAM || opt == OPT_RADAM;
+  if (two_betas && (h->beta1 >= 1.0 || h->beta2 >= 1.0 || h->beta1 < 0.0 || h->beta2 < 0.0))
+    return fail(FORGE_ERR_INVALID_ARG, "%s: betas must lie in [0, 1)", oname);
+  if (opt == OPT_RMSPROP && (h->beta2 >= 1.0 || h->beta2 < 0.0))
+    return fail(FORGE_ERR_INVALID_ARG, "rmsprop: alpha (beta2) must lie in [0, 1)");
+  if (opt == OPT_NADAM && !std::isfinite(h->momentum_decay))
+    return fail(FORGE_ERR_INVALID_ARG, "nadam: non-finite momentum_decay");
   if (step < 1) return fail(FORGE_ERR_INVALID_ARG, "%s: step must be >= 1 (got %lld)", oname, (long long)step);
   if (step > 0xFFFFFFFFll) return fail(FORGE_ERR_INVALID_ARG, "%s: step exceeds 2^32 - 1", oname);
   if (!finite(h->lr) || !finite(h->beta1) || !finite(h->beta2) || !finite(h->eps) || !finite(h->weight_decay))
     return fail(FORGE_ERR_INVALID_ARG, "%s: non-finite hyper-parameter", oname);
-  if (opt == OPT_ADAMW && (h->beta1 >= 1.0 || h->beta2 >= 1.0 || h->beta1 < 0.0 || h->beta2 < 0.0))
-    return fail(FORGE_ERR_INVALID_ARG, "adamw: betas must lie in [0, 1)");
   if (h->flags & ~(FORGE_FLAG_TILE_N_MASK | FORGE_FLAG_TEST_FORCE_TIMEOUT))
     return fail(FORGE_ERR_INVALID_ARG, "%s: unknown flags 0x%x", oname, h->flags);
 
@@ -212,21 +264,24 @@ forge_status wgrad_step(int opt, const forge_tensor* X, const forge_tensor* dY, 
   if ((st = check_tensor(X, "X", bt, d_in, true)) != FORGE_OK) return st;
   if ((st = check_tensor(dY, "dY", bt, d_out, true)) != FORGE_OK) return st;
   if ((st = check_tensor(W, "W", d_out, d_in, true)) != FORGE_OK) return st;
-  if ((st = check_tensor(m, "m", d_out, d_in, true)) != FORGE_OK) return st;
-  if (opt == OPT_ADAMW && (st = check_tensor(v, "v", d_out, d_in, true)) != FORGE_OK) return st;
+  if (nst >= 1 && (st = check_tensor(m, nst == 2 ? "m" : "state", d_out, d_in, true)) != FORGE_OK) return st;
+  if (nst == 2 && (st = check_tensor(v, "v", d_out, d_in, true)) != FORGE_OK) return st;
   if (W->dtype == FORGE_I8B128) return fail(FORGE_ERR_UNSUPPORTED, "%s: W must be f32 or bf16", oname);
-  if (opt == OPT_ADAMW && v->dtype != m->dtype)
-    return fail(FORGE_ERR_UNSUPPORTED, "adamw: m and v must share a dtype (got %s, %s)", dtype_name(m->dtype),
+  if (nst == 2 && v->dtype != m->dtype)
+    return fail(FORGE_ERR_UNSUPPORTED, "%s: m and v must share a dtype (got %s, %s)", oname, dtype_name(m->dtype),
                 dtype_name(v->dtype));
+  const int mdt = nst >= 1 ? m->dtype : FORGE_F32;
+  if (mdt == FORGE_I8B128 && !(opt == OPT_ADAMW || opt == OPT_SGDM || opt == OPT_LION))
+    return fail(FORGE_ERR_UNSUPPORTED, "%s: 8-bit block state exists for adamw, sgdm and lion", oname);
   if (d_in % 8 != 0 || d_out % 8 != 0)
     return fail(FORGE_ERR_UNSUPPORTED, "%s: D_in (%lld) and D_out (%lld) must be multiples of 8", oname,
                 (long long)d_in, (long long)d_out);
-  if (m->dtype == FORGE_I8B128 && d_in % 128 != 0)
+  if (mdt == FORGE_I8B128 && d_in % 128 != 0)
     return fail(FORGE_ERR_UNSUPPORTED, "%s: 8-bit block moments need D_in %% 128 == 0 (got %lld)", oname,
                 (long long)d_in);
   if (h->sr_w && W->dtype != FORGE_BF16)
     return fail(FORGE_ERR_INVALID_ARG, "%s: sr_w requires bf16 W", oname);
-  if (h->sr_moments && m->dtype != FORGE_BF16)
+  if (h->sr_moments && mdt != FORGE_BF16)
     return fail(FORGE_ERR_INVALID_ARG, "%s: sr_moments requires bf16 moments", oname);
   if (bt > 0x7FFFFFFF || d_in > 0x7FFFFFFF || d_out > 0x7FFFFFFF)
     return fail(FORGE_ERR_INVALID_ARG, "%s: dimension exceeds 2^31 - 1", oname);
@@ -236,7 +291,7 @@ forge_status wgrad_step(int opt, const forge_tensor* X, const forge_tensor* dY, 
   if ((st = device_info(&dev)) != FORGE_OK) return st;
   const StepScalars sc = fold(opt, h, step);
   const int wk = W->dtype == FORGE_F32 ? W_F32 : W_BF16;
-  const int mk = mkind(m->dtype);
+  const int mk = mkind(mdt);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
   if (!tc) {
@@ -246,11 +301,11 @@ forge_status wgrad_step(int opt, const forge_tensor* X, const forge_tensor* dY, 
     p.X = static_cast<const float*>(X->data);
     p.dY = static_cast<const float*>(dY->data);
     p.W = W->data;
-    p.m = m->data;
-    p.v = opt == OPT_ADAMW ? v->data : nullptr;
-    p.m_scale = static_cast<float*>(m->scale);
-    p.v_scale = opt == OPT_ADAMW ? static_cast<float*>(v->scale) : nullptr;
-    p.ld_x = X->ld; p.ld_dy = dY->ld; p.ld_w = W->ld; p.ld_m = m->ld; p.ld_v = opt == OPT_ADAMW ? v->ld : 0;
+    p.m = nst >= 1 ? m->data : nullptr;
+    p.v = nst == 2 ? v->data : nullptr;
+    p.m_scale = nst >= 1 ? static_cast<float*>(m->scale) : nullptr;
+    p.v_scale = nst == 2 ? static_cast<float*>(v->scale) : nullptr;
+    p.ld_x = X->ld; p.ld_dy = dY->ld; p.ld_w = W->ld; p.ld_m = nst >= 1 ? m->ld : 0; p.ld_v = nst == 2 ? v->ld : 0;
     p.d_out = static_cast<int>(d_out); p.d_in = static_cast<int>(d_in); p.bt = static_cast<int>(bt);
     p.sc = sc;
     p.step = static_cast<uint32_t>(step);
@@ -285,15 +340,19 @@ forge_status wgrad_step(int opt, const forge_tensor* X, const forge_tensor* dY, 
       return st;
   }
   if ((st = encode_state(&p.tm_w, W, "W")) != FORGE_OK) return st;
-  if ((st = encode_state(&p.tm_m, m, "m")) != FORGE_OK) return st;
-  if (opt == OPT_ADAMW) {
+  if (nst >= 1) {
+    if ((st = encode_state(&p.tm_m, m, "m")) != FORGE_OK) return st;
+  } else {
+    p.tm_m = p.tm_w;  // unused
+  }
+  if (nst == 2) {
     if ((st = encode_state(&p.tm_v, v, "v")) != FORGE_OK) return st;
   } else {
     p.tm_v = p.tm_m;  // unused
   }
   p.sc = sc;
-  p.m_scale = static_cast<float*>(m->scale);
-  p.v_scale = opt == OPT_ADAMW ? static_cast<float*>(v->scale) : nullptr;
+  p.m_scale = nst >= 1 ? static_cast<float*>(m->scale) : nullptr;
+  p.v_scale = nst == 2 ? static_cast<float*>(v->scale) : nullptr;
   p.status = dev->status;
   p.d_out = static_cast<int>(d_out);
   p.d_in = static_cast<int>(d_in);
@@ -315,9 +374,17 @@ forge_status wgrad_step(int opt, const forge_tensor* X, const forge_tensor* dY, 
   l.opt = opt; l.wk = wk; l.mk = mk; l.bn = bn; l.deep = deep;
   l.grid = p.num_tiles < dev->sms ? p.num_tiles : dev->sms;
   l.stream = s;
-  cudaError_t e = opt == OPT_ADAMW ? launch_wgrad_tc_adamw(p, l)
-                  : opt == OPT_SGDM ? launch_wgrad_tc_sgdm(p, l)
-                                    : launch_wgrad_tc_lion(p, l);
+  cudaError_t e;
+  switch (opt) {
+    case OPT_ADAMW: e = launch_wgrad_tc_adamw(p, l); break;
+    case OPT_SGDM: e = launch_wgrad_tc_sgdm(p, l); break;
+    case OPT_LION: e = launch_wgrad_tc_lion(p, l); break;
+    case OPT_SGD: e = launch_wgrad_tc_sgd(p, l); break;
+    case OPT_RMSPROP: e = launch_wgrad_tc_rmsprop(p, l); break;
+    case OPT_ADAGRAD: e = launch_wgrad_tc_adagrad(p, l); break;
+    case OPT_NADAM: e = launch_wgrad_tc_nadam(p, l); break;
+    default: e = launch_wgrad_tc_radam(p, l); break;
+  }
   if (e != cudaSuccess) return fail(FORGE_ERR_CUDA, "%s launch: %s", oname, cudaGetErrorString(e));
   return ok();
 }
@@ -340,6 +407,33 @@ forge_status forge_wgrad_step_sgdm(const forge_tensor* X, const forge_tensor* dY
 forge_status forge_wgrad_step_lion(const forge_tensor* X, const forge_tensor* dY, forge_tensor* W, forge_tensor* m,
                                    const forge_hyper* h, int64_t step, uint64_t seed, forge_stream_t stream) {
   return wgrad_step(OPT_LION, X, dY, W, m, nullptr, h, step, seed, stream);
+}
+
+forge_status forge_wgrad_step_sgd(const forge_tensor* X, const forge_tensor* dY, forge_tensor* W,
+                                  const forge_hyper* h, int64_t step, uint64_t seed, forge_stream_t stream) {
+  return wgrad_step(OPT_SGD, X, dY, W, nullptr, nullptr, h, step, seed, stream);
+}
+
+forge_status forge_wgrad_step_rmsprop(const forge_tensor* X, const forge_tensor* dY, forge_tensor* W, forge_tensor* v,
+                                      const forge_hyper* h, int64_t step, uint64_t seed, forge_stream_t stream) {
+  return wgrad_step(OPT_RMSPROP, X, dY, W, v, nullptr, h, step, seed, stream);
+}
+
+forge_status forge_wgrad_step_adagrad(const forge_tensor* X, const forge_tensor* dY, forge_tensor* W, forge_tensor* v,
+                                      const forge_hyper* h, int64_t step, uint64_t seed, forge_stream_t stream) {
+  return wgrad_step(OPT_ADAGRAD, X, dY, W, v, nullptr, h, step, seed, stream);
+}
+
+forge_status forge_wgrad_step_nadam(const forge_tensor* X, const forge_tensor* dY, forge_tensor* W, forge_tensor* m,
+                                    forge_tensor* v, const forge_hyper* h, int64_t step, uint64_t seed,
+                                    forge_stream_t stream) {
+  return wgrad_step(OPT_NADAM, X, dY, W, m, v, h, step, seed, stream);
+}
+
+forge_status forge_wgrad_step_radam(const forge_tensor* X, const forge_tensor* dY, forge_tensor* W, forge_tensor* m,
+                                    forge_tensor* v, const forge_hyper* h, int64_t step, uint64_t seed,
+                                    forge_stream_t stream) {
+  return wgrad_step(OPT_RADAM, X, dY, W, m, v, h, step, seed, stream);
 }
 
 forge_status forge_dgrad(const forge_tensor* dY, const forge_tensor* W_old, forge_tensor* dX, forge_stream_t stream) {
@@ -432,7 +526,7 @@ forge_status forge_sync_status(forge_stream_t stream) {
 
 const char* forge_last_error(void) { return g_last_error.c_str(); }
 
-const char* forge_version(void) { return "0.1.0"; }
+const char* forge_version(void) { return "0.2.0"; }
 
 size_t forge_workspace_bytes(int64_t, int64_t, int64_t) { return 0; }
 

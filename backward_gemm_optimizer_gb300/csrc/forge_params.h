@@ -97,6 +97,11 @@ struct TcLaunch {
 cudaError_t launch_wgrad_tc_adamw(const WgradTcParams& p, const TcLaunch& l);
 cudaError_t launch_wgrad_tc_sgdm(const WgradTcParams& p, const TcLaunch& l);
 cudaError_t launch_wgrad_tc_lion(const WgradTcParams& p, const TcLaunch& l);
+cudaError_t launch_wgrad_tc_sgd(const WgradTcParams& p, const TcLaunch& l);
+cudaError_t launch_wgrad_tc_rmsprop(const WgradTcParams& p, const TcLaunch& l);
+cudaError_t launch_wgrad_tc_adagrad(const WgradTcParams& p, const TcLaunch& l);
+cudaError_t launch_wgrad_tc_nadam(const WgradTcParams& p, const TcLaunch& l);
+cudaError_t launch_wgrad_tc_radam(const WgradTcParams& p, const TcLaunch& l);
 cudaError_t launch_wgrad_simt(const WgradSimtParams& p, int opt, int wk, int mk, cudaStream_t stream);
 cudaError_t launch_dgrad_tc(const DgradParams& p, int grid, cudaStream_t stream);
 

@@ -37,7 +37,8 @@ template <int OPT, int WK, int MK>
 __global__ void __launch_bounds__(128) wgrad_step_simt_kernel(const WgradSimtParams p) {
   __shared__ float dys[TT][SR];
   __shared__ float red[2][4][SR];
-  constexpr bool TWO = (OPT == OPT_ADAMW);
+  constexpr int NST = opt_nstate(OPT);
+  constexpr bool TWO = (NST == 2);
   const int t = threadIdx.x;
   const int q = blockIdx.x * SC + t;
   const int p0 = blockIdx.y * SR;
@@ -79,19 +80,18 @@ __global__ void __launch_bounds__(128) wgrad_step_simt_kernel(const WgradSimtPar
       if constexpr (TWO) sv_old[i] = p.v_scale[static_cast<int64_t>(jb) * p.d_out + row];
     }
     if (!qok) continue;
-    const float w = ld_val<WK == W_F32 ? 0 : 1>(p.W, static_cast<int64_t>(row) * p.ld_w + q);
-    float m, v = 0.0f;
+    float w = ld_val<WK == W_F32 ? 0 : 1>(p.W, static_cast<int64_t>(row) * p.ld_w + q);
+    float m = 0.0f, v = 0.0f;
     if constexpr (MK == M_Q8) {
       m = dequant_m(static_cast<const int8_t*>(p.m)[static_cast<int64_t>(row) * p.ld_m + q], sm_old[i]);
       if constexpr (TWO)
         v = dequant_v(static_cast<const uint8_t*>(p.v)[static_cast<int64_t>(row) * p.ld_v + q], sv_old[i]);
     } else {
-      m = ld_val<MK == M_F32 ? 0 : 1>(p.m, static_cast<int64_t>(row) * p.ld_m + q);
+      if constexpr (NST >= 1) m = ld_val<MK == M_F32 ? 0 : 1>(p.m, static_cast<int64_t>(row) * p.ld_m + q);
       if constexpr (TWO) v = ld_val<MK == M_F32 ? 0 : 1>(p.v, static_cast<int64_t>(row) * p.ld_v + q);
     }
-    if constexpr (OPT == OPT_ADAMW) adamw_elem(g[i], w, m, v, s, w1[i], m1[i], v1[i]);
-    else if constexpr (OPT == OPT_SGDM) sgdm_elem(g[i], w, m, s, w1[i], m1[i]);
-    else lion_elem(g[i], w, m, s, w1[i], m1[i]);
+    step_elem<OPT>(g[i], w, m, v, s);
+    w1[i] = w; m1[i] = m; v1[i] = v;
   }
 
   float sm_new[SR], sv_new[SR];
@@ -141,7 +141,8 @@ __global__ void __launch_bounds__(128) wgrad_step_simt_kernel(const WgradSimtPar
                                 : f32_to_bf16_rne(w1[i]);
       static_cast<uint16_t*>(p.W)[static_cast<int64_t>(row) * p.ld_w + q] = static_cast<uint16_t>(b);
     }
-    if constexpr (MK == M_F32) {
+    if constexpr (NST == 0) {
+    } else if constexpr (MK == M_F32) {
       static_cast<float*>(p.m)[static_cast<int64_t>(row) * p.ld_m + q] = m1[i];
       if constexpr (TWO) static_cast<float*>(p.v)[static_cast<int64_t>(row) * p.ld_v + q] = v1[i];
     } else if constexpr (MK == M_BF16) {
@@ -174,7 +175,8 @@ template <int OPT, int WK>
 cudaError_t launch2(const WgradSimtParams& p, int mk, cudaStream_t stream) {
   if (mk == M_F32) return launch3<OPT, WK, M_F32>(p, stream);
   if (mk == M_BF16) return launch3<OPT, WK, M_BF16>(p, stream);
-  if (mk == M_Q8) return launch3<OPT, WK, M_Q8>(p, stream);
+  if constexpr (OPT == OPT_ADAMW || OPT == OPT_SGDM || OPT == OPT_LION)
+    if (mk == M_Q8) return launch3<OPT, WK, M_Q8>(p, stream);
   return cudaErrorInvalidValue;
 }
 
@@ -189,6 +191,11 @@ cudaError_t launch_wgrad_simt(const WgradSimtParams& p, int opt, int wk, int mk,
   if (opt == OPT_ADAMW) return launch1<OPT_ADAMW>(p, wk, mk, stream);
   if (opt == OPT_SGDM) return launch1<OPT_SGDM>(p, wk, mk, stream);
   if (opt == OPT_LION) return launch1<OPT_LION>(p, wk, mk, stream);
+  if (opt == OPT_SGD) return launch1<OPT_SGD>(p, wk, mk, stream);
+  if (opt == OPT_RMSPROP) return launch1<OPT_RMSPROP>(p, wk, mk, stream);
+  if (opt == OPT_ADAGRAD) return launch1<OPT_ADAGRAD>(p, wk, mk, stream);
+  if (opt == OPT_NADAM) return launch1<OPT_NADAM>(p, wk, mk, stream);
+  if (opt == OPT_RADAM) return launch1<OPT_RADAM>(p, wk, mk, stream);
   return cudaErrorInvalidValue;
 }
 

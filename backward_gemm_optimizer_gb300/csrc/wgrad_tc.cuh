@@ -47,7 +47,8 @@ struct TcCfg {
   static constexpr int STAGES = STAGES_;
   static constexpr int NBUF = NBUF_;
   static constexpr int NCH = BN / CW;  // chunks per tile
-  static constexpr bool TWO = (OPT == OPT_ADAMW);  // second moment present
+  static constexpr int NST = opt_nstate(OPT);      // state tensors (0, 1, 2)
+  static constexpr bool TWO = (NST == 2);           // a second state tensor
   static constexpr bool Q8 = (MK == M_Q8);
   static constexpr int WE = (WK == W_F32) ? 4 : 2;
   static constexpr int ME = (MK == M_F32) ? 4 : (MK == M_BF16 ? 2 : 1);
@@ -55,7 +56,7 @@ struct TcCfg {
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int W_CH = BM * CW * WE;
-  static constexpr int M_CH = BM * CW * ME;
+  static constexpr int M_CH = NST >= 1 ? BM * CW * ME : 0;
   static constexpr int V_CH = TWO ? M_CH : 0;
   static constexpr int SLOT_BYTES = ((W_CH + M_CH + V_CH + 1023) / 1024) * 1024;
   static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NBUF * SLOT_BYTES;
@@ -197,6 +198,7 @@ __global__ void __launch_bounds__(128 + 512, 1) wgrad_step_tc_kernel(const __gri
   using C = TcCfg<OPT, WK, MK, BN, STAGES, NBUF>;
   static_assert(BN == 64 || BN == 128, "tile width");
   static_assert(!C::Q8 || BN == 128, "8-bit blocks span one 128-column tile row");
+  static_assert(!C::Q8 || OPT == OPT_ADAMW || OPT == OPT_SGDM || OPT == OPT_LION, "8-bit state rules");
   static_assert(!C::Q8 || NBUF >= C::NCH, "8-bit moments hold a whole tile of slots");
   static_assert(NBUF >= 2 && STAGES >= 2, "pipelines");
   static_assert(C::SMEM_BYTES <= 227 * 1024, "shared memory");
@@ -238,7 +240,8 @@ __global__ void __launch_bounds__(128 + 512, 1) wgrad_step_tc_kernel(const __gri
   }
   if (warp == 0 && lane == 0) {
     if (p.num_kb > 0) { prefetch_tmap(&p.tm_dy); prefetch_tmap(&p.tm_x); }
-    prefetch_tmap(&p.tm_w); prefetch_tmap(&p.tm_m);
+    prefetch_tmap(&p.tm_w);
+    if constexpr (C::NST >= 1) prefetch_tmap(&p.tm_m);
     if constexpr (C::TWO) prefetch_tmap(&p.tm_v);
   }
   if (warp == 1) {
@@ -331,7 +334,7 @@ __global__ void __launch_bounds__(128 + 512, 1) wgrad_step_tc_kernel(const __gri
           const int x = tn * BN + c * C::CW, y = tm * C::BM;
           mbar_arrive_expect_tx(&st_full[s], C::W_CH + C::M_CH + C::V_CH);
           tma_load_2d(slot, &p.tm_w, &st_full[s], x, y);
-          tma_load_2d(slot + C::W_CH, &p.tm_m, &st_full[s], x, y);
+          if constexpr (C::NST >= 1) tma_load_2d(slot + C::W_CH, &p.tm_m, &st_full[s], x, y);
           if constexpr (C::TWO) tma_load_2d(slot + C::W_CH + C::M_CH, &p.tm_v, &st_full[s], x, y);
         }
       }
@@ -352,7 +355,7 @@ __global__ void __launch_bounds__(128 + 512, 1) wgrad_step_tc_kernel(const __gri
           const uint8_t* slot = st_base + s * C::SLOT_BYTES;
           const int x = tn * BN + c * C::CW, y = tm * C::BM;
           tma_store_2d(&p.tm_w, slot, x, y);
-          tma_store_2d(&p.tm_m, slot + C::W_CH, x, y);
+          if constexpr (C::NST >= 1) tma_store_2d(&p.tm_m, slot + C::W_CH, x, y);
           if constexpr (C::TWO) tma_store_2d(&p.tm_v, slot + C::W_CH + C::M_CH, x, y);
           bulk_commit_group();
           bulk_wait_group_read0();
@@ -408,18 +411,10 @@ __global__ void __launch_bounds__(128 + 512, 1) wgrad_step_tc_kernel(const __gri
           uint8_t* sv = slot + C::W_CH + C::M_CH;
           float w[8], m[8], v[8];
           ld8<WK == W_F32 ? 0 : 1>(sw, r, h, w);
-          ld8<MK == M_F32 ? 0 : 1>(sm, r, h, m);
+          if constexpr (C::NST >= 1) ld8<MK == M_F32 ? 0 : 1>(sm, r, h, m);
           if constexpr (C::TWO) ld8<MK == M_F32 ? 0 : 1>(sv, r, h, v);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float g = __uint_as_float(gr[j]);
-            float w1, m1, v1 = 0.0f;
-            if constexpr (OPT == OPT_ADAMW) adamw_elem(g, w[j], m[j], v[j], sc, w1, m1, v1);
-            else if constexpr (OPT == OPT_SGDM) sgdm_elem(g, w[j], m[j], sc, w1, m1);
-            else lion_elem(g, w[j], m[j], sc, w1, m1);
-            w[j] = w1; m[j] = m1;
-            if constexpr (C::TWO) v[j] = v1;
-          }
+          for (int j = 0; j < 8; ++j) step_elem<OPT>(__uint_as_float(gr[j]), w[j], m[j], v[j], sc);
           // Element index of this thread's first column; 8-aligned (D_in % 8 == 0).
           const uint64_t idx8 =
               (static_cast<uint64_t>(row) * static_cast<uint64_t>(p.d_in) + (tn * BN + c * C::CW + h * 8)) >> 3;
@@ -430,7 +425,8 @@ __global__ void __launch_bounds__(128 + 512, 1) wgrad_step_tc_kernel(const __gri
             to_bf16x8(w, p.sr_w != 0, idx8, 0u, p, b);
             st8_bf16(sw, r, h, b);
           }
-          if constexpr (MK == M_F32) {
+          if constexpr (C::NST == 0) {
+          } else if constexpr (MK == M_F32) {
             st8_f32(sm, r, h, m);
             if constexpr (C::TWO) st8_f32(sv, r, h, v);
           } else {

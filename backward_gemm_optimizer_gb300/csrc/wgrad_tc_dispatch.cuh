@@ -54,14 +54,22 @@ cudaError_t launch_mk(const WgradTcParams& p, const TcLaunch& l) {
 
 template <int OPT>
 cudaError_t launch_opt(const WgradTcParams& p, const TcLaunch& l) {
-  if (l.wk == W_F32) {
-    if (l.mk == M_F32) return launch_mk<OPT, W_F32, M_F32>(p, l);
-    if (l.mk == M_BF16) return launch_mk<OPT, W_F32, M_BF16>(p, l);
-    if (l.mk == M_Q8) return launch_mk<OPT, W_F32, M_Q8>(p, l);
+  constexpr bool kQ8 = (OPT == OPT_ADAMW || OPT == OPT_SGDM || OPT == OPT_LION);
+  if constexpr (opt_nstate(OPT) == 0) {
+    // No state tensor: the moment storage does not matter.
+    return l.wk == W_F32 ? launch_mk<OPT, W_F32, M_F32>(p, l) : launch_mk<OPT, W_BF16, M_F32>(p, l);
   } else {
-    if (l.mk == M_F32) return launch_mk<OPT, W_BF16, M_F32>(p, l);
-    if (l.mk == M_BF16) return launch_mk<OPT, W_BF16, M_BF16>(p, l);
-    if (l.mk == M_Q8) return launch_mk<OPT, W_BF16, M_Q8>(p, l);
+    if (l.wk == W_F32) {
+      if (l.mk == M_F32) return launch_mk<OPT, W_F32, M_F32>(p, l);
+      if (l.mk == M_BF16) return launch_mk<OPT, W_F32, M_BF16>(p, l);
+      if constexpr (kQ8)
+        if (l.mk == M_Q8) return launch_mk<OPT, W_F32, M_Q8>(p, l);
+    } else {
+      if (l.mk == M_F32) return launch_mk<OPT, W_BF16, M_F32>(p, l);
+      if (l.mk == M_BF16) return launch_mk<OPT, W_BF16, M_BF16>(p, l);
+      if constexpr (kQ8)
+        if (l.mk == M_Q8) return launch_mk<OPT, W_BF16, M_Q8>(p, l);
+    }
   }
   return cudaErrorInvalidValue;
 }

@@ -104,6 +104,7 @@ typedef struct {
   int32_t sr_w;         /* bf16 W only: 1 = stochastic rounding, 0 = round-to-nearest-even */
   int32_t sr_moments;   /* bf16 moments only: 1 = stochastic rounding, 0 = RNE */
   uint32_t flags;       /* FORGE_FLAG_* */
+  double momentum_decay; /* NAdam psi (PyTorch's default is 4e-3); unused by the other rules */
 } forge_hyper;
 
 /*
@@ -171,6 +172,47 @@ forge_status forge_wgrad_step_lion(const forge_tensor* X, const forge_tensor* dY
                                    forge_tensor* W, forge_tensor* m,
                                    const forge_hyper* h, int64_t step, uint64_t seed,
                                    forge_stream_t stream);
+
+/*
+ * The remaining element-wise rules the paper fuses (Appendix N (i): SGD,
+ * RMSprop, AdaGrad, NAdam, RAdam) are named there without formulas; each
+ * follows the PyTorch optimizer of the same name with its defaults
+ * (coupled L2 weight decay g~ = g + wd*W, no momentum / centring / lr decay
+ * for RMSprop and AdaGrad, initial accumulator 0). Arguments as for
+ * forge_wgrad_step_adamw; the state tensors are FORGE_F32 or FORGE_BF16
+ * (no 8-bit variant). fp32 op sequences (correctly rounded, no FMA):
+ *
+ * forge_wgrad_step_sgd:      g~ = g + wd*W;  W' = W - lr*g~.  No state.
+ * forge_wgrad_step_rmsprop:  v' = a*v + (1-a)*(g~*g~);  W' = W - lr*(g~/(sqrt(v') + eps)),
+ *                            a = h->beta2 (PyTorch's alpha).
+ * forge_wgrad_step_adagrad:  v' = v + g~*g~;  W' = W - lr*(g~/(sqrt(v') + eps)).
+ * forge_wgrad_step_nadam:    m' = b1*m + (1-b1)*g~;  v' = b2*v + (1-b2)*(g~*g~);
+ *                            d = sqrt(v')*(1/sqrt(1-b2^t)) + eps;
+ *                            W' = W - (c1*g~ + c2*m')/d, with mu_i = b1 (1 - 0.5*0.96^(i psi)),
+ *                            P_t = prod_{i<=t} mu_i, c1 = lr (1 - mu_t)/(1 - P_t),
+ *                            c2 = lr mu_{t+1}/(1 - P_t mu_{t+1}), psi = h->momentum_decay.
+ * forge_wgrad_step_radam:    m', v' as NAdam; rho_inf = 2/(1-b2) - 1,
+ *                            rho_t = rho_inf - 2 t b2^t/(1-b2^t); if rho_t > 5:
+ *                            r_t = sqrt((rho_t-4)(rho_t-2) rho_inf/((rho_inf-4)(rho_inf-2) rho_t)),
+ *                            W' = W - (lr r_t sqrt(1-b2^t)/(1-b1^t))*(m'/(sqrt(v') + eps));
+ *                            else W' = W - (lr/(1-b1^t))*m'.
+ * The per-step scalars (c1, c2, r_t, ...) are computed in double on the host
+ * and rounded to float once.
+ */
+forge_status forge_wgrad_step_sgd(const forge_tensor* X, const forge_tensor* dY, forge_tensor* W,
+                                  const forge_hyper* h, int64_t step, uint64_t seed, forge_stream_t stream);
+forge_status forge_wgrad_step_rmsprop(const forge_tensor* X, const forge_tensor* dY, forge_tensor* W,
+                                      forge_tensor* v, const forge_hyper* h, int64_t step, uint64_t seed,
+                                      forge_stream_t stream);
+forge_status forge_wgrad_step_adagrad(const forge_tensor* X, const forge_tensor* dY, forge_tensor* W,
+                                      forge_tensor* v, const forge_hyper* h, int64_t step, uint64_t seed,
+                                      forge_stream_t stream);
+forge_status forge_wgrad_step_nadam(const forge_tensor* X, const forge_tensor* dY, forge_tensor* W,
+                                    forge_tensor* m, forge_tensor* v, const forge_hyper* h, int64_t step,
+                                    uint64_t seed, forge_stream_t stream);
+forge_status forge_wgrad_step_radam(const forge_tensor* X, const forge_tensor* dY, forge_tensor* W,
+                                    forge_tensor* m, forge_tensor* v, const forge_hyper* h, int64_t step,
+                                    uint64_t seed, forge_stream_t stream);
 
 /*
  * forge_dgrad -- input gradient dX = dY W_old (Remark 1, Appendix A).

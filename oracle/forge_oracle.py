@@ -84,6 +84,7 @@ class Hyper:
     beta2: float = 0.999
     eps: float = 1e-8
     weight_decay: float = 0.0
+    momentum_decay: float = 4e-3   # NAdam psi
 
 
 # --------------------------------------------------------------------------
@@ -144,6 +145,81 @@ def lion_f64(W, m, G, h: Hyper, t: int):
     return W1, m1
 
 
+# The remaining element-wise families of Appendix N (i), read as the PyTorch
+# optimizers of the same name with their defaults (coupled L2 decay
+# g~ = g + lambda W; RMSprop without momentum or centring, alpha = beta2;
+# AdaGrad without lr decay, initial accumulator 0). The one state tensor of
+# RMSprop and AdaGrad is their second moment.
+
+
+def sgd_f64(W, G, h: Hyper, t: int):
+    """Plain SGD (Appendix N (i).7)."""
+    W = np.asarray(W, np.float64); G = np.asarray(G, np.float64)
+    return W - h.lr * (G + h.weight_decay * W)
+
+
+def rmsprop_f64(W, v, G, h: Hyper, t: int):
+    """RMSprop (Appendix N (i).5): second moment only."""
+    W = np.asarray(W, np.float64); v = np.asarray(v, np.float64); G = np.asarray(G, np.float64)
+    gt = G + h.weight_decay * W
+    v1 = h.beta2 * v + (1.0 - h.beta2) * gt * gt
+    return W - h.lr * gt / (np.sqrt(v1) + h.eps), v1
+
+
+def adagrad_f64(W, v, G, h: Hyper, t: int):
+    """AdaGrad (Appendix N (i).6): cumulative squared gradient."""
+    W = np.asarray(W, np.float64); v = np.asarray(v, np.float64); G = np.asarray(G, np.float64)
+    gt = G + h.weight_decay * W
+    v1 = v + gt * gt
+    return W - h.lr * gt / (np.sqrt(v1) + h.eps), v1
+
+
+def nadam_mu(h: Hyper, i: float) -> float:
+    """NAdam's momentum schedule mu_i = beta1 (1 - 0.5 * 0.96^(i psi))."""
+    return h.beta1 * (1.0 - 0.5 * 0.96 ** (i * h.momentum_decay))
+
+
+def nadam_f64(W, m, v, G, h: Hyper, t: int):
+    """NAdam (Appendix N (i).2): Nesterov-corrected Adam."""
+    W = np.asarray(W, np.float64); m = np.asarray(m, np.float64)
+    v = np.asarray(v, np.float64); G = np.asarray(G, np.float64)
+    gt = G + h.weight_decay * W
+    m1 = h.beta1 * m + (1.0 - h.beta1) * gt
+    v1 = h.beta2 * v + (1.0 - h.beta2) * gt * gt
+    prod = 1.0
+    for i in range(1, t + 1):
+        prod *= nadam_mu(h, i)
+    mu_t, mu_n = nadam_mu(h, t), nadam_mu(h, t + 1)
+    denom = np.sqrt(v1 / (1.0 - h.beta2 ** t)) + h.eps
+    W1 = W - h.lr * (1.0 - mu_t) / (1.0 - prod) * gt / denom - h.lr * mu_n / (1.0 - prod * mu_n) * m1 / denom
+    return W1, m1, v1
+
+
+def radam_rect(h: Hyper, t: int):
+    """(rectified?, r_t) of RAdam at step t."""
+    rho_inf = 2.0 / (1.0 - h.beta2) - 1.0
+    rho_t = rho_inf - 2.0 * t * h.beta2 ** t / (1.0 - h.beta2 ** t)
+    if rho_t > 5.0:
+        return True, np.sqrt((rho_t - 4) * (rho_t - 2) * rho_inf / ((rho_inf - 4) * (rho_inf - 2) * rho_t))
+    return False, 1.0
+
+
+def radam_f64(W, m, v, G, h: Hyper, t: int):
+    """RAdam (Appendix N (i).3): Adam with the variance rectification."""
+    W = np.asarray(W, np.float64); m = np.asarray(m, np.float64)
+    v = np.asarray(v, np.float64); G = np.asarray(G, np.float64)
+    gt = G + h.weight_decay * W
+    m1 = h.beta1 * m + (1.0 - h.beta1) * gt
+    v1 = h.beta2 * v + (1.0 - h.beta2) * gt * gt
+    mhat = m1 / (1.0 - h.beta1 ** t)
+    rect, r = radam_rect(h, t)
+    if rect:
+        W1 = W - h.lr * mhat * r * np.sqrt(1.0 - h.beta2 ** t) / (np.sqrt(v1) + h.eps)
+    else:
+        W1 = W - h.lr * mhat
+    return W1, m1, v1
+
+
 # --------------------------------------------------------------------------
 # Phase 2 as a float32 op sequence
 # --------------------------------------------------------------------------
@@ -172,6 +248,27 @@ def fold_scalars(opt: str, h: Hyper, t: int) -> dict:
             b1=F32(h.beta1), omb1=F32(1.0 - h.beta1),
             b2=F32(h.beta2), omb2=F32(1.0 - h.beta2),
             decay=F32(1.0 - h.lr * h.weight_decay), lr=F32(h.lr))
+    if opt in ("sgd", "adagrad"):
+        return dict(wd=F32(h.weight_decay), lr=F32(h.lr), eps=F32(h.eps))
+    if opt == "rmsprop":
+        return dict(wd=F32(h.weight_decay), lr=F32(h.lr), eps=F32(h.eps),
+                    a=F32(h.beta2), oma=F32(1.0 - h.beta2))
+    if opt == "nadam":
+        prod = 1.0
+        for i in range(1, t + 1):
+            prod *= nadam_mu(h, i)
+        mu_t, mu_n = nadam_mu(h, t), nadam_mu(h, t + 1)
+        return dict(wd=F32(h.weight_decay), b1=F32(h.beta1), omb1=F32(1.0 - h.beta1),
+                    b2=F32(h.beta2), omb2=F32(1.0 - h.beta2), eps=F32(h.eps),
+                    inv_sqrt_bc2=F32(1.0 / np.sqrt(1.0 - h.beta2 ** t)),
+                    c1=F32(h.lr * (1.0 - mu_t) / (1.0 - prod)),
+                    c2=F32(h.lr * mu_n / (1.0 - prod * mu_n)))
+    if opt == "radam":
+        rect, r = radam_rect(h, t)
+        bc1, bc2 = 1.0 - h.beta1 ** t, 1.0 - h.beta2 ** t
+        c = h.lr * r * np.sqrt(bc2) / bc1 if rect else h.lr / bc1
+        return dict(wd=F32(h.weight_decay), b1=F32(h.beta1), omb1=F32(1.0 - h.beta1),
+                    b2=F32(h.beta2), omb2=F32(1.0 - h.beta2), eps=F32(h.eps), rect=rect, c=F32(c))
     raise ValueError(opt)
 
 
@@ -215,6 +312,55 @@ def lion_f32(W, m, G, s: dict):
     W1 = s["decay"] * W - s["lr"] * sg
     m1 = s["b2"] * m + s["omb2"] * G
     return W1, m1
+
+
+def sgd_f32(W, G, s: dict):
+    """g~ = g + wd*W; W' = W - lr*g~."""
+    W, G = _f32(W), _f32(G)
+    return W - s["lr"] * (G + s["wd"] * W)
+
+
+def rmsprop_f32(W, v, G, s: dict):
+    """g~ = g + wd*W; v' = a*v + (1-a)*(g~*g~); W' = W - lr*(g~/(sqrt(v') + eps))."""
+    W, v, G = _f32(W), _f32(v), _f32(G)
+    gt = G + s["wd"] * W
+    v1 = s["a"] * v + s["oma"] * (gt * gt)
+    return W - s["lr"] * (gt / (np.sqrt(v1) + s["eps"])), v1
+
+
+def adagrad_f32(W, v, G, s: dict):
+    """g~ = g + wd*W; v' = v + g~*g~; W' = W - lr*(g~/(sqrt(v') + eps))."""
+    W, v, G = _f32(W), _f32(v), _f32(G)
+    gt = G + s["wd"] * W
+    v1 = v + gt * gt
+    return W - s["lr"] * (gt / (np.sqrt(v1) + s["eps"])), v1
+
+
+def nadam_f32(W, m, v, G, s: dict):
+    """g~; m' = b1*m + (1-b1)*g~; v' = b2*v + (1-b2)*(g~*g~);
+    d = sqrt(v')*inv_sqrt_bc2 + eps; W' = W - (c1*g~ + c2*m')/d."""
+    W, m, v, G = _f32(W), _f32(m), _f32(v), _f32(G)
+    gt = G + s["wd"] * W
+    m1 = s["b1"] * m + s["omb1"] * gt
+    v1 = s["b2"] * v + s["omb2"] * (gt * gt)
+    d = np.sqrt(v1) * s["inv_sqrt_bc2"] + s["eps"]
+    return W - (s["c1"] * gt + s["c2"] * m1) / d, m1, v1
+
+
+def radam_f32(W, m, v, G, s: dict):
+    """g~; m', v' as NAdam; rectified: W' = W - c*(m'/(sqrt(v') + eps)); else W' = W - c*m'."""
+    W, m, v, G = _f32(W), _f32(m), _f32(v), _f32(G)
+    gt = G + s["wd"] * W
+    m1 = s["b1"] * m + s["omb1"] * gt
+    v1 = s["b2"] * v + s["omb2"] * (gt * gt)
+    if s["rect"]:
+        return W - s["c"] * (m1 / (np.sqrt(v1) + s["eps"])), m1, v1
+    return W - s["c"] * m1, m1, v1
+
+
+# Number of state tensors per rule (RMSprop / AdaGrad: their one state is
+# held in State.m).
+NSTATE = {"adamw": 2, "nadam": 2, "radam": 2, "sgdm": 1, "lion": 1, "rmsprop": 1, "adagrad": 1, "sgd": 0}
 
 
 # --------------------------------------------------------------------------
@@ -520,16 +666,28 @@ def step(opt: str, X, dY, st: State, h: Hyper, t: int, *, seed: int = 0,
     """
     if G is None:
         G = wgrad_f64(dY, X)
+    ns = NSTATE[opt]
     W0 = load_w(st)
-    m0 = load_m(st)
-    v0 = load_v(st) if opt == "adamw" else None
+    m0 = load_m(st) if ns >= 1 else None
+    v0 = load_v(st) if ns == 2 else None
+    m1 = v1 = None
     if mode == "f64":
         if opt == "adamw":
             W1, m1, v1 = adamw_f64(W0, m0, v0, G, h, t)
         elif opt == "sgdm":
-            (W1, m1), v1 = sgdm_f64(W0, m0, G, h, t), None
+            W1, m1 = sgdm_f64(W0, m0, G, h, t)
         elif opt == "lion":
-            (W1, m1), v1 = lion_f64(W0, m0, G, h, t), None
+            W1, m1 = lion_f64(W0, m0, G, h, t)
+        elif opt == "sgd":
+            W1 = sgd_f64(W0, G, h, t)
+        elif opt == "rmsprop":
+            W1, m1 = rmsprop_f64(W0, m0, G, h, t)
+        elif opt == "adagrad":
+            W1, m1 = adagrad_f64(W0, m0, G, h, t)
+        elif opt == "nadam":
+            W1, m1, v1 = nadam_f64(W0, m0, v0, G, h, t)
+        elif opt == "radam":
+            W1, m1, v1 = radam_f64(W0, m0, v0, G, h, t)
         else:
             raise ValueError(opt)
     elif mode == "f32emu":
@@ -538,17 +696,28 @@ def step(opt: str, X, dY, st: State, h: Hyper, t: int, *, seed: int = 0,
         if opt == "adamw":
             W1, m1, v1 = adamw_f32(W0, m0, v0, g32, s)
         elif opt == "sgdm":
-            (W1, m1), v1 = sgdm_f32(W0, m0, g32, s), None
+            W1, m1 = sgdm_f32(W0, m0, g32, s)
         elif opt == "lion":
-            (W1, m1), v1 = lion_f32(W0, m0, g32, s), None
+            W1, m1 = lion_f32(W0, m0, g32, s)
+        elif opt == "sgd":
+            W1 = sgd_f32(W0, g32, s)
+        elif opt == "rmsprop":
+            W1, m1 = rmsprop_f32(W0, m0, g32, s)
+        elif opt == "adagrad":
+            W1, m1 = adagrad_f32(W0, m0, g32, s)
+        elif opt == "nadam":
+            W1, m1, v1 = nadam_f32(W0, m0, v0, g32, s)
+        elif opt == "radam":
+            W1, m1, v1 = radam_f32(W0, m0, v0, g32, s)
         else:
             raise ValueError(opt)
     else:
         raise ValueError(mode)
 
     Wn = _store_w(W1, st, mode, sr_w, seed, t)
-    mn, msn = _store_moment(m1, "m", st, mode, sr_moments, seed, t)
-    vn = vsn = None
+    mn = msn = vn = vsn = None
+    if m1 is not None:
+        mn, msn = _store_moment(m1, "m", st, mode, sr_moments, seed, t)
     if v1 is not None:
         vn, vsn = _store_moment(v1, "v", st, mode, sr_moments, seed, t)
     return State(W=Wn, m=mn, v=vn, m_scale=msn, v_scale=vsn, w_dtype=st.w_dtype, state=st.state)
@@ -558,13 +727,27 @@ def step_values(opt: str, X, dY, st: State, h: Hyper, t: int, G: Optional[np.nda
     """Unrounded float64 outputs of Phase 2 (W', m', v') and G; for tolerances."""
     if G is None:
         G = wgrad_f64(dY, X)
-    W0, m0 = load_w(st), load_m(st)
+    ns = NSTATE[opt]
+    W0 = load_w(st)
+    m0 = load_m(st) if ns >= 1 else None
+    v0 = load_v(st) if ns == 2 else None
+    m1 = v1 = None
     if opt == "adamw":
-        W1, m1, v1 = adamw_f64(W0, m0, load_v(st), G, h, t)
+        W1, m1, v1 = adamw_f64(W0, m0, v0, G, h, t)
     elif opt == "sgdm":
-        (W1, m1), v1 = sgdm_f64(W0, m0, G, h, t), None
+        W1, m1 = sgdm_f64(W0, m0, G, h, t)
+    elif opt == "lion":
+        W1, m1 = lion_f64(W0, m0, G, h, t)
+    elif opt == "sgd":
+        W1 = sgd_f64(W0, G, h, t)
+    elif opt == "rmsprop":
+        W1, m1 = rmsprop_f64(W0, m0, G, h, t)
+    elif opt == "adagrad":
+        W1, m1 = adagrad_f64(W0, m0, G, h, t)
+    elif opt == "nadam":
+        W1, m1, v1 = nadam_f64(W0, m0, v0, G, h, t)
     else:
-        (W1, m1), v1 = lion_f64(W0, m0, G, h, t), None
+        W1, m1, v1 = radam_f64(W0, m0, v0, G, h, t)
     return W1, m1, v1, G
 
 

@@ -97,3 +97,47 @@ def bf16_ulp_distance(a_bits, b_bits) -> np.ndarray:
         b = np.asarray(b).astype(np.int64)
         return np.where(b & 0x8000, -(b & 0x7FFF), b & 0x7FFF)
     return np.abs(key(a_bits) - key(b_bits))
+
+
+def generic_tol(opt: str, W, s0, s1, G, A, h: Hyper, t: int, rtol: float = 1e-5):
+    """Tolerances (W', s0', s1') of any element-wise rule by explicit perturbation.
+
+    Every input of the step is moved by a relative rtol (the gradient by
+    rtol * A) at each of the 16 sign corners; the tolerance of an output is
+    its largest move plus rtol of its own magnitude. The rules are
+    element-wise, so all elements are perturbed at once.
+    """
+    from . import forge_oracle as O
+
+    def run(Wp, a, b, Gp):
+        if opt == "adamw":
+            return O.adamw_f64(Wp, a, b, Gp, h, t)
+        if opt == "sgdm":
+            return (*O.sgdm_f64(Wp, a, Gp, h, t), None)
+        if opt == "lion":
+            return (*O.lion_f64(Wp, a, Gp, h, t), None)
+        if opt == "sgd":
+            return O.sgd_f64(Wp, Gp, h, t), None, None
+        if opt == "rmsprop":
+            return (*O.rmsprop_f64(Wp, a, Gp, h, t), None)
+        if opt == "adagrad":
+            return (*O.adagrad_f64(Wp, a, Gp, h, t), None)
+        if opt == "nadam":
+            return O.nadam_f64(Wp, a, b, Gp, h, t)
+        return O.radam_f64(Wp, a, b, Gp, h, t)
+
+    W = np.asarray(W, np.float64); G = np.asarray(G, np.float64); A = np.asarray(A, np.float64)
+    z = np.zeros_like(W)
+    s0 = z if s0 is None else np.asarray(s0, np.float64)
+    s1 = z if s1 is None else np.asarray(s1, np.float64)
+    base = run(W, s0, s1, G)
+    dev = [np.zeros_like(W) if x is not None else None for x in base]
+    for sw in (-1, 1):
+        for sa in (-1, 1):
+            for sb in (-1, 1):
+                for sg in (-1, 1):
+                    out = run(W * (1 + sw * rtol), s0 * (1 + sa * rtol), s1 * (1 + sb * rtol), G + sg * rtol * A)
+                    for i, (o, b) in enumerate(zip(out, base)):
+                        if o is not None:
+                            dev[i] = np.maximum(dev[i], np.abs(o - b))
+    return tuple(None if d is None else d + rtol * np.abs(b) for d, b in zip(dev, base))

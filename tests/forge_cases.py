@@ -15,7 +15,14 @@ HYPER = {
     "adamw": dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01),
     "sgdm": dict(lr=2e-5, beta1=0.9, beta2=0.0, eps=0.0, weight_decay=1e-2),
     "lion": dict(lr=3e-6, beta1=0.9, beta2=0.99, eps=0.0, weight_decay=1.0),
+    # Appendix N, Table 20 (lr, wd, eps) for the remaining families
+    "sgd": dict(lr=2e-5, beta1=0.0, beta2=0.0, eps=0.0, weight_decay=1e-2),
+    "rmsprop": dict(lr=2e-5, beta1=0.0, beta2=0.99, eps=1e-8, weight_decay=1e-2),
+    "adagrad": dict(lr=2e-5, beta1=0.0, beta2=0.0, eps=1e-10, weight_decay=1e-2),
+    "nadam": dict(lr=2e-5, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=1e-2, momentum_decay=4e-3),
+    "radam": dict(lr=2e-5, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=1e-2),
 }
+NSTATE = O.NSTATE
 
 # (W storage, moment storage) combinations with a kernel.
 VARIANTS = [("f32", "f32"), ("f32", "bf16"), ("bf16", "bf16"), ("f32", "q8"), ("bf16", "q8"), ("bf16", "f32")]
@@ -28,8 +35,21 @@ def to_np(t: torch.Tensor) -> np.ndarray:
     return t.numpy().copy()
 
 
-def oracle_state(prob: S.LinearProblem, w_dtype: str, state: str) -> O.State:
-    return O.State(W=to_np(prob.W), m=to_np(prob.m), v=to_np(prob.v) if prob.v is not None else None,
+def state_tensors(opt, prob):
+    """(s0, s1) of a problem for rule `opt`: RMSprop / AdaGrad take the
+    (non-negative) second-moment draw as their one state."""
+    ns = NSTATE[opt]
+    if ns == 0:
+        return None, None
+    if opt in ("rmsprop", "adagrad"):
+        return prob.v, None
+    return prob.m, (prob.v if ns == 2 else None)
+
+
+def oracle_state(prob: S.LinearProblem, w_dtype: str, state: str, opt: str = "adamw") -> O.State:
+    s0, s1 = state_tensors(opt, prob)
+    return O.State(W=to_np(prob.W), m=to_np(s0) if s0 is not None else None,
+                   v=to_np(s1) if s1 is not None else None,
                    m_scale=to_np(prob.m_scale) if prob.m_scale is not None else None,
                    v_scale=to_np(prob.v_scale) if prob.v_scale is not None else None,
                    w_dtype=w_dtype, state=state)
@@ -40,29 +60,43 @@ def gpu_step(opt: str, prob: S.LinearProblem, t: int, *, seed: int = 0, sr_w=Fal
     """Copy the problem to the GPU, run one fused step, return the new state (CPU numpy)."""
     hp = dict(HYPER[opt] if hyper is None else hyper)
     X, dY, W = prob.X.to(dev), prob.dY.to(dev), prob.W.to(dev)
-    m = prob.m.to(dev)
-    ms = prob.m_scale.to(dev) if prob.m_scale is not None else None
-    common = dict(step=t, seed=seed, sr_w=sr_w, sr_moments=sr_moments, flags=flags)
+    s0, s1 = state_tensors(opt, prob)
+    m = s0.to(dev) if s0 is not None else None
+    v = s1.to(dev) if s1 is not None else None
+    ms = prob.m_scale.to(dev) if (prob.m_scale is not None and m is not None) else None
+    vs = prob.v_scale.to(dev) if (prob.v_scale is not None and v is not None) else None
+    common = dict(step=t, seed=seed, sr_w=sr_w, flags=flags)
+    lr, wd = hp["lr"], hp["weight_decay"]
     if opt == "adamw":
-        v = prob.v.to(dev)
-        vs = prob.v_scale.to(dev) if prob.v_scale is not None else None
-        F.wgrad_step_adamw(X, dY, W, m, v, m_scale=ms, v_scale=vs, **hp, **common)
+        F.wgrad_step_adamw(X, dY, W, m, v, m_scale=ms, v_scale=vs, lr=lr, beta1=hp["beta1"], beta2=hp["beta2"],
+                           eps=hp["eps"], weight_decay=wd, sr_moments=sr_moments, **common)
     elif opt == "sgdm":
-        v = vs = None
-        F.wgrad_step_sgdm(X, dY, W, m, lr=hp["lr"], momentum=hp["beta1"], weight_decay=hp["weight_decay"],
-                          m_scale=ms, **common)
+        F.wgrad_step_sgdm(X, dY, W, m, lr=lr, momentum=hp["beta1"], weight_decay=wd, m_scale=ms,
+                          sr_moments=sr_moments, **common)
+    elif opt == "lion":
+        F.wgrad_step_lion(X, dY, W, m, lr=lr, beta1=hp["beta1"], beta2=hp["beta2"], weight_decay=wd, m_scale=ms,
+                          sr_moments=sr_moments, **common)
+    elif opt == "sgd":
+        F.wgrad_step_sgd(X, dY, W, lr=lr, weight_decay=wd, **common)
+    elif opt == "rmsprop":
+        F.wgrad_step_rmsprop(X, dY, W, m, lr=lr, alpha=hp["beta2"], eps=hp["eps"], weight_decay=wd,
+                             sr_moments=sr_moments, **common)
+    elif opt == "adagrad":
+        F.wgrad_step_adagrad(X, dY, W, m, lr=lr, eps=hp["eps"], weight_decay=wd, sr_moments=sr_moments, **common)
+    elif opt == "nadam":
+        F.wgrad_step_nadam(X, dY, W, m, v, lr=lr, beta1=hp["beta1"], beta2=hp["beta2"], eps=hp["eps"],
+                           weight_decay=wd, momentum_decay=hp["momentum_decay"], sr_moments=sr_moments, **common)
     else:
-        v = vs = None
-        F.wgrad_step_lion(X, dY, W, m, lr=hp["lr"], beta1=hp["beta1"], beta2=hp["beta2"],
-                          weight_decay=hp["weight_decay"], m_scale=ms, **common)
+        F.wgrad_step_radam(X, dY, W, m, v, lr=lr, beta1=hp["beta1"], beta2=hp["beta2"], eps=hp["eps"],
+                           weight_decay=wd, sr_moments=sr_moments, **common)
     F.sync_status()
-    return O.State(W=to_np(W), m=to_np(m), v=to_np(v) if v is not None else None,
+    return O.State(W=to_np(W), m=to_np(m) if m is not None else None, v=to_np(v) if v is not None else None,
                    m_scale=to_np(ms) if ms is not None else None, v_scale=to_np(vs) if vs is not None else None)
 
 
 def oracle_step(opt, prob, w_dtype, state, t, *, seed=0, sr_w=False, sr_moments=False, mode="f64", hyper=None):
     hp = dict(HYPER[opt] if hyper is None else hyper)
-    st = oracle_state(prob, w_dtype, state)
+    st = oracle_state(prob, w_dtype, state, opt)
     Xn = prob.X.float().numpy()
     dYn = prob.dY.float().numpy()
     return O.step(opt, Xn, dYn, st, O.Hyper(**hp), t, seed=seed, sr_w=sr_w, sr_moments=sr_moments, mode=mode)
@@ -77,10 +111,11 @@ def assert_bit_exact(got: O.State, ref: O.State, opt: str):
         nbad = int(np.sum(a != b))
         assert nbad == 0, f"{name}: {nbad} of {a.size} elements differ; first at {np.argwhere(a != b)[:3].tolist()}"
     eq(got.W, ref.W, "W")
-    eq(got.m, ref.m, "m")
+    if ref.m is not None:
+        eq(got.m, ref.m, "m")
     if ref.m_scale is not None:
         eq(got.m_scale, ref.m_scale, "m_scale")
-    if opt == "adamw":
+    if ref.v is not None:
         eq(got.v, ref.v, "v")
         if ref.v_scale is not None:
             eq(got.v_scale, ref.v_scale, "v_scale")
@@ -97,18 +132,22 @@ def check_tolerance(opt, prob, w_dtype, state, t, got: O.State, *, seed=0, sr_w=
     """Compare a random-input GPU step with the float64 oracle; returns a report dict."""
     hp = dict(HYPER[opt] if hyper is None else hyper)
     h = O.Hyper(**hp)
-    st = oracle_state(prob, w_dtype, state)
+    st = oracle_state(prob, w_dtype, state, opt)
     Xn = prob.X.float().numpy(); dYn = prob.dY.float().numpy()
     G = O.wgrad_f64(dYn, Xn)
     A = O.abs_wgrad_f64(dYn, Xn)
     ref = O.step(opt, None, None, st, h, t, seed=seed, sr_w=sr_w, sr_moments=sr_moments, G=G)
-    W0, m0 = O.load_w(st), O.load_m(st)
+    W0 = O.load_w(st)
+    m0 = O.load_m(st) if NSTATE[opt] >= 1 else None
     if opt == "adamw":
         tw, tm, tv = T.adamw_tol(W0, m0, O.load_v(st), G, A, h, t, rtol)
     elif opt == "sgdm":
         (tw, tm), tv = T.sgdm_tol(W0, m0, G, A, h, t, rtol), None
-    else:
+    elif opt == "lion":
         (tw, tm), tv = T.lion_tol(W0, m0, G, A, h, t, rtol), None
+    else:
+        v0 = O.load_v(st) if NSTATE[opt] == 2 else None
+        tw, tm, tv = T.generic_tol(opt, W0, m0, v0, G, A, h, t, rtol)
     rep = {}
 
     def cmp(name, g, r, tol, kind):
@@ -133,8 +172,9 @@ def check_tolerance(opt, prob, w_dtype, state, t, got: O.State, *, seed=0, sr_w=
 
     cmp("W", got.W, ref.W, tw, w_dtype)
     if state in ("f32", "bf16"):
-        cmp("m", got.m, ref.m, tm, state)
-        if opt == "adamw":
+        if ref.m is not None:
+            cmp("m", got.m, ref.m, tm, state)
+        if ref.v is not None:
             cmp("v", got.v, ref.v, tv, state)
     else:
         # 8-bit: codes within one step of the oracle's, rare differences.

@@ -326,3 +326,42 @@ def test_dgrad_f32_and_bf16_weights_agree_bit_for_bit(shape):
         F.dgrad(dY, W32, out)
         F.sync_status()
         assert torch.equal(out, ref), int((out != ref).sum())
+
+
+# ---------------------------------------------------------------------------
+# The remaining element-wise families (Appendix N (i))
+# ---------------------------------------------------------------------------
+
+NEW_OPTS = ["sgd", "rmsprop", "adagrad", "nadam", "radam"]
+NEW_VARIANTS = [("f32", "f32"), ("f32", "bf16"), ("bf16", "bf16"), ("bf16", "f32")]
+
+
+@pytest.mark.parametrize("opt", NEW_OPTS)
+@pytest.mark.parametrize("variant", NEW_VARIANTS, ids=lambda v: f"W{v[0]}-m{v[1]}")
+@pytest.mark.parametrize("shape", SHAPES[:2], ids=lambda s: "x".join(map(str, s)))
+def test_more_families_exact_bit_exact(opt, variant, shape):
+    w, st = variant
+    prob = _prob(shape, 17, "bf16", w, st, exact=True)
+    for t in (1, 7):   # RAdam: step 1 unrectified, step 7 rectified
+        got = gpu_step(opt, prob, t, seed=99, sr_w=w == "bf16", sr_moments=st == "bf16")
+        ref = oracle_step(opt, prob, w, st, t, seed=99, sr_w=w == "bf16", sr_moments=st == "bf16", mode="f32emu")
+        assert_bit_exact(got, ref, opt)
+
+
+@pytest.mark.parametrize("opt", NEW_OPTS)
+@pytest.mark.parametrize("variant", [("f32", "f32"), ("bf16", "bf16")], ids=lambda v: f"W{v[0]}-m{v[1]}")
+def test_more_families_random_within_tolerance(opt, variant):
+    w, st = variant
+    prob = _prob((256, 384, 200), 23, "bf16", w, st, exact=False)
+    for t in (2, 9):
+        got = gpu_step(opt, prob, t, seed=5, sr_w=w == "bf16")
+        rep = check_tolerance(opt, prob, w, st, t, got, seed=5, sr_w=w == "bf16")
+        print(opt, w, st, t, rep)
+
+
+@pytest.mark.parametrize("opt", NEW_OPTS)
+def test_more_families_fp32_inputs_bit_exact(opt):
+    prob = _prob((64, 256, 40), 4, "f32", "f32", "f32", exact=True)
+    got = gpu_step(opt, prob, 3)
+    ref = oracle_step(opt, prob, "f32", "f32", 3, mode="f32emu")
+    assert_bit_exact(got, ref, opt)

@@ -539,3 +539,93 @@ def test_planted_transposed_gradient_is_caught(monkeypatch):
     monkeypatch.setattr(O, "wgrad_f64", lambda dY, X: np.asarray(X, float).T @ np.asarray(dY, float))
     with pytest.raises(AssertionError):
         test_wgrad_brute_force_triple_loop()
+
+
+# ---------------------------------------------------------------------------
+# The element-wise families against PyTorch's optimizers of the same name
+# (float64, CPU): an independent library implementation of each rule.
+# ---------------------------------------------------------------------------
+
+def _torch_opt(name, p, h):
+    kw = dict(lr=h.lr, weight_decay=h.weight_decay, foreach=False)
+    if name == "adamw":
+        return torch.optim.AdamW([p], betas=(h.beta1, h.beta2), eps=h.eps, **kw)
+    if name == "sgdm":
+        return torch.optim.SGD([p], momentum=h.beta1, **kw)
+    if name == "sgd":
+        return torch.optim.SGD([p], momentum=0.0, **kw)
+    if name == "rmsprop":
+        return torch.optim.RMSprop([p], alpha=h.beta2, eps=h.eps, **kw)
+    if name == "adagrad":
+        return torch.optim.Adagrad([p], eps=h.eps, **kw)
+    if name == "nadam":
+        return torch.optim.NAdam([p], betas=(h.beta1, h.beta2), eps=h.eps, momentum_decay=h.momentum_decay, **kw)
+    if name == "radam":
+        return torch.optim.RAdam([p], betas=(h.beta1, h.beta2), eps=h.eps, **kw)
+    raise ValueError(name)
+
+
+_TORCH_STATE = {"adamw": ("exp_avg", "exp_avg_sq"), "nadam": ("exp_avg", "exp_avg_sq"),
+                "radam": ("exp_avg", "exp_avg_sq"), "sgdm": ("momentum_buffer",),
+                "rmsprop": ("square_avg",), "adagrad": ("sum",), "sgd": ()}
+
+
+@pytest.mark.parametrize("name", ["adamw", "sgdm", "sgd", "rmsprop", "adagrad", "nadam", "radam"])
+def test_rules_match_torch_optim_float64(name):
+    prev = torch.get_default_dtype()
+    torch.set_default_dtype(torch.float64)
+    try:
+        rs = np.random.RandomState(21)
+        W0 = rs.randn(5, 7) * 0.02
+        h = O.Hyper(lr=1e-3, beta1=0.9, beta2=0.99 if name == "rmsprop" else 0.999, eps=1e-8,
+                    weight_decay=0.01, momentum_decay=4e-3)
+        p = torch.nn.Parameter(torch.tensor(W0))
+        topt = _torch_opt(name, p, h)
+        W = W0.copy()
+        s0 = np.zeros_like(W0)
+        s1 = np.zeros_like(W0)
+        for t in range(1, 13):
+            G = rs.randn(5, 7) * 3.0
+            p.grad = torch.tensor(G)
+            topt.step()
+            if name == "adamw":
+                W, s0, s1 = O.adamw_f64(W, s0, s1, G, h, t)
+            elif name == "sgdm":
+                W, s0 = O.sgdm_f64(W, s0, G, h, t)
+            elif name == "sgd":
+                W = O.sgd_f64(W, G, h, t)
+            elif name == "rmsprop":
+                W, s0 = O.rmsprop_f64(W, s0, G, h, t)
+            elif name == "adagrad":
+                W, s0 = O.adagrad_f64(W, s0, G, h, t)
+            elif name == "nadam":
+                W, s0, s1 = O.nadam_f64(W, s0, s1, G, h, t)
+            else:
+                W, s0, s1 = O.radam_f64(W, s0, s1, G, h, t)
+            np.testing.assert_allclose(W, p.detach().numpy(), rtol=1e-12, atol=1e-15, err_msg=f"{name} W, t={t}")
+            st = topt.state[p]
+            for key, ours in zip(_TORCH_STATE[name], (s0, s1)):
+                np.testing.assert_allclose(ours, st[key].numpy(), rtol=1e-12, atol=1e-18,
+                                           err_msg=f"{name} {key}, t={t}")
+    finally:
+        torch.set_default_dtype(prev)
+
+
+def test_radam_crosses_its_rectification_threshold():
+    # With beta2 = 0.999 the rectification applies from step 6 on (rho_t > 5).
+    h = O.Hyper(lr=1e-3, beta1=0.9, beta2=0.999)
+    flags = [O.radam_rect(h, t)[0] for t in range(1, 9)]
+    assert flags == [False] * 5 + [True] * 3
+
+
+def test_nadam_first_step_closed_form():
+    # From zero state at t = 1 with constant g: m' = (1-b1) g, v' = (1-b2) g^2,
+    # so W' = W - lr g / (|g| + eps) * (1 + mu_2 (1 - b1) / (1 - mu_1 mu_2)).
+    h = O.Hyper(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, momentum_decay=4e-3)
+    mu1 = 0.9 * (1 - 0.5 * 0.96 ** 0.004)
+    mu2 = 0.9 * (1 - 0.5 * 0.96 ** 0.008)
+    G = np.array([[2.0, -0.5]]); W = np.array([[0.1, 0.2]])
+    W1, _, _ = O.nadam_f64(W, np.zeros_like(W), np.zeros_like(W), G, h, 1)
+    factor = 1 + mu2 * 0.1 / (1 - mu1 * mu2)
+    np.testing.assert_allclose(W1, W - 1e-3 * G / (np.abs(G) + 1e-8) * factor, rtol=1e-13)
+    assert abs(factor - 1.0564522) < 1e-6
