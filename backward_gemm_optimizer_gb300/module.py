@@ -1,0 +1,203 @@
+"""A PyTorch linear layer whose backward pass runs the fused step.
+
+``ForgeLinear`` computes ``y = x W^T`` in its forward pass. Its backward
+pass enqueues, on the current stream, the input gradient
+``dX = dY W`` (``forge_dgrad``, which must read the weights before they
+change: FORGE paper, Appendix A, Remark 1) and then the fused weight-
+gradient + optimizer step (``forge_wgrad_step_<rule>``), which updates
+the weight and its optimizer state in place. ``W.grad`` is never formed:
+the weight is a trainable parameter (so that autograd always reaches the
+backward, whether or not the input needs a gradient), but the backward
+returns no gradient for it.
+
+``ForgeStepManager`` plays the role of the pages' optimizer manager: it
+holds the hyper-parameters shared by the fused layers, and its
+``pre_step(lr=...)`` advances the step counter (and optionally the
+learning rate) before each forward/backward.
+
+Weights read by more than one backward path in a step (tied embeddings,
+experts reduced across ranks) must not be fused (Remark 1); keep those on
+a standard optimizer. The forward GEMM is a plain library GEMM
+(``torch.nn.functional.linear``) on a bf16 view of the weights; every
+backward computation runs in this library's kernels.
+"""
+
+from __future__ import annotations
+
+import dataclasses
+from typing import Dict, Iterable, List, Optional
+
+import torch
+
+from . import _lib as F
+
+_RULES = ("adamw", "sgdm", "lion", "sgd", "rmsprop", "adagrad", "nadam", "radam")
+_NSTATE = {"adamw": 2, "nadam": 2, "radam": 2, "sgdm": 1, "lion": 1, "rmsprop": 1, "adagrad": 1, "sgd": 0}
+
+
+@dataclasses.dataclass
+class StepConfig:
+    """Hyper-parameters of the fused rule and the current step (1-based)."""
+
+    rule: str = "adamw"
+    lr: float = 1e-3
+    beta1: float = 0.9
+    beta2: float = 0.999
+    eps: float = 1e-8
+    weight_decay: float = 0.0
+    momentum_decay: float = 4e-3
+    sr_w: bool = False
+    sr_moments: bool = False
+    seed: int = 0
+    step: int = 0
+
+
+class _ForgeLinearFn(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, x2d, weight, layer):
+        ctx.layer = layer
+        ctx.save_for_backward(x2d)
+        w = weight if weight.dtype == x2d.dtype else weight.to(x2d.dtype)
+        return torch.nn.functional.linear(x2d, w)
+
+    @staticmethod
+    def backward(ctx, dy2d):
+        (x2d,) = ctx.saved_tensors
+        layer: ForgeLinear = ctx.layer
+        dy2d = dy2d.contiguous()
+        dx = None
+        if ctx.needs_input_grad[0]:
+            dx = torch.empty(x2d.shape, dtype=x2d.dtype, device=x2d.device)
+            F.dgrad(dy2d, layer.weight, dx)                # reads W before the step (Remark 1)
+        layer._fused_step(x2d, dy2d)
+        return dx, None, None
+
+
+class ForgeLinear(torch.nn.Module):
+    """``y = x W^T`` (no bias) with the optimizer step fused into backward.
+
+    weight_dtype: storage of W (float32 master weights or bfloat16).
+    state_dtype: storage of the optimizer state (float32 or bfloat16).
+    config: a StepConfig shared with a ForgeStepManager (one is made if None).
+    """
+
+    def __init__(self, in_features: int, out_features: int, *, rule: str = "adamw",
+                 weight_dtype=torch.float32, state_dtype=torch.float32, config: Optional[StepConfig] = None,
+                 device=None):
+        super().__init__()
+        if rule not in _RULES:
+            raise ValueError(f"unknown rule {rule!r}; one of {_RULES}")
+        self.in_features, self.out_features = in_features, out_features
+        self.config = config if config is not None else StepConfig(rule=rule)
+        self.config.rule = rule
+        w = torch.empty((out_features, in_features), dtype=weight_dtype, device=device)
+        torch.nn.init.normal_(w, std=0.02)
+        self.weight = torch.nn.Parameter(w, requires_grad=True)
+        n = _NSTATE[rule]
+        for i, name in enumerate(("state0", "state1")):
+            t = torch.zeros((out_features, in_features), dtype=state_dtype, device=device) if i < n else None
+            self.register_buffer(name, t)
+
+    @classmethod
+    def from_linear(cls, linear: torch.nn.Linear, *, rule: str = "adamw", weight_dtype=torch.float32,
+                    state_dtype=torch.float32, config: Optional[StepConfig] = None) -> "ForgeLinear":
+        if linear.bias is not None:
+            raise ValueError("ForgeLinear has no bias; keep biased layers on a standard optimizer")
+        m = cls(linear.in_features, linear.out_features, rule=rule, weight_dtype=weight_dtype,
+                state_dtype=state_dtype, config=config, device=linear.weight.device)
+        with torch.no_grad():
+            m.weight.copy_(linear.weight.to(weight_dtype))
+        return m
+
+    def forward(self, x: torch.Tensor) -> torch.Tensor:
+        if not x.is_cuda:
+            raise RuntimeError("ForgeLinear runs on CUDA tensors only (there is no CPU path)")
+        if self.config.step < 1:
+            raise RuntimeError("call ForgeStepManager.pre_step() (step counter is 0) before the first forward")
+        shape = x.shape
+        x2d = x.reshape(-1, self.in_features)
+        if not x2d.is_contiguous():
+            x2d = x2d.contiguous()
+        y = _ForgeLinearFn.apply(x2d, self.weight, self)
+        return y.reshape(*shape[:-1], self.out_features)
+
+    def _fused_step(self, x2d: torch.Tensor, dy2d: torch.Tensor):
+        c = self.config
+        W, s0, s1 = self.weight, self.state0, self.state1
+        common = dict(step=c.step, seed=c.seed, sr_w=c.sr_w)
+        if c.rule == "adamw":
+            F.wgrad_step_adamw(x2d, dy2d, W, s0, s1, lr=c.lr, beta1=c.beta1, beta2=c.beta2, eps=c.eps,
+                               weight_decay=c.weight_decay, sr_moments=c.sr_moments, **common)
+        elif c.rule == "sgdm":
+            F.wgrad_step_sgdm(x2d, dy2d, W, s0, lr=c.lr, momentum=c.beta1, weight_decay=c.weight_decay,
+                              sr_moments=c.sr_moments, **common)
+        elif c.rule == "lion":
+            F.wgrad_step_lion(x2d, dy2d, W, s0, lr=c.lr, beta1=c.beta1, beta2=c.beta2,
+                              weight_decay=c.weight_decay, sr_moments=c.sr_moments, **common)
+        elif c.rule == "sgd":
+            F.wgrad_step_sgd(x2d, dy2d, W, lr=c.lr, weight_decay=c.weight_decay, **common)
+        elif c.rule == "rmsprop":
+            F.wgrad_step_rmsprop(x2d, dy2d, W, s0, lr=c.lr, alpha=c.beta2, eps=c.eps,
+                                 weight_decay=c.weight_decay, sr_moments=c.sr_moments, **common)
+        elif c.rule == "adagrad":
+            F.wgrad_step_adagrad(x2d, dy2d, W, s0, lr=c.lr, eps=c.eps, weight_decay=c.weight_decay,
+                                 sr_moments=c.sr_moments, **common)
+        elif c.rule == "nadam":
+            F.wgrad_step_nadam(x2d, dy2d, W, s0, s1, lr=c.lr, beta1=c.beta1, beta2=c.beta2, eps=c.eps,
+                               weight_decay=c.weight_decay, momentum_decay=c.momentum_decay,
+                               sr_moments=c.sr_moments, **common)
+        else:
+            F.wgrad_step_radam(x2d, dy2d, W, s0, s1, lr=c.lr, beta1=c.beta1, beta2=c.beta2, eps=c.eps,
+                               weight_decay=c.weight_decay, sr_moments=c.sr_moments, **common)
+
+    def extra_repr(self) -> str:
+        return (f"in_features={self.in_features}, out_features={self.out_features}, rule={self.config.rule}, "
+                f"weight={self.weight.dtype}, state={None if self.state0 is None else self.state0.dtype}")
+
+
+class ForgeStepManager:
+    """Shared step configuration of a model's ForgeLinear layers.
+
+    pre_step(lr=...) advances the 1-based step counter (and sets the learning
+    rate) before the forward/backward in which the fused layers update.
+    """
+
+    def __init__(self, model: torch.nn.Module, config: Optional[StepConfig] = None):
+        self.layers: List[ForgeLinear] = [m for m in model.modules() if isinstance(m, ForgeLinear)]
+        self.config = config if config is not None else (self.layers[0].config if self.layers else StepConfig())
+        for m in self.layers:
+            m.config = self.config
+        self._fused_ids = {id(m.weight) for m in self.layers}
+        self._model = model
+
+    def pre_step(self, lr: Optional[float] = None):
+        if lr is not None:
+            self.config.lr = float(lr)
+        self.config.step += 1
+
+    def get_non_fused_params(self) -> Iterable[torch.nn.Parameter]:
+        """Parameters a standard optimizer should still step (norms, embeddings...)."""
+        return [p for p in self._model.parameters() if id(p) not in self._fused_ids and p.requires_grad]
+
+    def fused_params(self) -> Iterable[torch.nn.Parameter]:
+        """The weights stepped inside backward (leave them out of any other optimizer)."""
+        return [m.weight for m in self.layers]
+
+    def state_dict(self) -> Dict:
+        return dataclasses.asdict(self.config)
+
+    def load_state_dict(self, d: Dict):
+        for k, v in d.items():
+            setattr(self.config, k, v)
+
+
+def replace_linears(model: torch.nn.Module, *, rule: str = "adamw", weight_dtype=torch.float32,
+                    state_dtype=torch.float32, config: Optional[StepConfig] = None) -> StepConfig:
+    """Swap every bias-free nn.Linear of `model` for a ForgeLinear sharing one StepConfig."""
+    cfg = config if config is not None else StepConfig(rule=rule)
+    for parent in list(model.modules()):
+        for name, child in list(parent.named_children()):
+            if isinstance(child, torch.nn.Linear) and child.bias is None:
+                setattr(parent, name, ForgeLinear.from_linear(child, rule=rule, weight_dtype=weight_dtype,
+                                                              state_dtype=state_dtype, config=cfg))
+    return cfg
