@@ -20,6 +20,8 @@ LIB_PATH = os.path.join(_HERE, "libforge.so")
 F32, BF16, I8B128 = 0, 1, 2
 FLAG_TILE_N_AUTO, FLAG_TILE_N_128, FLAG_TILE_N_64 = 0, 1, 2
 FLAG_TEST_FORCE_TIMEOUT = 0x100
+FLAG_BACKWARD_FUSED, FLAG_BACKWARD_SPLIT = 0x200, 0x400
+RULES = {"adamw": 0, "sgdm": 1, "lion": 2, "sgd": 3, "rmsprop": 4, "adagrad": 5, "nadam": 6, "radam": 7}
 
 STATUS_NAMES = {0: "FORGE_OK", 1: "FORGE_ERR_INVALID_ARG", 2: "FORGE_ERR_UNSUPPORTED",
                 3: "FORGE_ERR_ALIGNMENT", 4: "FORGE_ERR_CUDA", 5: "FORGE_ERR_TIMEOUT"}
@@ -27,7 +29,7 @@ STATUS_NAMES = {0: "FORGE_OK", 1: "FORGE_ERR_INVALID_ARG", 2: "FORGE_ERR_UNSUPPO
 EXPORTED = ("forge_wgrad_step_adamw", "forge_wgrad_step_sgdm", "forge_wgrad_step_lion",
             "forge_wgrad_step_sgd", "forge_wgrad_step_rmsprop", "forge_wgrad_step_adagrad",
             "forge_wgrad_step_nadam", "forge_wgrad_step_radam",
-            "forge_dgrad", "forge_sync_status", "forge_last_error", "forge_version",
+            "forge_dgrad", "forge_backward_step", "forge_sync_status", "forge_last_error", "forge_version",
             "forge_workspace_bytes")
 
 
@@ -67,10 +69,13 @@ def _load() -> ctypes.CDLL:
     lib.forge_wgrad_step_nadam.argtypes = [P(T), P(T), P(T), P(T), P(T), P(H), i64, u64, vp]
     lib.forge_wgrad_step_radam.argtypes = [P(T), P(T), P(T), P(T), P(T), P(H), i64, u64, vp]
     lib.forge_dgrad.argtypes = [P(T), P(T), P(T), vp]
+    lib.forge_backward_step.argtypes = [ctypes.c_int, P(T), P(T), P(T), P(T), P(T), P(T), P(H), i64, u64, vp,
+                                        ctypes.c_size_t, vp]
     lib.forge_sync_status.argtypes = [vp]
     for f in ("forge_wgrad_step_adamw", "forge_wgrad_step_sgdm", "forge_wgrad_step_lion",
               "forge_wgrad_step_sgd", "forge_wgrad_step_rmsprop", "forge_wgrad_step_adagrad",
-              "forge_wgrad_step_nadam", "forge_wgrad_step_radam", "forge_dgrad", "forge_sync_status"):
+              "forge_wgrad_step_nadam", "forge_wgrad_step_radam", "forge_dgrad", "forge_backward_step",
+              "forge_sync_status"):
         getattr(lib, f).restype = ctypes.c_int
     lib.forge_last_error.restype = ctypes.c_char_p
     lib.forge_version.restype = ctypes.c_char_p
@@ -215,6 +220,35 @@ def dgrad(dY, W_old, dX, *, stream=None):
     """dX = dY W_old (forge_dgrad); enqueue before the step that overwrites W."""
     tdY, tW, tdX = tensor_desc(dY), tensor_desc(W_old), tensor_desc(dX)
     _check(lib().forge_dgrad(ctypes.byref(tdY), ctypes.byref(tW), ctypes.byref(tdX), _stream(stream)))
+
+
+def backward_step(rule, X, dY, W, s0, s1, dX, *, lr, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0,
+                  momentum_decay=4e-3, momentum=None, alpha=None, step, seed=0, sr_w=False, sr_moments=False,
+                  workspace=None, flags=0, stream=None):
+    """dX = dY W_old and the fused step of `rule` on W and its state (forge_backward_step).
+
+    s0 / s1 are the rule's state tensors as the wgrad_step_<rule> call takes
+    them (None where the rule has fewer). `momentum` (SGD-momentum) and
+    `alpha` (RMSprop) are aliases of beta1 / beta2. `workspace`: a device
+    tensor of at least workspace_bytes(D_out, D_in, BT) bytes enables the
+    fused input-gradient path; without it dgrad and the step run apart.
+    """
+    if rule not in RULES:
+        raise ValueError(f"unknown rule {rule!r}; one of {tuple(RULES)}")
+    if momentum is not None:
+        beta1 = momentum
+    if alpha is not None:
+        beta2 = alpha
+    tX, tdY, tW, tdX = tensor_desc(X), tensor_desc(dY), tensor_desc(W), tensor_desc(dX)
+    t0 = tensor_desc(s0) if s0 is not None else None
+    t1 = tensor_desc(s1) if s1 is not None else None
+    h = _hyper(lr, beta1, beta2, eps, weight_decay, sr_w, sr_moments, flags, momentum_decay)
+    ws_ptr = ctypes.c_void_p(workspace.data_ptr() if workspace is not None and workspace.numel() else 0)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().forge_backward_step(RULES[rule], ctypes.byref(tX), ctypes.byref(tdY), ctypes.byref(tW),
+                                     ctypes.byref(t0) if t0 is not None else None,
+                                     ctypes.byref(t1) if t1 is not None else None, ctypes.byref(tdX),
+                                     ctypes.byref(h), int(step), _seed(seed), ws_ptr, ws_bytes, _stream(stream)))
 
 
 def sync_status(stream=None):

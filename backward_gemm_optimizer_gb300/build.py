@@ -32,6 +32,7 @@ SOURCES = [
     "wgrad_tc_radam.cu",
     "wgrad_simt.cu",
     "dgrad_tc.cu",
+    "dx_reduce.cu",
 ]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -231,10 +231,52 @@ int mkind(int dt) { return dt == FORGE_F32 ? M_F32 : dt == FORGE_BF16 ? M_BF16 :
 
 constexpr uint64_t kTimeoutNs = 4000000000ull;  // 4 s: far beyond any healthy wait
 
+// ------------------------------------------------------------------ fused input gradient: geometry
+
+// The fused backward kernel uses 64-column tiles, walks them column by
+// column in contiguous per-CTA ranges, and keeps a dX partial for up to six
+// 128-token blocks in tensor memory beside its two gradient accumulators.
+constexpr int kDxBN = 64;
+constexpr int64_t kDxMaxTokens = 768;
+
+struct DxGeometry {
+  int tiles_m = 0, tiles_n = 0, num_tiles = 0, grid = 0, runs = 0, num_kb = 0;
+  int64_t slab = 0;    // floats per partial slab
+  size_t bytes = 0;    // workspace bytes
+};
+
+DxGeometry dx_geometry(int64_t d_out, int64_t d_in, int64_t bt, int sms) {
+  DxGeometry g;
+  if (bt < 1 || bt > kDxMaxTokens || d_out < 1 || d_in < 1 || sms < 1) return g;
+  g.tiles_m = static_cast<int>((d_out + 127) / 128);
+  g.tiles_n = static_cast<int>((d_in + kDxBN - 1) / kDxBN);
+  g.num_tiles = g.tiles_m * g.tiles_n;
+  g.grid = g.num_tiles < sms ? g.num_tiles : sms;
+  const int64_t T = g.num_tiles, G = g.grid;
+  for (int64_t c = 0; c < G; ++c) {
+    const int64_t lo = c * T / G, hi = (c + 1) * T / G;
+    if (hi <= lo) continue;
+    const int r = static_cast<int>((hi - 1) / g.tiles_m - lo / g.tiles_m + 1);
+    if (r > g.runs) g.runs = r;
+  }
+  g.num_kb = static_cast<int>((bt + 127) / 128);
+  g.slab = static_cast<int64_t>(g.num_kb) * 128 * kDxBN;
+  g.bytes = static_cast<size_t>(G) * g.runs * g.slab * sizeof(float);
+  return g;
+}
+
+// Extra arguments of the fused backward pass (dX and its workspace).
+struct DxArgs {
+  forge_tensor* dX;
+  void* ws;
+  size_t ws_bytes;
+};
+
 // ------------------------------------------------------------------ the fused step
 
 forge_status wgrad_step(int opt, const forge_tensor* X, const forge_tensor* dY, forge_tensor* W, forge_tensor* m,
-                        forge_tensor* v, const forge_hyper* h, int64_t step, uint64_t seed, forge_stream_t stream) {
+                        forge_tensor* v, const forge_hyper* h, int64_t step, uint64_t seed, forge_stream_t stream,
+                        const DxArgs* dx = nullptr) {
   const char* oname = opt_name(opt);
   const int nst = opt_nstate(opt);
   if (X == nullptr || dY == nullptr || W == nullptr || h == nullptr || (nst >= 1 && m == nullptr))
@@ -251,7 +293,8 @@ forge_status wgrad_step(int opt, const forge_tensor* X, const forge_tensor* dY, 
   if (step > 0xFFFFFFFFll) return fail(FORGE_ERR_INVALID_ARG, "%s: step exceeds 2^32 - 1", oname);
   if (!finite(h->lr) || !finite(h->beta1) || !finite(h->beta2) || !finite(h->eps) || !finite(h->weight_decay))
     return fail(FORGE_ERR_INVALID_ARG, "%s: non-finite hyper-parameter", oname);
-  if (h->flags & ~(FORGE_FLAG_TILE_N_MASK | FORGE_FLAG_TEST_FORCE_TIMEOUT))
+  if (h->flags & ~(FORGE_FLAG_TILE_N_MASK | FORGE_FLAG_TEST_FORCE_TIMEOUT | FORGE_FLAG_BACKWARD_FUSED |
+                   FORGE_FLAG_BACKWARD_SPLIT))
     return fail(FORGE_ERR_INVALID_ARG, "%s: unknown flags 0x%x", oname, h->flags);
 
   const int64_t bt = X->rows, d_in = X->cols, d_out = dY->cols;
@@ -320,23 +363,25 @@ forge_status wgrad_step(int opt, const forge_tensor* X, const forge_tensor* dY, 
   const int tiles_m = static_cast<int>((d_out + 127) / 128);
   int bn = 128;
   const uint32_t force = h->flags & FORGE_FLAG_TILE_N_MASK;
-  if (force == FORGE_FLAG_TILE_N_64) bn = 64;
+  if (dx != nullptr) bn = kDxBN;  // the fused input gradient fixes the tile width
+  else if (force == FORGE_FLAG_TILE_N_64) bn = 64;
   else if (force == FORGE_FLAG_TILE_N_128) bn = 128;
   else if (force != FORGE_FLAG_TILE_N_AUTO) return fail(FORGE_ERR_INVALID_ARG, "%s: bad tile flag", oname);
   else if (mk != M_Q8 && tiles_m * ((d_in + 127) / 128) < dev->sms) bn = 64;  // too few tiles for one wave
   if (mk == M_Q8 && bn != 128)
     return fail(FORGE_ERR_UNSUPPORTED, "%s: 8-bit block moments need 128-column tiles", oname);
-  const int deep = (bt >= 1024 && bn == 128) ? 1 : 0;
+  const int deep = (dx == nullptr && bt >= 1024 && bn == 128) ? 1 : 0;
   const int tiles_n = static_cast<int>((d_in + bn - 1) / bn);
+  const uint32_t box_tokens = dx != nullptr ? 128u : 64u;  // tokens per operand stage
 
   WgradTcParams p;
   std::memset(&p, 0, sizeof(p));
   if (bt > 0) {  // with BT = 0 the kernel issues no operand loads and needs no operand maps
-    if ((st = encode_2d(&p.tm_dy, dY, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B,
-                        "dY")) != FORGE_OK)
+    if ((st = encode_2d(&p.tm_dy, dY, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, box_tokens,
+                        CU_TENSOR_MAP_SWIZZLE_128B, "dY")) != FORGE_OK)
       return st;
-    if ((st = encode_2d(&p.tm_x, X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B, "X")) !=
-        FORGE_OK)
+    if ((st = encode_2d(&p.tm_x, X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, box_tokens, CU_TENSOR_MAP_SWIZZLE_128B,
+                        "X")) != FORGE_OK)
       return st;
   }
   if ((st = encode_state(&p.tm_w, W, "W")) != FORGE_OK) return st;
@@ -360,7 +405,7 @@ forge_status wgrad_step(int opt, const forge_tensor* X, const forge_tensor* dY, 
   p.tiles_m = tiles_m;
   p.tiles_n = tiles_n;
   p.num_tiles = tiles_m * tiles_n;
-  p.num_kb = static_cast<int>((bt + 63) / 64);
+  p.num_kb = static_cast<int>((bt + box_tokens - 1) / box_tokens);
   p.group_m = 8;
   p.step = static_cast<uint32_t>(step);
   p.seed_lo = static_cast<uint32_t>(seed);
@@ -371,9 +416,25 @@ forge_status wgrad_step(int opt, const forge_tensor* X, const forge_tensor* dY, 
   p.timeout_ns = kTimeoutNs;
 
   TcLaunch l{};
-  l.opt = opt; l.wk = wk; l.mk = mk; l.bn = bn; l.deep = deep;
+  l.opt = opt; l.wk = wk; l.mk = mk; l.bn = bn; l.deep = deep; l.dx = dx != nullptr ? 1 : 0;
   l.grid = p.num_tiles < dev->sms ? p.num_tiles : dev->sms;
   l.stream = s;
+  DxGeometry g;
+  if (dx != nullptr) {
+    g = dx_geometry(d_out, d_in, bt, dev->sms);
+    if (g.grid != l.grid || g.num_tiles != p.num_tiles || g.num_kb != p.num_kb)
+      return fail(FORGE_ERR_INVALID_ARG, "%s: internal geometry mismatch", oname);
+    if (dx->ws == nullptr || dx->ws_bytes < g.bytes)
+      return fail(FORGE_ERR_INVALID_ARG, "%s: fused backward needs %zu workspace bytes (got %zu)", oname, g.bytes,
+                  dx->ws_bytes);
+    if (reinterpret_cast<uintptr_t>(dx->ws) % 16 != 0)
+      return fail(FORGE_ERR_ALIGNMENT, "%s: workspace not 16-byte aligned", oname);
+    p.w_ptr = W->data;
+    p.ld_w = W->ld;
+    p.dx_ws = static_cast<float*>(dx->ws);
+    p.dx_runs = g.runs;
+    p.dx_slab = g.slab;
+  }
   cudaError_t e;
   switch (opt) {
     case OPT_ADAMW: e = launch_wgrad_tc_adamw(p, l); break;
@@ -386,7 +447,80 @@ forge_status wgrad_step(int opt, const forge_tensor* X, const forge_tensor* dY, 
     default: e = launch_wgrad_tc_radam(p, l); break;
   }
   if (e != cudaSuccess) return fail(FORGE_ERR_CUDA, "%s launch: %s", oname, cudaGetErrorString(e));
+  if (dx != nullptr) {
+    DxReduceParams r{};
+    r.ws = static_cast<const float*>(dx->ws);
+    r.dX = dx->dX->data;
+    r.ld_dx = dx->dX->ld;
+    r.dx_bf16 = dx->dX->dtype == FORGE_BF16 ? 1 : 0;
+    r.bt = static_cast<int>(bt);
+    r.d_in = static_cast<int>(d_in);
+    r.tiles_m = g.tiles_m;
+    r.num_tiles = g.num_tiles;
+    r.grid = g.grid;
+    r.runs = g.runs;
+    r.slab = g.slab;
+    e = launch_dx_reduce(r, dev->sms, s);
+    if (e != cudaSuccess) return fail(FORGE_ERR_CUDA, "%s: dX reduction launch: %s", oname, cudaGetErrorString(e));
+  }
   return ok();
+}
+
+// Whether the fused backward pass beats dgrad + step for this layer: it
+// saves the dgrad kernel's read of W and its launch, and costs writing and
+// re-reading one fp32 dX partial slab per (CTA, column) pair.
+bool dx_worthwhile(const DxGeometry& g, int64_t d_out, int64_t d_in, int w_bytes) {
+  const double saved = static_cast<double>(d_out) * static_cast<double>(d_in) * w_bytes;
+  const double partial = 2.0 * static_cast<double>(g.grid + g.tiles_n) * static_cast<double>(g.slab) * 4.0;
+  return saved >= partial;
+}
+
+forge_status dgrad_impl(const forge_tensor* dY, const forge_tensor* W_old, forge_tensor* dX, forge_stream_t stream);
+
+forge_status backward_step(int opt, const forge_tensor* X, const forge_tensor* dY, forge_tensor* W, forge_tensor* s0,
+                           forge_tensor* s1, forge_tensor* dX, const forge_hyper* h, int64_t step, uint64_t seed,
+                           void* ws, size_t ws_bytes, forge_stream_t stream) {
+  const char* oname = opt_name(opt);
+  if (X == nullptr || dY == nullptr || W == nullptr || dX == nullptr || h == nullptr)
+    return fail(FORGE_ERR_INVALID_ARG, "backward_step(%s): null argument", oname);
+  const bool want_fused = (h->flags & FORGE_FLAG_BACKWARD_FUSED) != 0;
+  const bool want_split = (h->flags & FORGE_FLAG_BACKWARD_SPLIT) != 0;
+  if (want_fused && want_split)
+    return fail(FORGE_ERR_INVALID_ARG, "backward_step(%s): both BACKWARD_FUSED and BACKWARD_SPLIT set", oname);
+  const int64_t bt = X->rows, d_in = X->cols, d_out = dY->cols;
+  if (dX->dtype != FORGE_BF16 && dX->dtype != FORGE_F32)
+    return fail(FORGE_ERR_UNSUPPORTED, "backward_step(%s): dX must be bf16 or f32", oname);
+  forge_status st;
+  if ((st = check_tensor(dX, "dX", bt, d_in, true)) != FORGE_OK) return st;
+  const int nst = opt_nstate(opt);
+  const bool q8 = nst >= 1 && s0 != nullptr && s0->dtype == FORGE_I8B128;
+  const uint32_t tile = h->flags & FORGE_FLAG_TILE_N_MASK;
+  const bool possible = X->dtype == FORGE_BF16 && !q8 && bt >= 1 && bt <= kDxMaxTokens && d_in > 0 && d_out > 0 &&
+                        (tile == FORGE_FLAG_TILE_N_AUTO || tile == FORGE_FLAG_TILE_N_64);
+  bool fused = false;
+  if (possible && !want_split) {
+    DeviceInfo* dev = nullptr;
+    if ((st = device_info(&dev)) != FORGE_OK) return st;
+    const DxGeometry g = dx_geometry(d_out, d_in, bt, dev->sms);
+    fused = want_fused || (ws != nullptr && ws_bytes >= g.bytes && dx_worthwhile(g, d_out, d_in, W->dtype == FORGE_F32 ? 4 : 2));
+  }
+  if (want_fused && !fused)
+    return fail(FORGE_ERR_UNSUPPORTED,
+                "backward_step(%s): the fused input gradient needs bf16 X/dY, fp32 or bf16 state, 1 <= BT <= %lld "
+                "and 64-column tiles",
+                oname, (long long)kDxMaxTokens);
+  if (fused) {
+    const DxArgs a{dX, ws, ws_bytes};
+    return wgrad_step(opt, X, dY, W, s0, s1, h, step, seed, stream, &a);
+  }
+  // Split path: dX from the weights before the step, then the step.
+  if (X->dtype != FORGE_BF16)
+    return fail(FORGE_ERR_UNSUPPORTED, "backward_step(%s): dX needs bf16 dY (the fp32-input step has no dgrad)",
+                oname);
+  if ((st = dgrad_impl(dY, W, dX, stream)) != FORGE_OK) return st;
+  forge_hyper h2 = *h;
+  h2.flags &= ~(FORGE_FLAG_BACKWARD_FUSED | FORGE_FLAG_BACKWARD_SPLIT);
+  return wgrad_step(opt, X, dY, W, s0, s1, &h2, step, seed, stream);
 }
 
 }  // namespace
@@ -436,7 +570,25 @@ forge_status forge_wgrad_step_radam(const forge_tensor* X, const forge_tensor* d
   return wgrad_step(OPT_RADAM, X, dY, W, m, v, h, step, seed, stream);
 }
 
+forge_status forge_backward_step(forge_rule rule, const forge_tensor* X, const forge_tensor* dY, forge_tensor* W,
+                                 forge_tensor* s0, forge_tensor* s1, forge_tensor* dX, const forge_hyper* h,
+                                 int64_t step, uint64_t seed, void* workspace, size_t workspace_bytes,
+                                 forge_stream_t stream) {
+  if (static_cast<int>(rule) < OPT_ADAMW || static_cast<int>(rule) > OPT_RADAM)
+    return fail(FORGE_ERR_INVALID_ARG, "backward_step: unknown rule %d", static_cast<int>(rule));
+  return backward_step(static_cast<int>(rule), X, dY, W, s0, s1, dX, h, step, seed, workspace, workspace_bytes,
+                       stream);
+}
+
 forge_status forge_dgrad(const forge_tensor* dY, const forge_tensor* W_old, forge_tensor* dX, forge_stream_t stream) {
+  return dgrad_impl(dY, W_old, dX, stream);
+}
+
+}  // extern "C"
+
+namespace {
+
+forge_status dgrad_impl(const forge_tensor* dY, const forge_tensor* W_old, forge_tensor* dX, forge_stream_t stream) {
   if (dY == nullptr || W_old == nullptr || dX == nullptr) return fail(FORGE_ERR_INVALID_ARG, "dgrad: null argument");
   const int64_t bt = dY->rows, d_out = dY->cols, d_in = W_old->cols;
   if (bt < 0 || d_out < 0 || d_in < 0) return fail(FORGE_ERR_INVALID_ARG, "dgrad: negative size");
@@ -494,6 +646,10 @@ forge_status forge_dgrad(const forge_tensor* dY, const forge_tensor* W_old, forg
   return ok();
 }
 
+}  // namespace
+
+extern "C" {
+
 forge_status forge_sync_status(forge_stream_t stream) {
   cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(FORGE_ERR_CUDA, "cudaStreamSynchronize: %s", cudaGetErrorString(e));
@@ -517,6 +673,10 @@ forge_status forge_sync_status(forge_stream_t stream) {
       case WAIT_TEST_HOOK: what = "forced-timeout test hook"; break;
       case WAIT_MMA_DRAIN: what = "MMA issuer draining after an abort"; break;
       case WAIT_DRAIN: what = "producer draining after an abort"; break;
+      case WAIT_WB_FULL: what = "MMA issuer waiting for the bf16 W_old tile"; break;
+      case WAIT_WB_EMPTY: what = "converters waiting for the W_old buffer"; break;
+      case WAIT_DX_FULL: what = "converters waiting for a dX partial"; break;
+      case WAIT_DX_EMPTY: what = "MMA issuer waiting for the dX partial to be written out"; break;
       default: break;
     }
     return fail(FORGE_ERR_TIMEOUT, "device wait gave up: %s (code 0x%x)", what, host[0]);
@@ -526,8 +686,12 @@ forge_status forge_sync_status(forge_stream_t stream) {
 
 const char* forge_last_error(void) { return g_last_error.c_str(); }
 
-const char* forge_version(void) { return "0.2.0"; }
+const char* forge_version(void) { return "0.3.0"; }
 
-size_t forge_workspace_bytes(int64_t, int64_t, int64_t) { return 0; }
+size_t forge_workspace_bytes(int64_t d_out, int64_t d_in, int64_t bt) {
+  DeviceInfo* dev = nullptr;
+  if (device_info(&dev) != FORGE_OK) return 0;
+  return dx_geometry(d_out, d_in, bt, dev->sms).bytes;
+}
 
 }  // extern "C"

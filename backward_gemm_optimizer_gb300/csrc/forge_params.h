@@ -27,6 +27,10 @@ enum : uint32_t {
   WAIT_TEST_HOOK = 0xF009,    // epilogue: the forced-timeout test barrier
   WAIT_MMA_DRAIN = 0xF00A,    // MMA issuer: in-flight MMAs after an abort
   WAIT_DRAIN = 0xF00B,        // a producer's in-flight loads after an abort
+  WAIT_WB_FULL = 0xF00C,      // MMA issuer: bf16 W_old tile converted (fused dX)
+  WAIT_WB_EMPTY = 0xF00D,     // converters: previous W_old tile consumed
+  WAIT_DX_FULL = 0xF00E,      // converters: dX partial complete
+  WAIT_DX_EMPTY = 0xF00F,     // MMA issuer: dX partial written out
 };
 
 constexpr uint32_t FLAG_TILE_N_MASK = 7u;
@@ -50,6 +54,23 @@ struct alignas(128) WgradTcParams {
   int sr_w, sr_m;
   uint32_t flags;
   uint64_t timeout_ns;
+  // Fused input gradient (DX kernels only).
+  void* w_ptr;        // W_old, read by the converters
+  int64_t ld_w;
+  float* dx_ws;       // workspace: [grid][dx_runs] slabs of dx_slab floats
+  int dx_runs;        // column runs per CTA (slab slots)
+  int64_t dx_slab;    // floats per slab: num_kb * 128 * 64
+};
+
+// Deterministic reduction of the dX partial slabs into dX.
+struct DxReduceParams {
+  const float* ws;
+  void* dX;
+  int64_t ld_dx;
+  int dx_bf16;
+  int bt, d_in;
+  int tiles_m, num_tiles, grid, runs;
+  int64_t slab;
 };
 
 // fp32 fused step (fp32 X / dY), plain CUDA cores.
@@ -89,6 +110,7 @@ struct TcLaunch {
   int opt, wk, mk;
   int bn;       // tile width (64 or 128)
   int deep;     // 1: deeper operand pipeline for long token axes
+  int dx;       // 1: fused input gradient (64-column tiles, fp32 / bf16 state)
   int grid;
   cudaStream_t stream;
 };
@@ -104,6 +126,7 @@ cudaError_t launch_wgrad_tc_nadam(const WgradTcParams& p, const TcLaunch& l);
 cudaError_t launch_wgrad_tc_radam(const WgradTcParams& p, const TcLaunch& l);
 cudaError_t launch_wgrad_simt(const WgradSimtParams& p, int opt, int wk, int mk, cudaStream_t stream);
 cudaError_t launch_dgrad_tc(const DgradParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_dx_reduce(const DxReduceParams& p, int sms, cudaStream_t stream);
 
 // Whether a (opt, wk, mk, bn, deep) variant has a tensor-core kernel.
 bool wgrad_tc_supported(int opt, int wk, int mk, int bn, int deep);

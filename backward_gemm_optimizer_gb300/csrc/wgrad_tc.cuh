@@ -20,6 +20,25 @@
 //               latency of the per-element arithmetic (divide, square root,
 //               Philox rounds).
 //
+// With DX (the fused backward pass) the same kernel also forms the input
+// gradient dX = dY W_old from the W tile it is about to update (Appendix A,
+// Remark 1: dX must see the weights before the step):
+//
+//   * operand stages hold 128 tokens, so each dY stage serves both
+//     products -- read MN-major as the A operand of G = dY^T X, and K-major
+//     as the A operand of dX = dY W;
+//   * warps 20-23 (converters) read each tile's W_old from global memory
+//     ahead of its MMAs, round it to bf16 and write it as the MN-major B
+//     operand of dX (Wb); the state ring reads the same W again for the
+//     update, mostly from L2;
+//   * each CTA walks a contiguous range of tiles ordered column by column,
+//     and a persistent fp32 dX partial (all tokens x the tile's 64 columns)
+//     accumulates in TMEM beside the gradient accumulators while the CTA
+//     stays in one column; when the column changes, the converter warps
+//     (which between them reach all four TMEM lane quadrants) write the
+//     partial to a workspace slab, and a separate reduction sums a
+//     column's slabs in a fixed order (deterministic dX).
+//
 // The accumulator never leaves TMEM / registers: no gradient tile is ever
 // written to global memory (Proposition 3). Both operands are token-major
 // in memory, so A = dY^T and B = X are fed to the tensor cores as MN-major
@@ -38,11 +57,13 @@
 
 namespace forge {
 
-template <int OPT, int WK, int MK, int BN_, int STAGES_, int NBUF_>
+template <int OPT, int WK, int MK, int BN_, int STAGES_, int NBUF_, bool DX_ = false>
 struct TcCfg {
+  static constexpr bool DX = DX_;      // fused input gradient (see above)
   static constexpr int BM = 128;       // tile rows (D_out), one per TMEM lane
   static constexpr int BN = BN_;       // tile columns (D_in)
-  static constexpr int BK = 64;        // tokens per operand stage
+  static constexpr int BK = DX ? 128 : 64;  // tokens per operand stage
+  static constexpr int BOX = BK * 128; // bytes of one 64-column operand box (BK rows of 128 bytes)
   static constexpr int CW = 32;        // state chunk width (columns)
   static constexpr int STAGES = STAGES_;
   static constexpr int NBUF = NBUF_;
@@ -58,14 +79,20 @@ struct TcCfg {
   static constexpr int W_CH = BM * CW * WE;
   static constexpr int M_CH = NST >= 1 ? BM * CW * ME : 0;
   static constexpr int V_CH = TWO ? M_CH : 0;
-  static constexpr int SLOT_BYTES = ((W_CH + M_CH + V_CH + 1023) / 1024) * 1024;
-  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NBUF * SLOT_BYTES;
-  static constexpr int TMEM_COLS = (2 * BN <= 128) ? 128 : (2 * BN <= 256 ? 256 : 512);
+  static constexpr int SLOT_BYTES = W_CH + M_CH + V_CH > 0 ? ((W_CH + M_CH + V_CH + 1023) / 1024) * 1024 : 1024;
+  static constexpr int WB_BYTES = DX ? BM * BN * 2 : 0;   // bf16 W_old tile (B operand of dX)
+  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + WB_BYTES + NBUF * SLOT_BYTES;
+  static constexpr int TMEM_COLS = DX ? 512 : ((2 * BN <= 128) ? 128 : (2 * BN <= 256 ? 256 : 512));
+  static constexpr int DX_COL = 2 * BN;          // first TMEM column of the dX partial
+  static constexpr int DX_MAX_BLOCKS = DX ? (512 - DX_COL) / BN : 0;  // 128-token blocks that fit
   static constexpr int EPI_WARPS = 16;
   static constexpr int EPI_THREADS = EPI_WARPS * 32;
-  static constexpr int NUM_THREADS = 128 + EPI_THREADS;
+  static constexpr int CONV_THREADS = DX ? 128 : 0;  // warps 20-23
+  static constexpr int NUM_THREADS = 128 + EPI_THREADS + CONV_THREADS;
   static constexpr int QCOLS = 8;                // columns per epilogue thread per chunk
   static constexpr uint32_t IDESC = make_idesc_bf16(BM, BN, 1, 1);
+  // dX: A = dY (M = 128 tokens, K-major), B = Wb (N = BN, MN-major).
+  static constexpr uint32_t IDESC_DX = make_idesc_bf16(128, BN, 0, 1);
 
 };
 
@@ -156,6 +183,56 @@ __device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, 
   tn = in_g / gsize;
 }
 
+// The tiles one CTA processes: a grid-stride walk of the grouped raster, or
+// (fused input gradient) a contiguous range of the column-major tile order,
+// so that consecutive tiles share a column and its dX partial.
+struct TileWalk {
+  int first, step, end;
+};
+
+template <bool DX>
+__device__ __forceinline__ TileWalk tile_walk(const WgradTcParams& p) {
+  if constexpr (DX) {
+    const int64_t T = p.num_tiles, G = gridDim.x, c = blockIdx.x;
+    return TileWalk{static_cast<int>(c * T / G), 1, static_cast<int>((c + 1) * T / G)};
+  } else {
+    return TileWalk{static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), p.num_tiles};
+  }
+}
+
+template <bool DX>
+__device__ __forceinline__ void walk_coords(const WgradTcParams& p, int tile, int& tm, int& tn) {
+  if constexpr (DX) {
+    tm = tile % p.tiles_m;
+    tn = tile / p.tiles_m;
+  } else {
+    tile_coords(tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+  }
+}
+
+// Write a CTA's dX partial (tokens x BN fp32, token-major) from tensor
+// memory to its workspace slab: the warp with TMEM lane quadrant q writes
+// tokens 32q .. 32q + 31 of every 128-token block, one token row per
+// thread. Runs once per tile column of the CTA.
+template <int BN>
+__device__ __forceinline__ void write_dx_partial(float* slab, uint32_t tmem_dx, int q, int lane, int num_kb) {
+  for (int b = 0; b < num_kb; ++b) {
+    const int tok = b * 128 + q * 32 + lane;
+    const uint32_t ta = tmem_dx + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(b * BN);
+    float4* dst = reinterpret_cast<float4*>(slab + static_cast<int64_t>(tok) * BN);
+#pragma unroll 1
+    for (int c16 = 0; c16 < BN / 16; ++c16) {
+      uint32_t d[16];
+      tmem_ld_32x32b_x16(ta + c16 * 16, d);
+      tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        dst[c16 * 4 + j] = make_float4(__uint_as_float(d[4 * j]), __uint_as_float(d[4 * j + 1]),
+                                       __uint_as_float(d[4 * j + 2]), __uint_as_float(d[4 * j + 3]));
+    }
+  }
+}
+
 // Bounded wait on an mbarrier phase. Returns false if the CTA is aborting
 // (another role gave up) or if this wait exceeded `limit_ns`, in which case
 // it raises the abort flag and records `code` in the device status word.
@@ -193,10 +270,12 @@ __device__ __forceinline__ void drain_ring(uint64_t* full, int ring, uint32_t is
   }
 }
 
-template <int OPT, int WK, int MK, int BN, int STAGES, int NBUF>
-__global__ void __launch_bounds__(128 + 512, 1) wgrad_step_tc_kernel(const __grid_constant__ WgradTcParams p) {
-  using C = TcCfg<OPT, WK, MK, BN, STAGES, NBUF>;
+template <int OPT, int WK, int MK, int BN, int STAGES, int NBUF, bool DX>
+__global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX>::NUM_THREADS, 1)
+    wgrad_step_tc_kernel(const __grid_constant__ WgradTcParams p) {
+  using C = TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX>;
   static_assert(BN == 64 || BN == 128, "tile width");
+  static_assert(!DX || (BN == 64 && !C::Q8), "fused input gradient: 64-column tiles, fp32 / bf16 state");
   static_assert(!C::Q8 || BN == 128, "8-bit blocks span one 128-column tile row");
   static_assert(!C::Q8 || OPT == OPT_ADAMW || OPT == OPT_SGDM || OPT == OPT_LION, "8-bit state rules");
   static_assert(!C::Q8 || NBUF >= C::NCH, "8-bit moments hold a whole tile of slots");
@@ -209,13 +288,16 @@ __global__ void __launch_bounds__(128 + 512, 1) wgrad_step_tc_kernel(const __gri
   __shared__ __align__(8) uint64_t tm_full[2], tm_empty[2];
   __shared__ __align__(8) uint64_t red_bar[2];
   __shared__ __align__(8) uint64_t never_bar, mma_drain_bar;
+  __shared__ __align__(8) uint64_t wb_full, wb_empty, dx_full, dx_empty;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
-  __shared__ float red_sh[2][2][4][128];  // [tile parity][|m'| | v'][column quarter][row]
+  __shared__ float red_sh[C::Q8 ? 2 : 1][2][4][128];  // [tile parity][|m'| | v'][column quarter][row]
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* op_base = smem;
-  uint8_t* st_base = smem + STAGES * C::STAGE_BYTES;
+  uint8_t* wb_base = smem + STAGES * C::STAGE_BYTES;
+  uint8_t* st_base = wb_base + C::WB_BYTES;
+  const TileWalk tw = tile_walk<DX>(p);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -235,6 +317,10 @@ __global__ void __launch_bounds__(128 + 512, 1) wgrad_step_tc_kernel(const __gri
     }
     mbar_init(&never_bar, 1);
     mbar_init(&mma_drain_bar, 1);
+    mbar_init(&wb_full, C::CONV_THREADS > 0 ? C::CONV_THREADS : 1);
+    mbar_init(&wb_empty, 1);
+    mbar_init(&dx_full, 1);
+    mbar_init(&dx_empty, 4);
     abort_sh = 0;
     fence_mbar_init();
   }
@@ -259,9 +345,9 @@ __global__ void __launch_bounds__(128 + 512, 1) wgrad_step_tc_kernel(const __gri
     if (lane == 0) {
       uint32_t kseq = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+      for (int tile = tw.first; ok && tile < tw.end; tile += tw.step) {
         int tm, tn;
-        tile_coords(tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+        walk_coords<DX>(p, tile, tm, tn);
         for (int kb = 0; kb < p.num_kb; ++kb, ++kseq) {
           const int s = static_cast<int>(kseq % STAGES);
           const uint32_t ph = (kseq / STAGES) & 1u;
@@ -270,10 +356,10 @@ __global__ void __launch_bounds__(128 + 512, 1) wgrad_step_tc_kernel(const __gri
           uint8_t* b = a + C::A_BYTES;
           mbar_arrive_expect_tx(&op_full[s], C::STAGE_BYTES);
           tma_load_2d(a, &p.tm_dy, &op_full[s], tm * C::BM, kb * C::BK);
-          tma_load_2d(a + 8192, &p.tm_dy, &op_full[s], tm * C::BM + 64, kb * C::BK);
+          tma_load_2d(a + C::BOX, &p.tm_dy, &op_full[s], tm * C::BM + 64, kb * C::BK);
 #pragma unroll
           for (int bb = 0; bb < BN / 64; ++bb)
-            tma_load_2d(b + bb * 8192, &p.tm_x, &op_full[s], tn * BN + bb * 64, kb * C::BK);
+            tma_load_2d(b + bb * C::BOX, &p.tm_x, &op_full[s], tn * BN + bb * 64, kb * C::BK);
         }
       }
       if (!ok) drain_ring(op_full, STAGES, kseq, p.status);
@@ -284,12 +370,16 @@ __global__ void __launch_bounds__(128 + 512, 1) wgrad_step_tc_kernel(const __gri
       uint32_t kseq = 0;
       bool ok = true;
       int it = 0;
-      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++it) {
+      uint32_t runs_done = 0;  // dX partials handed to the epilogue
+      for (int tile = tw.first; ok && tile < tw.end; tile += tw.step, ++it) {
         const int buf = it & 1;
         const uint32_t eph = ((it >> 1) & 1) ^ 1u;
         if (!bwait(&tm_empty[buf], eph, abort_flag, p.status, WAIT_TMEM_EMPTY, lim)) { ok = false; break; }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
+        // dX: the first tile of a column starts a fresh partial.
+        const bool run_first = DX && (tile == tw.first || tile % p.tiles_m == 0);
+        const bool run_last = DX && (tile + 1 == tw.end || (tile + 1) % p.tiles_m == 0);
         for (int kb = 0; kb < p.num_kb; ++kb, ++kseq) {
           const int s = static_cast<int>(kseq % STAGES);
           const uint32_t ph = (kseq / STAGES) & 1u;
@@ -299,14 +389,48 @@ __global__ void __launch_bounds__(128 + 512, 1) wgrad_step_tc_kernel(const __gri
           const uint32_t b0 = a0 + C::A_BYTES;
 #pragma unroll
           for (int kk = 0; kk < C::BK / 16; ++kk) {
-            // 16 tokens = two 8-row K groups of 1024 bytes; MN atoms 8192 bytes apart.
-            const uint64_t ad = make_smem_desc(a0 + kk * 2048, 8192, 1024, 2);
-            const uint64_t bd = make_smem_desc(b0 + kk * 2048, 8192, 1024, 2);
+            // 16 tokens = two 8-row K groups of 1024 bytes; MN atoms one box apart.
+            const uint64_t ad = make_smem_desc(a0 + kk * 2048, C::BOX, 1024, 2);
+            const uint64_t bd = make_smem_desc(b0 + kk * 2048, C::BOX, 1024, 2);
             umma_f16(d_tmem, ad, bd, C::IDESC, (kb > 0 || kk > 0) ? 1u : 0u);
+          }
+          if constexpr (DX) {
+            if (kb == 0) {
+              // The previous column's partial must have been written out, and
+              // this tile's bf16 W_old must be in place.
+              if (run_first && runs_done > 0 &&
+                  !bwait(&dx_empty, (runs_done - 1) & 1u, abort_flag, p.status, WAIT_DX_EMPTY, lim)) {
+                ok = false;
+                break;
+              }
+              if (!bwait(&wb_full, it & 1, abort_flag, p.status, WAIT_WB_FULL, lim)) { ok = false; break; }
+              tc_fence_after_sync();
+            }
+            // dX[128 tokens of stage kb][BN] += dY[tokens][128 rows of the tile] * Wb.
+            // A: K-major (K = D_out rows of the tile, 64 per 128-byte box row),
+            // 8-token groups 1024 bytes apart; a K step of 16 advances 32 bytes.
+            // B: MN-major Wb, 8-row K groups of 1024 bytes, 16 rows = 2048 bytes.
+            const uint32_t dx_tmem = tmem_base + static_cast<uint32_t>(C::DX_COL + kb * BN);
+            const uint32_t wb0 = smem_u32(wb_base);
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t ad = make_smem_desc(a0 + hh * C::BOX + kk * 32, 16, 1024, 2);
+                const uint64_t bd = make_smem_desc(wb0 + (hh * 4 + kk) * 2048, 8192, 1024, 2);
+                umma_f16(dx_tmem, ad, bd, C::IDESC_DX, (run_first && hh == 0 && kk == 0) ? 0u : 1u);
+              }
+            }
           }
           umma_commit(&op_empty[s]);
         }
         if (!ok) break;
+        if constexpr (DX) {
+          if (p.num_kb > 0) {
+            umma_commit(&wb_empty);
+            if (run_last) { umma_commit(&dx_full); ++runs_done; }
+          }
+        }
         umma_commit(&tm_full[buf]);
       }
       if (!ok) {
@@ -323,9 +447,9 @@ __global__ void __launch_bounds__(128 + 512, 1) wgrad_step_tc_kernel(const __gri
     if (lane == 0) {
       uint32_t cseq = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+      for (int tile = tw.first; ok && tile < tw.end; tile += tw.step) {
         int tm, tn;
-        tile_coords(tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+        walk_coords<DX>(p, tile, tm, tn);
         for (int c = 0; c < C::NCH; ++c, ++cseq) {
           const int s = static_cast<int>(cseq % NBUF);
           const uint32_t ph = (cseq / NBUF) & 1u;
@@ -345,9 +469,9 @@ __global__ void __launch_bounds__(128 + 512, 1) wgrad_step_tc_kernel(const __gri
     if (lane == 0) {
       uint32_t cseq = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+      for (int tile = tw.first; ok && tile < tw.end; tile += tw.step) {
         int tm, tn;
-        tile_coords(tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+        walk_coords<DX>(p, tile, tm, tn);
         for (int c = 0; c < C::NCH; ++c, ++cseq) {
           const int s = static_cast<int>(cseq % NBUF);
           const uint32_t ph = (cseq / NBUF) & 1u;
@@ -364,13 +488,14 @@ __global__ void __launch_bounds__(128 + 512, 1) wgrad_step_tc_kernel(const __gri
       }
       bulk_wait_group0();
     }
-  } else {
+  } else if (warp < 4 + C::EPI_WARPS) {
     // ------------------------------------------------------------ epilogue (warps 4..19)
     const int q = warp & 3;          // TMEM lane quadrant this warp may access
     const int h = (warp - 4) >> 2;   // 8-column quarter of each 32-column chunk
     const int r = q * 32 + lane;     // tile row == TMEM lane
     const StepScalars sc = p.sc;
     uint32_t cseq = 0;
+    uint32_t run_seq = 0;            // dX partials written out
     int it = 0;
     bool ok = true;
 
@@ -380,9 +505,9 @@ __global__ void __launch_bounds__(128 + 512, 1) wgrad_step_tc_kernel(const __gri
       ok = __all_sync(0xFFFFFFFFu, ok);
     }
 
-    for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++it) {
+    for (int tile = tw.first; ok && tile < tw.end; tile += tw.step, ++it) {
       int tm, tn;
-      tile_coords(tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+      walk_coords<DX>(p, tile, tm, tn);
       const int buf = it & 1;
       ok = bwait(&tm_full[buf], (it >> 1) & 1, abort_flag, p.status, WAIT_TMEM_FULL, lim);
       ok = __all_sync(0xFFFFFFFFu, ok);
@@ -568,6 +693,85 @@ __global__ void __launch_bounds__(128 + 512, 1) wgrad_step_tc_kernel(const __gri
       if (lane == 0) mbar_arrive(&tm_empty[buf]);
     }
   }
+  if constexpr (DX) {
+    if (warp >= 4 + C::EPI_WARPS) {
+      // ---------------------------------------------------------- converters (warps 20-23)
+      // Per tile: load this thread's 8 items of W_old (tile row r = item / 8,
+      // 8-column group g = item % 8), round to bf16, and once the MMAs of
+      // the previous tile have released Wb, write them MN-major with the
+      // 128-byte swizzle (row r is 128 bytes, group g lands at g ^ (r % 8)).
+      // After the last tile of a column: write the dX partial out.
+      const int ct = threadIdx.x - (128 + C::EPI_THREADS);
+      const int q = warp & 3;  // TMEM lane quadrant of this warp
+      int it = 0;
+      uint32_t run_seq = 0;
+      bool ok = p.num_kb > 0;
+      for (int tile = tw.first; ok && tile < tw.end; tile += tw.step, ++it) {
+        int tm, tn;
+        walk_coords<DX>(p, tile, tm, tn);
+        uint4 o[8];
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          if constexpr (WK == W_F32) {
+            float4 u[4][2];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int item = ct + 128 * (half * 4 + j);
+              const int orow = tm * C::BM + (item >> 3), col = tn * BN + (item & 7) * 8;
+              if (orow < p.d_out && col < p.d_in) {  // D_in % 8 == 0: all 8 columns or none
+                const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(p.w_ptr) +
+                                                                    static_cast<int64_t>(orow) * p.ld_w + col);
+                u[j][0] = __ldcg(src);
+                u[j][1] = __ldcg(src + 1);
+              } else {
+                u[j][0] = make_float4(0.f, 0.f, 0.f, 0.f);
+                u[j][1] = u[j][0];
+              }
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              o[half * 4 + j] = make_uint4(pack_bf16x2_rn(u[j][0].x, u[j][0].y), pack_bf16x2_rn(u[j][0].z, u[j][0].w),
+                                           pack_bf16x2_rn(u[j][1].x, u[j][1].y), pack_bf16x2_rn(u[j][1].z, u[j][1].w));
+          } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int item = ct + 128 * (half * 4 + j);
+              const int orow = tm * C::BM + (item >> 3), col = tn * BN + (item & 7) * 8;
+              o[half * 4 + j] = (orow < p.d_out && col < p.d_in)
+                                    ? __ldcg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.w_ptr) +
+                                                                            static_cast<int64_t>(orow) * p.ld_w + col))
+                                    : make_uint4(0u, 0u, 0u, 0u);
+            }
+          }
+        }
+        ok = bwait(&wb_empty, (it & 1) ^ 1u, abort_flag, p.status, WAIT_WB_EMPTY, lim);
+        ok = __all_sync(0xFFFFFFFFu, ok);
+        if (!ok) break;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int item = ct + 128 * j;
+          const int rr = item >> 3, g = item & 7;
+          *reinterpret_cast<uint4*>(wb_base + rr * 128 + ((g ^ (rr & 7)) << 4)) = o[j];
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&wb_full);
+
+        if (tile + 1 == tw.end || (tile + 1) % p.tiles_m == 0) {
+          ok = bwait(&dx_full, run_seq & 1u, abort_flag, p.status, WAIT_DX_FULL, lim);
+          ok = __all_sync(0xFFFFFFFFu, ok);
+          if (!ok) break;
+          tc_fence_after_sync();
+          const int run = tn - tw.first / p.tiles_m;
+          float* slab = p.dx_ws + (static_cast<int64_t>(blockIdx.x) * p.dx_runs + run) * p.dx_slab;
+          write_dx_partial<BN>(slab, tmem_base + static_cast<uint32_t>(C::DX_COL), q, lane, p.num_kb);
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&dx_empty);
+          ++run_seq;
+        }
+      }
+    }
+  }
 
   // ------------------------------------------------------------ teardown
   tc_fence_before_sync();
@@ -579,10 +783,10 @@ __global__ void __launch_bounds__(128 + 512, 1) wgrad_step_tc_kernel(const __gri
   }
 }
 
-template <int OPT, int WK, int MK, int BN, int STAGES, int NBUF>
+template <int OPT, int WK, int MK, int BN, int STAGES, int NBUF, bool DX>
 cudaError_t launch_tc_variant(const WgradTcParams& p, int grid, cudaStream_t stream) {
-  using C = TcCfg<OPT, WK, MK, BN, STAGES, NBUF>;
-  auto kern = wgrad_step_tc_kernel<OPT, WK, MK, BN, STAGES, NBUF>;
+  using C = TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX>;
+  auto kern = wgrad_step_tc_kernel<OPT, WK, MK, BN, STAGES, NBUF, DX>;
   // The opt-in shared-memory size is a per-device function attribute: set
   // it once per device (bit d of the mask) before the first launch there.
   static unsigned long long attr_mask = 0ull;

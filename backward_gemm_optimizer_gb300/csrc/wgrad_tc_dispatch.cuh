@@ -11,10 +11,10 @@ namespace forge {
 // shared memory (barriers + the 8 KB absmax exchange) is accounted for.
 constexpr int kDynSmemBudget = 227 * 1024 - 9 * 1024;
 
-template <int OPT, int WK, int MK, int BN, int STAGES>
+template <int OPT, int WK, int MK, int BN, int STAGES, bool DX = false>
 constexpr int slots_that_fit() {
-  using C = TcCfg<OPT, WK, MK, BN, STAGES, 2>;
-  const int avail = kDynSmemBudget - 1024 - STAGES * C::STAGE_BYTES;
+  using C = TcCfg<OPT, WK, MK, BN, STAGES, 2, DX>;
+  const int avail = kDynSmemBudget - 1024 - STAGES * C::STAGE_BYTES - C::WB_BYTES;
   const int n = avail / C::SLOT_BYTES;
   return n > 8 ? 8 : n;
 }
@@ -33,11 +33,23 @@ cudaError_t launch_one(const WgradTcParams& p, int grid, cudaStream_t stream) {
   constexpr int S = pick_stages<OPT, WK, MK, BN, DEEP>();
   constexpr int N = slots_that_fit<OPT, WK, MK, BN, S>();
   static_assert(N >= ((MK == M_Q8) ? 4 : 2), "state ring does not fit");
-  return launch_tc_variant<OPT, WK, MK, BN, S, N>(p, grid, stream);
+  return launch_tc_variant<OPT, WK, MK, BN, S, N, false>(p, grid, stream);
+}
+
+// Fused input gradient: 64-column tiles, two 128-token operand stages.
+template <int OPT, int WK, int MK>
+cudaError_t launch_dx(const WgradTcParams& p, int grid, cudaStream_t stream) {
+  constexpr int N = slots_that_fit<OPT, WK, MK, 64, 2, true>();
+  static_assert(N >= 2, "state ring does not fit");
+  return launch_tc_variant<OPT, WK, MK, 64, 2, N, true>(p, grid, stream);
 }
 
 template <int OPT, int WK, int MK>
 cudaError_t launch_mk(const WgradTcParams& p, const TcLaunch& l) {
+  if (l.dx) {
+    if constexpr (MK == M_Q8) return cudaErrorInvalidValue;
+    else return l.bn == 64 && !l.deep ? launch_dx<OPT, WK, MK>(p, l.grid, l.stream) : cudaErrorInvalidValue;
+  }
   if constexpr (MK == M_Q8) {
     if (l.bn != 128) return cudaErrorInvalidValue;
     return l.deep ? launch_one<OPT, WK, MK, 128, 1>(p, l.grid, l.stream)

@@ -94,6 +94,22 @@ typedef struct {
  * step returns without touching W or its moments; forge_sync_status() then
  * reports FORGE_ERR_TIMEOUT. */
 #define FORGE_FLAG_TEST_FORCE_TIMEOUT 0x100u
+/* forge_backward_step only: force the fused input gradient (an error if
+ * this layer or workspace cannot take it), or force dgrad + step. */
+#define FORGE_FLAG_BACKWARD_FUSED 0x200u
+#define FORGE_FLAG_BACKWARD_SPLIT 0x400u
+
+/* Optimizer rule of forge_backward_step. */
+typedef enum {
+  FORGE_RULE_ADAMW = 0,
+  FORGE_RULE_SGDM = 1,
+  FORGE_RULE_LION = 2,
+  FORGE_RULE_SGD = 3,
+  FORGE_RULE_RMSPROP = 4,
+  FORGE_RULE_ADAGRAD = 5,
+  FORGE_RULE_NADAM = 6,
+  FORGE_RULE_RADAM = 7
+} forge_rule;
 
 typedef struct {
   double lr;            /* eta */
@@ -227,6 +243,38 @@ forge_status forge_dgrad(const forge_tensor* dY, const forge_tensor* W_old, forg
                          forge_stream_t stream);
 
 /*
+ * forge_backward_step -- the whole backward pass of one linear layer with
+ * its optimizer step: dX = dY W_old (Remark 1, Appendix A) and the fused
+ * weight-gradient step of `rule` (Algorithm 1 for AdamW; Appendix N (i)
+ * for the other element-wise rules).
+ *
+ * s0, s1: the rule's state, as the forge_wgrad_step_<rule> call takes it
+ * (AdamW / NAdam / RAdam: m, v; SGD-momentum / Lion: m; RMSprop /
+ * AdaGrad: v; SGD: none -- pass NULL for unused slots). dX: FORGE_BF16 or
+ * FORGE_F32, BT x D_in.
+ *
+ * Two paths. The fused path reads each W tile once: the tile that is about
+ * to be updated also feeds a second tensor-core product, dY_tile x
+ * W_old_tile, whose fp32 partial sums accumulate in tensor memory per
+ * column of tiles and are added up in a fixed order by a second kernel
+ * (deterministic dX). It needs bf16 X / dY, fp32 or bf16 state,
+ * 1 <= BT <= 768, and `workspace` of forge_workspace_bytes(D_out, D_in, BT)
+ * bytes (device memory, 16-byte aligned, owned by the caller, contents
+ * need not be initialised; it must not be shared by calls in flight at the
+ * same time). The split path enqueues forge_dgrad and then the step.
+ * With no FORGE_FLAG_BACKWARD_* flag the library takes the fused path when
+ * it applies, the workspace is large enough, and it saves more traffic
+ * than its partial sums cost; FORGE_FLAG_BACKWARD_FUSED /
+ * FORGE_FLAG_BACKWARD_SPLIT force a path. The fused path uses 128 x 64
+ * gradient tiles (a FORGE_FLAG_TILE_N_128 request selects the split path).
+ * dX differs between the paths only in the fp32 summation order.
+ */
+forge_status forge_backward_step(forge_rule rule, const forge_tensor* X, const forge_tensor* dY, forge_tensor* W,
+                                 forge_tensor* s0, forge_tensor* s1, forge_tensor* dX, const forge_hyper* h,
+                                 int64_t step, uint64_t seed, void* workspace, size_t workspace_bytes,
+                                 forge_stream_t stream);
+
+/*
  * forge_sync_status -- synchronise `stream`, then read and clear the
  * device status word of the current device. Returns FORGE_ERR_TIMEOUT if
  * a kernel's bounded wait gave up since the last call (the message names
@@ -237,13 +285,17 @@ forge_status forge_sync_status(forge_stream_t stream);
 /* Message of the last failed call on this thread ("" if none). */
 const char* forge_last_error(void);
 
-/* Library version, e.g. "0.1.0". */
+/* Library version, e.g. "0.3.0". */
 const char* forge_version(void);
 
 /*
- * forge_workspace_bytes -- device scratch the steps need beyond their
- * arguments. It is 0: the persistent scheduler keeps its state on chip,
- * and the gradient never leaves the tensor-memory accumulators.
+ * forge_workspace_bytes -- device scratch that forge_backward_step's fused
+ * path needs for a layer of this shape on the current device: one fp32
+ * slab of ceil(BT/128)*128 x 64 dX partial sums per (CTA, tile column)
+ * pair. 0 when the fused path does not apply (BT = 0 or BT > 768) or the
+ * device cannot be queried. The forge_wgrad_step_* calls and forge_dgrad
+ * need no scratch: their schedulers keep their state on chip and the
+ * gradient never leaves the tensor-memory accumulators.
  */
 size_t forge_workspace_bytes(int64_t d_out, int64_t d_in, int64_t bt);
 
