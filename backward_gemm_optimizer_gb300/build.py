@@ -33,6 +33,7 @@ SOURCES = [
     "wgrad_simt.cu",
     "dgrad_tc.cu",
     "dx_reduce.cu",
+    "forge_no_alloc.cu",
 ]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -39,6 +39,18 @@ forge_status ok() {
   return FORGE_OK;
 }
 
+}  // namespace
+
+namespace forge {
+
+// Records `msg` as the calling thread's forge_last_error() and returns `st`
+// (for entry points defined in other translation units).
+forge_status set_error(forge_status st, const char* msg) { return fail(st, "%s", msg); }
+
+}  // namespace forge
+
+namespace {
+
 // ------------------------------------------------------------------ driver entry points
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,

@@ -275,6 +275,36 @@ forge_status forge_backward_step(forge_rule rule, const forge_tensor* X, const f
                                  forge_stream_t stream);
 
 /*
+ * forge_backward_step_no_alloc -- forge_backward_step on the fused path,
+ * for callers that cannot allocate device memory: code running under a
+ * framework whose allocator owns the whole device, plug-ins that get
+ * tensors but no allocator, or hosts that forbid allocation once training
+ * has started. The paper has no counterpart of this entry point.
+ *
+ * Same arguments and results as forge_backward_step with
+ * FORGE_FLAG_BACKWARD_FUSED, minus the workspace: the dX partial sums go
+ * to a 64 MiB array compiled into the library (held on every GPU that
+ * loads this part of the library, until the process exits). It calls no
+ * allocator. A layer whose forge_workspace_bytes() exceeds 64 MiB is
+ * rejected with FORGE_ERR_UNSUPPORTED before any work; every
+ * Llama-3.1-8B projection fits at BT <= 512 on a 152-SM GPU. Layers the
+ * fused path does not take (8-bit state, BT > 768) return
+ * FORGE_ERR_UNSUPPORTED as well.
+ *
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * All calls share the one array and it keeps what the last call left
+ * there; nothing in it needs to start at zero, since every partial sum is
+ * written before it is read. Calls whose kernels overlap on the GPU (on
+ * different streams, or from different threads) race on the array: order
+ * them on one stream.
+ */
+forge_status forge_backward_step_no_alloc(forge_rule rule, const forge_tensor* X, const forge_tensor* dY,
+                                          forge_tensor* W, forge_tensor* s0, forge_tensor* s1, forge_tensor* dX,
+                                          const forge_hyper* h, int64_t step, uint64_t seed,
+                                          forge_stream_t stream);
+
+/*
  * forge_sync_status -- synchronise `stream`, then read and clear the
  * device status word of the current device. Returns FORGE_ERR_TIMEOUT if
  * a kernel's bounded wait gave up since the last call (the message names
