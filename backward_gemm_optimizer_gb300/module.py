@@ -1,11 +1,13 @@
 """A PyTorch linear layer whose backward pass runs the fused step.
 
 ``ForgeLinear`` computes ``y = x W^T`` in its forward pass. Its backward
-pass enqueues, on the current stream, the input gradient
-``dX = dY W`` (``forge_dgrad``, which must read the weights before they
-change: FORGE paper, Appendix A, Remark 1) and then the fused weight-
-gradient + optimizer step (``forge_wgrad_step_<rule>``), which updates
-the weight and its optimizer state in place. ``W.grad`` is never formed:
+pass enqueues, on the current stream, one ``forge_backward_step``: the
+input gradient ``dX = dY W`` from the weights before they change (FORGE
+paper, Appendix A, Remark 1) and the fused weight-gradient + optimizer
+step, which updates the weight and its optimizer state in place -- in one
+pass over W where the library's policy takes the fused path (it gets a
+workspace from a per-stream cache here), else as ``forge_dgrad`` followed
+by ``forge_wgrad_step_<rule>``. ``W.grad`` is never formed:
 the weight is a trainable parameter (so that autograd always reaches the
 backward, whether or not the input needs a gradient), but the backward
 returns no gradient for it.
@@ -50,6 +52,24 @@ class StepConfig:
     sr_moments: bool = False
     seed: int = 0
     step: int = 0
+    backward_flags: int = 0  # FLAG_BACKWARD_FUSED / FLAG_BACKWARD_SPLIT force a path; 0 = library policy
+
+
+# Workspaces of the fused backward path, one per (device, stream): calls on
+# one stream run in order, so they can share one; grown on demand.
+_WORKSPACES: Dict[tuple, torch.Tensor] = {}
+
+
+def _workspace(device: torch.device, nbytes: int) -> Optional[torch.Tensor]:
+    if nbytes <= 0:
+        return None
+    stream = torch.cuda.current_stream(device)
+    key = (device.index, stream.cuda_stream)
+    buf = _WORKSPACES.get(key)
+    if buf is None or buf.numel() < nbytes:
+        buf = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        _WORKSPACES[key] = buf
+    return buf
 
 
 class _ForgeLinearFn(torch.autograd.Function):
@@ -68,8 +88,9 @@ class _ForgeLinearFn(torch.autograd.Function):
         dx = None
         if ctx.needs_input_grad[0]:
             dx = torch.empty(x2d.shape, dtype=x2d.dtype, device=x2d.device)
-            F.dgrad(dy2d, layer.weight, dx)                # reads W before the step (Remark 1)
-        layer._fused_step(x2d, dy2d)
+            layer._backward(x2d, dy2d, dx)                 # dX from W before the step (Remark 1)
+        else:
+            layer._fused_step(x2d, dy2d)
         return dx, None, None
 
 
@@ -120,6 +141,14 @@ class ForgeLinear(torch.nn.Module):
             x2d = x2d.contiguous()
         y = _ForgeLinearFn.apply(x2d, self.weight, self)
         return y.reshape(*shape[:-1], self.out_features)
+
+    def _backward(self, x2d: torch.Tensor, dy2d: torch.Tensor, dx: torch.Tensor):
+        c = self.config
+        ws = _workspace(x2d.device, F.workspace_bytes(self.out_features, self.in_features, x2d.shape[0]))
+        F.backward_step(c.rule, x2d, dy2d, self.weight, self.state0, self.state1, dx, lr=c.lr, beta1=c.beta1,
+                        beta2=c.beta2, eps=c.eps, weight_decay=c.weight_decay, momentum_decay=c.momentum_decay,
+                        step=c.step, seed=c.seed, sr_w=c.sr_w, sr_moments=c.sr_moments, workspace=ws,
+                        flags=c.backward_flags)
 
     def _fused_step(self, x2d: torch.Tensor, dy2d: torch.Tensor):
         c = self.config

@@ -3,10 +3,13 @@ weight-gradient / optimizer step of one Llama-3.1-8B linear layer.
 
 Default workload (the headline configuration): the MLP up-projection,
 W 14336 x 4096 fp32 master weights with fp32 AdamW moments, BT = 512
-tokens of bf16 activations X and upstream gradients dY. One step =
-forge_dgrad (dX = dY W_old) followed by forge_wgrad_step_adamw (G = dY^T X
-and the AdamW step, fused). The state (1.4 GB) is far larger than L2 and
-L2 is also flushed between timed steps.
+tokens of bf16 activations X and upstream gradients dY. One step = one
+forge_backward_step call: the input gradient dX = dY W_old and the fused
+weight-gradient / AdamW step, in one pass over W where the layer allows it
+(BT <= 768, fp32 / bf16 state), else forge_dgrad followed by
+forge_wgrad_step_adamw. The state (1.4 GB) is far larger than L2 and L2 is
+also flushed between timed steps. The two-kernel split path is timed as
+well and reported beside the headline (split_* keys).
 
 Prints one JSON line (see the keys below). ``--impl reference`` times the
 CPU oracle instead (a bounded row sample, extrapolated).
@@ -59,12 +62,22 @@ def algorithmic_bytes(d_out, d_in, bt, w, st):
     return int(round(d_out * d_in * state_bytes_per_param(w, st))) + 2 * bt * (d_in + d_out)
 
 
+def backward_algorithmic_bytes(d_out, d_in, bt, w, st):
+    """The fused backward pass: the step's bytes plus the bf16 dX written once."""
+    return algorithmic_bytes(d_out, d_in, bt, w, st) + 2 * bt * d_in
+
+
+def fused_path(bt, st):
+    """Whether forge_backward_step can take the one-pass path for this workload."""
+    return 1 <= bt <= 768 and st != "q8"
+
+
 def dgrad_algorithmic_bytes(d_out, d_in, bt, w):
     return d_out * d_in * (4 if w == "f32" else 2) + 2 * bt * d_out + 2 * bt * d_in
 
 
 KERNEL_SOURCES = ["wgrad_tc.cuh", "wgrad_tc_dispatch.cuh", "wgrad_tc_adamw.cu", "forge_math.cuh", "forge_ptx.cuh",
-                  "forge_params.h"]
+                  "forge_params.h", "dx_reduce.cu"]
 
 
 def kernel_source_hash() -> str:
@@ -240,10 +253,27 @@ def make_state(d_out, d_in, bt, w, st, dev, seed=0):
     return out, host
 
 
-def one_step(F, s, w, st, t, stream):
+def one_step(F, s, w, st, t, stream, ws, flags):
+    """One backward pass of the layer through the public API."""
+    if st == "q8":  # 8-bit state descriptors carry their scales: dgrad, then the rule's call
+        F.dgrad(s["dY"], s["W"], s["dX"], stream=stream)
+        F.wgrad_step_adamw(s["X"], s["dY"], s["W"], s["m"], s["v"], m_scale=s.get("m_scale"),
+                           v_scale=s.get("v_scale"), step=t, seed=1234, sr_w=(w == "bf16"), stream=stream, **HYPER)
+    else:
+        F.backward_step("adamw", s["X"], s["dY"], s["W"], s["m"], s["v"], s["dX"], step=t, seed=1234,
+                        sr_w=(w == "bf16"), workspace=ws, flags=flags, stream=stream, **HYPER)
+
+
+def split_step(F, s, w, t, stream, events=None):
+    if events is not None:
+        events[0].record(stream)
     F.dgrad(s["dY"], s["W"], s["dX"], stream=stream)
+    if events is not None:
+        events[1].record(stream)
     F.wgrad_step_adamw(s["X"], s["dY"], s["W"], s["m"], s["v"], m_scale=s.get("m_scale"),
                        v_scale=s.get("v_scale"), step=t, seed=1234, sr_w=(w == "bf16"), stream=stream, **HYPER)
+    if events is not None:
+        events[2].record(stream)
 
 
 def run_gpu(args, rank, world, local_rank):
@@ -257,13 +287,17 @@ def run_gpu(args, rank, world, local_rank):
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)   # 256 MB > L2
 
+    fused = fused_path(bt, st)
+    flags = F.FLAG_BACKWARD_FUSED if fused else F.FLAG_BACKWARD_SPLIT
+    ws = torch.empty(max(16, F.workspace_bytes(d_out, d_in, bt)), dtype=torch.uint8, device=dev) if fused else None
     t = 1
     for _ in range(args.warmup):
-        one_step(F, s, w, st, t, stream); t += 1
+        one_step(F, s, w, st, t, stream, ws, flags); t += 1
     F.sync_status(stream)
 
+    # ---- the headline: one backward pass per step, inputs resident in HBM
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
     sampler = ClockSampler(local_rank)
     barrier(world)
     torch.cuda.synchronize(dev)
@@ -273,22 +307,30 @@ def run_gpu(args, rank, world, local_rank):
     for i in range(K):
         flush.fill_(float(i))                      # evict L2 between steps (not timed)
         ev[i][0].record(stream)
-        F.dgrad(s["dY"], s["W"], s["dX"], stream=stream)
+        one_step(F, s, w, st, t, stream, ws, flags)
         ev[i][1].record(stream)
-        F.wgrad_step_adamw(s["X"], s["dY"], s["W"], s["m"], s["v"], m_scale=s.get("m_scale"),
-                           v_scale=s.get("v_scale"), step=t, seed=1234, sr_w=(w == "bf16"), stream=stream,
-                           **HYPER)
-        ev[i][2].record(stream)
         t += 1
     torch.cuda.synchronize(dev)
     wall = time.perf_counter() - wall0
     barrier(world)
     clocks = sampler.stop()
     F.sync_status(stream)
-    step_ms = [ev[i][0].elapsed_time(ev[i][2]) for i in range(K)]
-    dgrad_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
-    fused_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    step_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
     total_ms = max_over_ranks(sum(step_ms), world, dev)
+
+    # ---- the split path (forge_dgrad, then the fused step), for comparison
+    KS = max(1, min(K, args.split_steps))
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(KS)]
+    for _ in range(3):
+        split_step(F, s, w, t, stream); t += 1
+    for i in range(KS):
+        flush.fill_(float(i))
+        split_step(F, s, w, t, stream, evs[i]); t += 1
+    torch.cuda.synchronize(dev)
+    F.sync_status(stream)
+    split_ms = [evs[i][0].elapsed_time(evs[i][2]) for i in range(KS)]
+    dgrad_ms = [evs[i][0].elapsed_time(evs[i][1]) for i in range(KS)]
+    wstep_ms = [evs[i][1].elapsed_time(evs[i][2]) for i in range(KS)]
 
     # ---- end to end through the public API, host buffers, copies timed
     KE = max(1, min(args.e2e_steps, K))
@@ -299,7 +341,7 @@ def run_gpu(args, rank, world, local_rank):
     for i in range(KE):
         s["X"].copy_(host["X"], non_blocking=True)
         s["dY"].copy_(host["dY"], non_blocking=True)
-        one_step(F, s, w, st, t, stream); t += 1
+        one_step(F, s, w, st, t, stream, ws, flags); t += 1
         host["dX"].copy_(s["dX"], non_blocking=True)
         F.sync_status(stream)                       # reads the status word back each step
     e1.record(stream)
@@ -312,36 +354,47 @@ def run_gpu(args, rank, world, local_rank):
         return
     hbm, tflops, peak_src = load_peaks()
     us = total_ms * 1000.0 / K
-    fused_us = statistics.mean(fused_ms) * 1000.0
-    fused_med = statistics.median(fused_ms) * 1000.0
-    dgrad_us = statistics.mean(dgrad_ms) * 1000.0
-    abytes = algorithmic_bytes(d_out, d_in, bt, w, st)
-    achieved = abytes / (fused_us * 1e-6) / 1e9
-    flops = 2.0 * bt * d_out * d_in
+    med_us = statistics.median(step_ms) * 1000.0
+    flops = 2.0 * bt * d_out * d_in * (2 if fused else 1)
+    if fused:
+        abytes = backward_algorithmic_bytes(d_out, d_in, bt, w, st)
+        kern_us = statistics.mean(step_ms) * 1000.0
+        kernel = "wgrad_step_tc_kernel with the fused input gradient + dx_reduce_kernel (one forge_backward_step)"
+    else:
+        abytes = algorithmic_bytes(d_out, d_in, bt, w, st)
+        kern_us = statistics.mean(wstep_ms) * 1000.0
+        kernel = "wgrad_step_tc_kernel (split path: the step after forge_dgrad)"
+    achieved = abytes / (kern_us * 1e-6) / 1e9
+    tfl = flops / (kern_us * 1e-6) / 1e12
     t_roof = max(abytes / (hbm * 1e9), flops / (tflops * 1e12)) * 1e6
     bound = "hbm" if abytes / (hbm * 1e9) >= flops / (tflops * 1e12) else "tensor"
     traffic, _ = load_traffic(args.workload)
+    split_us = statistics.mean(split_ms) * 1000.0
+    wstep_us = statistics.mean(wstep_ms) * 1000.0
+    sbytes = algorithmic_bytes(d_out, d_in, bt, w, st)
     line = {
         "metric": METRIC, "value": round(us, 2), "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(us / 1000.0, 4), "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": args.workload, "d_out": d_out, "d_in": d_in, "bt": bt, "w_storage": w,
-                   "moment_storage": st, "optimizer": "adamw", "step": "forge_dgrad + forge_wgrad_step_adamw",
+                   "moment_storage": st, "optimizer": "adamw",
+                   "step": "forge_backward_step, fused input gradient (one pass over W)" if fused else
+                           "forge_dgrad + forge_wgrad_step_adamw",
                    "l2": "flushed between steps (256 MB write) and state 1.4 GB > L2",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "fused_kernel_us": round(fused_us, 2), "fused_kernel_median_us": round(fused_med, 2),
-        "dgrad_kernel_us": round(dgrad_us, 2),
-        "fused_GBps": round(achieved, 1), "fused_TFLOPs": round(flops / (fused_us * 1e-6) / 1e12, 1),
-        "fused_roofline_us": round(t_roof, 2), "fused_frac_of_roofline": round(t_roof / fused_us, 4),
-        "roofline": {"bound": bound, "achieved": round(achieved, 1) if bound == "hbm" else
-                     round(flops / (fused_us * 1e-6) / 1e12, 1),
+        "step_median_us": round(med_us, 2),
+        "roofline_us": round(t_roof, 2), "frac_of_roofline": round(t_roof / kern_us, 4),
+        "GBps": round(achieved, 1), "TFLOPs": round(tfl, 1),
+        "roofline": {"bound": bound, "achieved": round(achieved, 1) if bound == "hbm" else round(tfl, 1),
                      "peak": hbm if bound == "hbm" else tflops, "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
-                     "frac": round((achieved / hbm) if bound == "hbm" else
-                                   (flops / (fused_us * 1e-6) / 1e12) / tflops, 4),
+                     "frac": round((achieved / hbm) if bound == "hbm" else tfl / tflops, 4),
                      "traffic": traffic, "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_src == "measured" else peak_src,
-                     "algorithmic_bytes": abytes, "kernel": "wgrad_step_tc_kernel",
+                     "algorithmic_bytes": abytes, "kernel": kernel,
                      "kernel_source_hash": kernel_source_hash()},
+        "split_step_us": round(split_us, 2), "split_dgrad_us": round(statistics.mean(dgrad_ms) * 1000.0, 2),
+        "split_wgrad_step_us": round(wstep_us, 2),
+        "split_wgrad_step_frac_of_hbm": round(sbytes / (wstep_us * 1e-6) / 1e9 / hbm, 4),
         "e2e": {"value": round(e2e_ms * 1000.0, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": 2 * K,
@@ -368,7 +421,8 @@ def run_gpu(args, rank, world, local_rank):
 
 def run_stack(args, rank, world, local_rank):
     """One step = backward over the 224 linears of Llama-3.1-8B (layer 31 .. 0,
-    down, up, gate, o, v, k, q): forge_dgrad then the fused step, per linear."""
+    down, up, gate, o, v, k, q): one forge_backward_step per linear, on the
+    path the library picks for each shape (the split path is timed too)."""
     import torch
     import backward_gemm_optimizer_gb300 as F
     from backward_gemm_optimizer_gb300 import synthetic as S
@@ -404,30 +458,36 @@ def run_stack(args, rank, world, local_rank):
     stream = torch.cuda.current_stream(dev)
     sr = stname == "bf16state"
 
-    def stack_step(t, events=None):
+    # One workspace serves every linear: the calls run one after another on one stream.
+    ws_bytes = max(F.workspace_bytes(d_out, d_in, bt) for _, d_out, d_in in order)
+    ws = torch.empty(max(16, ws_bytes), dtype=torch.uint8, device=dev)
+
+    def backward(L, t, stream_, flags=0):
+        dxb = dX[L["d_in"]]
+        if opt == "adamw":
+            F.backward_step("adamw", L["X"], L["dY"], L["W"], L["m"], L["v"], dxb, step=t, seed=1234, sr_w=sr,
+                            workspace=ws, flags=flags, stream=stream_, **hp)
+        elif opt == "lion":
+            F.backward_step("lion", L["X"], L["dY"], L["W"], L["m"], None, dxb, lr=hp["lr"], beta1=hp["beta1"],
+                            beta2=hp["beta2"], weight_decay=hp["weight_decay"], step=t, seed=1234, sr_w=sr,
+                            workspace=ws, flags=flags, stream=stream_)
+        else:
+            F.backward_step("sgdm", L["X"], L["dY"], L["W"], L["m"], None, dxb, lr=hp["lr"], momentum=hp["beta1"],
+                            weight_decay=hp["weight_decay"], step=t, seed=1234, sr_w=sr, workspace=ws, flags=flags,
+                            stream=stream_)
+
+    def stack_step(t, events=None, flags=0, stream_=None):
+        stream_ = stream if stream_ is None else stream_
         i = 0
         for layer in reversed(range(len(layers))):
             for name, _, _ in order:
                 L = layers[layer][name]
                 if events is not None:
-                    events[i][0].record(stream)
-                F.dgrad(L["dY"], L["W"], dX[L["d_in"]], stream=stream)
+                    events[i][0].record(stream_)
+                backward(L, t, stream_, flags)
                 if events is not None:
-                    events[i][1].record(stream)
-                launch_step_only(L, t)
-                if events is not None:
-                    events[i][2].record(stream)
+                    events[i][1].record(stream_)
                 i += 1
-
-    def launch_step_only(L, t):
-        if opt == "adamw":
-            F.wgrad_step_adamw(L["X"], L["dY"], L["W"], L["m"], L["v"], step=t, seed=1234, sr_w=sr, stream=stream, **hp)
-        elif opt == "lion":
-            F.wgrad_step_lion(L["X"], L["dY"], L["W"], L["m"], lr=hp["lr"], beta1=hp["beta1"], beta2=hp["beta2"],
-                              weight_decay=hp["weight_decay"], step=t, seed=1234, sr_w=sr, stream=stream)
-        else:
-            F.wgrad_step_sgdm(L["X"], L["dY"], L["W"], L["m"], lr=hp["lr"], momentum=hp["beta1"],
-                              weight_decay=hp["weight_decay"], step=t, seed=1234, sr_w=sr, stream=stream)
 
     t = 1
     for _ in range(args.warmup):
@@ -435,69 +495,62 @@ def run_stack(args, rank, world, local_rank):
     F.sync_status(stream)
     n_lin = len(layers) * len(order)
     K = args.steps
-    # per-linear events for one instrumented pass (per-shape breakdown)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_lin)]
-    torch.cuda.synchronize(dev)
-    stack_step(t, ev); t += 1
-    torch.cuda.synchronize(dev)
+    # per-linear events for one instrumented pass of each path (per-shape breakdown)
     per_shape = {}
-    i = 0
-    for layer in reversed(range(len(layers))):
-        for name, d_out, d_in in order:
-            a = per_shape.setdefault(name, {"d_out": d_out, "d_in": d_in, "dgrad_us": 0.0, "step_us": 0.0, "n": 0})
-            a["dgrad_us"] += ev[i][0].elapsed_time(ev[i][1]) * 1000.0
-            a["step_us"] += ev[i][1].elapsed_time(ev[i][2]) * 1000.0
-            a["n"] += 1
-            i += 1
+    for key, flags in (("backward_us", 0), ("split_us", F.FLAG_BACKWARD_SPLIT)):
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n_lin)]
+        torch.cuda.synchronize(dev)
+        stack_step(t, ev, flags); t += 1
+        torch.cuda.synchronize(dev)
+        i = 0
+        for layer in reversed(range(len(layers))):
+            for name, d_out, d_in in order:
+                a = per_shape.setdefault(name, {"d_out": d_out, "d_in": d_in, "backward_us": 0.0, "split_us": 0.0,
+                                                "n": 0})
+                a[key] += ev[i][0].elapsed_time(ev[i][1]) * 1000.0
+                if key == "backward_us":
+                    a["n"] += 1
+                i += 1
     hbm, tflops, _ = load_peaks()
     for name, a in per_shape.items():
-        a["dgrad_us"] = round(a["dgrad_us"] / a["n"], 2)
-        a["step_us"] = round(a["step_us"] / a["n"], 2)
+        for key in ("backward_us", "split_us"):
+            a[key] = round(a[key] / a["n"], 2)
         eb = 4 if stname == "f32state" else 2
         sb = 2 * eb * (3 if two else 2)     # W and each moment read + written once
-        ab = a["d_out"] * a["d_in"] * sb + 2 * bt * (a["d_out"] + a["d_in"])
-        a["step_GBps"] = round(ab / (a["step_us"] * 1e-6) / 1e9, 1)
-        a["step_frac_of_hbm"] = round(a["step_GBps"] / hbm, 4)
-    # timed: plain launches, then the same step replayed as a CUDA graph
+        ab = a["d_out"] * a["d_in"] * sb + 2 * bt * (a["d_out"] + 2 * a["d_in"])   # + X, dY read, dX written
+        a["backward_GBps"] = round(ab / (a["backward_us"] * 1e-6) / 1e9, 1)
+        a["backward_frac_of_hbm"] = round(a["backward_GBps"] / hbm, 4)
+
+    def timed(flags):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        nonlocal t
+        for _ in range(K):
+            stack_step(t, None, flags); t += 1
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        F.sync_status(stream)
+        return max_over_ranks(e0.elapsed_time(e1) / K, world, dev)
+
     sampler = ClockSampler(local_rank)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    torch.cuda.synchronize(dev)
     sampler.start()
     time.sleep(0.2)
-    e0.record(stream)
-    for _ in range(K):
-        stack_step(t); t += 1
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
+    eager_ms = timed(0)
     clocks = sampler.stop()
-    F.sync_status(stream)
-    eager_ms = max_over_ranks(e0.elapsed_time(e1) / K, world, dev)
+    split_ms = timed(F.FLAG_BACKWARD_SPLIT)
     graph_ms = None
     if args.graph:
         g = torch.cuda.CUDAGraph()
         side = torch.cuda.Stream(dev)
         side.wait_stream(stream)
         # capture on a side stream: the library launches on the stream it is given
-        tg = t
         with torch.cuda.graph(g, stream=side):
-            cap = torch.cuda.current_stream(dev)
-            for layer in reversed(range(len(layers))):
-                for name, _, _ in order:
-                    L = layers[layer][name]
-                    F.dgrad(L["dY"], L["W"], dX[L["d_in"]], stream=cap)
-                    if opt == "adamw":
-                        F.wgrad_step_adamw(L["X"], L["dY"], L["W"], L["m"], L["v"], step=tg, seed=1234, sr_w=sr,
-                                           stream=cap, **hp)
-                    elif opt == "lion":
-                        F.wgrad_step_lion(L["X"], L["dY"], L["W"], L["m"], lr=hp["lr"], beta1=hp["beta1"],
-                                          beta2=hp["beta2"], weight_decay=hp["weight_decay"], step=tg, seed=1234,
-                                          sr_w=sr, stream=cap)
-                    else:
-                        F.wgrad_step_sgdm(L["X"], L["dY"], L["W"], L["m"], lr=hp["lr"], momentum=hp["beta1"],
-                                          weight_decay=hp["weight_decay"], step=tg, seed=1234, sr_w=sr, stream=cap)
+            stack_step(t, None, 0, torch.cuda.current_stream(dev))
         torch.cuda.synchronize(dev)
         g.replay(); torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for _ in range(K):
             g.replay()     # the same step index each replay (graph parameters are fixed)
@@ -508,17 +561,15 @@ def run_stack(args, rank, world, local_rank):
     if rank != 0:
         return
     params = sum(a["d_out"] * a["d_in"] * a["n"] for a in per_shape.values())
-    step_total_us = sum(a["step_us"] * a["n"] for a in per_shape.values())
-    dgrad_total_us = sum(a["dgrad_us"] * a["n"] for a in per_shape.values())
     line = {
         "metric": METRIC, "value": round(eager_ms * 1000.0, 1), "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(eager_ms, 3), "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": args.workload, "linears": n_lin, "params": params, "bt": bt, "optimizer": opt,
-                   "state": stname, "step": "224 x (forge_dgrad + fused step), layer 31..0",
+                   "state": stname, "step": "224 x forge_backward_step (library's path choice), layer 31..0",
                    "l2": "state 84 GB (fp32) / 42 GB (bf16) >> L2"},
         "graph_ms_per_step": round(graph_ms, 3) if graph_ms is not None else None,
-        "fused_steps_us_total": round(step_total_us, 1), "dgrads_us_total": round(dgrad_total_us, 1),
+        "split_ms_per_step": round(split_ms, 3),
         "per_shape": per_shape, "gpu_launches": 2 * n_lin * K, "clocks": clocks,
     }
     print(json.dumps(line), flush=True)
@@ -533,6 +584,7 @@ def main():
     ap.add_argument("--workload", default=DEFAULT, choices=sorted(WORKLOADS) + sorted(STACKS))
     ap.add_argument("--graph", action="store_true", help="stack workloads: also replay the step as a CUDA graph")
     ap.add_argument("--e2e-steps", type=int, default=100)
+    ap.add_argument("--split-steps", type=int, default=200, help="steps of the split-path comparison")
     ap.add_argument("--cpu-rows", type=int, default=14336)
     ap.add_argument("--cpu-min-s", type=float, default=10.0)
     ap.add_argument("--cpu-budget-s", type=float, default=120.0)

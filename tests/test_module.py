@@ -43,13 +43,15 @@ def test_manager_lists_non_fused_params():
 
 
 @pytest.mark.gpu
+@pytest.mark.parametrize("path", ["auto", "fused"])
 @pytest.mark.parametrize("rule", ["adamw", "sgdm", "lion", "nadam", "rmsprop"])
-def test_backward_equals_direct_abi_calls(rule):
+def test_backward_equals_direct_abi_calls(rule, path):
     torch.manual_seed(0)
     dev = "cuda:0"
     layer = ForgeLinear(384, 256, rule=rule, device=dev)
     mgr = ForgeStepManager(layer)
     mgr.config.lr, mgr.config.weight_decay = 1e-3, 0.01
+    mgr.config.backward_flags = F.FLAG_BACKWARD_FUSED if path == "fused" else 0
     x = torch.randn(2, 100, 384, device=dev).bfloat16().requires_grad_(True)
     g = torch.randn(2, 100, 256, device=dev).bfloat16()
     W0 = layer.weight.detach().clone()
@@ -69,22 +71,11 @@ def test_backward_equals_direct_abi_calls(rule):
     # the same step through the C ABI directly
     x2d, dy2d = x.detach().reshape(-1, 384), g.reshape(-1, 256).contiguous()
     dx = torch.empty_like(x2d)
-    F.dgrad(dy2d, W0, dx)
     c = mgr.config
-    kw = dict(step=2, seed=c.seed)
-    if rule == "adamw":
-        F.wgrad_step_adamw(x2d, dy2d, W0, s0, s1, lr=c.lr, beta1=c.beta1, beta2=c.beta2, eps=c.eps,
-                           weight_decay=c.weight_decay, **kw)
-    elif rule == "sgdm":
-        F.wgrad_step_sgdm(x2d, dy2d, W0, s0, lr=c.lr, momentum=c.beta1, weight_decay=c.weight_decay, **kw)
-    elif rule == "lion":
-        F.wgrad_step_lion(x2d, dy2d, W0, s0, lr=c.lr, beta1=c.beta1, beta2=c.beta2,
-                          weight_decay=c.weight_decay, **kw)
-    elif rule == "nadam":
-        F.wgrad_step_nadam(x2d, dy2d, W0, s0, s1, lr=c.lr, beta1=c.beta1, beta2=c.beta2, eps=c.eps,
-                           weight_decay=c.weight_decay, momentum_decay=c.momentum_decay, **kw)
-    else:
-        F.wgrad_step_rmsprop(x2d, dy2d, W0, s0, lr=c.lr, alpha=c.beta2, eps=c.eps, weight_decay=c.weight_decay, **kw)
+    ws = torch.empty(max(16, F.workspace_bytes(256, 384, x2d.shape[0])), dtype=torch.uint8, device=dev)
+    F.backward_step(rule, x2d, dy2d, W0, s0, s1, dx, lr=c.lr, beta1=c.beta1, beta2=c.beta2, eps=c.eps,
+                    weight_decay=c.weight_decay, momentum_decay=c.momentum_decay, step=2, seed=c.seed,
+                    workspace=ws, flags=c.backward_flags)
     F.sync_status()
     assert torch.equal(layer.weight, W0)
     assert torch.equal(x.grad.reshape(-1, 384), dx)
