@@ -387,12 +387,16 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX>::NUM_
           tc_fence_after_sync();
           const uint32_t a0 = smem_u32(op_base + s * C::STAGE_BYTES);
           const uint32_t b0 = a0 + C::A_BYTES;
+          // Descriptors are built once per stage; a K step only moves the
+          // 14-bit start-address field (16-byte units; shared addresses stay
+          // below 2^18 bytes, so the field never carries into its neighbour).
+          const uint64_t ad0 = make_smem_desc(a0, C::BOX, 1024, 2);
+          const uint64_t bd0 = make_smem_desc(b0, C::BOX, 1024, 2);
 #pragma unroll
           for (int kk = 0; kk < C::BK / 16; ++kk) {
             // 16 tokens = two 8-row K groups of 1024 bytes; MN atoms one box apart.
-            const uint64_t ad = make_smem_desc(a0 + kk * 2048, C::BOX, 1024, 2);
-            const uint64_t bd = make_smem_desc(b0 + kk * 2048, C::BOX, 1024, 2);
-            umma_f16(d_tmem, ad, bd, C::IDESC, (kb > 0 || kk > 0) ? 1u : 0u);
+            const uint64_t step = static_cast<uint64_t>(kk * 2048 >> 4);
+            umma_f16(d_tmem, ad0 + step, bd0 + step, C::IDESC, (kb > 0 || kk > 0) ? 1u : 0u);
           }
           if constexpr (DX) {
             if (kb == 0) {
@@ -411,14 +415,16 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX>::NUM_
             // 8-token groups 1024 bytes apart; a K step of 16 advances 32 bytes.
             // B: MN-major Wb, 8-row K groups of 1024 bytes, 16 rows = 2048 bytes.
             const uint32_t dx_tmem = tmem_base + static_cast<uint32_t>(C::DX_COL + kb * BN);
-            const uint32_t wb0 = smem_u32(wb_base);
+            const uint64_t xa0 = make_smem_desc(a0, 16, 1024, 2);
+            const uint64_t xb0 = make_smem_desc(smem_u32(wb_base), 8192, 1024, 2);
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t ad = make_smem_desc(a0 + hh * C::BOX + kk * 32, 16, 1024, 2);
-                const uint64_t bd = make_smem_desc(wb0 + (hh * 4 + kk) * 2048, 8192, 1024, 2);
-                umma_f16(dx_tmem, ad, bd, C::IDESC_DX, (run_first && hh == 0 && kk == 0) ? 0u : 1u);
+                const uint64_t astep = static_cast<uint64_t>((hh * C::BOX + kk * 32) >> 4);
+                const uint64_t bstep = static_cast<uint64_t>(((hh * 4 + kk) * 2048) >> 4);
+                umma_f16(dx_tmem, xa0 + astep, xb0 + bstep, C::IDESC_DX,
+                         (run_first && hh == 0 && kk == 0) ? 0u : 1u);
               }
             }
           }
