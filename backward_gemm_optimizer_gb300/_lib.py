@@ -29,7 +29,8 @@ STATUS_NAMES = {0: "FORGE_OK", 1: "FORGE_ERR_INVALID_ARG", 2: "FORGE_ERR_UNSUPPO
 EXPORTED = ("forge_wgrad_step_adamw", "forge_wgrad_step_sgdm", "forge_wgrad_step_lion",
             "forge_wgrad_step_sgd", "forge_wgrad_step_rmsprop", "forge_wgrad_step_adagrad",
             "forge_wgrad_step_nadam", "forge_wgrad_step_radam",
-            "forge_dgrad", "forge_backward_step", "forge_backward_step_no_alloc", "forge_sync_status", "forge_last_error", "forge_version",
+            "forge_dgrad", "forge_backward_step", "forge_backward_step_no_alloc", "forge_wgrad_accumulate",
+            "forge_wgrad_step_accumulated", "forge_sync_status", "forge_last_error", "forge_version",
             "forge_workspace_bytes")
 
 
@@ -73,11 +74,15 @@ def _load() -> ctypes.CDLL:
                                         ctypes.c_size_t, vp]
     lib.forge_backward_step_no_alloc.argtypes = [ctypes.c_int, P(T), P(T), P(T), P(T), P(T), P(T), P(H), i64,
                                                  u64, vp]
+    lib.forge_wgrad_accumulate.argtypes = [P(T), P(T), P(T), ctypes.c_int, vp]
+    lib.forge_wgrad_step_accumulated.argtypes = [ctypes.c_int, P(T), P(T), P(T), P(T), P(T), P(T), P(H), i64, u64,
+                                                 vp]
     lib.forge_sync_status.argtypes = [vp]
     for f in ("forge_wgrad_step_adamw", "forge_wgrad_step_sgdm", "forge_wgrad_step_lion",
               "forge_wgrad_step_sgd", "forge_wgrad_step_rmsprop", "forge_wgrad_step_adagrad",
               "forge_wgrad_step_nadam", "forge_wgrad_step_radam", "forge_dgrad", "forge_backward_step",
-              "forge_backward_step_no_alloc", "forge_sync_status"):
+              "forge_backward_step_no_alloc", "forge_wgrad_accumulate", "forge_wgrad_step_accumulated",
+              "forge_sync_status"):
         getattr(lib, f).restype = ctypes.c_int
     lib.forge_last_error.restype = ctypes.c_char_p
     lib.forge_version.restype = ctypes.c_char_p
@@ -272,6 +277,34 @@ def backward_step_no_alloc(rule, X, dY, W, s0, s1, dX, *, lr, beta1=0.9, beta2=0
                                               ctypes.byref(t0) if t0 is not None else None,
                                               ctypes.byref(t1) if t1 is not None else None, ctypes.byref(tdX),
                                               ctypes.byref(h), int(step), _seed(seed), _stream(stream)))
+
+
+def wgrad_accumulate(X, dY, G_acc, *, overwrite=False, stream=None):
+    """G_acc (+)= dY^T X for one micro-batch (forge_wgrad_accumulate); overwrite on the first."""
+    tX, tdY, tG = tensor_desc(X), tensor_desc(dY), tensor_desc(G_acc)
+    _check(lib().forge_wgrad_accumulate(ctypes.byref(tX), ctypes.byref(tdY), ctypes.byref(tG), int(bool(overwrite)),
+                                        _stream(stream)))
+
+
+def wgrad_step_accumulated(rule, X, dY, G_acc, W, s0, s1, *, lr, beta1=0.9, beta2=0.999, eps=1e-8,
+                           weight_decay=0.0, momentum_decay=4e-3, momentum=None, alpha=None, step, seed=0,
+                           sr_w=False, sr_moments=False, flags=0, stream=None):
+    """The last micro-batch: G = G_acc + dY^T X per tile, then the fused step of `rule`
+    (forge_wgrad_step_accumulated). s0 / s1 as for backward_step."""
+    if rule not in RULES:
+        raise ValueError(f"unknown rule {rule!r}; one of {tuple(RULES)}")
+    if momentum is not None:
+        beta1 = momentum
+    if alpha is not None:
+        beta2 = alpha
+    tX, tdY, tG, tW = tensor_desc(X), tensor_desc(dY), tensor_desc(G_acc), tensor_desc(W)
+    t0 = tensor_desc(s0) if s0 is not None else None
+    t1 = tensor_desc(s1) if s1 is not None else None
+    h = _hyper(lr, beta1, beta2, eps, weight_decay, sr_w, sr_moments, flags, momentum_decay)
+    _check(lib().forge_wgrad_step_accumulated(RULES[rule], ctypes.byref(tX), ctypes.byref(tdY), ctypes.byref(tG),
+                                              ctypes.byref(tW), ctypes.byref(t0) if t0 is not None else None,
+                                              ctypes.byref(t1) if t1 is not None else None, ctypes.byref(h),
+                                              int(step), _seed(seed), _stream(stream)))
 
 
 def sync_status(stream=None):

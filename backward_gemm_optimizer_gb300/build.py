@@ -30,6 +30,7 @@ SOURCES = [
     "wgrad_tc_adagrad.cu",
     "wgrad_tc_nadam.cu",
     "wgrad_tc_radam.cu",
+    "wgrad_tc_accum.cu",
     "wgrad_simt.cu",
     "dgrad_tc.cu",
     "dx_reduce.cu",

@@ -235,7 +235,9 @@ const char* opt_name(int opt) {
     case OPT_RMSPROP: return "rmsprop";
     case OPT_ADAGRAD: return "adagrad";
     case OPT_NADAM: return "nadam";
-    default: return "radam";
+    case OPT_RADAM: return "radam";
+    case OPT_ACCUM: return "accumulate";
+    default: return "accumulate(first)";
   }
 }
 
@@ -288,7 +290,7 @@ struct DxArgs {
 
 forge_status wgrad_step(int opt, const forge_tensor* X, const forge_tensor* dY, forge_tensor* W, forge_tensor* m,
                         forge_tensor* v, const forge_hyper* h, int64_t step, uint64_t seed, forge_stream_t stream,
-                        const DxArgs* dx = nullptr) {
+                        const DxArgs* dx = nullptr, const forge_tensor* G_acc = nullptr) {
   const char* oname = opt_name(opt);
   const int nst = opt_nstate(opt);
   if (X == nullptr || dY == nullptr || W == nullptr || h == nullptr || (nst >= 1 && m == nullptr))
@@ -315,7 +317,17 @@ forge_status wgrad_step(int opt, const forge_tensor* X, const forge_tensor* dY, 
     return fail(FORGE_ERR_UNSUPPORTED, "%s: X and dY must both be bf16 or both f32 (got %s, %s)", oname,
                 dtype_name(X->dtype), dtype_name(dY->dtype));
   const bool tc = X->dtype == FORGE_BF16;
+  const bool accum = opt == OPT_ACCUM || opt == OPT_ACCSET;
   forge_status st;
+  if ((accum || G_acc != nullptr) && !tc)
+    return fail(FORGE_ERR_UNSUPPORTED, "%s: gradient accumulation runs on the tensor-core path (bf16 X, dY)", oname);
+  if (accum && W != nullptr && W->dtype != FORGE_F32)
+    return fail(FORGE_ERR_UNSUPPORTED, "%s: the gradient accumulator must be f32", oname);
+  if (G_acc != nullptr) {
+    if ((st = check_tensor(G_acc, "G_acc", d_out, d_in, true)) != FORGE_OK) return st;
+    if (G_acc->dtype != FORGE_F32) return fail(FORGE_ERR_UNSUPPORTED, "%s: G_acc must be f32", oname);
+    if (dx != nullptr) return fail(FORGE_ERR_UNSUPPORTED, "%s: no fused input gradient with G_acc", oname);
+  }
   if ((st = check_tensor(X, "X", bt, d_in, true)) != FORGE_OK) return st;
   if ((st = check_tensor(dY, "dY", bt, d_out, true)) != FORGE_OK) return st;
   if ((st = check_tensor(W, "W", d_out, d_in, true)) != FORGE_OK) return st;
@@ -382,7 +394,9 @@ forge_status wgrad_step(int opt, const forge_tensor* X, const forge_tensor* dY, 
   else if (mk != M_Q8 && tiles_m * ((d_in + 127) / 128) < dev->sms) bn = 64;  // too few tiles for one wave
   if (mk == M_Q8 && bn != 128)
     return fail(FORGE_ERR_UNSUPPORTED, "%s: 8-bit block moments need 128-column tiles", oname);
-  const int deep = (dx == nullptr && bt >= 1024 && bn == 128) ? 1 : 0;
+  if (mk == M_Q8 && G_acc != nullptr)
+    return fail(FORGE_ERR_UNSUPPORTED, "%s: the accumulated-gradient step has no 8-bit state variant", oname);
+  const int deep = (dx == nullptr && G_acc == nullptr && bt >= 1024 && bn == 128) ? 1 : 0;
   const int tiles_n = static_cast<int>((d_in + bn - 1) / bn);
   const uint32_t box_tokens = dx != nullptr ? 128u : 64u;  // tokens per operand stage
 
@@ -407,6 +421,11 @@ forge_status wgrad_step(int opt, const forge_tensor* X, const forge_tensor* dY, 
   } else {
     p.tm_v = p.tm_m;  // unused
   }
+  if (G_acc != nullptr) {
+    if ((st = encode_state(&p.tm_g, G_acc, "G_acc")) != FORGE_OK) return st;
+  } else {
+    p.tm_g = p.tm_w;  // unused
+  }
   p.sc = sc;
   p.m_scale = nst >= 1 ? static_cast<float*>(m->scale) : nullptr;
   p.v_scale = nst == 2 ? static_cast<float*>(v->scale) : nullptr;
@@ -429,6 +448,7 @@ forge_status wgrad_step(int opt, const forge_tensor* X, const forge_tensor* dY, 
 
   TcLaunch l{};
   l.opt = opt; l.wk = wk; l.mk = mk; l.bn = bn; l.deep = deep; l.dx = dx != nullptr ? 1 : 0;
+  l.ga = G_acc != nullptr ? 1 : 0;
   l.grid = p.num_tiles < dev->sms ? p.num_tiles : dev->sms;
   l.stream = s;
   DxGeometry g;
@@ -456,7 +476,8 @@ forge_status wgrad_step(int opt, const forge_tensor* X, const forge_tensor* dY, 
     case OPT_RMSPROP: e = launch_wgrad_tc_rmsprop(p, l); break;
     case OPT_ADAGRAD: e = launch_wgrad_tc_adagrad(p, l); break;
     case OPT_NADAM: e = launch_wgrad_tc_nadam(p, l); break;
-    default: e = launch_wgrad_tc_radam(p, l); break;
+    case OPT_RADAM: e = launch_wgrad_tc_radam(p, l); break;
+    default: e = launch_wgrad_tc_accum(p, l); break;
   }
   if (e != cudaSuccess) return fail(FORGE_ERR_CUDA, "%s launch: %s", oname, cudaGetErrorString(e));
   if (dx != nullptr) {
@@ -594,6 +615,24 @@ forge_status forge_backward_step(forge_rule rule, const forge_tensor* X, const f
 
 forge_status forge_dgrad(const forge_tensor* dY, const forge_tensor* W_old, forge_tensor* dX, forge_stream_t stream) {
   return dgrad_impl(dY, W_old, dX, stream);
+}
+
+forge_status forge_wgrad_accumulate(const forge_tensor* X, const forge_tensor* dY, forge_tensor* G_acc, int overwrite,
+                                    forge_stream_t stream) {
+  if (G_acc == nullptr) return fail(FORGE_ERR_INVALID_ARG, "accumulate: null G_acc");
+  forge_hyper h;
+  std::memset(&h, 0, sizeof(h));
+  return wgrad_step(overwrite ? OPT_ACCSET : OPT_ACCUM, X, dY, G_acc, nullptr, nullptr, &h, 1, 0, stream);
+}
+
+forge_status forge_wgrad_step_accumulated(forge_rule rule, const forge_tensor* X, const forge_tensor* dY,
+                                          const forge_tensor* G_acc, forge_tensor* W, forge_tensor* s0,
+                                          forge_tensor* s1, const forge_hyper* h, int64_t step, uint64_t seed,
+                                          forge_stream_t stream) {
+  if (static_cast<int>(rule) < OPT_ADAMW || static_cast<int>(rule) > OPT_RADAM)
+    return fail(FORGE_ERR_INVALID_ARG, "step_accumulated: unknown rule %d", static_cast<int>(rule));
+  if (G_acc == nullptr) return fail(FORGE_ERR_INVALID_ARG, "step_accumulated: null G_acc");
+  return wgrad_step(static_cast<int>(rule), X, dY, W, s0, s1, h, step, seed, stream, nullptr, G_acc);
 }
 
 }  // extern "C"

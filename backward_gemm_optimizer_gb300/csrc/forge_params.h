@@ -43,6 +43,7 @@ struct alignas(128) WgradTcParams {
   CUtensorMap tm_w;   // W   [D_out][D_in], box 32 cols x 128 rows
   CUtensorMap tm_m;   // m   (values or 8-bit codes), box 32 x 128
   CUtensorMap tm_v;   // v   (AdamW only)
+  CUtensorMap tm_g;   // G_acc fp32 [D_out][D_in], box 32 x 128 (accumulated-gradient step only)
   StepScalars sc;
   float* m_scale;     // 8-bit state: [D_in/128][D_out]
   float* v_scale;
@@ -111,6 +112,7 @@ struct TcLaunch {
   int bn;       // tile width (64 or 128)
   int deep;     // 1: deeper operand pipeline for long token axes
   int dx;       // 1: fused input gradient (64-column tiles, fp32 / bf16 state)
+  int ga;       // 1: add the accumulated gradient G_acc (tm_g) to each tile
   int grid;
   cudaStream_t stream;
 };
@@ -124,6 +126,7 @@ cudaError_t launch_wgrad_tc_rmsprop(const WgradTcParams& p, const TcLaunch& l);
 cudaError_t launch_wgrad_tc_adagrad(const WgradTcParams& p, const TcLaunch& l);
 cudaError_t launch_wgrad_tc_nadam(const WgradTcParams& p, const TcLaunch& l);
 cudaError_t launch_wgrad_tc_radam(const WgradTcParams& p, const TcLaunch& l);
+cudaError_t launch_wgrad_tc_accum(const WgradTcParams& p, const TcLaunch& l);
 cudaError_t launch_wgrad_simt(const WgradSimtParams& p, int opt, int wk, int mk, cudaStream_t stream);
 cudaError_t launch_dgrad_tc(const DgradParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_dx_reduce(const DxReduceParams& p, int sms, cudaStream_t stream);

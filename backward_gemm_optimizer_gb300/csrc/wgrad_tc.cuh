@@ -57,9 +57,11 @@
 
 namespace forge {
 
-template <int OPT, int WK, int MK, int BN_, int STAGES_, int NBUF_, bool DX_ = false>
+template <int OPT, int WK, int MK, int BN_, int STAGES_, int NBUF_, bool DX_ = false, bool GA_ = false>
 struct TcCfg {
   static constexpr bool DX = DX_;      // fused input gradient (see above)
+  static constexpr bool GA = GA_;      // add an fp32 accumulated gradient G_acc to each tile
+  static constexpr bool LOAD_W = OPT != OPT_ACCSET;  // the set-accumulator rule never reads its target
   static constexpr int BM = 128;       // tile rows (D_out), one per TMEM lane
   static constexpr int BN = BN_;       // tile columns (D_in)
   static constexpr int BK = DX ? 128 : 64;  // tokens per operand stage
@@ -79,7 +81,10 @@ struct TcCfg {
   static constexpr int W_CH = BM * CW * WE;
   static constexpr int M_CH = NST >= 1 ? BM * CW * ME : 0;
   static constexpr int V_CH = TWO ? M_CH : 0;
-  static constexpr int SLOT_BYTES = W_CH + M_CH + V_CH > 0 ? ((W_CH + M_CH + V_CH + 1023) / 1024) * 1024 : 1024;
+  static constexpr int G_CH = GA ? BM * CW * 4 : 0;
+  static constexpr int G_OFF = W_CH + M_CH + V_CH;   // G_acc chunk after W, m, v in a slot
+  static constexpr int LOAD_BYTES = (LOAD_W ? W_CH : 0) + M_CH + V_CH + G_CH;
+  static constexpr int SLOT_BYTES = ((W_CH + M_CH + V_CH + G_CH + 1023) / 1024) * 1024;
   static constexpr int WB_BYTES = DX ? BM * BN * 2 : 0;   // bf16 W_old tile (B operand of dX)
   static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + WB_BYTES + NBUF * SLOT_BYTES;
   static constexpr int TMEM_COLS = DX ? 512 : ((2 * BN <= 128) ? 128 : (2 * BN <= 256 ? 256 : 512));
@@ -270,10 +275,12 @@ __device__ __forceinline__ void drain_ring(uint64_t* full, int ring, uint32_t is
   }
 }
 
-template <int OPT, int WK, int MK, int BN, int STAGES, int NBUF, bool DX>
-__global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX>::NUM_THREADS, 1)
+template <int OPT, int WK, int MK, int BN, int STAGES, int NBUF, bool DX, bool GA>
+__global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA>::NUM_THREADS, 1)
     wgrad_step_tc_kernel(const __grid_constant__ WgradTcParams p) {
-  using C = TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX>;
+  using C = TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA>;
+  static_assert(!GA || (!DX && !C::Q8), "accumulated-gradient step: split path, fp32 / bf16 state");
+  static_assert(!(OPT == OPT_ACCUM || OPT == OPT_ACCSET) || (WK == W_F32 && !GA), "fp32 gradient accumulator");
   static_assert(BN == 64 || BN == 128, "tile width");
   static_assert(!DX || (BN == 64 && !C::Q8), "fused input gradient: 64-column tiles, fp32 / bf16 state");
   static_assert(!C::Q8 || BN == 128, "8-bit blocks span one 128-column tile row");
@@ -327,6 +334,7 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX>::NUM_
   if (warp == 0 && lane == 0) {
     if (p.num_kb > 0) { prefetch_tmap(&p.tm_dy); prefetch_tmap(&p.tm_x); }
     prefetch_tmap(&p.tm_w);
+    if constexpr (GA) prefetch_tmap(&p.tm_g);
     if constexpr (C::NST >= 1) prefetch_tmap(&p.tm_m);
     if constexpr (C::TWO) prefetch_tmap(&p.tm_v);
   }
@@ -462,10 +470,11 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX>::NUM_
           if (!bwait(&st_empty[s], ph ^ 1u, abort_flag, p.status, WAIT_ST_EMPTY, lim)) { ok = false; break; }
           uint8_t* slot = st_base + s * C::SLOT_BYTES;
           const int x = tn * BN + c * C::CW, y = tm * C::BM;
-          mbar_arrive_expect_tx(&st_full[s], C::W_CH + C::M_CH + C::V_CH);
-          tma_load_2d(slot, &p.tm_w, &st_full[s], x, y);
+          mbar_arrive_expect_tx(&st_full[s], C::LOAD_BYTES);
+          if constexpr (C::LOAD_W) tma_load_2d(slot, &p.tm_w, &st_full[s], x, y);
           if constexpr (C::NST >= 1) tma_load_2d(slot + C::W_CH, &p.tm_m, &st_full[s], x, y);
           if constexpr (C::TWO) tma_load_2d(slot + C::W_CH + C::M_CH, &p.tm_v, &st_full[s], x, y);
+          if constexpr (GA) tma_load_2d(slot + C::G_OFF, &p.tm_g, &st_full[s], x, y);
         }
       }
       if (!ok) drain_ring(st_full, NBUF, cseq, p.status);
@@ -540,12 +549,21 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX>::NUM_
           uint8_t* sw = slot;
           uint8_t* sm = slot + C::W_CH;
           uint8_t* sv = slot + C::W_CH + C::M_CH;
-          float w[8], m[8], v[8];
-          ld8<WK == W_F32 ? 0 : 1>(sw, r, h, w);
+          float w[8], m[8], v[8], g[8];
+          if constexpr (C::LOAD_W) ld8<WK == W_F32 ? 0 : 1>(sw, r, h, w);
           if constexpr (C::NST >= 1) ld8<MK == M_F32 ? 0 : 1>(sm, r, h, m);
           if constexpr (C::TWO) ld8<MK == M_F32 ? 0 : 1>(sv, r, h, v);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) step_elem<OPT>(__uint_as_float(gr[j]), w[j], m[j], v[j], sc);
+          for (int j = 0; j < 8; ++j) g[j] = __uint_as_float(gr[j]);
+          if constexpr (GA) {
+            // The micro-batches accumulated so far: G = G_acc + this tile's G.
+            float ga[8];
+            ld8<0>(slot + C::G_OFF, r, h, ga);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) g[j] = __fadd_rn(ga[j], g[j]);
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j) step_elem<OPT>(g[j], w[j], m[j], v[j], sc);
           // Element index of this thread's first column; 8-aligned (D_in % 8 == 0).
           const uint64_t idx8 =
               (static_cast<uint64_t>(row) * static_cast<uint64_t>(p.d_in) + (tn * BN + c * C::CW + h * 8)) >> 3;
@@ -789,10 +807,10 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX>::NUM_
   }
 }
 
-template <int OPT, int WK, int MK, int BN, int STAGES, int NBUF, bool DX>
+template <int OPT, int WK, int MK, int BN, int STAGES, int NBUF, bool DX, bool GA = false>
 cudaError_t launch_tc_variant(const WgradTcParams& p, int grid, cudaStream_t stream) {
-  using C = TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX>;
-  auto kern = wgrad_step_tc_kernel<OPT, WK, MK, BN, STAGES, NBUF, DX>;
+  using C = TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA>;
+  auto kern = wgrad_step_tc_kernel<OPT, WK, MK, BN, STAGES, NBUF, DX, GA>;
   // The opt-in shared-memory size is a per-device function attribute: set
   // it once per device (bit d of the mask) before the first launch there.
   static unsigned long long attr_mask = 0ull;

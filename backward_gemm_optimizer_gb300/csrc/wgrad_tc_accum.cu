@@ -1,0 +1,31 @@
+// Gradient accumulation over micro-batches (FORGE, Appendix L, the exact
+// mode): the weight-gradient GEMM of each micro-batch adds its tiles into an
+// fp32 accumulator G_acc in HBM (or, on the first micro-batch, writes them
+// there), through the same tile kernel as the fused step with the
+// accumulator in place of the weights. The step itself fires once, at the
+// last micro-batch, through the accumulated-gradient variant of the rule
+// kernels.
+#include "wgrad_tc_dispatch.cuh"
+
+namespace forge {
+
+namespace {
+
+template <int OPT>
+cudaError_t launch_accum(const WgradTcParams& p, const TcLaunch& l) {
+  if (l.dx || l.ga || l.wk != W_F32) return cudaErrorInvalidValue;
+  if (l.bn == 64) {
+    if (l.deep) return cudaErrorInvalidValue;
+    return launch_one<OPT, W_F32, M_F32, 64, 0>(p, l.grid, l.stream);
+  }
+  return l.deep ? launch_one<OPT, W_F32, M_F32, 128, 1>(p, l.grid, l.stream)
+                : launch_one<OPT, W_F32, M_F32, 128, 0>(p, l.grid, l.stream);
+}
+
+}  // namespace
+
+cudaError_t launch_wgrad_tc_accum(const WgradTcParams& p, const TcLaunch& l) {
+  return l.opt == OPT_ACCSET ? launch_accum<OPT_ACCSET>(p, l) : launch_accum<OPT_ACCUM>(p, l);
+}
+
+}  // namespace forge

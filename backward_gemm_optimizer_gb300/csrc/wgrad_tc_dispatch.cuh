@@ -11,9 +11,9 @@ namespace forge {
 // shared memory (barriers + the 8 KB absmax exchange) is accounted for.
 constexpr int kDynSmemBudget = 227 * 1024 - 9 * 1024;
 
-template <int OPT, int WK, int MK, int BN, int STAGES, bool DX = false>
+template <int OPT, int WK, int MK, int BN, int STAGES, bool DX = false, bool GA = false>
 constexpr int slots_that_fit() {
-  using C = TcCfg<OPT, WK, MK, BN, STAGES, 2, DX>;
+  using C = TcCfg<OPT, WK, MK, BN, STAGES, 2, DX, GA>;
   const int avail = kDynSmemBudget - 1024 - STAGES * C::STAGE_BYTES - C::WB_BYTES;
   const int n = avail / C::SLOT_BYTES;
   return n > 8 ? 8 : n;
@@ -36,6 +36,15 @@ cudaError_t launch_one(const WgradTcParams& p, int grid, cudaStream_t stream) {
   return launch_tc_variant<OPT, WK, MK, BN, S, N, false>(p, grid, stream);
 }
 
+// Step with an accumulated gradient (the last micro-batch): two operand
+// stages, the state ring also carries the fp32 G_acc chunks.
+template <int OPT, int WK, int MK, int BN>
+cudaError_t launch_ga(const WgradTcParams& p, int grid, cudaStream_t stream) {
+  constexpr int N = slots_that_fit<OPT, WK, MK, BN, 2, false, true>();
+  static_assert(N >= 2, "state ring does not fit");
+  return launch_tc_variant<OPT, WK, MK, BN, 2, N, false, true>(p, grid, stream);
+}
+
 // Fused input gradient: 64-column tiles, two 128-token operand stages.
 template <int OPT, int WK, int MK>
 cudaError_t launch_dx(const WgradTcParams& p, int grid, cudaStream_t stream) {
@@ -46,6 +55,14 @@ cudaError_t launch_dx(const WgradTcParams& p, int grid, cudaStream_t stream) {
 
 template <int OPT, int WK, int MK>
 cudaError_t launch_mk(const WgradTcParams& p, const TcLaunch& l) {
+  if (l.ga) {
+    if constexpr (MK == M_Q8) return cudaErrorInvalidValue;
+    else {
+      if (l.dx || l.deep) return cudaErrorInvalidValue;
+      return l.bn == 64 ? launch_ga<OPT, WK, MK, 64>(p, l.grid, l.stream)
+                        : launch_ga<OPT, WK, MK, 128>(p, l.grid, l.stream);
+    }
+  }
   if (l.dx) {
     if constexpr (MK == M_Q8) return cudaErrorInvalidValue;
     else return l.bn == 64 && !l.deep ? launch_dx<OPT, WK, MK>(p, l.grid, l.stream) : cudaErrorInvalidValue;

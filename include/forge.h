@@ -275,6 +275,34 @@ forge_status forge_backward_step(forge_rule rule, const forge_tensor* X, const f
                                  forge_stream_t stream);
 
 /*
+ * forge_wgrad_accumulate -- one micro-batch of exact gradient accumulation
+ * (Appendix L): G_acc = G_acc + dY^T X, or G_acc = dY^T X when `overwrite`
+ * is nonzero (the first micro-batch of a window). Each 128-row tile of
+ * dY^T X is formed in tensor memory exactly as the fused step forms it and
+ * added to G_acc in fp32 (one rounding per micro-batch).
+ *
+ * G_acc: FORGE_F32, D_out x D_in, caller-owned; it is the one
+ * gradient-shaped buffer of this mode and lives for the accumulation
+ * window. X, dY: FORGE_BF16. The micro-batch's input gradient is a
+ * separate forge_dgrad call.
+ */
+forge_status forge_wgrad_accumulate(const forge_tensor* X, const forge_tensor* dY, forge_tensor* G_acc, int overwrite,
+                                    forge_stream_t stream);
+
+/*
+ * forge_wgrad_step_accumulated -- the last micro-batch of the window: each
+ * tile's gradient is G_acc + dY^T X (G_acc is read, not written) and the
+ * fused step of `rule` fires once on it, so the result is the step of the
+ * whole effective batch (Appendix L). X / dY may be empty (BT = 0): the step
+ * then uses G_acc alone. s0, s1 as for forge_backward_step; fp32 or bf16
+ * state (no 8-bit variant); bf16 X / dY.
+ */
+forge_status forge_wgrad_step_accumulated(forge_rule rule, const forge_tensor* X, const forge_tensor* dY,
+                                          const forge_tensor* G_acc, forge_tensor* W, forge_tensor* s0,
+                                          forge_tensor* s1, const forge_hyper* h, int64_t step, uint64_t seed,
+                                          forge_stream_t stream);
+
+/*
  * forge_backward_step_no_alloc -- forge_backward_step on the fused path,
  * for callers that cannot allocate device memory: code running under a
  * framework whose allocator owns the whole device, plug-ins that get

@@ -756,6 +756,23 @@ def step_values(opt: str, X, dY, st: State, h: Hyper, t: int, G: Optional[np.nda
 # --------------------------------------------------------------------------
 
 
+def accumulated_gradient_f64(micro_batches) -> np.ndarray:
+    """G = sum_i dY_i^T X_i over the micro-batches [(X_i, dY_i), ...], in
+    float64 (FORGE, Appendix L: exact gradient accumulation; the micro-step
+    GEMMs add into one accumulator and the step fires once, at the end)."""
+    G = None
+    for X, dY in micro_batches:
+        g = wgrad_f64(dY, X)
+        G = g if G is None else G + g
+    return G
+
+
+def accumulated_step(opt: str, micro_batches, st: "State", h: Hyper, t: int, **kw) -> "State":
+    """The step of ``opt`` fired once on the accumulated gradient of the window
+    (Appendix L); keyword arguments as for ``step``."""
+    return step(opt, None, None, st, h, t, G=accumulated_gradient_f64(micro_batches), **kw)
+
+
 def dgrad_f64(dY, W) -> np.ndarray:
     """dX = dY W in float64 (Remark 1, Appendix A). dY: [BT, D_out], W: [D_out, D_in]."""
     return np.asarray(dY, np.float64) @ np.asarray(W, np.float64)

@@ -629,3 +629,35 @@ def test_nadam_first_step_closed_form():
     factor = 1 + mu2 * 0.1 / (1 - mu1 * mu2)
     np.testing.assert_allclose(W1, W - 1e-3 * G / (np.abs(G) + 1e-8) * factor, rtol=1e-13)
     assert abs(factor - 1.0564522) < 1e-6
+
+
+def test_accumulated_gradient_equals_the_concatenated_batch():
+    # Appendix L: summing the micro-batch gradients is the gradient of the
+    # whole effective batch, since G = dY^T X is a sum over tokens.
+    rng = np.random.default_rng(7)
+    sizes = [5, 1, 12, 7]
+    mbs = [(rng.standard_normal((n, 6)), rng.standard_normal((n, 4))) for n in sizes]
+    G = O.accumulated_gradient_f64(mbs)
+    Xc = np.concatenate([x for x, _ in mbs]); dYc = np.concatenate([d for _, d in mbs])
+    np.testing.assert_allclose(G, dYc.T @ Xc, rtol=1e-13, atol=1e-13)
+    # brute force on one entry, and a single micro-batch is the plain gradient
+    assert abs(G[2, 3] - sum(float(d[t, 2] * x[t, 3]) for x, d in mbs for t in range(len(x)))) < 1e-12
+    np.testing.assert_array_equal(O.accumulated_gradient_f64(mbs[:1]), O.wgrad_f64(mbs[0][1], mbs[0][0]))
+
+
+def test_accumulated_step_is_the_large_batch_step():
+    # "Numerically identical to vanilla AdamW at the same effective batch":
+    # the step fired once on the accumulated gradient equals the step on the
+    # concatenated batch (exact here: integer inputs, float64 sums).
+    rng = np.random.default_rng(8)
+    mbs = [(rng.integers(-3, 4, (n, 8)).astype(np.float64), rng.integers(-3, 4, (n, 6)).astype(np.float64))
+           for n in (3, 9, 4)]
+    Xc = np.concatenate([x for x, _ in mbs]); dYc = np.concatenate([d for _, d in mbs])
+    W = rng.standard_normal((6, 8)) * 0.02
+    st = O.State(W=W.astype(np.float32), m=np.zeros((6, 8), np.float32), v=np.zeros((6, 8), np.float32),
+                 w_dtype="f32", state="f32")
+    h = O.Hyper(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01)
+    a = O.accumulated_step("adamw", mbs, st, h, 3)
+    b = O.step("adamw", Xc, dYc, st, h, 3)
+    for x, y in ((a.W, b.W), (a.m, b.m), (a.v, b.v)):
+        np.testing.assert_array_equal(x, y)
