@@ -396,7 +396,10 @@ forge_status wgrad_step(int opt, const forge_tensor* X, const forge_tensor* dY, 
     return fail(FORGE_ERR_UNSUPPORTED, "%s: 8-bit block moments need 128-column tiles", oname);
   if (mk == M_Q8 && G_acc != nullptr)
     return fail(FORGE_ERR_UNSUPPORTED, "%s: the accumulated-gradient step has no 8-bit state variant", oname);
-  const int deep = (dx == nullptr && G_acc == nullptr && bt >= 1024 && bn == 128) ? 1 : 0;
+  // Deep operand ring for long token axes, and for the accumulation rules at
+  // any length: their slots hold only the fp32 accumulator, so shared memory
+  // has room for four operand stages, and their tile time is the mainloop's.
+  const int deep = (dx == nullptr && G_acc == nullptr && (bt >= 1024 || accum) && bn == 128) ? 1 : 0;
   const int tiles_n = static_cast<int>((d_in + bn - 1) / bn);
   const uint32_t box_tokens = dx != nullptr ? 128u : 64u;  // tokens per operand stage
 

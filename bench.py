@@ -43,6 +43,9 @@ WORKLOADS = {
     "llama31_8b_up_proj_bt512_q8state": (14336, 4096, 512, "f32", "q8"),
 }
 DEFAULT = "llama31_8b_up_proj_bt512_f32state"
+# Exact gradient accumulation: micro-batches of BT tokens into an fp32
+# accumulator, the step fired once at the last one (name: (micro-batches, BT)).
+ACCUM = {"llama31_8b_up_proj_accum4x512_f32state": (4, 512)}
 # The full Llama-3.1-8B linear stack (32 layers x 7 linears, BT = 512).
 STACKS = {f"llama31_8b_stack_{o}_{st}": (o, st) for o in ("adamw", "lion", "sgdm") for st in ("f32state", "bf16state")}
 STACK_HYPER = {"adamw": dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01),
@@ -419,6 +422,93 @@ def run_gpu(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+def run_accum(args, rank, world, local_rank):
+    """One step = one accumulation window on the up-projection (fp32 W, m, v):
+    per micro-batch forge_dgrad, then forge_wgrad_accumulate (the first one
+    overwrites G_acc), and forge_wgrad_step_accumulated at the last."""
+    import torch
+    import backward_gemm_optimizer_gb300 as F
+    from backward_gemm_optimizer_gb300 import synthetic as S
+
+    nmb, bt = ACCUM[args.workload]
+    d_out, d_in = 14336, 4096
+    dev = torch.device(f"cuda:{local_rank}")
+    torch.cuda.set_device(dev)
+    seed = replica_seed(rank)
+    W = S.device_normal_(torch.empty((d_out, d_in), dtype=torch.float32, device=dev), 0.02, seed, 1)
+    m = S.device_normal_(torch.empty_like(W), 1e-3, seed, 2)
+    v = S.device_normal_(torch.empty_like(W), 1e-6, seed, 3, absolute=True)
+    G = torch.empty_like(W)
+    mbs = [(S.device_normal_(torch.empty((bt, d_in), dtype=torch.bfloat16, device=dev), 1.0, seed, 10 + 2 * k),
+            S.device_normal_(torch.empty((bt, d_out), dtype=torch.bfloat16, device=dev), 1.0, seed, 11 + 2 * k))
+           for k in range(nmb)]
+    dX = torch.empty((bt, d_in), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+
+    def window(t, ev=None):
+        for k, (X, dY) in enumerate(mbs):
+            if ev is not None:
+                ev[k][0].record(stream)
+            F.dgrad(dY, W, dX, stream=stream)
+            if ev is not None:
+                ev[k][1].record(stream)
+            if k < nmb - 1:
+                F.wgrad_accumulate(X, dY, G, overwrite=(k == 0), stream=stream)
+            else:
+                F.wgrad_step_accumulated("adamw", X, dY, G, W, m, v, step=t, stream=stream, **HYPER)
+            if ev is not None:
+                ev[k][2].record(stream)
+
+    t = 1
+    for _ in range(args.warmup):
+        window(t); t += 1
+    F.sync_status(stream)
+    K = args.steps
+    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(nmb)] for _ in range(K)]
+    sampler = ClockSampler(local_rank)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    time.sleep(0.3)
+    for i in range(K):
+        flush.fill_(float(i))
+        window(t, evs[i]); t += 1
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    F.sync_status(stream)
+    step_ms = [evs[i][0][0].elapsed_time(evs[i][-1][2]) for i in range(K)]
+    total_ms = max_over_ranks(sum(step_ms), world, dev)
+    if rank != 0:
+        return
+    hbm, _, _ = load_peaks()
+    acc_us = [statistics.mean(evs[i][k][1].elapsed_time(evs[i][k][2]) for i in range(K)) * 1000.0 for k in range(nmb)]
+    dgrad_us = statistics.mean(evs[i][k][0].elapsed_time(evs[i][k][1]) for i in range(K) for k in range(nmb)) * 1000.0
+    params = d_out * d_in
+    first_b = params * 4 + 2 * bt * (d_in + d_out)          # G_acc written
+    acc_b = params * 8 + 2 * bt * (d_in + d_out)            # G_acc read + written
+    last_b = params * 28 + 2 * bt * (d_in + d_out)          # W, m, v read + written, G_acc read
+    line = {
+        "metric": METRIC, "value": round(total_ms * 1000.0 / K, 1), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(total_ms / K, 3), "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "d_out": d_out, "d_in": d_in, "micro_batches": nmb, "bt": bt,
+                   "effective_batch": nmb * bt, "optimizer": "adamw", "state": "fp32 W, m, v; fp32 G_acc",
+                   "step": f"{nmb} x forge_dgrad, {nmb - 1} x forge_wgrad_accumulate, 1 x forge_wgrad_step_accumulated",
+                   "l2": "flushed between windows"},
+        "accumulate_first_us": round(acc_us[0], 2),
+        "accumulate_first_frac_of_hbm": round(first_b / (acc_us[0] * 1e-6) / 1e9 / hbm, 4),
+        "accumulate_us": round(statistics.mean(acc_us[1:-1]) if nmb > 2 else acc_us[0], 2),
+        "accumulate_frac_of_hbm": round(acc_b / (statistics.mean(acc_us[1:-1]) * 1e-6) / 1e9 / hbm, 4)
+        if nmb > 2 else None,
+        "accumulated_step_us": round(acc_us[-1], 2),
+        "accumulated_step_frac_of_hbm": round(last_b / (acc_us[-1] * 1e-6) / 1e9 / hbm, 4),
+        "dgrad_us": round(dgrad_us, 2),
+        "gpu_launches": 2 * nmb * K, "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def run_stack(args, rank, world, local_rank):
     """One step = backward over the 224 linears of Llama-3.1-8B (layer 31 .. 0,
     down, up, gate, o, v, k, q): one forge_backward_step per linear, on the
@@ -581,7 +671,7 @@ def main():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="forge", choices=["forge", "reference"])
-    ap.add_argument("--workload", default=DEFAULT, choices=sorted(WORKLOADS) + sorted(STACKS))
+    ap.add_argument("--workload", default=DEFAULT, choices=sorted(WORKLOADS) + sorted(STACKS) + sorted(ACCUM))
     ap.add_argument("--graph", action="store_true", help="stack workloads: also replay the step as a CUDA graph")
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--split-steps", type=int, default=200, help="steps of the split-path comparison")
@@ -605,6 +695,8 @@ def main():
     try:
         if args.workload in STACKS:
             run_stack(args, rank, world, local_rank)
+        elif args.workload in ACCUM:
+            run_accum(args, rank, world, local_rank)
         else:
             run_gpu(args, rank, world, local_rank)
     finally:
