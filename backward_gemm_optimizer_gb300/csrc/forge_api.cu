@@ -390,16 +390,22 @@ forge_status wgrad_step(int opt, const forge_tensor* X, const forge_tensor* dY, 
   if (dx != nullptr) bn = kDxBN;  // the fused input gradient fixes the tile width
   else if (force == FORGE_FLAG_TILE_N_64) bn = 64;
   else if (force == FORGE_FLAG_TILE_N_128) bn = 128;
+  else if (force == FORGE_FLAG_TILE_N_256) bn = 256;
   else if (force != FORGE_FLAG_TILE_N_AUTO) return fail(FORGE_ERR_INVALID_ARG, "%s: bad tile flag", oname);
   else if (mk != M_Q8 && tiles_m * ((d_in + 127) / 128) < dev->sms) bn = 64;  // too few tiles for one wave
+  else if (mk != M_Q8 && !accum && G_acc == nullptr && bt >= 1024 && tiles_m * ((d_in + 255) / 256) >= dev->sms)
+    bn = 256;  // long token axes: the GEMM dominates, wider tiles cut its operand traffic
   if (mk == M_Q8 && bn != 128)
     return fail(FORGE_ERR_UNSUPPORTED, "%s: 8-bit block moments need 128-column tiles", oname);
+  if (bn == 256 && (accum || G_acc != nullptr))
+    return fail(FORGE_ERR_UNSUPPORTED, "%s: 256-column tiles exist for the plain step only", oname);
   if (mk == M_Q8 && G_acc != nullptr)
     return fail(FORGE_ERR_UNSUPPORTED, "%s: the accumulated-gradient step has no 8-bit state variant", oname);
   // Deep operand ring for long token axes, and for the accumulation rules at
   // any length: their slots hold only the fp32 accumulator, so shared memory
   // has room for four operand stages, and their tile time is the mainloop's.
-  const int deep = (dx == nullptr && G_acc == nullptr && (bt >= 1024 || accum) && bn == 128) ? 1 : 0;
+  const bool deep128 = dx == nullptr && G_acc == nullptr && bn == 128 && (bt >= 1024 || accum);
+  const int deep = (deep128 || bn == 256) ? 1 : 0;  // 256-column tiles always use the deep ring
   const int tiles_n = static_cast<int>((d_in + bn - 1) / bn);
   const uint32_t box_tokens = dx != nullptr ? 128u : 64u;  // tokens per operand stage
 

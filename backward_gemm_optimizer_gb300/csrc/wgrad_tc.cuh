@@ -281,7 +281,8 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA>::
   using C = TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA>;
   static_assert(!GA || (!DX && !C::Q8), "accumulated-gradient step: split path, fp32 / bf16 state");
   static_assert(!(OPT == OPT_ACCUM || OPT == OPT_ACCSET) || (WK == W_F32 && !GA), "fp32 gradient accumulator");
-  static_assert(BN == 64 || BN == 128, "tile width");
+  static_assert(BN == 64 || BN == 128 || BN == 256, "tile width");
+  static_assert(BN != 256 || (!C::Q8 && !DX && !GA), "256-column tiles: plain step, fp32 / bf16 state");
   static_assert(!DX || (BN == 64 && !C::Q8), "fused input gradient: 64-column tiles, fp32 / bf16 state");
   static_assert(!C::Q8 || BN == 128, "8-bit blocks span one 128-column tile row");
   static_assert(!C::Q8 || OPT == OPT_ADAMW || OPT == OPT_SGDM || OPT == OPT_LION, "8-bit state rules");

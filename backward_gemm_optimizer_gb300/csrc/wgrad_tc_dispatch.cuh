@@ -20,12 +20,15 @@ constexpr int slots_that_fit() {
 }
 
 // Operand stages: 2 for short token axes (the step is bound by the state
-// stream), 4 (or 3 when the state slots would not fit) for long ones.
+// stream); for long ones as many as leave room for the state ring (4, else
+// 3, else 2).
 template <int OPT, int WK, int MK, int BN, int DEEP>
 constexpr int pick_stages() {
   if (!DEEP) return 2;
   constexpr int need = (MK == M_Q8) ? 4 : 2;
-  return slots_that_fit<OPT, WK, MK, BN, 4>() >= need ? 4 : 3;
+  if (slots_that_fit<OPT, WK, MK, BN, 4>() >= need) return 4;
+  if (slots_that_fit<OPT, WK, MK, BN, 3>() >= need) return 3;
+  return 2;
 }
 
 template <int OPT, int WK, int MK, int BN, int DEEP>
@@ -75,6 +78,12 @@ cudaError_t launch_mk(const WgradTcParams& p, const TcLaunch& l) {
     if (l.bn == 64) {
       if (l.deep) return cudaErrorInvalidValue;
       return launch_one<OPT, WK, MK, 64, 0>(p, l.grid, l.stream);
+    }
+    if (l.bn == 256) {
+      // 128 x 256 tiles for long token axes: a quarter less operand traffic
+      // per gradient element than 128 x 128, half the MMA instructions.
+      if (!l.deep) return cudaErrorInvalidValue;
+      return launch_one<OPT, WK, MK, 256, 1>(p, l.grid, l.stream);
     }
     return l.deep ? launch_one<OPT, WK, MK, 128, 1>(p, l.grid, l.stream)
                   : launch_one<OPT, WK, MK, 128, 0>(p, l.grid, l.stream);

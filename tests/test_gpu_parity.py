@@ -365,3 +365,34 @@ def test_more_families_fp32_inputs_bit_exact(opt):
     got = gpu_step(opt, prob, 3)
     ref = oracle_step(opt, prob, "f32", "f32", 3, mode="f32emu")
     assert_bit_exact(got, ref, opt)
+
+
+# ---------------------------------------------------------------------------
+# 128 x 256 tiles (long token axes)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("opt", ["adamw", "lion", "nadam"])
+@pytest.mark.parametrize("variant", [("f32", "f32"), ("f32", "bf16"), ("bf16", "bf16"), ("bf16", "f32")],
+                         ids=lambda v: f"W{v[0]}-m{v[1]}")
+@pytest.mark.parametrize("shape", [(384, 520, 1100), (136, 256, 70)], ids=lambda s: "x".join(map(str, s)))
+def test_wide_tiles_exact(opt, variant, shape):
+    w, st = variant
+    prob = _prob(shape, 17, "bf16", w, st, exact=True)
+    sr, srm = w == "bf16", st == "bf16"
+    got = gpu_step(opt, prob, 2, seed=5, sr_w=sr, sr_moments=srm, flags=F.FLAG_TILE_N_256)
+    ref = oracle_step(opt, prob, w, st, 2, seed=5, sr_w=sr, sr_moments=srm, mode="f32emu")
+    assert_bit_exact(got, ref, opt)
+
+
+@pytest.mark.parametrize("exact", [True, False])
+def test_tile_width_invariance_wide(exact):
+    prob = _prob((512, 768, 1088), 18, "bf16", "f32", "f32", exact=exact)
+    a = gpu_step("adamw", prob, 1, flags=F.FLAG_TILE_N_256)
+    b = gpu_step("adamw", prob, 1, flags=F.FLAG_TILE_N_128)
+    assert_bit_exact(a, b, "adamw")
+
+
+def test_wide_tiles_random_within_tolerance():
+    prob = _prob((640, 1024, 2048), 19, "bf16", "f32", "f32", exact=False)
+    got = gpu_step("adamw", prob, 3, flags=F.FLAG_TILE_N_256)
+    check_tolerance("adamw", prob, "f32", "f32", 3, got)
