@@ -22,28 +22,33 @@ namespace forge {
 
 namespace {
 
-constexpr int BM = 128, BN = 128, BK = 64;
+constexpr int BM = 128, BK = 64;
 constexpr int A_BYTES = BM * BK * 2;       // 16 KB: dY tile, K-major
-constexpr int B_BYTES = BK * BN * 2;       // 16 KB: bf16 W tile, MN-major
-constexpr int STG_BYTES = BK * BN * 4;     // 32 KB: fp32 W tile as four 32-column swizzled boxes
-constexpr int TMEM_COLS = 256;
 constexpr int NUM_THREADS = 512;
 constexpr int CONV_THREADS = 256;          // warps 8-15
-constexpr uint32_t IDESC = make_idesc_bf16(BM, BN, 0, 1);
 
 // Three rings, each released by its own consumer, so that a load is never
 // held back by an unrelated stage: dY tiles (released by the MMA), fp32
 // staging tiles (released by the converters once read) and bf16 W tiles
-// (filled by TMA or by the converters, released by the MMA).
-template <bool F32W>
+// (filled by TMA or by the converters, released by the MMA). Tiles are 128
+// tokens x BN input features: 128, or 256 for bf16 weights when the wider
+// tiles still fill the GPU (half the operand traffic of dY per output).
+template <bool F32W, int BN_>
 struct DCfg {
-  static constexpr int SA = F32W ? 3 : 6;
-  static constexpr int SB = F32W ? 2 : 6;
+  static constexpr int BN = BN_;
+  static constexpr int B_BYTES = BK * BN * 2;    // bf16 W tile, MN-major, 64-column atoms 8 KB apart
+  static constexpr int STG_BYTES = BK * BN * 4;  // fp32 W tile as 32-column swizzled boxes
+  static constexpr int SA = F32W ? 3 : (BN == 256 ? 4 : 6);
+  static constexpr int SB = F32W ? 2 : (BN == 256 ? 4 : 6);
   static constexpr int SS = F32W ? 4 : 0;
   static constexpr int A_OFF = 0;
   static constexpr int B_OFF = SA * A_BYTES;
   static constexpr int S_OFF = B_OFF + SB * B_BYTES;
   static constexpr int SMEM_BYTES = 1024 + S_OFF + SS * STG_BYTES;
+  static constexpr int TMEM_COLS = 2 * BN;
+  static constexpr uint32_t IDESC = make_idesc_bf16(BM, BN, 0, 1);
+  static_assert(!F32W || BN == 128, "fp32 weight staging is sized for 128-column tiles");
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 };
 
 __device__ __forceinline__ bool dwait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
@@ -84,9 +89,11 @@ __device__ __forceinline__ void dtile(int tile, int tiles_m, int tiles_n, int gr
   tn = in_g / gsize;
 }
 
-template <bool F32W>
+template <bool F32W, int BN>
 __global__ void __launch_bounds__(NUM_THREADS, 1) dgrad_tc_kernel(const __grid_constant__ DgradParams p) {
-  using C = DCfg<F32W>;
+  using C = DCfg<F32W, BN>;
+  constexpr int B_BYTES = C::B_BYTES, STG_BYTES = C::STG_BYTES, TMEM_COLS = C::TMEM_COLS;
+  constexpr uint32_t IDESC = C::IDESC;
   constexpr int SA = C::SA, SB = C::SB, SS = C::SS > 0 ? C::SS : 1;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t a_full[SA], a_empty[SA], b_full[SB], b_empty[SB], s_full[SS], s_empty[SS];
@@ -165,8 +172,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dgrad_tc_kernel(const __grid_c
             }
             uint8_t* b = b_ring + s * B_BYTES;
             mbar_arrive_expect_tx(&b_full[s], B_BYTES);
-            tma_load_2d(b, &p.tm_w, &b_full[s], tn * BN, kb * BK);
-            tma_load_2d(b + 8192, &p.tm_w, &b_full[s], tn * BN + 64, kb * BK);
+#pragma unroll
+            for (int bb = 0; bb < BN / 64; ++bb)
+              tma_load_2d(b + bb * 8192, &p.tm_w, &b_full[s], tn * BN + bb * 64, kb * BK);
           }
         }
       }
@@ -337,27 +345,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dgrad_tc_kernel(const __grid_c
   }
 }
 
-template <bool F32W>
+template <bool F32W, int BN>
 cudaError_t launch_d(const DgradParams& p, int grid, cudaStream_t stream) {
-  auto kern = dgrad_tc_kernel<F32W>;
+  auto kern = dgrad_tc_kernel<F32W, BN>;
   static unsigned long long attr_mask = 0ull;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   const unsigned long long bit = 1ull << (dev & 63);
   if (!(__atomic_load_n(&attr_mask, __ATOMIC_ACQUIRE) & bit)) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DCfg<F32W>::SMEM_BYTES);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DCfg<F32W, BN>::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     __atomic_fetch_or(&attr_mask, bit, __ATOMIC_ACQ_REL);
   }
-  kern<<<grid, NUM_THREADS, DCfg<F32W>::SMEM_BYTES, stream>>>(p);
+  kern<<<grid, NUM_THREADS, DCfg<F32W, BN>::SMEM_BYTES, stream>>>(p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_dgrad_tc(const DgradParams& p, int grid, cudaStream_t stream) {
-  return p.w_f32 ? launch_d<true>(p, grid, stream) : launch_d<false>(p, grid, stream);
+  if (p.w_f32) return p.bn == 128 ? launch_d<true, 128>(p, grid, stream) : cudaErrorInvalidValue;
+  return p.bn == 256 ? launch_d<false, 256>(p, grid, stream) : launch_d<false, 128>(p, grid, stream);
 }
 
 }  // namespace forge

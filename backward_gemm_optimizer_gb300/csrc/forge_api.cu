@@ -695,7 +695,10 @@ forge_status dgrad_impl(const forge_tensor* dY, const forge_tensor* W_old, forge
   p.d_out = static_cast<int>(d_out);
   p.d_in = static_cast<int>(d_in);
   p.tiles_m = static_cast<int>((bt + 127) / 128);
-  p.tiles_n = static_cast<int>((d_in + 127) / 128);
+  // 128 x 256 tiles for bf16 weights when they still fill the GPU (long
+  // token axes): half the dY operand traffic per output of 128 x 128.
+  p.bn = (W_old->dtype == FORGE_BF16 && p.tiles_m * ((d_in + 255) / 256) >= dev->sms) ? 256 : 128;
+  p.tiles_n = static_cast<int>((d_in + p.bn - 1) / p.bn);
   p.num_tiles = p.tiles_m * p.tiles_n;
   p.num_kb = static_cast<int>((d_out + 63) / 64);
   p.group_m = 8;

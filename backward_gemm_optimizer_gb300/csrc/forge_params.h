@@ -103,6 +103,7 @@ struct alignas(128) DgradParams {
   int bt, d_out, d_in;
   int tiles_m, tiles_n, num_tiles, num_kb;
   int group_m;
+  int bn;             // tile width (input features): 128, or 256 for bf16 W
   uint32_t flags;
   uint64_t timeout_ns;
 };

@@ -275,8 +275,10 @@ def test_forced_device_timeout_reports_and_leaves_state():
 @pytest.mark.parametrize("w_dtype", ["bf16", "f32"])
 @pytest.mark.parametrize("dx_dtype", ["bf16", "f32"])
 @pytest.mark.parametrize("shape", [(256, 384, 200), (136, 200, 70), (1024, 512, 512), (2048, 1024, 64),
-                                   (1024, 512, 640)])
+                                   (1024, 512, 640), (1024, 4000, 1300)])
 def test_dgrad_exact(w_dtype, dx_dtype, shape):
+    # (1024, 4000, 1300): with bf16 weights, 128 x 256 tiles with ragged
+    # token and feature tails.
     d_out, d_in, bt = shape
     dev = "cuda:0"
     dY = S.small_integers((bt, d_out), -3, 3, 1, S.STREAM_DY, "bf16")
