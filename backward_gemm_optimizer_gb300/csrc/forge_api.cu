@@ -160,15 +160,19 @@ forge_status encode_2d(CUtensorMap* map, const forge_tensor* t, CUtensorMapDataT
   return FORGE_OK;
 }
 
-// Chunk maps of the W / m / v tiles: 32 columns x 128 rows, swizzle = row bytes.
-forge_status encode_state(CUtensorMap* map, const forge_tensor* t, const char* name) {
+// Chunk maps of the W / m / v tiles: `cw` columns (32, or 16 for the fp32
+// fused-input-gradient kernel) x 128 rows, swizzle = row bytes.
+forge_status encode_state(CUtensorMap* map, const forge_tensor* t, const char* name, int cw = 32) {
   CUtensorMapDataType dt;
-  CUtensorMapSwizzle swz;
   int es;
-  if (t->dtype == FORGE_F32) { dt = CU_TENSOR_MAP_DATA_TYPE_FLOAT32; es = 4; swz = CU_TENSOR_MAP_SWIZZLE_128B; }
-  else if (t->dtype == FORGE_BF16) { dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16; es = 2; swz = CU_TENSOR_MAP_SWIZZLE_64B; }
-  else { dt = CU_TENSOR_MAP_DATA_TYPE_UINT8; es = 1; swz = CU_TENSOR_MAP_SWIZZLE_32B; }
-  return encode_2d(map, t, dt, es, 32, 128, swz, name);
+  if (t->dtype == FORGE_F32) { dt = CU_TENSOR_MAP_DATA_TYPE_FLOAT32; es = 4; }
+  else if (t->dtype == FORGE_BF16) { dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16; es = 2; }
+  else { dt = CU_TENSOR_MAP_DATA_TYPE_UINT8; es = 1; }
+  const int row_bytes = cw * es;
+  const CUtensorMapSwizzle swz = row_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                 : row_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                   : CU_TENSOR_MAP_SWIZZLE_32B;
+  return encode_2d(map, t, dt, es, static_cast<uint32_t>(cw), 128, swz, name);
 }
 
 // ------------------------------------------------------------------ scalars
@@ -419,14 +423,19 @@ forge_status wgrad_step(int opt, const forge_tensor* X, const forge_tensor* dY, 
                         "X")) != FORGE_OK)
       return st;
   }
-  if ((st = encode_state(&p.tm_w, W, "W")) != FORGE_OK) return st;
+  // State chunk width: 16 columns for the fused input gradient with fp32 W
+  // and two fp32 moments at BT <= 256 (measured: the deeper state ring wins
+  // when the mainloop is short; at BT 512 the extra chunk turns cost more).
+  const bool narrow = dx != nullptr && wk == W_F32 && mk == M_F32 && nst == 2 && bt <= 256;
+  const int cw = narrow ? 16 : 32;
+  if ((st = encode_state(&p.tm_w, W, "W", cw)) != FORGE_OK) return st;
   if (nst >= 1) {
-    if ((st = encode_state(&p.tm_m, m, "m")) != FORGE_OK) return st;
+    if ((st = encode_state(&p.tm_m, m, "m", cw)) != FORGE_OK) return st;
   } else {
     p.tm_m = p.tm_w;  // unused
   }
   if (nst == 2) {
-    if ((st = encode_state(&p.tm_v, v, "v")) != FORGE_OK) return st;
+    if ((st = encode_state(&p.tm_v, v, "v", cw)) != FORGE_OK) return st;
   } else {
     p.tm_v = p.tm_m;  // unused
   }
@@ -458,6 +467,7 @@ forge_status wgrad_step(int opt, const forge_tensor* X, const forge_tensor* dY, 
   TcLaunch l{};
   l.opt = opt; l.wk = wk; l.mk = mk; l.bn = bn; l.deep = deep; l.dx = dx != nullptr ? 1 : 0;
   l.ga = G_acc != nullptr ? 1 : 0;
+  l.narrow = narrow ? 1 : 0;
   l.grid = p.num_tiles < dev->sms ? p.num_tiles : dev->sms;
   l.stream = s;
   DxGeometry g;

@@ -114,6 +114,7 @@ struct TcLaunch {
   int deep;     // 1: deeper operand pipeline for long token axes
   int dx;       // 1: fused input gradient (64-column tiles, fp32 / bf16 state)
   int ga;       // 1: add the accumulated gradient G_acc (tm_g) to each tile
+  int narrow;   // 1: 16-column state chunks (fused kernel, fp32 W and moments, short token axes)
   int grid;
   cudaStream_t stream;
 };

@@ -57,7 +57,8 @@
 
 namespace forge {
 
-template <int OPT, int WK, int MK, int BN_, int STAGES_, int NBUF_, bool DX_ = false, bool GA_ = false>
+template <int OPT, int WK, int MK, int BN_, int STAGES_, int NBUF_, bool DX_ = false, bool GA_ = false,
+          bool NARROW_ = false>
 struct TcCfg {
   static constexpr bool DX = DX_;      // fused input gradient (see above)
   static constexpr bool GA = GA_;      // add an fp32 accumulated gradient G_acc to each tile
@@ -66,7 +67,14 @@ struct TcCfg {
   static constexpr int BN = BN_;       // tile columns (D_in)
   static constexpr int BK = DX ? 128 : 64;  // tokens per operand stage
   static constexpr int BOX = BK * 128; // bytes of one 64-column operand box (BK rows of 128 bytes)
-  static constexpr int CW = 32;        // state chunk width (columns)
+  // State chunk width (columns): 32, or 16 (NARROW) for the fused-input-
+  // gradient kernel with fp32 W and two fp32 moments on short token axes --
+  // its shared memory holds two 48 KB slots of 32 columns or four of 16, and
+  // with a short mainloop the deeper ring's extra loads in flight pay for
+  // the extra chunk turns.
+  static constexpr bool NARROW = NARROW_;
+  static constexpr int CW = NARROW ? 16 : 32;
+  static constexpr int QC = CW / 4;    // columns per epilogue thread per chunk (one quarter)
   static constexpr int STAGES = STAGES_;
   static constexpr int NBUF = NBUF_;
   static constexpr int NCH = BN / CW;  // chunks per tile
@@ -94,7 +102,6 @@ struct TcCfg {
   static constexpr int EPI_THREADS = EPI_WARPS * 32;
   static constexpr int CONV_THREADS = DX ? 128 : 0;  // warps 20-23
   static constexpr int NUM_THREADS = 128 + EPI_THREADS + CONV_THREADS;
-  static constexpr int QCOLS = 8;                // columns per epilogue thread per chunk
   static constexpr uint32_t IDESC = make_idesc_bf16(BM, BN, 1, 1);
   // dX: A = dY (M = 128 tokens, K-major), B = Wb (N = BN, MN-major).
   static constexpr uint32_t IDESC_DX = make_idesc_bf16(128, BN, 0, 1);
@@ -136,6 +143,17 @@ __device__ __forceinline__ void st8_f32(uint8_t* base, int r, int h, const float
   for (int k = 0; k < 2; ++k)
     *reinterpret_cast<float4*>(base + swz<4>(r, 2 * h + k)) =
         make_float4(o[4 * k + 0], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+}
+
+// 4 consecutive fp32 values of row r, columns [4h, 4h + 4) of a 16-column
+// chunk (64-byte rows, 64-byte swizzle: one 16-byte piece).
+__device__ __forceinline__ void ld4_f32(const uint8_t* base, int r, int h, float (&o)[4]) {
+  const float4 t = *reinterpret_cast<const float4*>(base + swz<2>(r, h));
+  o[0] = t.x; o[1] = t.y; o[2] = t.z; o[3] = t.w;
+}
+
+__device__ __forceinline__ void st4_f32(uint8_t* base, int r, int h, const float (&o)[4]) {
+  *reinterpret_cast<float4*>(base + swz<2>(r, h)) = make_float4(o[0], o[1], o[2], o[3]);
 }
 
 __device__ __forceinline__ void st8_bf16(uint8_t* base, int r, int h, const uint4& t) {
@@ -275,10 +293,11 @@ __device__ __forceinline__ void drain_ring(uint64_t* full, int ring, uint32_t is
   }
 }
 
-template <int OPT, int WK, int MK, int BN, int STAGES, int NBUF, bool DX, bool GA>
-__global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA>::NUM_THREADS, 1)
+template <int OPT, int WK, int MK, int BN, int STAGES, int NBUF, bool DX, bool GA, bool NARROW>
+__global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, NARROW>::NUM_THREADS, 1)
     wgrad_step_tc_kernel(const __grid_constant__ WgradTcParams p) {
-  using C = TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA>;
+  using C = TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, NARROW>;
+  static_assert(!NARROW || (DX && WK == W_F32 && MK == M_F32 && C::TWO), "16-column chunks: fp32 fused kernel");
   static_assert(!GA || (!DX && !C::Q8), "accumulated-gradient step: split path, fp32 / bf16 state");
   static_assert(!(OPT == OPT_ACCUM || OPT == OPT_ACCSET) || (WK == W_F32 && !GA), "fp32 gradient accumulator");
   static_assert(BN == 64 || BN == 128 || BN == 256, "tile width");
@@ -538,24 +557,32 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA>::
           ok = bwait(&st_full[s], (cseq / NBUF) & 1u, abort_flag, p.status, WAIT_ST_FULL, lim);
           ok = __all_sync(0xFFFFFFFFu, ok);
           if (!ok) break;
-          uint32_t gr[8];
+          constexpr int Q = C::QC;
+          uint32_t gr[Q];
           if (p.num_kb > 0) {
-            tmem_ld_32x32b_x8(t_lane + c * C::CW + h * 8, gr);
+            if constexpr (Q == 8) tmem_ld_32x32b_x8(t_lane + c * C::CW + h * Q, gr);
+            else tmem_ld_32x32b_x4(t_lane + c * C::CW + h * Q, gr);
             tmem_ld_wait();
           } else {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) gr[j] = 0u;
+            for (int j = 0; j < Q; ++j) gr[j] = 0u;
           }
           uint8_t* slot = st_base + s * C::SLOT_BYTES;
           uint8_t* sw = slot;
           uint8_t* sm = slot + C::W_CH;
           uint8_t* sv = slot + C::W_CH + C::M_CH;
-          float w[8], m[8], v[8], g[8];
-          if constexpr (C::LOAD_W) ld8<WK == W_F32 ? 0 : 1>(sw, r, h, w);
-          if constexpr (C::NST >= 1) ld8<MK == M_F32 ? 0 : 1>(sm, r, h, m);
-          if constexpr (C::TWO) ld8<MK == M_F32 ? 0 : 1>(sv, r, h, v);
+          float w[Q], m[Q], v[Q], g[Q];
+          if constexpr (Q == 4) {  // fp32 W and moments (the 16-column chunks)
+            ld4_f32(sw, r, h, w);
+            ld4_f32(sm, r, h, m);
+            ld4_f32(sv, r, h, v);
+          } else {
+            if constexpr (C::LOAD_W) ld8<WK == W_F32 ? 0 : 1>(sw, r, h, w);
+            if constexpr (C::NST >= 1) ld8<MK == M_F32 ? 0 : 1>(sm, r, h, m);
+            if constexpr (C::TWO) ld8<MK == M_F32 ? 0 : 1>(sv, r, h, v);
+          }
 #pragma unroll
-          for (int j = 0; j < 8; ++j) g[j] = __uint_as_float(gr[j]);
+          for (int j = 0; j < Q; ++j) g[j] = __uint_as_float(gr[j]);
           if constexpr (GA) {
             // The micro-batches accumulated so far: G = G_acc + this tile's G.
             float ga[8];
@@ -564,7 +591,15 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA>::
             for (int j = 0; j < 8; ++j) g[j] = __fadd_rn(ga[j], g[j]);
           }
 #pragma unroll
-          for (int j = 0; j < 8; ++j) step_elem<OPT>(g[j], w[j], m[j], v[j], sc);
+          for (int j = 0; j < Q; ++j) step_elem<OPT>(g[j], w[j], m[j], v[j], sc);
+          if constexpr (Q == 4) {
+            st4_f32(sw, r, h, w);
+            st4_f32(sm, r, h, m);
+            st4_f32(sv, r, h, v);
+            fence_proxy_async_smem();
+            mbar_arrive(&st_written[s]);
+            continue;
+          } else {
           // Element index of this thread's first column; 8-aligned (D_in % 8 == 0).
           const uint64_t idx8 =
               (static_cast<uint64_t>(row) * static_cast<uint64_t>(p.d_in) + (tn * BN + c * C::CW + h * 8)) >> 3;
@@ -590,6 +625,7 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA>::
           }
           fence_proxy_async_smem();
           mbar_arrive(&st_written[s]);
+          }
         }
         if (!ok) break;
       } else {
@@ -808,10 +844,10 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA>::
   }
 }
 
-template <int OPT, int WK, int MK, int BN, int STAGES, int NBUF, bool DX, bool GA = false>
+template <int OPT, int WK, int MK, int BN, int STAGES, int NBUF, bool DX, bool GA = false, bool NARROW = false>
 cudaError_t launch_tc_variant(const WgradTcParams& p, int grid, cudaStream_t stream) {
-  using C = TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA>;
-  auto kern = wgrad_step_tc_kernel<OPT, WK, MK, BN, STAGES, NBUF, DX, GA>;
+  using C = TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, NARROW>;
+  auto kern = wgrad_step_tc_kernel<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, NARROW>;
   // The opt-in shared-memory size is a per-device function attribute: set
   // it once per device (bit d of the mask) before the first launch there.
   static unsigned long long attr_mask = 0ull;

@@ -11,9 +11,9 @@ namespace forge {
 // shared memory (barriers + the 8 KB absmax exchange) is accounted for.
 constexpr int kDynSmemBudget = 227 * 1024 - 9 * 1024;
 
-template <int OPT, int WK, int MK, int BN, int STAGES, bool DX = false, bool GA = false>
+template <int OPT, int WK, int MK, int BN, int STAGES, bool DX = false, bool GA = false, bool NARROW = false>
 constexpr int slots_that_fit() {
-  using C = TcCfg<OPT, WK, MK, BN, STAGES, 2, DX, GA>;
+  using C = TcCfg<OPT, WK, MK, BN, STAGES, 2, DX, GA, NARROW>;
   const int avail = kDynSmemBudget - 1024 - STAGES * C::STAGE_BYTES - C::WB_BYTES;
   const int n = avail / C::SLOT_BYTES;
   return n > 8 ? 8 : n;
@@ -49,11 +49,11 @@ cudaError_t launch_ga(const WgradTcParams& p, int grid, cudaStream_t stream) {
 }
 
 // Fused input gradient: 64-column tiles, two 128-token operand stages.
-template <int OPT, int WK, int MK>
+template <int OPT, int WK, int MK, bool NARROW = false>
 cudaError_t launch_dx(const WgradTcParams& p, int grid, cudaStream_t stream) {
-  constexpr int N = slots_that_fit<OPT, WK, MK, 64, 2, true>();
+  constexpr int N = slots_that_fit<OPT, WK, MK, 64, 2, true, false, NARROW>();
   static_assert(N >= 2, "state ring does not fit");
-  return launch_tc_variant<OPT, WK, MK, 64, 2, N, true>(p, grid, stream);
+  return launch_tc_variant<OPT, WK, MK, 64, 2, N, true, false, NARROW>(p, grid, stream);
 }
 
 template <int OPT, int WK, int MK>
@@ -68,7 +68,12 @@ cudaError_t launch_mk(const WgradTcParams& p, const TcLaunch& l) {
   }
   if (l.dx) {
     if constexpr (MK == M_Q8) return cudaErrorInvalidValue;
-    else return l.bn == 64 && !l.deep ? launch_dx<OPT, WK, MK>(p, l.grid, l.stream) : cudaErrorInvalidValue;
+    else {
+      if (l.bn != 64 || l.deep) return cudaErrorInvalidValue;
+      if constexpr (WK == W_F32 && MK == M_F32 && opt_nstate(OPT) == 2)
+        if (l.narrow) return launch_dx<OPT, WK, MK, true>(p, l.grid, l.stream);
+      return l.narrow ? cudaErrorInvalidValue : launch_dx<OPT, WK, MK>(p, l.grid, l.stream);
+    }
   }
   if constexpr (MK == M_Q8) {
     if (l.bn != 128) return cudaErrorInvalidValue;
