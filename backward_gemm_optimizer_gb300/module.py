@@ -15,7 +15,14 @@ returns no gradient for it.
 ``ForgeStepManager`` plays the role of the pages' optimizer manager: it
 holds the hyper-parameters shared by the fused layers, and its
 ``pre_step(lr=...)`` advances the step counter (and optionally the
-learning rate) before each forward/backward.
+learning rate) before each forward/backward. With
+``accumulation_steps = K > 1`` (exact gradient accumulation, FORGE
+Appendix L) ``pre_step`` is called before every micro-batch: the first
+K - 1 backward passes of a window add their weight gradients into a
+per-layer fp32 accumulator (``forge_wgrad_accumulate``) and the K-th fires
+the fused step once on the whole window's gradient
+(``forge_wgrad_step_accumulated``); the step counter advances once per
+window.
 
 Weights read by more than one backward path in a step (tied embeddings,
 experts reduced across ranks) must not be fused (Remark 1); keep those on
@@ -53,6 +60,8 @@ class StepConfig:
     seed: int = 0
     step: int = 0
     backward_flags: int = 0  # FLAG_BACKWARD_FUSED / FLAG_BACKWARD_SPLIT force a path; 0 = library policy
+    accumulation_steps: int = 1  # micro-batches per optimizer step
+    micro: int = 0               # 0-based micro-batch of the current window
 
 
 # Workspaces of the fused backward path, one per (device, stream): calls on
@@ -86,7 +95,12 @@ class _ForgeLinearFn(torch.autograd.Function):
         layer: ForgeLinear = ctx.layer
         dy2d = dy2d.contiguous()
         dx = None
-        if ctx.needs_input_grad[0]:
+        if layer.config.accumulation_steps > 1:
+            if ctx.needs_input_grad[0]:
+                dx = torch.empty(x2d.shape, dtype=x2d.dtype, device=x2d.device)
+                F.dgrad(dy2d, layer.weight, dx)            # W is unchanged until the window's last micro-batch
+            layer._accumulate(x2d, dy2d)
+        elif ctx.needs_input_grad[0]:
             dx = torch.empty(x2d.shape, dtype=x2d.dtype, device=x2d.device)
             layer._backward(x2d, dy2d, dx)                 # dX from W before the step (Remark 1)
         else:
@@ -142,6 +156,19 @@ class ForgeLinear(torch.nn.Module):
         y = _ForgeLinearFn.apply(x2d, self.weight, self)
         return y.reshape(*shape[:-1], self.out_features)
 
+    def _accumulate(self, x2d: torch.Tensor, dy2d: torch.Tensor):
+        c = self.config
+        if getattr(self, "grad_acc", None) is None or self.grad_acc.shape != self.weight.shape:
+            # The one gradient-shaped buffer of the accumulation mode, live for the run.
+            self.grad_acc = torch.empty(self.weight.shape, dtype=torch.float32, device=self.weight.device)
+        if c.micro < c.accumulation_steps - 1:
+            F.wgrad_accumulate(x2d, dy2d, self.grad_acc, overwrite=(c.micro == 0))
+        else:
+            F.wgrad_step_accumulated(c.rule, x2d, dy2d, self.grad_acc, self.weight, self.state0, self.state1,
+                                     lr=c.lr, beta1=c.beta1, beta2=c.beta2, eps=c.eps,
+                                     weight_decay=c.weight_decay, momentum_decay=c.momentum_decay, step=c.step,
+                                     seed=c.seed, sr_w=c.sr_w, sr_moments=c.sr_moments)
+
     def _backward(self, x2d: torch.Tensor, dy2d: torch.Tensor, dx: torch.Tensor):
         c = self.config
         ws = _workspace(x2d.device, F.workspace_bytes(self.out_features, self.in_features, x2d.shape[0]))
@@ -191,18 +218,26 @@ class ForgeStepManager:
     rate) before the forward/backward in which the fused layers update.
     """
 
-    def __init__(self, model: torch.nn.Module, config: Optional[StepConfig] = None):
+    def __init__(self, model: torch.nn.Module, config: Optional[StepConfig] = None, accumulation_steps: int = 1):
+        if accumulation_steps < 1:
+            raise ValueError("accumulation_steps must be >= 1")
         self.layers: List[ForgeLinear] = [m for m in model.modules() if isinstance(m, ForgeLinear)]
         self.config = config if config is not None else (self.layers[0].config if self.layers else StepConfig())
         for m in self.layers:
             m.config = self.config
+        self.config.accumulation_steps = accumulation_steps
+        self.config.micro = accumulation_steps - 1  # the first pre_step opens a window
         self._fused_ids = {id(m.weight) for m in self.layers}
         self._model = model
 
     def pre_step(self, lr: Optional[float] = None):
+        """Call before each forward/backward (each micro-batch when accumulating)."""
+        c = self.config
         if lr is not None:
-            self.config.lr = float(lr)
-        self.config.step += 1
+            c.lr = float(lr)
+        c.micro = (c.micro + 1) % c.accumulation_steps
+        if c.micro == 0:
+            c.step += 1
 
     def get_non_fused_params(self) -> Iterable[torch.nn.Parameter]:
         """Parameters a standard optimizer should still step (norms, embeddings...)."""

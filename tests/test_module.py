@@ -106,3 +106,40 @@ def test_small_model_trains_with_fused_layers():
     F.sync_status()
     assert losses[-1] < 0.7 * losses[0], losses
     assert all(m.weight.grad is None for m in mgr.layers)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("rule", ["adamw", "lion"])
+def test_accumulation_window_equals_one_step_on_the_whole_batch(rule):
+    # Exact gradient accumulation (Appendix L): K micro-batches through the
+    # layer with accumulation_steps = K update W exactly as one step on the
+    # concatenated batch (integer-valued inputs: every sum is exact).
+    dev = "cuda:0"
+    torch.manual_seed(3)
+    K, d_in, d_out = 3, 256, 384
+    xs = [torch.randint(-3, 4, (n, d_in), device=dev).bfloat16() for n in (64, 100, 37)]
+    gs = [torch.randint(-3, 4, (n, d_out), device=dev).bfloat16() for n in (64, 100, 37)]
+    acc = ForgeLinear(d_in, d_out, rule=rule, device=dev)
+    one = ForgeLinear(d_in, d_out, rule=rule, device=dev)
+    with torch.no_grad():
+        one.weight.copy_(acc.weight)
+    m_acc = ForgeStepManager(acc, accumulation_steps=K)
+    m_one = ForgeStepManager(one)
+    for cfg in (m_acc.config, m_one.config):
+        cfg.lr, cfg.weight_decay = 1e-3, 0.01
+    W0 = acc.weight.detach().clone()
+    for x, g in zip(xs, gs):
+        m_acc.pre_step()
+        x = x.clone().requires_grad_(True)
+        (acc(x).float() * g.float()).sum().backward()
+        if m_acc.config.micro < K - 1:
+            assert torch.equal(acc.weight, W0)          # no step before the window's last micro-batch
+    m_one.pre_step()
+    xc = torch.cat(xs).requires_grad_(True)
+    (one(xc).float() * torch.cat(gs).float()).sum().backward()
+    F.sync_status()
+    assert m_acc.config.step == m_one.config.step == 1
+    assert torch.equal(acc.weight, one.weight)
+    assert torch.equal(acc.state0, one.state0)
+    if acc.state1 is not None:
+        assert torch.equal(acc.state1, one.state1)
