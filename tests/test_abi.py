@@ -150,3 +150,45 @@ def test_dgrad_validation():
     dY.dtype = 1
     W.rows = 31
     assert lib.forge_dgrad(ctypes.byref(dY), ctypes.byref(W), ctypes.byref(dX), None) == INVALID
+
+
+def test_backward_step_host_checks():
+    lib = F.lib()
+    X, dY, W, m, v = _shapes()
+    dX = _t(dtype=1, rows=16, cols=64)
+    h = _h()
+    args = (ctypes.byref(X), ctypes.byref(dY), ctypes.byref(W), ctypes.byref(m), ctypes.byref(v),
+            ctypes.byref(dX), ctypes.byref(h), 1, 0, None, 0, None)
+    assert lib.forge_backward_step(99, *args) == INVALID                     # unknown rule
+    assert lib.forge_backward_step(-1, *args) == INVALID
+    h2 = _h(flags=F.FLAG_BACKWARD_FUSED | F.FLAG_BACKWARD_SPLIT)
+    r = lib.forge_backward_step(0, ctypes.byref(X), ctypes.byref(dY), ctypes.byref(W), ctypes.byref(m),
+                                ctypes.byref(v), ctypes.byref(dX), ctypes.byref(h2), 1, 0, None, 0, None)
+    assert r == INVALID and "both" in lib.forge_last_error().decode()
+    bad_dx = _t(dtype=2, rows=16, cols=64)
+    r = lib.forge_backward_step(0, ctypes.byref(X), ctypes.byref(dY), ctypes.byref(W), ctypes.byref(m),
+                                ctypes.byref(v), ctypes.byref(bad_dx), ctypes.byref(h), 1, 0, None, 0, None)
+    assert r == UNSUPPORTED                                                  # dX must be bf16 or f32
+    assert lib.forge_backward_step_no_alloc(7, None, None, None, None, None, None, None, 1, 0, None) == INVALID
+
+
+def test_accumulation_host_checks():
+    lib = F.lib()
+    X, dY, W, m, v = _shapes()
+    G = _t(dtype=0, rows=32, cols=64)
+    h = _h()
+    assert lib.forge_wgrad_accumulate(ctypes.byref(X), ctypes.byref(dY), None, 0, None) == INVALID
+    G16 = _t(dtype=1, rows=32, cols=64)
+    assert lib.forge_wgrad_accumulate(ctypes.byref(X), ctypes.byref(dY), ctypes.byref(G16), 0, None) == UNSUPPORTED
+    Xf, dYf = _t(dtype=0, rows=16, cols=64), _t(dtype=0, rows=16, cols=32)
+    assert lib.forge_wgrad_accumulate(ctypes.byref(Xf), ctypes.byref(dYf), ctypes.byref(G), 1, None) == UNSUPPORTED
+    r = lib.forge_wgrad_step_accumulated(42, ctypes.byref(X), ctypes.byref(dY), ctypes.byref(G), ctypes.byref(W),
+                                         ctypes.byref(m), ctypes.byref(v), ctypes.byref(h), 1, 0, None)
+    assert r == INVALID
+    r = lib.forge_wgrad_step_accumulated(0, ctypes.byref(X), ctypes.byref(dY), None, ctypes.byref(W),
+                                         ctypes.byref(m), ctypes.byref(v), ctypes.byref(h), 1, 0, None)
+    assert r == INVALID
+    Gbad = _t(dtype=0, rows=31, cols=64)
+    r = lib.forge_wgrad_step_accumulated(0, ctypes.byref(X), ctypes.byref(dY), ctypes.byref(Gbad), ctypes.byref(W),
+                                         ctypes.byref(m), ctypes.byref(v), ctypes.byref(h), 1, 0, None)
+    assert r == INVALID and "G_acc" in lib.forge_last_error().decode()
