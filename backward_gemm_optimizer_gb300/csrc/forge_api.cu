@@ -409,7 +409,9 @@ forge_status wgrad_step(int opt, const forge_tensor* X, const forge_tensor* dY, 
   // any length: their slots hold only the fp32 accumulator, so shared memory
   // has room for four operand stages, and their tile time is the mainloop's.
   const bool deep128 = dx == nullptr && G_acc == nullptr && bn == 128 && (bt >= 1024 || accum);
-  const int deep = (deep128 || bn == 256) ? 1 : 0;  // 256-column tiles always use the deep ring
+  // 256-column tiles always use the deep ring; the fused input gradient takes
+  // a third operand stage past 512 tokens (its mainloop then sets the pace).
+  const int deep = (deep128 || bn == 256 || (dx != nullptr && bt > 512)) ? 1 : 0;
   const int tiles_n = static_cast<int>((d_in + bn - 1) / bn);
   const uint32_t box_tokens = dx != nullptr ? 128u : 64u;  // tokens per operand stage
 
@@ -425,8 +427,10 @@ forge_status wgrad_step(int opt, const forge_tensor* X, const forge_tensor* dY, 
   }
   // State chunk width: 16 columns for the fused input gradient with fp32 W
   // and two fp32 moments at BT <= 256 (measured: the deeper state ring wins
-  // when the mainloop is short; at BT 512 the extra chunk turns cost more).
-  const bool narrow = dx != nullptr && wk == W_F32 && mk == M_F32 && nst == 2 && bt <= 256;
+  // when the mainloop is short; at BT 512 the extra chunk turns cost more)
+  // and past 512 tokens (the narrow slots leave room for a third operand
+  // stage: 398 -> 351 us at BT 768 on the up-projection).
+  const bool narrow = dx != nullptr && wk == W_F32 && mk == M_F32 && nst == 2 && (bt <= 256 || bt > 512);
   const int cw = narrow ? 16 : 32;
   if ((st = encode_state(&p.tm_w, W, "W", cw)) != FORGE_OK) return st;
   if (nst >= 1) {

@@ -48,12 +48,15 @@ cudaError_t launch_ga(const WgradTcParams& p, int grid, cudaStream_t stream) {
   return launch_tc_variant<OPT, WK, MK, BN, 2, N, false, true>(p, grid, stream);
 }
 
-// Fused input gradient: 64-column tiles, two 128-token operand stages.
-template <int OPT, int WK, int MK, bool NARROW = false>
+// Fused input gradient: 64-column tiles, two 128-token operand stages, or
+// three (DEEP: long token axes, where the mainloop sets the pace) when the
+// state ring still keeps two slots.
+template <int OPT, int WK, int MK, bool NARROW = false, bool DEEP = false>
 cudaError_t launch_dx(const WgradTcParams& p, int grid, cudaStream_t stream) {
-  constexpr int N = slots_that_fit<OPT, WK, MK, 64, 2, true, false, NARROW>();
+  constexpr int S = (DEEP && slots_that_fit<OPT, WK, MK, 64, 3, true, false, NARROW>() >= 2) ? 3 : 2;
+  constexpr int N = slots_that_fit<OPT, WK, MK, 64, S, true, false, NARROW>();
   static_assert(N >= 2, "state ring does not fit");
-  return launch_tc_variant<OPT, WK, MK, 64, 2, N, true, false, NARROW>(p, grid, stream);
+  return launch_tc_variant<OPT, WK, MK, 64, S, N, true, false, NARROW>(p, grid, stream);
 }
 
 template <int OPT, int WK, int MK>
@@ -69,10 +72,14 @@ cudaError_t launch_mk(const WgradTcParams& p, const TcLaunch& l) {
   if (l.dx) {
     if constexpr (MK == M_Q8) return cudaErrorInvalidValue;
     else {
-      if (l.bn != 64 || l.deep) return cudaErrorInvalidValue;
+      if (l.bn != 64) return cudaErrorInvalidValue;
       if constexpr (WK == W_F32 && MK == M_F32 && opt_nstate(OPT) == 2)
-        if (l.narrow) return launch_dx<OPT, WK, MK, true>(p, l.grid, l.stream);
-      return l.narrow ? cudaErrorInvalidValue : launch_dx<OPT, WK, MK>(p, l.grid, l.stream);
+        if (l.narrow)
+          return l.deep ? launch_dx<OPT, WK, MK, true, true>(p, l.grid, l.stream)
+                        : launch_dx<OPT, WK, MK, true, false>(p, l.grid, l.stream);
+      if (l.narrow) return cudaErrorInvalidValue;
+      return l.deep ? launch_dx<OPT, WK, MK, false, true>(p, l.grid, l.stream)
+                    : launch_dx<OPT, WK, MK, false, false>(p, l.grid, l.stream);
     }
   }
   if constexpr (MK == M_Q8) {
