@@ -2,23 +2,30 @@
 // sm_103a (FORGE, Algorithm 1, re-designed for tcgen05 tensor cores).
 //
 // One persistent CTA per SM walks a grouped raster of 128 x BN gradient
-// tiles G_ij = sum_k dY_k,i^T X_k,j (Eq. 5). Warp roles (640 threads):
+// tiles G_ij = sum_k dY_k,i^T X_k,j (Eq. 5), BN = 64, 128 or 256. Warp
+// roles (640 threads):
 //
-//   warp 0      operand producer: TMA loads of the 64-token slabs of dY and
-//               X into a STAGES-deep shared-memory ring;
+//   warp 0      operand producer: TMA loads of the BK-token slabs of dY and
+//               X (BK = 64, or 128 with the fused input gradient) into a
+//               STAGES-deep shared-memory ring;
 //   warp 1      MMA issuer: one thread issues tcgen05.mma (M = 128, N = BN,
 //               K = 16) into a double-buffered fp32 TMEM accumulator; the
 //               warp also owns the TMEM allocation;
-//   warp 2      state producer: TMA loads of the W / m / v tiles, in
-//               32-column chunks, into an NBUF-deep slot ring;
+//   warp 2      state producer: TMA loads of the W / m / v tiles (and of an
+//               accumulated gradient G_acc, GA), in CW-column chunks
+//               (CW = 32, or 16: NARROW), into an NBUF-deep slot ring;
 //   warp 3      state storer: TMA stores of each finished chunk;
 //   warps 4-19  epilogue: warp w reads TMEM lane quadrant w % 4 (row p of
-//               the tile = TMEM lane) and 8-column quarter (w - 4) / 4 of each
-//               32-column chunk, applies the optimizer element-wise in fp32
-//               and writes the new W / m / v back into the slot (Algorithm 1
-//               phase 2-3). Four epilogue warps per scheduler hide the
-//               latency of the per-element arithmetic (divide, square root,
-//               Philox rounds).
+//               the tile = TMEM lane) and column quarter (w - 4) / 4 of each
+//               chunk, applies the optimizer element-wise in fp32 and writes
+//               the new W / m / v back into the slot (Algorithm 1 phase 2-3).
+//               Four epilogue warps per scheduler hide the latency of the
+//               per-element arithmetic (divide, square root, Philox rounds).
+//
+// The same template serves gradient accumulation over micro-batches
+// (Appendix L): with the OPT_ACCUM / OPT_ACCSET rules the "weight" is an fp32
+// accumulator G_acc that the tile is added to (or written to), and with GA
+// the step of any rule adds a streamed G_acc chunk to each tile first.
 //
 // With DX (the fused backward pass) the same kernel also forms the input
 // gradient dX = dY W_old from the W tile it is about to update (Appendix A,
@@ -68,10 +75,10 @@ struct TcCfg {
   static constexpr int BK = DX ? 128 : 64;  // tokens per operand stage
   static constexpr int BOX = BK * 128; // bytes of one 64-column operand box (BK rows of 128 bytes)
   // State chunk width (columns): 32, or 16 (NARROW) for the fused-input-
-  // gradient kernel with fp32 W and two fp32 moments on short token axes --
-  // its shared memory holds two 48 KB slots of 32 columns or four of 16, and
-  // with a short mainloop the deeper ring's extra loads in flight pay for
-  // the extra chunk turns.
+  // gradient kernel with fp32 W and two fp32 moments -- its shared memory
+  // holds two 48 KB slots of 32 columns or four of 16: on short token axes
+  // the deeper state ring pays for the extra chunk turns, and on long ones
+  // the narrow slots leave room for a third operand stage.
   static constexpr bool NARROW = NARROW_;
   static constexpr int CW = NARROW ? 16 : 32;
   static constexpr int QC = CW / 4;    // columns per epilogue thread per chunk (one quarter)
@@ -530,7 +537,6 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, N
     const int r = q * 32 + lane;     // tile row == TMEM lane
     const StepScalars sc = p.sc;
     uint32_t cseq = 0;
-    uint32_t run_seq = 0;            // dX partials written out
     int it = 0;
     bool ok = true;
 
