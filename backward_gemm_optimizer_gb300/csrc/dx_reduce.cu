@@ -27,6 +27,9 @@ constexpr int kBN = 64;  // columns per tile of the fused kernel
 constexpr int kTokens = 64;
 
 __global__ void __launch_bounds__(256) dx_reduce_kernel(const DxReduceParams p) {
+  // Launched as a programmatic dependent of the fused kernel: the blocks may
+  // start while it finishes; its slab writes are visible after this wait.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int q = blockIdx.x;
   const int t0 = blockIdx.y * kTokens;
   const int64_t T = p.num_tiles, G = p.grid;
@@ -38,22 +41,32 @@ __global__ void __launch_bounds__(256) dx_reduce_kernel(const DxReduceParams p) 
   float4 acc[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int64_t c = c0; c <= c1; ++c) {
-    const int64_t slot = c * p.runs + (q - (c * T / G) / p.tiles_m);
-    const float* slab = p.ws + slot * p.slab + col;
-    float4 v[4];
+  // Two slabs' loads in flight per thread, added in increasing CTA order.
+  for (int64_t c = c0; c <= c1; c += 2) {
+    float4 v[2][4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int t = t0 + (threadIdx.x >> 4) + 16 * k;
-      v[k] = t < p.bt ? __ldcg(reinterpret_cast<const float4*>(slab + static_cast<int64_t>(t) * kBN))
+    for (int u = 0; u < 2; ++u) {
+      const int64_t cc = c + u;
+      const float* slab =
+          cc <= c1 ? p.ws + (cc * p.runs + (q - (cc * T / G) / p.tiles_m)) * p.slab + col : nullptr;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int t = t0 + (threadIdx.x >> 4) + 16 * k;
+        v[u][k] = (slab != nullptr && t < p.bt)
+                      ? __ldcg(reinterpret_cast<const float4*>(slab + static_cast<int64_t>(t) * kBN))
                       : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
     }
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      acc[k].x = __fadd_rn(acc[k].x, v[k].x);
-      acc[k].y = __fadd_rn(acc[k].y, v[k].y);
-      acc[k].z = __fadd_rn(acc[k].z, v[k].z);
-      acc[k].w = __fadd_rn(acc[k].w, v[k].w);
+    for (int u = 0; u < 2; ++u) {
+      if (c + u > c1) break;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        acc[k].x = __fadd_rn(acc[k].x, v[u][k].x);
+        acc[k].y = __fadd_rn(acc[k].y, v[u][k].y);
+        acc[k].z = __fadd_rn(acc[k].z, v[u][k].z);
+        acc[k].w = __fadd_rn(acc[k].w, v[u][k].w);
+      }
     }
   }
   if (i >= p.d_in) return;
@@ -74,9 +87,16 @@ __global__ void __launch_bounds__(256) dx_reduce_kernel(const DxReduceParams p) 
 
 cudaError_t launch_dx_reduce(const DxReduceParams& p, int, cudaStream_t stream) {
   if (p.bt == 0 || p.d_in == 0) return cudaSuccess;
-  const dim3 grid(static_cast<unsigned>((p.d_in + kBN - 1) / kBN), static_cast<unsigned>((p.bt + kTokens - 1) / kTokens));
-  dx_reduce_kernel<<<grid, 256, 0, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((p.d_in + kBN - 1) / kBN), static_cast<unsigned>((p.bt + kTokens - 1) / kTokens));
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, dx_reduce_kernel, p);
 }
 
 }  // namespace forge
