@@ -127,7 +127,7 @@ typedef struct {
 /*
  * forge_wgrad_step_adamw -- fused G = dY^T X and AdamW step, in place.
  *
- * Computes, per element (p, q), with t = step (Algorithm 1, lines 11-14):
+ * Computes, per element (p, q), with t = step (Algorithm 1, phase 2):
  *   m' = b1 m + (1 - b1) g
  *   v' = b2 v + (1 - b2) g^2
  *   W' = (1 - lr wd) W - lr (m' / (1 - b1^t)) / (sqrt(v' / (1 - b2^t)) + eps)

@@ -28,7 +28,7 @@ stochastic-rounding decision and every 8-bit code.
 Readings of points the paper leaves open (each is also listed with the
 design notes of this library):
 
-* step t is 1-based (Algorithm 1, line 13 uses 1 - beta^t);
+* step t is 1-based (Algorithm 1's bias correction uses 1 - beta^t);
 * SGD-momentum, which Appendix N only names ("single moment"), is the
   common library rule with coupled L2 decay, no dampening, no Nesterov:
   g~ = g + lambda W; m' = mu m + g~; W' = W - eta m';
@@ -73,7 +73,7 @@ U32_MASK = np.uint64(0xFFFFFFFF)
 
 @dataclasses.dataclass
 class Hyper:
-    """(eta, beta1, beta2, eps, lambda) of Algorithm 1, line 1.
+    """(eta, beta1, beta2, eps, lambda) of Algorithm 1.
 
     For SGD-momentum ``beta1`` is the momentum mu; Lion uses beta1 for the
     interpolation and beta2 for the moment decay.
@@ -112,7 +112,7 @@ def abs_wgrad_f64(dY: np.ndarray, X: np.ndarray) -> np.ndarray:
 
 
 def adamw_f64(W, m, v, G, h: Hyper, t: int):
-    """AdamW, Algorithm 1 lines 11-14 (decoupled decay on the old W)."""
+    """AdamW, Algorithm 1 phase 2 (decoupled decay on the old W)."""
     assert t >= 1
     W = np.asarray(W, np.float64); m = np.asarray(m, np.float64)
     v = np.asarray(v, np.float64); G = np.asarray(G, np.float64)

@@ -110,7 +110,7 @@ def test_prop1_tile_partition_exact(opt, mode):
 
 
 # ---------------------------------------------------------------------------
-# lr = 0 leaves W unchanged (Algorithm 1 line 14 with eta = 0)
+# lr = 0 leaves W unchanged (Algorithm 1's weight update with eta = 0)
 # ---------------------------------------------------------------------------
 
 @pytest.mark.parametrize("opt", ["adamw", "sgdm", "lion"])
