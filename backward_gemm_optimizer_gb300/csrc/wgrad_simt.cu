@@ -83,9 +83,11 @@ __global__ void __launch_bounds__(128) wgrad_step_simt_kernel(const WgradSimtPar
     float w = ld_val<WK == W_F32 ? 0 : 1>(p.W, static_cast<int64_t>(row) * p.ld_w + q);
     float m = 0.0f, v = 0.0f;
     if constexpr (MK == M_Q8) {
-      m = dequant_m(static_cast<const int8_t*>(p.m)[static_cast<int64_t>(row) * p.ld_m + q], sm_old[i]);
+      m = dequant_m(small_int_to_f32(static_cast<const int8_t*>(p.m)[static_cast<int64_t>(row) * p.ld_m + q]),
+                    sm_old[i]);
       if constexpr (TWO)
-        v = dequant_v(static_cast<const uint8_t*>(p.v)[static_cast<int64_t>(row) * p.ld_v + q], sv_old[i]);
+        v = dequant_v(small_int_to_f32(static_cast<const uint8_t*>(p.v)[static_cast<int64_t>(row) * p.ld_v + q]),
+                      sv_old[i]);
     } else {
       if constexpr (NST >= 1) m = ld_val<MK == M_F32 ? 0 : 1>(p.m, static_cast<int64_t>(row) * p.ld_m + q);
       if constexpr (TWO) v = ld_val<MK == M_F32 ? 0 : 1>(p.v, static_cast<int64_t>(row) * p.ld_v + q);

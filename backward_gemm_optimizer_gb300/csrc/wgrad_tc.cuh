@@ -102,8 +102,10 @@ struct TcCfg {
   static constexpr int SLOT_BYTES = ((W_CH + M_CH + V_CH + G_CH + 1023) / 1024) * 1024;
   static constexpr int WB_BYTES = DX ? BM * BN * 2 : 0;   // bf16 W_old tile (B operand of dX)
   static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + WB_BYTES + NBUF * SLOT_BYTES;
-  static constexpr int TMEM_COLS = DX ? 512 : ((2 * BN <= 128) ? 128 : (2 * BN <= 256 ? 256 : 512));
+  static constexpr int TMEM_COLS =
+      (DX || Q8) ? 512 : ((2 * BN <= 128) ? 128 : (2 * BN <= 256 ? 256 : 512));
   static constexpr int DX_COL = 2 * BN;          // first TMEM column of the dX partial
+  static constexpr int KEEP_COL = 2 * BN;        // 8-bit moments: the new moments of the tile in the epilogue
   static constexpr int DX_MAX_BLOCKS = DX ? (512 - DX_COL) / BN : 0;  // 128-token blocks that fit
   static constexpr int EPI_WARPS = 16;
   static constexpr int EPI_THREADS = EPI_WARPS * 32;
@@ -167,20 +169,16 @@ __device__ __forceinline__ void st8_bf16(uint8_t* base, int r, int h, const uint
   *reinterpret_cast<uint4*>(base + swz<2>(r, h)) = t;
 }
 
-// 8 codes of row r, columns [8h, 8h + 8): half (h % 2) of 16-byte chunk h / 2.
-__device__ __forceinline__ void ld8_codes(const uint8_t* base, int r, int h, uint32_t (&c)[8]) {
-  const uint2 t = *reinterpret_cast<const uint2*>(base + swz<1>(r, h >> 1) + (h & 1) * 8);
-#pragma unroll
-  for (int i = 0; i < 8; ++i) c[i] = ((i < 4 ? t.x : t.y) >> (8 * (i & 3))) & 0xFFu;
+// The 8 codes of row r, columns [8h, 8h + 8) of a 32-column chunk (half
+// h % 2 of 16-byte chunk h / 2) as two words, byte i = column 8h + i.
+__device__ __forceinline__ uint2 ld8_code_words(const uint8_t* base, int r, int h) {
+  return *reinterpret_cast<const uint2*>(base + swz<1>(r, h >> 1) + (h & 1) * 8);
 }
 
+// Stores the low bytes of c[0..7] as those 8 codes.
 __device__ __forceinline__ void st8_codes(uint8_t* base, int r, int h, const uint32_t (&c)[8]) {
-  uint2 t = make_uint2(0u, 0u);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) t.x |= (c[i] & 0xFFu) << (8 * i);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) t.y |= (c[4 + i] & 0xFFu) << (8 * i);
-  *reinterpret_cast<uint2*>(base + swz<1>(r, h >> 1) + (h & 1) * 8) = t;
+  *reinterpret_cast<uint2*>(base + swz<1>(r, h >> 1) + (h & 1) * 8) =
+      make_uint2(pack_low_bytes(c[0], c[1], c[2], c[3]), pack_low_bytes(c[4], c[5], c[6], c[7]));
 }
 
 // Eight bf16 stores of `x` packed in four words: stochastic rounding with
@@ -199,8 +197,6 @@ __device__ __forceinline__ void to_bf16x8(const float (&x)[8], bool sr, uint64_t
                    pack_bf16x2_rn(x[6], x[7]));
   }
 }
-
-__device__ __forceinline__ int32_t sext8(uint32_t b) { return static_cast<int32_t>(static_cast<int8_t>(b & 0xFFu)); }
 
 __device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, int group_m, int& tm, int& tn) {
   const int per_group = group_m * tiles_n;
@@ -637,9 +633,13 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, N
       } else {
         // -------------------------------------------------- 8-bit block moments
         // The 128 columns of this tile row are one quantisation block, so the
-        // new block absmax needs every chunk: pass 1 forms the new moments
-        // and their absmax, pass 2 recomputes them, steps W and quantises.
+        // new block absmax needs every chunk. Pass 1 forms the new moments
+        // (Lion: and its update direction), keeps them in the free half of
+        // tensor memory and takes their absmax; the accumulator buffer is
+        // then handed back. Pass 2 reads them back, steps W and quantises.
         const int jb = tn;  // block column (BN == 128)
+        const uint32_t t_keep = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(C::KEEP_COL);
+        constexpr bool KEEP2 = OPT != OPT_SGDM;   // a second kept value: v' (AdamW), the direction (Lion)
         float sm_old = 0.0f, sv_old = 0.0f;
         if (row < p.d_out) {
           sm_old = p.m_scale[static_cast<int64_t>(jb) * p.d_out + row];
@@ -661,29 +661,43 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, N
             for (int j = 0; j < 8; ++j) gr[j] = 0u;
           }
           const uint8_t* slot = st_base + s * C::SLOT_BYTES;
-          uint32_t cm[8], cv[8];
-          float w[8];
-          ld8_codes(slot + C::W_CH, r, h, cm);
-          if constexpr (C::TWO) ld8_codes(slot + C::W_CH + C::M_CH, r, h, cv);
+          float c0[8], c1[8], w[8];
+          const uint2 tm8 = ld8_code_words(slot + C::W_CH, r, h);
+          codes_s8_to_f32(tm8.x, tm8.y, c0);
+          if constexpr (C::TWO) {
+            const uint2 tv8 = ld8_code_words(slot + C::W_CH + C::M_CH, r, h);
+            codes_u8_to_f32(tv8.x, tv8.y, c1);
+          }
           if constexpr (OPT == OPT_SGDM) ld8<WK == W_F32 ? 0 : 1>(slot, r, h, w);
+          uint32_t k0[8], k1[8];
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const float g = __uint_as_float(gr[j]);
-            const float m0 = dequant_m(sext8(cm[j]), sm_old);
+            const float m0 = dequant_m(c0[j], sm_old);
             float m1;
             if constexpr (OPT == OPT_ADAMW) {
               float v1;
-              adamw_moments(g, m0, dequant_v(cv[j], sv_old), sc, m1, v1);
+              adamw_moments(g, m0, dequant_v(c1[j], sv_old), sc, m1, v1);
               au = fmaxf(au, v1);     // max v'; sqrt is taken once per row below
+              k1[j] = __float_as_uint(v1);
             } else if constexpr (OPT == OPT_SGDM) {
-              m1 = __fadd_rn(__fmul_rn(sc.b1, m0), __fadd_rn(g, __fmul_rn(sc.wd, w[j])));
+              m1 = sgdm_moment(g, w[j], m0, sc);
             } else {
-              m1 = __fadd_rn(__fmul_rn(sc.b2, m0), __fmul_rn(sc.omb2, g));
+              k1[j] = __float_as_uint(lion_dir(g, m0, sc));
+              m1 = lion_moment(g, m0, sc);
             }
             am = fmaxf(am, fabsf(m1));
+            k0[j] = __float_as_uint(m1);
           }
+          tmem_st_32x32b_x8(t_keep + c * C::CW + h * 8, k0);
+          if constexpr (KEEP2) tmem_st_32x32b_x8(t_keep + BN + c * C::CW + h * 8, k1);
         }
+        tmem_st_wait();
         if (!ok) break;
+        // The accumulator is not read again for this tile.
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tm_empty[buf]);
         // Combine the four column quarters of each row (bounded, abort-aware).
         red_sh[it & 1][0][h][r] = am;
         red_sh[it & 1][1][h][r] = au;
@@ -706,14 +720,10 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, N
         }
         for (int c = 0; c < C::NCH; ++c, ++cseq) {
           const int s = static_cast<int>(cseq % NBUF);
-          uint32_t gr[8];
-          if (p.num_kb > 0) {
-            tmem_ld_32x32b_x8(t_lane + c * C::CW + h * 8, gr);
-            tmem_ld_wait();
-          } else {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) gr[j] = 0u;
-          }
+          uint32_t k0[8], k1[8];
+          tmem_ld_32x32b_x8(t_keep + c * C::CW + h * 8, k0);
+          if constexpr (KEEP2) tmem_ld_32x32b_x8(t_keep + BN + c * C::CW + h * 8, k1);
+          tmem_ld_wait();
           uint8_t* slot = st_base + s * C::SLOT_BYTES;
           uint8_t* sw = slot;
           uint8_t* smc = slot + C::W_CH;
@@ -721,24 +731,22 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, N
           uint32_t cm[8], cv[8];
           float w[8];
           ld8<WK == W_F32 ? 0 : 1>(sw, r, h, w);
-          ld8_codes(smc, r, h, cm);
-          if constexpr (C::TWO) ld8_codes(svc, r, h, cv);
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            const float g = __uint_as_float(gr[j]);
-            const float m0 = dequant_m(sext8(cm[j]), sm_old);
-            float w1, m1;
+            const float m1 = __uint_as_float(k0[j]);
+            float w1;
             if constexpr (OPT == OPT_ADAMW) {
-              float v1, sq1;
-              adamw_elem(g, w[j], m0, dequant_v(cv[j], sv_old), sc, w1, m1, v1, sq1);
-              cv[j] = quant_v(v1, sq1, sv_new, iv_new);
+              const float v1 = __uint_as_float(k1[j]);
+              float sq1;
+              adamw_apply(w[j], m1, v1, sc, w1, sq1);
+              cv[j] = quant_v_byte(v1, sq1, sv_new, iv_new);
             } else if constexpr (OPT == OPT_SGDM) {
-              sgdm_elem(g, w[j], m0, sc, w1, m1);
+              w1 = sgdm_apply(w[j], m1, sc);
             } else {
-              lion_elem(g, w[j], m0, sc, w1, m1);
+              w1 = lion_apply(w[j], __uint_as_float(k1[j]), sc);
             }
             w[j] = w1;
-            cm[j] = static_cast<uint32_t>(quant_m(m1, sm_new, im_new)) & 0xFFu;
+            cm[j] = quant_m_byte(m1, sm_new, im_new);
           }
           if constexpr (WK == W_F32) {
             st8_f32(sw, r, h, w);
@@ -755,9 +763,11 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, N
           mbar_arrive(&st_written[s]);
         }
       }
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tm_empty[buf]);
+      if constexpr (!C::Q8) {
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tm_empty[buf]);
+      }
     }
   }
   if constexpr (DX) {
