@@ -30,7 +30,7 @@ EXPORTED = ("forge_wgrad_step_adamw", "forge_wgrad_step_sgdm", "forge_wgrad_step
             "forge_wgrad_step_sgd", "forge_wgrad_step_rmsprop", "forge_wgrad_step_adagrad",
             "forge_wgrad_step_nadam", "forge_wgrad_step_radam",
             "forge_dgrad", "forge_backward_step", "forge_backward_step_no_alloc", "forge_wgrad_accumulate",
-            "forge_wgrad_step_accumulated", "forge_sync_status", "forge_last_error", "forge_version",
+            "forge_backward_accumulate", "forge_wgrad_step_accumulated", "forge_sync_status", "forge_last_error", "forge_version",
             "forge_workspace_bytes")
 
 
@@ -75,13 +75,16 @@ def _load() -> ctypes.CDLL:
     lib.forge_backward_step_no_alloc.argtypes = [ctypes.c_int, P(T), P(T), P(T), P(T), P(T), P(T), P(H), i64,
                                                  u64, vp]
     lib.forge_wgrad_accumulate.argtypes = [P(T), P(T), P(T), ctypes.c_int, vp]
+    lib.forge_backward_accumulate.argtypes = [P(T), P(T), P(T), P(T), P(T), ctypes.c_int, ctypes.c_uint32, vp,
+                                              ctypes.c_size_t, vp]
     lib.forge_wgrad_step_accumulated.argtypes = [ctypes.c_int, P(T), P(T), P(T), P(T), P(T), P(T), P(H), i64, u64,
                                                  vp]
     lib.forge_sync_status.argtypes = [vp]
     for f in ("forge_wgrad_step_adamw", "forge_wgrad_step_sgdm", "forge_wgrad_step_lion",
               "forge_wgrad_step_sgd", "forge_wgrad_step_rmsprop", "forge_wgrad_step_adagrad",
               "forge_wgrad_step_nadam", "forge_wgrad_step_radam", "forge_dgrad", "forge_backward_step",
-              "forge_backward_step_no_alloc", "forge_wgrad_accumulate", "forge_wgrad_step_accumulated",
+              "forge_backward_step_no_alloc", "forge_wgrad_accumulate", "forge_backward_accumulate",
+              "forge_wgrad_step_accumulated",
               "forge_sync_status"):
         getattr(lib, f).restype = ctypes.c_int
     lib.forge_last_error.restype = ctypes.c_char_p
@@ -284,6 +287,18 @@ def wgrad_accumulate(X, dY, G_acc, *, overwrite=False, stream=None):
     tX, tdY, tG = tensor_desc(X), tensor_desc(dY), tensor_desc(G_acc)
     _check(lib().forge_wgrad_accumulate(ctypes.byref(tX), ctypes.byref(tdY), ctypes.byref(tG), int(bool(overwrite)),
                                         _stream(stream)))
+
+
+def backward_accumulate(X, dY, W, G_acc, dX, *, overwrite=False, workspace=None, flags=0, stream=None):
+    """dX = dY W and G_acc (+)= dY^T X for a micro-batch that is not the window's last
+    (forge_backward_accumulate): one pass when `workspace` (workspace_bytes(D_out, D_in, BT)
+    bytes) is given and the layer allows it, else dgrad and wgrad_accumulate."""
+    tX, tdY, tW, tG, tdX = (tensor_desc(t) for t in (X, dY, W, G_acc, dX))
+    ws_ptr = ctypes.c_void_p(workspace.data_ptr() if workspace is not None and workspace.numel() else 0)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().forge_backward_accumulate(ctypes.byref(tX), ctypes.byref(tdY), ctypes.byref(tW), ctypes.byref(tG),
+                                           ctypes.byref(tdX), int(bool(overwrite)), int(flags), ws_ptr, ws_bytes,
+                                           _stream(stream)))
 
 
 def wgrad_step_accumulated(rule, X, dY, G_acc, W, s0, s1, *, lr, beta1=0.9, beta2=0.999, eps=1e-8,

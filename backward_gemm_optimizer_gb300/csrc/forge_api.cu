@@ -283,11 +283,14 @@ DxGeometry dx_geometry(int64_t d_out, int64_t d_in, int64_t bt, int sms) {
   return g;
 }
 
-// Extra arguments of the fused backward pass (dX and its workspace).
+// Extra arguments of the fused backward pass (dX and its workspace). W_dx:
+// the weights dX is formed from when they are not the step's first tensor
+// (the accumulation rules, whose first tensor is G_acc); null otherwise.
 struct DxArgs {
   forge_tensor* dX;
   void* ws;
   size_t ws_bytes;
+  const forge_tensor* W_dx;
 };
 
 // ------------------------------------------------------------------ the fused step
@@ -358,10 +361,19 @@ forge_status wgrad_step(int opt, const forge_tensor* X, const forge_tensor* dY, 
     return fail(FORGE_ERR_INVALID_ARG, "%s: dimension exceeds 2^31 - 1", oname);
   if (d_in == 0 || d_out == 0) return ok();
 
+  const forge_tensor* w_dx = (dx != nullptr && dx->W_dx != nullptr) ? dx->W_dx : W;
+  if (w_dx != W) {
+    if ((st = check_tensor(w_dx, "W", d_out, d_in, true)) != FORGE_OK) return st;
+    if (w_dx->dtype != FORGE_F32 && w_dx->dtype != FORGE_BF16)
+      return fail(FORGE_ERR_UNSUPPORTED, "%s: W must be f32 or bf16", oname);
+  }
+
   DeviceInfo* dev = nullptr;
   if ((st = device_info(&dev)) != FORGE_OK) return st;
   const StepScalars sc = fold(opt, h, step);
-  const int wk = W->dtype == FORGE_F32 ? W_F32 : W_BF16;
+  // With the fused input gradient of an accumulation rule, the kernel's
+  // weight kind is that of the weights read for dX (the slot holds G_acc).
+  const int wk = w_dx->dtype == FORGE_F32 ? W_F32 : W_BF16;
   const int mk = mkind(mdt);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
@@ -411,7 +423,9 @@ forge_status wgrad_step(int opt, const forge_tensor* X, const forge_tensor* dY, 
   const bool deep128 = dx == nullptr && G_acc == nullptr && bn == 128 && (bt >= 1024 || accum);
   // 256-column tiles always use the deep ring; the fused input gradient takes
   // a third operand stage past 512 tokens (its mainloop then sets the pace).
-  const int deep = (deep128 || bn == 256 || (dx != nullptr && bt > 512)) ? 1 : 0;
+  // The fused input gradient takes a third operand stage past 512 tokens, and
+  // with the accumulation rules at any length (their state is one fp32 tensor).
+  const int deep = (deep128 || bn == 256 || (dx != nullptr && (bt > 512 || accum))) ? 1 : 0;
   const int tiles_n = static_cast<int>((d_in + bn - 1) / bn);
   const uint32_t box_tokens = dx != nullptr ? 128u : 64u;  // tokens per operand stage
 
@@ -484,8 +498,8 @@ forge_status wgrad_step(int opt, const forge_tensor* X, const forge_tensor* dY, 
                   dx->ws_bytes);
     if (reinterpret_cast<uintptr_t>(dx->ws) % 16 != 0)
       return fail(FORGE_ERR_ALIGNMENT, "%s: workspace not 16-byte aligned", oname);
-    p.w_ptr = W->data;
-    p.ld_w = W->ld;
+    p.w_ptr = w_dx->data;
+    p.ld_w = w_dx->ld;
     p.dx_ws = static_cast<float*>(dx->ws);
     p.dx_runs = g.runs;
     p.dx_slab = g.slab;
@@ -573,7 +587,7 @@ forge_status backward_step(int opt, const forge_tensor* X, const forge_tensor* d
                 "and 64-column tiles",
                 oname, (long long)kDxMaxTokens);
   if (fused) {
-    const DxArgs a{dX, ws, ws_bytes};
+    const DxArgs a{dX, ws, ws_bytes, nullptr};
     return wgrad_step(opt, X, dY, W, s0, s1, h, step, seed, stream, &a);
   }
   // Split path: dX from the weights before the step, then the step.
@@ -584,6 +598,52 @@ forge_status backward_step(int opt, const forge_tensor* X, const forge_tensor* d
   forge_hyper h2 = *h;
   h2.flags &= ~(FORGE_FLAG_BACKWARD_FUSED | FORGE_FLAG_BACKWARD_SPLIT);
   return wgrad_step(opt, X, dY, W, s0, s1, &h2, step, seed, stream);
+}
+
+// One micro-batch of an accumulation window that is not its last: dX from
+// the (unchanged) weights and G_acc (+)= dY^T X, fused into one pass when
+// the layer allows it, else dgrad and the accumulation kernel.
+forge_status backward_accumulate(const forge_tensor* X, const forge_tensor* dY, const forge_tensor* W,
+                                 forge_tensor* G_acc, forge_tensor* dX, int overwrite, uint32_t flags, void* ws,
+                                 size_t ws_bytes, forge_stream_t stream) {
+  if (X == nullptr || dY == nullptr || W == nullptr || G_acc == nullptr || dX == nullptr)
+    return fail(FORGE_ERR_INVALID_ARG, "backward_accumulate: null argument");
+  if (flags & ~(FORGE_FLAG_BACKWARD_FUSED | FORGE_FLAG_BACKWARD_SPLIT))
+    return fail(FORGE_ERR_INVALID_ARG, "backward_accumulate: unknown flags 0x%x", flags);
+  const bool want_fused = (flags & FORGE_FLAG_BACKWARD_FUSED) != 0;
+  const bool want_split = (flags & FORGE_FLAG_BACKWARD_SPLIT) != 0;
+  if (want_fused && want_split)
+    return fail(FORGE_ERR_INVALID_ARG, "backward_accumulate: both BACKWARD_FUSED and BACKWARD_SPLIT set");
+  const int64_t bt = X->rows, d_in = X->cols, d_out = dY->cols;
+  if (dX->dtype != FORGE_BF16 && dX->dtype != FORGE_F32)
+    return fail(FORGE_ERR_UNSUPPORTED, "backward_accumulate: dX must be bf16 or f32");
+  forge_status st;
+  if ((st = check_tensor(dX, "dX", bt, d_in, true)) != FORGE_OK) return st;
+  if ((st = check_tensor(W, "W", d_out, d_in, true)) != FORGE_OK) return st;
+  if (W->dtype != FORGE_F32 && W->dtype != FORGE_BF16)
+    return fail(FORGE_ERR_UNSUPPORTED, "backward_accumulate: W must be f32 or bf16");
+  const int opt = overwrite ? OPT_ACCSET : OPT_ACCUM;
+  forge_hyper h;
+  std::memset(&h, 0, sizeof(h));
+  bool fused = false;
+  if (X->dtype == FORGE_BF16 && bt >= 1 && bt <= kDxMaxTokens && d_in > 0 && d_out > 0 && !want_split) {
+    DeviceInfo* dev = nullptr;
+    if ((st = device_info(&dev)) != FORGE_OK) return st;
+    const DxGeometry g = dx_geometry(d_out, d_in, bt, dev->sms);
+    fused = want_fused || (ws != nullptr && ws_bytes >= g.bytes);
+  }
+  if (want_fused && !fused)
+    return fail(FORGE_ERR_UNSUPPORTED,
+                "backward_accumulate: the fused input gradient needs bf16 X/dY and 1 <= BT <= %lld",
+                (long long)kDxMaxTokens);
+  if (fused) {
+    const DxArgs a{dX, ws, ws_bytes, W};
+    return wgrad_step(opt, X, dY, G_acc, nullptr, nullptr, &h, 1, 0, stream, &a);
+  }
+  if (X->dtype != FORGE_BF16)
+    return fail(FORGE_ERR_UNSUPPORTED, "backward_accumulate: gradient accumulation needs bf16 X, dY");
+  if ((st = dgrad_impl(dY, W, dX, stream)) != FORGE_OK) return st;
+  return wgrad_step(opt, X, dY, G_acc, nullptr, nullptr, &h, 1, 0, stream);
 }
 
 }  // namespace
@@ -653,6 +713,12 @@ forge_status forge_wgrad_accumulate(const forge_tensor* X, const forge_tensor* d
   forge_hyper h;
   std::memset(&h, 0, sizeof(h));
   return wgrad_step(overwrite ? OPT_ACCSET : OPT_ACCUM, X, dY, G_acc, nullptr, nullptr, &h, 1, 0, stream);
+}
+
+forge_status forge_backward_accumulate(const forge_tensor* X, const forge_tensor* dY, const forge_tensor* W,
+                                       forge_tensor* G_acc, forge_tensor* dX, int overwrite, uint32_t flags,
+                                       void* workspace, size_t workspace_bytes, forge_stream_t stream) {
+  return backward_accumulate(X, dY, W, G_acc, dX, overwrite, flags, workspace, workspace_bytes, stream);
 }
 
 forge_status forge_wgrad_step_accumulated(forge_rule rule, const forge_tensor* X, const forge_tensor* dY,

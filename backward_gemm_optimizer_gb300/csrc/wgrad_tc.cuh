@@ -38,6 +38,11 @@
 //     ahead of its MMAs, round it to bf16 and write it as the MN-major B
 //     operand of dX (Wb); the state ring reads the same W again for the
 //     update, mostly from L2;
+//   * warp 24 issues the dX MMAs (M = 128 tokens, N = 64, K = 16 rows of
+//     the tile) beside warp 1's weight-gradient MMAs: with 64-column tiles
+//     the two products need 64 MMAs per tile, more than one issuing thread
+//     keeps up with; a stage returns to the producer once both issuers'
+//     MMAs on it have completed;
 //   * each CTA walks a contiguous range of tiles ordered column by column,
 //     and a persistent fp32 dX partial (all tokens x the tile's 64 columns)
 //     accumulates in TMEM beside the gradient accumulators while the CTA
@@ -88,7 +93,12 @@ struct TcCfg {
   static constexpr int NST = opt_nstate(OPT);      // state tensors (0, 1, 2)
   static constexpr bool TWO = (NST == 2);           // a second state tensor
   static constexpr bool Q8 = (MK == M_Q8);
-  static constexpr int WE = (WK == W_F32) ? 4 : 2;
+  // The accumulation rules keep the fp32 accumulator G_acc where the other
+  // rules keep W; with the fused input gradient, WK then names the dtype of
+  // the weights the converter warps read for dX.
+  static constexpr bool ACC = (OPT == OPT_ACCUM || OPT == OPT_ACCSET);
+  static constexpr bool SLOT_F32 = (WK == W_F32) || ACC;  // fp32 values in the slot's first tensor
+  static constexpr int WE = SLOT_F32 ? 4 : 2;
   static constexpr int ME = (MK == M_F32) ? 4 : (MK == M_BF16 ? 2 : 1);
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
@@ -110,7 +120,10 @@ struct TcCfg {
   static constexpr int EPI_WARPS = 16;
   static constexpr int EPI_THREADS = EPI_WARPS * 32;
   static constexpr int CONV_THREADS = DX ? 128 : 0;  // warps 20-23
-  static constexpr int NUM_THREADS = 128 + EPI_THREADS + CONV_THREADS;
+  // DX: warp 24 issues the dX MMAs while warp 1 issues the weight-gradient
+  // ones (a single issuing thread is the pass's bottleneck otherwise).
+  static constexpr int DXMMA_WARP = 4 + EPI_WARPS + 4;
+  static constexpr int NUM_THREADS = 128 + EPI_THREADS + CONV_THREADS + (DX ? 32 : 0);
   static constexpr uint32_t IDESC = make_idesc_bf16(BM, BN, 1, 1);
   // dX: A = dY (M = 128 tokens, K-major), B = Wb (N = BN, MN-major).
   static constexpr uint32_t IDESC_DX = make_idesc_bf16(128, BN, 0, 1);
@@ -302,7 +315,7 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, N
   using C = TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, NARROW>;
   static_assert(!NARROW || (DX && WK == W_F32 && MK == M_F32 && C::TWO), "16-column chunks: fp32 fused kernel");
   static_assert(!GA || (!DX && !C::Q8), "accumulated-gradient step: split path, fp32 / bf16 state");
-  static_assert(!(OPT == OPT_ACCUM || OPT == OPT_ACCSET) || (WK == W_F32 && !GA), "fp32 gradient accumulator");
+  static_assert(!C::ACC || ((WK == W_F32 || DX) && !GA), "fp32 gradient accumulator");
   static_assert(BN == 64 || BN == 128 || BN == 256, "tile width");
   static_assert(BN != 256 || (!C::Q8 && !DX && !GA), "256-column tiles: plain step, fp32 / bf16 state");
   static_assert(!DX || (BN == 64 && !C::Q8), "fused input gradient: 64-column tiles, fp32 / bf16 state");
@@ -317,7 +330,7 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, N
   __shared__ __align__(8) uint64_t st_full[NBUF], st_empty[NBUF], st_written[NBUF];
   __shared__ __align__(8) uint64_t tm_full[2], tm_empty[2];
   __shared__ __align__(8) uint64_t red_bar[2];
-  __shared__ __align__(8) uint64_t never_bar, mma_drain_bar;
+  __shared__ __align__(8) uint64_t never_bar, mma_drain_bar, dx_drain_bar;
   __shared__ __align__(8) uint64_t wb_full, wb_empty, dx_full, dx_empty;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
@@ -334,7 +347,8 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, N
   volatile int* abort_flag = &abort_sh;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) { mbar_init(&op_full[s], 1); mbar_init(&op_empty[s], 1); }
+    // DX: a stage is released by both MMA-issuing threads.
+    for (int s = 0; s < STAGES; ++s) { mbar_init(&op_full[s], 1); mbar_init(&op_empty[s], DX ? 2 : 1); }
     for (int s = 0; s < NBUF; ++s) {
       mbar_init(&st_full[s], 1);
       mbar_init(&st_empty[s], 1);
@@ -347,6 +361,7 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, N
     }
     mbar_init(&never_bar, 1);
     mbar_init(&mma_drain_bar, 1);
+    mbar_init(&dx_drain_bar, 1);
     mbar_init(&wb_full, C::CONV_THREADS > 0 ? C::CONV_THREADS : 1);
     mbar_init(&wb_empty, 1);
     mbar_init(&dx_full, 1);
@@ -396,21 +411,17 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, N
       if (!ok) drain_ring(op_full, STAGES, kseq, p.status);
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ MMA issuer (weight gradient)
     if (lane == 0) {
       uint32_t kseq = 0;
       bool ok = true;
       int it = 0;
-      uint32_t runs_done = 0;  // dX partials handed to the epilogue
       for (int tile = tw.first; ok && tile < tw.end; tile += tw.step, ++it) {
         const int buf = it & 1;
         const uint32_t eph = ((it >> 1) & 1) ^ 1u;
         if (!bwait(&tm_empty[buf], eph, abort_flag, p.status, WAIT_TMEM_EMPTY, lim)) { ok = false; break; }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
-        // dX: the first tile of a column starts a fresh partial.
-        const bool run_first = DX && (tile == tw.first || tile % p.tiles_m == 0);
-        const bool run_last = DX && (tile + 1 == tw.end || (tile + 1) % p.tiles_m == 0);
         for (int kb = 0; kb < p.num_kb; ++kb, ++kseq) {
           const int s = static_cast<int>(kseq % STAGES);
           const uint32_t ph = (kseq / STAGES) & 1u;
@@ -429,45 +440,9 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, N
             const uint64_t step = static_cast<uint64_t>(kk * 2048 >> 4);
             umma_f16(d_tmem, ad0 + step, bd0 + step, C::IDESC, (kb > 0 || kk > 0) ? 1u : 0u);
           }
-          if constexpr (DX) {
-            if (kb == 0) {
-              // The previous column's partial must have been written out, and
-              // this tile's bf16 W_old must be in place.
-              if (run_first && runs_done > 0 &&
-                  !bwait(&dx_empty, (runs_done - 1) & 1u, abort_flag, p.status, WAIT_DX_EMPTY, lim)) {
-                ok = false;
-                break;
-              }
-              if (!bwait(&wb_full, it & 1, abort_flag, p.status, WAIT_WB_FULL, lim)) { ok = false; break; }
-              tc_fence_after_sync();
-            }
-            // dX[128 tokens of stage kb][BN] += dY[tokens][128 rows of the tile] * Wb.
-            // A: K-major (K = D_out rows of the tile, 64 per 128-byte box row),
-            // 8-token groups 1024 bytes apart; a K step of 16 advances 32 bytes.
-            // B: MN-major Wb, 8-row K groups of 1024 bytes, 16 rows = 2048 bytes.
-            const uint32_t dx_tmem = tmem_base + static_cast<uint32_t>(C::DX_COL + kb * BN);
-            const uint64_t xa0 = make_smem_desc(a0, 16, 1024, 2);
-            const uint64_t xb0 = make_smem_desc(smem_u32(wb_base), 8192, 1024, 2);
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t astep = static_cast<uint64_t>((hh * C::BOX + kk * 32) >> 4);
-                const uint64_t bstep = static_cast<uint64_t>(((hh * 4 + kk) * 2048) >> 4);
-                umma_f16(dx_tmem, xa0 + astep, xb0 + bstep, C::IDESC_DX,
-                         (run_first && hh == 0 && kk == 0) ? 0u : 1u);
-              }
-            }
-          }
           umma_commit(&op_empty[s]);
         }
         if (!ok) break;
-        if constexpr (DX) {
-          if (p.num_kb > 0) {
-            umma_commit(&wb_empty);
-            if (run_last) { umma_commit(&dx_full); ++runs_done; }
-          }
-        }
         umma_commit(&tm_full[buf]);
       }
       if (!ok) {
@@ -579,7 +554,7 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, N
             ld4_f32(sm, r, h, m);
             ld4_f32(sv, r, h, v);
           } else {
-            if constexpr (C::LOAD_W) ld8<WK == W_F32 ? 0 : 1>(sw, r, h, w);
+            if constexpr (C::LOAD_W) ld8<C::SLOT_F32 ? 0 : 1>(sw, r, h, w);
             if constexpr (C::NST >= 1) ld8<MK == M_F32 ? 0 : 1>(sm, r, h, m);
             if constexpr (C::TWO) ld8<MK == M_F32 ? 0 : 1>(sv, r, h, v);
           }
@@ -605,7 +580,7 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, N
           // Element index of this thread's first column; 8-aligned (D_in % 8 == 0).
           const uint64_t idx8 =
               (static_cast<uint64_t>(row) * static_cast<uint64_t>(p.d_in) + (tn * BN + c * C::CW + h * 8)) >> 3;
-          if constexpr (WK == W_F32) {
+          if constexpr (C::SLOT_F32) {
             st8_f32(sw, r, h, w);
           } else {
             uint4 b;
@@ -771,7 +746,7 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, N
     }
   }
   if constexpr (DX) {
-    if (warp >= 4 + C::EPI_WARPS) {
+    if (warp >= 4 + C::EPI_WARPS && warp < C::DXMMA_WARP) {
       // ---------------------------------------------------------- converters (warps 20-23)
       // Per tile: load this thread's 8 items of W_old (tile row r = item / 8,
       // 8-column group g = item % 8), round to bf16, and once the MMAs of
@@ -845,6 +820,70 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, N
           __syncwarp();
           if (lane == 0) mbar_arrive(&dx_empty);
           ++run_seq;
+        }
+      }
+    }
+  }
+
+  if constexpr (DX) {
+    if (warp == C::DXMMA_WARP && lane == 0) {
+      // ---------------------------------------------------------- MMA issuer (input gradient, warp 24)
+      // dX[128 tokens of stage kb][BN] += dY[tokens][128 rows of the tile] * Wb,
+      // into the persistent partial of the current tile column; the stage is
+      // released once both issuers' MMAs on it have completed.
+      uint32_t kseq = 0;
+      bool ok = true;
+      int it = 0;
+      uint32_t runs_done = 0;  // dX partials handed to the converter warps
+      for (int tile = tw.first; ok && tile < tw.end; tile += tw.step, ++it) {
+        // The first tile of a column starts a fresh partial.
+        const bool run_first = tile == tw.first || tile % p.tiles_m == 0;
+        const bool run_last = tile + 1 == tw.end || (tile + 1) % p.tiles_m == 0;
+        for (int kb = 0; kb < p.num_kb; ++kb, ++kseq) {
+          const int s = static_cast<int>(kseq % STAGES);
+          const uint32_t ph = (kseq / STAGES) & 1u;
+          if (!bwait(&op_full[s], ph, abort_flag, p.status, WAIT_OP_FULL, lim)) { ok = false; break; }
+          if (kb == 0) {
+            // The previous column's partial must have been written out, and
+            // this tile's bf16 W_old must be in place.
+            if (run_first && runs_done > 0 &&
+                !bwait(&dx_empty, (runs_done - 1) & 1u, abort_flag, p.status, WAIT_DX_EMPTY, lim)) {
+              ok = false;
+              break;
+            }
+            if (!bwait(&wb_full, it & 1, abort_flag, p.status, WAIT_WB_FULL, lim)) { ok = false; break; }
+          }
+          tc_fence_after_sync();
+          const uint32_t a0 = smem_u32(op_base + s * C::STAGE_BYTES);
+          // A: dY K-major (K = D_out rows of the tile, 64 per 128-byte box row),
+          // 8-token groups 1024 bytes apart; a K step of 16 advances 32 bytes.
+          // B: MN-major Wb, 8-row K groups of 1024 bytes, 16 rows = 2048 bytes.
+          const uint32_t dx_tmem = tmem_base + static_cast<uint32_t>(C::DX_COL + kb * BN);
+          const uint64_t xa0 = make_smem_desc(a0, 16, 1024, 2);
+          const uint64_t xb0 = make_smem_desc(smem_u32(wb_base), 8192, 1024, 2);
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t astep = static_cast<uint64_t>((hh * C::BOX + kk * 32) >> 4);
+              const uint64_t bstep = static_cast<uint64_t>(((hh * 4 + kk) * 2048) >> 4);
+              umma_f16(dx_tmem, xa0 + astep, xb0 + bstep, C::IDESC_DX, (run_first && hh == 0 && kk == 0) ? 0u : 1u);
+            }
+          }
+          umma_commit(&op_empty[s]);
+        }
+        if (!ok) break;
+        if (p.num_kb > 0) {
+          umma_commit(&wb_empty);
+          if (run_last) { umma_commit(&dx_full); ++runs_done; }
+        }
+      }
+      if (!ok) {
+        // Let every dX MMA already issued finish before TMEM is released.
+        umma_commit(&dx_drain_bar);
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(&dx_drain_bar, 0)) {
+          if (globaltimer_ns() - t0 > 200000000ull) { atomicCAS(p.status, 0u, WAIT_MMA_DRAIN); break; }
         }
       }
     }

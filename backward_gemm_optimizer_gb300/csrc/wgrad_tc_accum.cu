@@ -2,9 +2,10 @@
 // mode): the weight-gradient GEMM of each micro-batch adds its tiles into an
 // fp32 accumulator G_acc in HBM (or, on the first micro-batch, writes them
 // there), through the same tile kernel as the fused step with the
-// accumulator in place of the weights. The step itself fires once, at the
-// last micro-batch, through the accumulated-gradient variant of the rule
-// kernels.
+// accumulator in place of the weights -- optionally with the micro-batch's
+// input gradient dX = dY W formed in the same pass, as in the fused
+// backward step. The step itself fires once, at the last micro-batch,
+// through the accumulated-gradient variant of the rule kernels.
 #include "wgrad_tc_dispatch.cuh"
 
 namespace forge {
@@ -13,7 +14,16 @@ namespace {
 
 template <int OPT>
 cudaError_t launch_accum(const WgradTcParams& p, const TcLaunch& l) {
-  if (l.dx || l.ga || l.wk != W_F32) return cudaErrorInvalidValue;
+  if (l.ga || l.narrow) return cudaErrorInvalidValue;
+  if (l.dx) {
+    // With the input gradient of the same micro-batch (wk: the dtype of the
+    // weights read for dX); three 128-token operand stages, since the
+    // accumulator alone leaves the state ring little to do.
+    if (l.bn != 64 || !l.deep) return cudaErrorInvalidValue;
+    return l.wk == W_F32 ? launch_dx<OPT, W_F32, M_F32, false, true>(p, l.grid, l.stream)
+                         : launch_dx<OPT, W_BF16, M_F32, false, true>(p, l.grid, l.stream);
+  }
+  if (l.wk != W_F32) return cudaErrorInvalidValue;
   if (l.bn == 64) {
     if (l.deep) return cudaErrorInvalidValue;
     return launch_one<OPT, W_F32, M_F32, 64, 0>(p, l.grid, l.stream);

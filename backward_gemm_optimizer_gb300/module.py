@@ -19,7 +19,8 @@ learning rate) before each forward/backward. With
 ``accumulation_steps = K > 1`` (exact gradient accumulation, FORGE
 Appendix L) ``pre_step`` is called before every micro-batch: the first
 K - 1 backward passes of a window add their weight gradients into a
-per-layer fp32 accumulator (``forge_wgrad_accumulate``) and the K-th fires
+per-layer fp32 accumulator, each in one pass with its input gradient
+(``forge_backward_accumulate``), and the K-th fires
 the fused step once on the whole window's gradient
 (``forge_wgrad_step_accumulated``); the step counter advances once per
 window.
@@ -67,6 +68,7 @@ class StepConfig:
 # Workspaces of the fused backward path, one per (device, stream): calls on
 # one stream run in order, so they can share one; grown on demand.
 _WORKSPACES: Dict[tuple, torch.Tensor] = {}
+_PATH_FLAGS = F.FLAG_BACKWARD_FUSED | F.FLAG_BACKWARD_SPLIT
 
 
 def _workspace(device: torch.device, nbytes: int) -> Optional[torch.Tensor]:
@@ -98,8 +100,7 @@ class _ForgeLinearFn(torch.autograd.Function):
         if layer.config.accumulation_steps > 1:
             if ctx.needs_input_grad[0]:
                 dx = torch.empty(x2d.shape, dtype=x2d.dtype, device=x2d.device)
-                F.dgrad(dy2d, layer.weight, dx)            # W is unchanged until the window's last micro-batch
-            layer._accumulate(x2d, dy2d)
+            layer._accumulate(x2d, dy2d, dx)               # W is unchanged until the window's last micro-batch
         elif ctx.needs_input_grad[0]:
             dx = torch.empty(x2d.shape, dtype=x2d.dtype, device=x2d.device)
             layer._backward(x2d, dy2d, dx)                 # dX from W before the step (Remark 1)
@@ -156,14 +157,21 @@ class ForgeLinear(torch.nn.Module):
         y = _ForgeLinearFn.apply(x2d, self.weight, self)
         return y.reshape(*shape[:-1], self.out_features)
 
-    def _accumulate(self, x2d: torch.Tensor, dy2d: torch.Tensor):
+    def _accumulate(self, x2d: torch.Tensor, dy2d: torch.Tensor, dx: Optional[torch.Tensor]):
         c = self.config
         if getattr(self, "grad_acc", None) is None or self.grad_acc.shape != self.weight.shape:
             # The one gradient-shaped buffer of the accumulation mode, live for the run.
             self.grad_acc = torch.empty(self.weight.shape, dtype=torch.float32, device=self.weight.device)
         if c.micro < c.accumulation_steps - 1:
-            F.wgrad_accumulate(x2d, dy2d, self.grad_acc, overwrite=(c.micro == 0))
+            if dx is None:
+                F.wgrad_accumulate(x2d, dy2d, self.grad_acc, overwrite=(c.micro == 0))
+            else:   # dX and the accumulation in one pass where the layer allows it
+                ws = _workspace(x2d.device, F.workspace_bytes(self.out_features, self.in_features, x2d.shape[0]))
+                F.backward_accumulate(x2d, dy2d, self.weight, self.grad_acc, dx, overwrite=(c.micro == 0),
+                                      workspace=ws, flags=c.backward_flags & _PATH_FLAGS)
         else:
+            if dx is not None:
+                F.dgrad(dy2d, self.weight, dx)             # from W before the step (Remark 1)
             F.wgrad_step_accumulated(c.rule, x2d, dy2d, self.grad_acc, self.weight, self.state0, self.state1,
                                      lr=c.lr, beta1=c.beta1, beta2=c.beta2, eps=c.eps,
                                      weight_decay=c.weight_decay, momentum_decay=c.momentum_decay, step=c.step,

@@ -464,8 +464,11 @@ def run_gpu(args, rank, world, local_rank):
 
 def run_accum(args, rank, world, local_rank):
     """One step = one accumulation window on the up-projection (fp32 W, m, v):
-    per micro-batch forge_dgrad, then forge_wgrad_accumulate (the first one
-    overwrites G_acc), and forge_wgrad_step_accumulated at the last."""
+    every micro-batch but the last runs forge_backward_accumulate (dX and the
+    accumulation into G_acc in one pass; the first overwrites G_acc), the last
+    forge_dgrad and forge_wgrad_step_accumulated. The same window with
+    forge_dgrad + forge_wgrad_accumulate per micro-batch is timed after it
+    (split_* keys)."""
     import torch
     import backward_gemm_optimizer_gb300 as F
     from backward_gemm_optimizer_gb300 import synthetic as S
@@ -483,67 +486,93 @@ def run_accum(args, rank, world, local_rank):
             S.device_normal_(torch.empty((bt, d_out), dtype=torch.bfloat16, device=dev), 1.0, seed, 11 + 2 * k))
            for k in range(nmb)]
     dX = torch.empty((bt, d_in), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(max(16, F.workspace_bytes(d_out, d_in, bt)), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
 
-    def window(t, ev=None):
+    def window(t, ev=None, split=False):
         for k, (X, dY) in enumerate(mbs):
+            last = k == nmb - 1
             if ev is not None:
                 ev[k][0].record(stream)
-            F.dgrad(dY, W, dX, stream=stream)
+            if last or split:
+                F.dgrad(dY, W, dX, stream=stream)
             if ev is not None:
                 ev[k][1].record(stream)
-            if k < nmb - 1:
+            if last:
+                F.wgrad_step_accumulated("adamw", X, dY, G, W, m, v, step=t, stream=stream, **HYPER)
+            elif split:
                 F.wgrad_accumulate(X, dY, G, overwrite=(k == 0), stream=stream)
             else:
-                F.wgrad_step_accumulated("adamw", X, dY, G, W, m, v, step=t, stream=stream, **HYPER)
+                F.backward_accumulate(X, dY, W, G, dX, overwrite=(k == 0), workspace=ws,
+                                      flags=F.FLAG_BACKWARD_FUSED, stream=stream)
             if ev is not None:
                 ev[k][2].record(stream)
+
+    def timed(K, split, t):
+        evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(nmb)] for _ in range(K)]
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        for i in range(K):
+            flush.fill_(float(i))
+            window(t, evs[i], split); t += 1
+        torch.cuda.synchronize(dev)
+        return evs, t
 
     t = 1
     for _ in range(args.warmup):
         window(t); t += 1
+        window(t, split=True); t += 1
     F.sync_status(stream)
     K = args.steps
-    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(nmb)] for _ in range(K)]
     sampler = ClockSampler(local_rank)
-    barrier(world)
-    torch.cuda.synchronize(dev)
     sampler.start()
     time.sleep(0.3)
-    for i in range(K):
-        flush.fill_(float(i))
-        window(t, evs[i]); t += 1
-    torch.cuda.synchronize(dev)
+    evs, t = timed(K, False, t)
     clocks = sampler.stop()
     F.sync_status(stream)
-    step_ms = [evs[i][0][0].elapsed_time(evs[i][-1][2]) for i in range(K)]
-    total_ms = max_over_ranks(sum(step_ms), world, dev)
+    total_ms = max_over_ranks(sum(evs[i][0][0].elapsed_time(evs[i][-1][2]) for i in range(K)), world, dev)
+    KS = max(1, min(K, args.split_steps))
+    sev, t = timed(KS, True, t)
+    F.sync_status(stream)
+    split_ms = max_over_ranks(sum(sev[i][0][0].elapsed_time(sev[i][-1][2]) for i in range(KS)), world, dev)
     if rank != 0:
         return
     hbm, _, _ = load_peaks()
-    acc_us = [statistics.mean(evs[i][k][1].elapsed_time(evs[i][k][2]) for i in range(K)) * 1000.0 for k in range(nmb)]
-    dgrad_us = statistics.mean(evs[i][k][0].elapsed_time(evs[i][k][1]) for i in range(K) for k in range(nmb)) * 1000.0
+
+    def part(e, n, k, a, b):
+        return statistics.mean(e[i][k][a].elapsed_time(e[i][k][b]) for i in range(n)) * 1000.0
+
     params = d_out * d_in
-    first_b = params * 4 + 2 * bt * (d_in + d_out)          # G_acc written
-    acc_b = params * 8 + 2 * bt * (d_in + d_out)            # G_acc read + written
-    last_b = params * 28 + 2 * bt * (d_in + d_out)          # W, m, v read + written, G_acc read
+    ops_b = 2 * bt * (d_in + d_out)
+    first_b = params * 4 + params * 4 + ops_b + 2 * bt * d_in   # G_acc written, W read, dX written
+    acc_b = params * 8 + params * 4 + ops_b + 2 * bt * d_in     # G_acc read + written, W read, dX written
+    last_b = params * 28 + ops_b                                # W, m, v read + written, G_acc read
+    mid = list(range(1, nmb - 1))
+    fa_first = part(evs, K, 0, 1, 2)
+    fa_mid = statistics.mean(part(evs, K, k, 1, 2) for k in mid) if mid else None
+    s_first = part(sev, KS, 0, 1, 2)
+    s_mid = statistics.mean(part(sev, KS, k, 1, 2) for k in mid) if mid else None
     line = {
         "metric": METRIC, "value": round(total_ms * 1000.0 / K, 1), "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(total_ms / K, 3), "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": args.workload, "d_out": d_out, "d_in": d_in, "micro_batches": nmb, "bt": bt,
                    "effective_batch": nmb * bt, "optimizer": "adamw", "state": "fp32 W, m, v; fp32 G_acc",
-                   "step": f"{nmb} x forge_dgrad, {nmb - 1} x forge_wgrad_accumulate, 1 x forge_wgrad_step_accumulated",
+                   "step": f"{nmb - 1} x forge_backward_accumulate (fused), 1 x forge_dgrad + "
+                           "forge_wgrad_step_accumulated",
                    "l2": "flushed between windows"},
-        "accumulate_first_us": round(acc_us[0], 2),
-        "accumulate_first_frac_of_hbm": round(first_b / (acc_us[0] * 1e-6) / 1e9 / hbm, 4),
-        "accumulate_us": round(statistics.mean(acc_us[1:-1]) if nmb > 2 else acc_us[0], 2),
-        "accumulate_frac_of_hbm": round(acc_b / (statistics.mean(acc_us[1:-1]) * 1e-6) / 1e9 / hbm, 4)
-        if nmb > 2 else None,
-        "accumulated_step_us": round(acc_us[-1], 2),
-        "accumulated_step_frac_of_hbm": round(last_b / (acc_us[-1] * 1e-6) / 1e9 / hbm, 4),
-        "dgrad_us": round(dgrad_us, 2),
+        "backward_accumulate_first_us": round(fa_first, 2),
+        "backward_accumulate_first_frac_of_hbm": round(first_b / (fa_first * 1e-6) / 1e9 / hbm, 4),
+        "backward_accumulate_us": round(fa_mid, 2) if fa_mid is not None else None,
+        "backward_accumulate_frac_of_hbm": round(acc_b / (fa_mid * 1e-6) / 1e9 / hbm, 4) if mid else None,
+        "accumulated_step_us": round(part(evs, K, nmb - 1, 1, 2), 2),
+        "accumulated_step_frac_of_hbm": round(last_b / (part(evs, K, nmb - 1, 1, 2) * 1e-6) / 1e9 / hbm, 4),
+        "dgrad_us": round(part(evs, K, nmb - 1, 0, 1), 2),
+        "split_us_per_window": round(split_ms * 1000.0 / KS, 1),
+        "split_accumulate_first_us": round(s_first, 2),
+        "split_accumulate_us": round(s_mid, 2) if s_mid is not None else None,
+        "split_dgrad_us": round(statistics.mean(part(sev, KS, k, 0, 1) for k in range(nmb)), 2),
         "gpu_launches": 2 * nmb * K, "clocks": clocks,
     }
     print(json.dumps(line), flush=True)

@@ -285,10 +285,36 @@ forge_status forge_backward_step(forge_rule rule, const forge_tensor* X, const f
  * G_acc: FORGE_F32, D_out x D_in, caller-owned; it is the one
  * gradient-shaped buffer of this mode and lives for the accumulation
  * window. X, dY: FORGE_BF16. The micro-batch's input gradient is a
- * separate forge_dgrad call.
+ * separate forge_dgrad call, or use forge_backward_accumulate for both.
  */
 forge_status forge_wgrad_accumulate(const forge_tensor* X, const forge_tensor* dY, forge_tensor* G_acc, int overwrite,
                                     forge_stream_t stream);
+
+/*
+ * forge_backward_accumulate -- the whole backward pass of a layer for one
+ * micro-batch of an accumulation window other than its last (Appendix L):
+ * dX = dY W (the weights are not updated inside the window, so dX always
+ * reads the current W) and the accumulation of forge_wgrad_accumulate,
+ * G_acc = [G_acc +] dY^T X (`overwrite` nonzero: the window's first
+ * micro-batch). Where the layer allows it (bf16 X / dY, 1 <= BT <= 768)
+ * both run in one pass: the 128 x 64 tile kernel of the fused backward
+ * step, with G_acc in place of the state and the W tile read once, rounded
+ * to bf16, as the B operand of the dX product; dX is summed from fp32
+ * partials in a fixed order, as in forge_backward_step. Otherwise
+ * forge_dgrad and forge_wgrad_accumulate run one after the other.
+ *
+ * W: FORGE_F32 or FORGE_BF16, D_out x D_in, read only. G_acc: FORGE_F32.
+ * dX: BT x D_in, FORGE_BF16 or FORGE_F32. workspace / workspace_bytes: as
+ * for forge_backward_step (forge_workspace_bytes(D_out, D_in, BT) bytes
+ * enable the fused pass). flags: 0 (the library chooses: fused when it
+ * applies and the workspace suffices), FORGE_FLAG_BACKWARD_FUSED or
+ * FORGE_FLAG_BACKWARD_SPLIT; any other bit is FORGE_ERR_INVALID_ARG. G_acc
+ * is identical on both paths up to the fp32 summation order inside a tile
+ * (bit-identical when the tile sums are exact); so is dX.
+ */
+forge_status forge_backward_accumulate(const forge_tensor* X, const forge_tensor* dY, const forge_tensor* W,
+                                       forge_tensor* G_acc, forge_tensor* dX, int overwrite, uint32_t flags,
+                                       void* workspace, size_t workspace_bytes, forge_stream_t stream);
 
 /*
  * forge_wgrad_step_accumulated -- the last micro-batch of the window: each

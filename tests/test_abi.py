@@ -192,3 +192,27 @@ def test_accumulation_host_checks():
     r = lib.forge_wgrad_step_accumulated(0, ctypes.byref(X), ctypes.byref(dY), ctypes.byref(Gbad), ctypes.byref(W),
                                          ctypes.byref(m), ctypes.byref(v), ctypes.byref(h), 1, 0, None)
     assert r == INVALID and "G_acc" in lib.forge_last_error().decode()
+
+
+def test_backward_accumulate_host_checks():
+    lib = F.lib()
+    X, dY, W, m, v = _shapes()
+    G = _t(dtype=0, rows=32, cols=64)
+    dX = _t(dtype=1, rows=16, cols=64)
+    b = ctypes.byref
+    f = lib.forge_backward_accumulate
+    assert f(b(X), b(dY), None, b(G), b(dX), 0, 0, None, 0, None) == INVALID             # null W
+    assert f(b(X), b(dY), b(W), None, b(dX), 0, 0, None, 0, None) == INVALID             # null G_acc
+    assert f(b(X), b(dY), b(W), b(G), b(dX), 0, 0x1, None, 0, None) == INVALID           # not a path flag
+    both = F.FLAG_BACKWARD_FUSED | F.FLAG_BACKWARD_SPLIT
+    assert f(b(X), b(dY), b(W), b(G), b(dX), 0, both, None, 0, None) == INVALID
+    assert "both" in lib.forge_last_error().decode()
+    bad_dx = _t(dtype=2, rows=16, cols=64)
+    assert f(b(X), b(dY), b(W), b(G), b(bad_dx), 0, 0, None, 0, None) == UNSUPPORTED    # dX must be bf16 / f32
+    short_dx = _t(dtype=1, rows=15, cols=64)
+    assert f(b(X), b(dY), b(W), b(G), b(short_dx), 0, 0, None, 0, None) == INVALID      # dX is BT x D_in
+    w8 = _t(dtype=2, rows=32, cols=64, scale=0x2000)
+    assert f(b(X), b(dY), b(w8), b(G), b(dX), 0, 0, None, 0, None) == UNSUPPORTED       # W is f32 or bf16
+    Xf, dYf = _t(dtype=0, rows=16, cols=64), _t(dtype=0, rows=16, cols=32)
+    assert f(b(Xf), b(dYf), b(W), b(G), b(dX), 0, 0, None, 0, None) == UNSUPPORTED      # bf16 inputs only
+    assert f(b(Xf), b(dYf), b(W), b(G), b(dX), 0, F.FLAG_BACKWARD_FUSED, None, 0, None) == UNSUPPORTED

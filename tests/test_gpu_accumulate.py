@@ -10,6 +10,11 @@ oracle's float32 op-sequence mode bit for bit -- and equal, bit for bit, one
 fused step on the concatenated batch. Random cases hold the final state to
 the element-wise tolerance of oracle/tolerance.py with |dY|^T |X| summed over
 the micro-batches.
+
+forge_backward_accumulate also forms each micro-batch's input gradient
+dX = dY W: with integer W as well, dX is exact and must equal the float64
+product bit for bit (rounded once for a bf16 dX), on the fused pass and on
+the split one; random cases hold it to |dX - dY W16| <= 1e-5 |dY| |W16|.
 """
 
 import numpy as np
@@ -179,4 +184,147 @@ def test_accumulation_rejects_what_it_does_not_support():
                                               ctypes.byref(tW), ctypes.byref(tm), ctypes.byref(tv), ctypes.byref(h),
                                               1, 0, _lib._stream(None))
     assert st == 2                                     # no 8-bit state variant
+    F.sync_status()
+
+
+# ---------------------------------------------------------------------------
+# forge_backward_accumulate: the micro-batch's dX and the accumulation in one
+# pass over the tiles (or dgrad + accumulate on the split path)
+# ---------------------------------------------------------------------------
+
+def _weights(d_out, d_in, w, seed, exact):
+    if exact:   # small integers: exact in bf16, so dX = dY W is exact in fp32
+        return S.small_integers((d_out, d_in), -3, 3, seed, S.STREAM_W, w)
+    return S.normal((d_out, d_in), 0.02, seed, S.STREAM_W, w)
+
+
+def run_backward_window(mbs, W, *, path, dx_dtype="bf16"):
+    """forge_backward_accumulate over every micro-batch; (G_acc, [dX_i]) on the CPU."""
+    d_out, d_in = W.shape
+    Wd = W.to(DEV)
+    G = torch.full((d_out, d_in), float("nan"), dtype=torch.float32, device=DEV)
+    flags = {"fused": F.FLAG_BACKWARD_FUSED, "split": F.FLAG_BACKWARD_SPLIT, "auto": 0}[path]
+    dxs = []
+    for i, (X, dY) in enumerate(mbs):
+        bt = X.shape[0]
+        ws = torch.empty(max(16, F.workspace_bytes(d_out, d_in, bt)), dtype=torch.uint8, device=DEV)
+        dX = torch.full((bt, d_in), float("nan"), device=DEV,
+                        dtype=torch.bfloat16 if dx_dtype == "bf16" else torch.float32)
+        F.backward_accumulate(X.to(DEV), dY.to(DEV), Wd, G, dX, overwrite=(i == 0), workspace=ws, flags=flags)
+        dxs.append(dX)
+    F.sync_status()
+    assert torch.equal(Wd.cpu(), W), "the weights are read only"
+    return G.cpu().numpy(), [d.float().cpu().numpy() for d in dxs]
+
+
+def _dx_reference(dY, W):
+    w16 = O.bf16_bits_to_f32(O.f32_to_bf16_rne(W.float().numpy())).astype(np.float64)
+    dYn = dY.float().numpy().astype(np.float64)
+    return O.dgrad_f64(dYn, w16), np.abs(dYn) @ np.abs(w16)
+
+
+@pytest.mark.parametrize("path", ["fused", "split"])
+@pytest.mark.parametrize("w", ["f32", "bf16"])
+@pytest.mark.parametrize("dx_dtype", ["bf16", "f32"])
+def test_backward_accumulate_exact(path, w, dx_dtype):
+    d_out, d_in = 384, 264
+    mbs = micro_batches(d_out, d_in, TOKENS, 11, exact=True)
+    W = _weights(d_out, d_in, w, 11, exact=True)
+    G, dxs = run_backward_window(mbs, W, path=path, dx_dtype=dx_dtype)
+    assert np.array_equal(G, O.accumulated_gradient_f64(_np(mbs)).astype(np.float32))
+    for i, ((_, dY), got) in enumerate(zip(mbs, dxs)):
+        ref, _ = _dx_reference(dY, W)
+        want = ref.astype(np.float32) if dx_dtype == "f32" else O.bf16_bits_to_f32(O.f64_to_bf16_rne(ref))
+        bad = np.argwhere(got != want)
+        assert bad.size == 0, f"micro-batch {i}: {len(bad)} dX elements differ, first {bad[:3].tolist()}"
+
+
+@pytest.mark.parametrize("shape", [(136, 200), (2048, 1280)], ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("w", ["f32", "bf16"])
+def test_backward_accumulate_random_within_tolerance(shape, w):
+    d_out, d_in = shape
+    mbs = micro_batches(d_out, d_in, TOKENS, 12, exact=False)
+    W = _weights(d_out, d_in, w, 12, exact=False)
+    G, dxs = run_backward_window(mbs, W, path="fused", dx_dtype="f32")
+    ref = O.accumulated_gradient_f64(_np(mbs))
+    A = sum(np.abs(d).T @ np.abs(x) for x, d in _np(mbs))
+    assert np.all(np.abs(G - ref) <= 1e-5 * A)
+    for i, ((_, dY), got) in enumerate(zip(mbs, dxs)):
+        dref, dA = _dx_reference(dY, W)
+        viol = float(np.max(np.abs(got - dref) / np.maximum(1e-5 * dA, 1e-300)))
+        assert viol <= 1.0, f"micro-batch {i}: dX at {viol:.3f} of the tolerance"
+
+
+def test_backward_accumulate_paths_agree():
+    # Random inputs: both paths add each micro-batch's fp32 tile sums to G_acc;
+    # dX sums the same products in another order.
+    d_out, d_in = 1024, 768
+    mbs = micro_batches(d_out, d_in, TOKENS, 13, exact=False)
+    W = _weights(d_out, d_in, "f32", 13, exact=False)
+    Gf, dxf = run_backward_window(mbs, W, path="fused", dx_dtype="f32")
+    Gs, dxs = run_backward_window(mbs, W, path="split", dx_dtype="f32")
+    A = sum(np.abs(d).T @ np.abs(x) for x, d in _np(mbs))
+    assert np.all(np.abs(Gf - Gs) <= 2e-5 * A)
+    for (_, dY), a, b in zip(mbs, dxf, dxs):
+        _, dA = _dx_reference(dY, W)
+        assert np.all(np.abs(a - b) <= 2e-5 * dA)
+    # The library's own choice with a workspace: the fused pass, run to run identical.
+    Ga, dxa = run_backward_window(mbs, W, path="auto", dx_dtype="f32")
+    assert np.array_equal(Ga, Gf) and all(np.array_equal(a, b) for a, b in zip(dxa, dxf))
+
+
+def test_backward_accumulate_window_equals_concatenated_step():
+    # A whole window on the fused passes (dX of the last micro-batch by
+    # forge_dgrad before the accumulated step) against one backward pass on
+    # the concatenated batch: exact inputs, so both are exact.
+    d_out, d_in = 256, 384
+    prob = S.linear_problem(d_out, d_in, 8, seed=14, x_dtype="bf16", w_dtype="f32", state="f32")
+    prob.W = _weights(d_out, d_in, "f32", 14, exact=True)
+    mbs = micro_batches(d_out, d_in, TOKENS, 14, exact=True)
+    W, m, v = prob.W.to(DEV), prob.m.to(DEV), prob.v.to(DEV)
+    G, dxs = run_backward_window(mbs[:-1], prob.W, path="fused", dx_dtype="f32")
+    G = torch.from_numpy(G).to(DEV)
+    Xl, dYl = mbs[-1][0].to(DEV), mbs[-1][1].to(DEV)
+    dX_last = torch.empty((Xl.shape[0], d_in), device=DEV)
+    F.dgrad(dYl, W, dX_last)
+    F.wgrad_step_accumulated("adamw", Xl, dYl, G, W, m, v, step=3, **_hkw("adamw"))
+    F.sync_status()
+    Wc, mc, vc = prob.W.to(DEV), prob.m.to(DEV), prob.v.to(DEV)
+    X = torch.cat([x for x, _ in mbs]).to(DEV); dY = torch.cat([d for _, d in mbs]).to(DEV)
+    dX_cat = torch.empty((X.shape[0], d_in), device=DEV)
+    ws = torch.empty(F.workspace_bytes(d_out, d_in, X.shape[0]), dtype=torch.uint8, device=DEV)
+    F.backward_step("adamw", X, dY, Wc, mc, vc, dX_cat, step=3, workspace=ws, flags=F.FLAG_BACKWARD_SPLIT,
+                    **_hkw("adamw"))
+    F.sync_status()
+    assert_bit_exact(O.State(W=to_np(W), m=to_np(m), v=to_np(v)), O.State(W=to_np(Wc), m=to_np(mc), v=to_np(vc)),
+                     "adamw")
+    got = np.concatenate(dxs + [dX_last.cpu().numpy()])
+    assert np.array_equal(got, dX_cat.cpu().numpy())
+
+
+def test_backward_accumulate_long_token_axis_takes_the_split_path():
+    d_out, d_in = 256, 384
+    mbs = micro_batches(d_out, d_in, (800, 130), 15, exact=True)
+    W = _weights(d_out, d_in, "bf16", 15, exact=True)
+    G, dxs = run_backward_window(mbs, W, path="auto", dx_dtype="f32")
+    assert np.array_equal(G, O.accumulated_gradient_f64(_np(mbs)).astype(np.float32))
+    for (_, dY), got in zip(mbs, dxs):
+        assert np.array_equal(got, _dx_reference(dY, W)[0].astype(np.float32))
+
+
+def test_backward_accumulate_rejects_what_it_cannot_do():
+    d_out, d_in = 128, 128
+    W = torch.zeros((d_out, d_in), device=DEV)
+    G = torch.zeros((d_out, d_in), device=DEV)
+    X = torch.zeros((800, d_in), dtype=torch.bfloat16, device=DEV)
+    dY = torch.zeros((800, d_out), dtype=torch.bfloat16, device=DEV)
+    dX = torch.empty((800, d_in), device=DEV)
+    with pytest.raises(F.ForgeError) as ei:            # more tokens than tensor memory holds
+        F.backward_accumulate(X, dY, W, G, dX, flags=F.FLAG_BACKWARD_FUSED)
+    assert ei.value.status == 2
+    X, dY, dX = X[:64], dY[:64], dX[:64]
+    small = torch.empty(16, dtype=torch.uint8, device=DEV)
+    with pytest.raises(F.ForgeError) as ei:            # forced fused pass, workspace too small
+        F.backward_accumulate(X, dY, W, G, dX, workspace=small, flags=F.FLAG_BACKWARD_FUSED)
+    assert ei.value.status == 1
     F.sync_status()

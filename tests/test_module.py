@@ -128,12 +128,18 @@ def test_accumulation_window_equals_one_step_on_the_whole_batch(rule):
     for cfg in (m_acc.config, m_one.config):
         cfg.lr, cfg.weight_decay = 1e-3, 0.01
     W0 = acc.weight.detach().clone()
+    w16 = W0.bfloat16().double()
     for x, g in zip(xs, gs):
         m_acc.pre_step()
         x = x.clone().requires_grad_(True)
         (acc(x).float() * g.float()).sum().backward()
         if m_acc.config.micro < K - 1:
             assert torch.equal(acc.weight, W0)          # no step before the window's last micro-batch
+        # dX of every micro-batch from the window's (unchanged) weights:
+        # fp32 sums of the bf16 products, one bf16 rounding.
+        ref = g.double() @ w16
+        tol = 1e-5 * (g.double().abs() @ w16.abs()) + ref.abs() * 2.0 ** -8
+        assert torch.all((x.grad.double() - ref).abs() <= tol)
     m_one.pre_step()
     xc = torch.cat(xs).requires_grad_(True)
     (one(xc).float() * torch.cat(gs).float()).sum().backward()
