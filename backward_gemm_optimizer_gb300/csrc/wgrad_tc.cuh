@@ -38,11 +38,12 @@
 //     ahead of its MMAs, round it to bf16 and write it as the MN-major B
 //     operand of dX (Wb); the state ring reads the same W again for the
 //     update, mostly from L2;
-//   * warp 24 issues the dX MMAs (M = 128 tokens, N = 64, K = 16 rows of
-//     the tile) beside warp 1's weight-gradient MMAs: with 64-column tiles
-//     the two products need 64 MMAs per tile, more than one issuing thread
-//     keeps up with; a stage returns to the producer once both issuers'
-//     MMAs on it have completed;
+//   * the dX MMAs (M = 128 tokens, N = 64, K = 16 rows of the tile) are
+//     issued by warp 1 after each stage's weight-gradient MMAs, or, where
+//     the state stream is light, by a warp of their own (warp 24): with
+//     64-column tiles the two products need 64 MMAs per tile, which one
+//     issuing thread barely keeps up with; a stage returns to the producer
+//     once every issuer's MMAs on it have completed;
 //   * each CTA walks a contiguous range of tiles ordered column by column,
 //     and a persistent fp32 dX partial (all tokens x the tile's 64 columns)
 //     accumulates in TMEM beside the gradient accumulators while the CTA
@@ -120,10 +121,16 @@ struct TcCfg {
   static constexpr int EPI_WARPS = 16;
   static constexpr int EPI_THREADS = EPI_WARPS * 32;
   static constexpr int CONV_THREADS = DX ? 128 : 0;  // warps 20-23
-  // DX: warp 24 issues the dX MMAs while warp 1 issues the weight-gradient
-  // ones (a single issuing thread is the pass's bottleneck otherwise).
+  // DX: where the state stream is light (bf16 or one-tensor state, the
+  // accumulation rules), warp 24 issues the dX MMAs while warp 1 issues the
+  // weight-gradient ones -- one issuing thread would set the pass's pace.
+  // With fp32 W and two fp32 moments the state stream does, and warp 1
+  // issues both (measured: 291.5 us against 294.5 us with two issuers on the
+  // Llama-3.1-8B up-projection at BT 512; the bf16-state pass goes from 238
+  // to 230 us with two).
+  static constexpr bool DX_ISSUER = DX && !(WK == W_F32 && MK == M_F32 && NST == 2);
   static constexpr int DXMMA_WARP = 4 + EPI_WARPS + 4;
-  static constexpr int NUM_THREADS = 128 + EPI_THREADS + CONV_THREADS + (DX ? 32 : 0);
+  static constexpr int NUM_THREADS = 128 + EPI_THREADS + CONV_THREADS + (DX_ISSUER ? 32 : 0);
   static constexpr uint32_t IDESC = make_idesc_bf16(BM, BN, 1, 1);
   // dX: A = dY (M = 128 tokens, K-major), B = Wb (N = BN, MN-major).
   static constexpr uint32_t IDESC_DX = make_idesc_bf16(128, BN, 0, 1);
@@ -309,6 +316,40 @@ __device__ __forceinline__ void drain_ring(uint64_t* full, int ring, uint32_t is
   }
 }
 
+// The dX MMAs of operand stage kb of a tile: dX[128 tokens of the stage][BN]
+// += dY[tokens][128 rows of the tile] * Wb, into the persistent partial of
+// the tile column (a fresh one on the column's first tile). A: dY K-major
+// (K = D_out rows of the tile, 64 per 128-byte box row), 8-token groups
+// 1024 bytes apart, a K step of 16 advancing 32 bytes. B: Wb MN-major,
+// 8-row K groups of 1024 bytes, 16 rows = 2048 bytes.
+template <class C>
+__device__ __forceinline__ void issue_dx_stage(uint32_t a0, uint32_t wb, uint32_t tmem_base, int kb,
+                                               bool run_first) {
+  const uint32_t dx_tmem = tmem_base + static_cast<uint32_t>(C::DX_COL + kb * C::BN);
+  const uint64_t xa0 = make_smem_desc(a0, 16, 1024, 2);
+  const uint64_t xb0 = make_smem_desc(wb, 8192, 1024, 2);
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      const uint64_t astep = static_cast<uint64_t>((hh * C::BOX + kk * 32) >> 4);
+      const uint64_t bstep = static_cast<uint64_t>(((hh * 4 + kk) * 2048) >> 4);
+      umma_f16(dx_tmem, xa0 + astep, xb0 + bstep, C::IDESC_DX, (run_first && hh == 0 && kk == 0) ? 0u : 1u);
+    }
+  }
+}
+
+// Before a tile's first dX MMAs: the previous column's partial must have
+// been written out (at a column's first tile), and this tile's bf16 W_old
+// must be in place. False if a wait gave up.
+__device__ __forceinline__ bool dx_tile_ready(bool run_first, uint32_t runs_done, int it, uint64_t* dx_empty,
+                                              uint64_t* wb_full, volatile int* abort_flag, unsigned int* status,
+                                              uint64_t lim) {
+  if (run_first && runs_done > 0 && !bwait(dx_empty, (runs_done - 1) & 1u, abort_flag, status, WAIT_DX_EMPTY, lim))
+    return false;
+  return bwait(wb_full, it & 1, abort_flag, status, WAIT_WB_FULL, lim);
+}
+
 template <int OPT, int WK, int MK, int BN, int STAGES, int NBUF, bool DX, bool GA, bool NARROW>
 __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, NARROW>::NUM_THREADS, 1)
     wgrad_step_tc_kernel(const __grid_constant__ WgradTcParams p) {
@@ -347,8 +388,11 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, N
   volatile int* abort_flag = &abort_sh;
 
   if (threadIdx.x == 0) {
-    // DX: a stage is released by both MMA-issuing threads.
-    for (int s = 0; s < STAGES; ++s) { mbar_init(&op_full[s], 1); mbar_init(&op_empty[s], DX ? 2 : 1); }
+    // With a dX issuer a stage is released by both MMA-issuing threads.
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&op_full[s], 1);
+      mbar_init(&op_empty[s], C::DX_ISSUER ? 2 : 1);
+    }
     for (int s = 0; s < NBUF; ++s) {
       mbar_init(&st_full[s], 1);
       mbar_init(&st_empty[s], 1);
@@ -416,12 +460,18 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, N
       uint32_t kseq = 0;
       bool ok = true;
       int it = 0;
+      uint32_t runs_done = 0;  // dX partials handed to the converter warps (no dX issuer)
       for (int tile = tw.first; ok && tile < tw.end; tile += tw.step, ++it) {
         const int buf = it & 1;
         const uint32_t eph = ((it >> 1) & 1) ^ 1u;
         if (!bwait(&tm_empty[buf], eph, abort_flag, p.status, WAIT_TMEM_EMPTY, lim)) { ok = false; break; }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
+        // dX issued here too (no dX issuer warp): the column's first tile
+        // starts a fresh partial.
+        constexpr bool DX_HERE = DX && !C::DX_ISSUER;
+        const bool run_first = DX_HERE && (tile == tw.first || tile % p.tiles_m == 0);
+        const bool run_last = DX_HERE && (tile + 1 == tw.end || (tile + 1) % p.tiles_m == 0);
         for (int kb = 0; kb < p.num_kb; ++kb, ++kseq) {
           const int s = static_cast<int>(kseq % STAGES);
           const uint32_t ph = (kseq / STAGES) & 1u;
@@ -440,9 +490,25 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, N
             const uint64_t step = static_cast<uint64_t>(kk * 2048 >> 4);
             umma_f16(d_tmem, ad0 + step, bd0 + step, C::IDESC, (kb > 0 || kk > 0) ? 1u : 0u);
           }
+          if constexpr (DX_HERE) {
+            if (kb == 0) {
+              if (!dx_tile_ready(run_first, runs_done, it, &dx_empty, &wb_full, abort_flag, p.status, lim)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after_sync();
+            }
+            issue_dx_stage<C>(a0, smem_u32(wb_base), tmem_base, kb, run_first);
+          }
           umma_commit(&op_empty[s]);
         }
         if (!ok) break;
+        if constexpr (DX_HERE) {
+          if (p.num_kb > 0) {
+            umma_commit(&wb_empty);
+            if (run_last) { umma_commit(&dx_full); ++runs_done; }
+          }
+        }
         umma_commit(&tm_full[buf]);
       }
       if (!ok) {
@@ -825,7 +891,7 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, N
     }
   }
 
-  if constexpr (DX) {
+  if constexpr (C::DX_ISSUER) {
     if (warp == C::DXMMA_WARP && lane == 0) {
       // ---------------------------------------------------------- MMA issuer (input gradient, warp 24)
       // dX[128 tokens of stage kb][BN] += dY[tokens][128 rows of the tile] * Wb,
@@ -843,33 +909,12 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, N
           const int s = static_cast<int>(kseq % STAGES);
           const uint32_t ph = (kseq / STAGES) & 1u;
           if (!bwait(&op_full[s], ph, abort_flag, p.status, WAIT_OP_FULL, lim)) { ok = false; break; }
-          if (kb == 0) {
-            // The previous column's partial must have been written out, and
-            // this tile's bf16 W_old must be in place.
-            if (run_first && runs_done > 0 &&
-                !bwait(&dx_empty, (runs_done - 1) & 1u, abort_flag, p.status, WAIT_DX_EMPTY, lim)) {
-              ok = false;
-              break;
-            }
-            if (!bwait(&wb_full, it & 1, abort_flag, p.status, WAIT_WB_FULL, lim)) { ok = false; break; }
+          if (kb == 0 && !dx_tile_ready(run_first, runs_done, it, &dx_empty, &wb_full, abort_flag, p.status, lim)) {
+            ok = false;
+            break;
           }
           tc_fence_after_sync();
-          const uint32_t a0 = smem_u32(op_base + s * C::STAGE_BYTES);
-          // A: dY K-major (K = D_out rows of the tile, 64 per 128-byte box row),
-          // 8-token groups 1024 bytes apart; a K step of 16 advances 32 bytes.
-          // B: MN-major Wb, 8-row K groups of 1024 bytes, 16 rows = 2048 bytes.
-          const uint32_t dx_tmem = tmem_base + static_cast<uint32_t>(C::DX_COL + kb * BN);
-          const uint64_t xa0 = make_smem_desc(a0, 16, 1024, 2);
-          const uint64_t xb0 = make_smem_desc(smem_u32(wb_base), 8192, 1024, 2);
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t astep = static_cast<uint64_t>((hh * C::BOX + kk * 32) >> 4);
-              const uint64_t bstep = static_cast<uint64_t>(((hh * 4 + kk) * 2048) >> 4);
-              umma_f16(dx_tmem, xa0 + astep, xb0 + bstep, C::IDESC_DX, (run_first && hh == 0 && kk == 0) ? 0u : 1u);
-            }
-          }
+          issue_dx_stage<C>(smem_u32(op_base + s * C::STAGE_BYTES), smem_u32(wb_base), tmem_base, kb, run_first);
           umma_commit(&op_empty[s]);
         }
         if (!ok) break;
