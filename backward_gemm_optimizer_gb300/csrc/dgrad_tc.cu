@@ -22,8 +22,7 @@ namespace forge {
 
 namespace {
 
-constexpr int BM = 128, BK = 64;
-constexpr int A_BYTES = BM * BK * 2;       // 16 KB: dY tile, K-major
+constexpr int BM = 128;
 constexpr int NUM_THREADS = 512;
 constexpr int CONV_THREADS = 256;          // warps 8-15
 
@@ -36,10 +35,18 @@ constexpr int CONV_THREADS = 256;          // warps 8-15
 template <bool F32W, int BN_>
 struct DCfg {
   static constexpr int BN = BN_;
-  static constexpr int B_BYTES = BK * BN * 2;    // bf16 W tile, MN-major, 64-column atoms 8 KB apart
+  // Rows of D_out per stage: 128 for bf16 weights on 128-column tiles --
+  // each stage costs a fixed hand-over time besides its bytes, so fewer,
+  // larger stages win there (up-projection, BT 512: 105 -> 72 us) -- and 64
+  // otherwise: the fp32 staging ring, and the 128 x 256 tiles, whose ring
+  // would shrink to two stages (measured slower).
+  static constexpr int BK = (F32W || BN == 256) ? 64 : 128;
+  static constexpr int A_BYTES = BM * BK * 2;    // dY tile, K-major: BK / 64 boxes of 64 columns, 16 KB apart
+  static constexpr int B_BYTES = BK * BN * 2;    // bf16 W tile, MN-major, 64-column atoms BK * 128 bytes apart
+  static constexpr int ATOM = BK * 128;          // bytes of one 64-column atom (box) of the bf16 W tile
   static constexpr int STG_BYTES = BK * BN * 4;  // fp32 W tile as 32-column swizzled boxes
-  static constexpr int SA = F32W ? 3 : (BN == 256 ? 4 : 6);
-  static constexpr int SB = F32W ? 2 : (BN == 256 ? 4 : 6);
+  static constexpr int SA = F32W ? 3 : (BN == 256 ? 4 : 3);
+  static constexpr int SB = F32W ? 2 : (BN == 256 ? 4 : 3);
   static constexpr int SS = F32W ? 4 : 0;
   static constexpr int A_OFF = 0;
   static constexpr int B_OFF = SA * A_BYTES;
@@ -92,7 +99,8 @@ __device__ __forceinline__ void dtile(int tile, int tiles_m, int tiles_n, int gr
 template <bool F32W, int BN>
 __global__ void __launch_bounds__(NUM_THREADS, 1) dgrad_tc_kernel(const __grid_constant__ DgradParams p) {
   using C = DCfg<F32W, BN>;
-  constexpr int B_BYTES = C::B_BYTES, STG_BYTES = C::STG_BYTES, TMEM_COLS = C::TMEM_COLS;
+  constexpr int A_BYTES = C::A_BYTES, B_BYTES = C::B_BYTES, STG_BYTES = C::STG_BYTES, TMEM_COLS = C::TMEM_COLS;
+  constexpr int BK = C::BK;
   constexpr uint32_t IDESC = C::IDESC;
   constexpr int SA = C::SA, SB = C::SB, SS = C::SS > 0 ? C::SS : 1;
   extern __shared__ uint8_t smem_raw[];
@@ -140,7 +148,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dgrad_tc_kernel(const __grid_c
             break;
           }
           mbar_arrive_expect_tx(&a_full[s], A_BYTES);
-          tma_load_2d(a_ring + s * A_BYTES, &p.tm_dy, &a_full[s], kb * BK, tm * BM);
+#pragma unroll
+          for (int h = 0; h < BK / 64; ++h)
+            tma_load_2d(a_ring + s * A_BYTES + h * 16384, &p.tm_dy, &a_full[s], kb * BK + h * 64, tm * BM);
         }
       }
       if (!ok) ddrain(a_full, SA, k, p.status);
@@ -174,7 +184,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dgrad_tc_kernel(const __grid_c
             mbar_arrive_expect_tx(&b_full[s], B_BYTES);
 #pragma unroll
             for (int bb = 0; bb < BN / 64; ++bb)
-              tma_load_2d(b + bb * 8192, &p.tm_w, &b_full[s], tn * BN + bb * 64, kb * BK);
+              tma_load_2d(b + bb * C::ATOM, &p.tm_w, &b_full[s], tn * BN + bb * 64, kb * BK);
           }
         }
       }
@@ -210,10 +220,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dgrad_tc_kernel(const __grid_c
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             // A: K-major, 128-byte swizzle, 8-row groups 1024 bytes apart; a
-            // K step of 16 elements advances the start by 32 bytes.
-            const uint64_t ad = make_smem_desc(a0 + kk * 32, 16, 1024, 2);
-            // B: MN-major, 64-column atoms 8192 bytes apart, 8-row K groups of 1024 bytes.
-            const uint64_t bd = make_smem_desc(b0 + kk * 2048, 8192, 1024, 2);
+            // K step of 16 elements advances the start by 32 bytes within a
+            // 64-column box, boxes 16 KB apart.
+            const uint64_t ad = make_smem_desc(a0 + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024, 2);
+            // B: MN-major, 64-column atoms C::ATOM bytes apart, 8-row K groups of 1024 bytes.
+            const uint64_t bd = make_smem_desc(b0 + kk * 2048, C::ATOM, 1024, 2);
             umma_f16(d, ad, bd, IDESC, (kb > 0 || kk > 0) ? 1u : 0u);
           }
           umma_commit(&a_empty[sa]);

@@ -787,7 +787,13 @@ forge_status dgrad_impl(const forge_tensor* dY, const forge_tensor* W_old, forge
   p.bn = (W_old->dtype == FORGE_BF16 && p.tiles_m * ((d_in + 255) / 256) >= dev->sms) ? 256 : 128;
   p.tiles_n = static_cast<int>((d_in + p.bn - 1) / p.bn);
   p.num_tiles = p.tiles_m * p.tiles_n;
-  p.num_kb = static_cast<int>((d_out + 63) / 64);
+  // Rows of D_out per stage: 128 for bf16 weights on 128-column tiles, else 64.
+  const int64_t rows_per_stage = (W_old->dtype == FORGE_BF16 && p.bn == 128) ? 128 : 64;
+  if (rows_per_stage == 128 &&
+      (st = encode_2d(&p.tm_w, W_old, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B,
+                      "W")) != FORGE_OK)
+    return st;
+  p.num_kb = static_cast<int>((d_out + rows_per_stage - 1) / rows_per_stage);
   p.group_m = 8;
   p.timeout_ns = kTimeoutNs;
   const int grid = p.num_tiles < dev->sms ? p.num_tiles : dev->sms;
