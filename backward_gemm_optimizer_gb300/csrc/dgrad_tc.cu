@@ -217,15 +217,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dgrad_tc_kernel(const __grid_c
           tc_fence_after_sync();
           const uint32_t a0 = smem_u32(a_ring + sa * A_BYTES);
           const uint32_t b0 = smem_u32(b_ring + sb * B_BYTES);
+          // A: K-major, 128-byte swizzle, 8-row groups 1024 bytes apart.
+          // B: MN-major, 64-column atoms C::ATOM bytes apart, 8-row K groups
+          // of 1024 bytes. Both descriptors are built once per stage; a K
+          // step only moves the 14-bit start-address field (16-byte units;
+          // shared addresses stay below 2^18 bytes, so it never carries).
+          const uint64_t ad0 = make_smem_desc(a0, 16, 1024, 2);
+          const uint64_t bd0 = make_smem_desc(b0, C::ATOM, 1024, 2);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
-            // A: K-major, 128-byte swizzle, 8-row groups 1024 bytes apart; a
-            // K step of 16 elements advances the start by 32 bytes within a
-            // 64-column box, boxes 16 KB apart.
-            const uint64_t ad = make_smem_desc(a0 + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024, 2);
-            // B: MN-major, 64-column atoms C::ATOM bytes apart, 8-row K groups of 1024 bytes.
-            const uint64_t bd = make_smem_desc(b0 + kk * 2048, C::ATOM, 1024, 2);
-            umma_f16(d, ad, bd, IDESC, (kb > 0 || kk > 0) ? 1u : 0u);
+            // A K step of 16 elements advances 32 bytes within a 64-column
+            // box (boxes 16 KB apart); B's advances 16 rows = 2048 bytes.
+            const uint64_t astep = static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+            const uint64_t bstep = static_cast<uint64_t>((kk * 2048) >> 4);
+            umma_f16(d, ad0 + astep, bd0 + bstep, IDESC, (kb > 0 || kk > 0) ? 1u : 0u);
           }
           umma_commit(&a_empty[sa]);
           umma_commit(&b_empty[sb]);
