@@ -2,12 +2,13 @@
 // (FORGE, Remark 1 in Appendix A: the input gradient must read the weights
 // before the fused step overwrites them, so it is enqueued first).
 //
-// Tiles of 128 tokens x 128 input features; the contraction runs over
-// D_out in 64-wide stages. A = dY is K-major (D_out contiguous), B = W is
+// Tiles of 128 tokens x 128 input features (128 x 256 for bf16 weights on
+// long token axes); the contraction runs over D_out in 128-row stages (64
+// on the wider tiles). A = dY is K-major (D_out contiguous), B = W is
 // MN-major (D_in contiguous). bf16 weights are fed by TMA directly; fp32
-// master weights are staged by TMA and four converter warps round them to
-// bf16 (round-to-nearest-even) into the swizzled operand layout before the
-// MMA consumes them.
+// master weights are staged by TMA in 64-row slots and eight converter
+// warps round them to bf16 (round-to-nearest-even) into the swizzled
+// operand layout before the MMA consumes them.
 //
 // Warp roles (512 threads): 0 dY producer, 1 MMA issuer + TMEM owner,
 // 2 W producer, 4-7 epilogue (TMEM lane quadrant = warp % 4, thread =
@@ -35,19 +36,20 @@ constexpr int CONV_THREADS = 256;          // warps 8-15
 template <bool F32W, int BN_>
 struct DCfg {
   static constexpr int BN = BN_;
-  // Rows of D_out per stage: 128 for bf16 weights on 128-column tiles --
-  // each stage costs a fixed hand-over time besides its bytes, so fewer,
-  // larger stages win there (up-projection, BT 512: 105 -> 72 us) -- and 64
-  // otherwise: the fp32 staging ring, and the 128 x 256 tiles, whose ring
-  // would shrink to two stages (measured slower).
-  static constexpr int BK = (F32W || BN == 256) ? 64 : 128;
+  // Rows of D_out per stage: 128 on 128-column tiles -- each stage costs a
+  // fixed hand-over time besides its bytes, so fewer, larger stages win
+  // (up-projection, BT 512, bf16 weights: 105 -> 72 us); fp32 weights are
+  // staged in 64-row slots, two per stage. 64 on 128 x 256 tiles, whose
+  // ring would shrink to two stages (measured slower).
+  static constexpr int BK = (BN == 256) ? 64 : 128;
   static constexpr int A_BYTES = BM * BK * 2;    // dY tile, K-major: BK / 64 boxes of 64 columns, 16 KB apart
   static constexpr int B_BYTES = BK * BN * 2;    // bf16 W tile, MN-major, 64-column atoms BK * 128 bytes apart
   static constexpr int ATOM = BK * 128;          // bytes of one 64-column atom (box) of the bf16 W tile
-  static constexpr int STG_BYTES = BK * BN * 4;  // fp32 W tile as 32-column swizzled boxes
-  static constexpr int SA = F32W ? 3 : (BN == 256 ? 4 : 3);
+  static constexpr int STG_ROWS = 64;             // fp32 staging slot: 64 rows of the stage
+  static constexpr int STG_BYTES = STG_ROWS * BN * 4;  // as four 32-column swizzled boxes
+  static constexpr int SA = F32W ? 2 : (BN == 256 ? 4 : 3);
   static constexpr int SB = F32W ? 2 : (BN == 256 ? 4 : 3);
-  static constexpr int SS = F32W ? 4 : 0;
+  static constexpr int SS = F32W ? 3 : 0;
   static constexpr int A_OFF = 0;
   static constexpr int B_OFF = SA * A_BYTES;
   static constexpr int S_OFF = B_OFF + SB * B_BYTES;
@@ -159,21 +161,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dgrad_tc_kernel(const __grid_c
     // ------------------------------------------------------------ W producer
     if (lane == 0) {
       uint32_t k = 0;
+      uint32_t ks = 0;  // fp32 staging slots filled
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
         int tm, tn;
         dtile(tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
         for (int kb = 0; kb < p.num_kb; ++kb, ++k) {
           if constexpr (F32W) {
-            const int s = static_cast<int>(k % SS);
-            if (!dwait(&s_empty[s], ((k / SS) & 1u) ^ 1u, abort_flag, p.status, WAIT_OP_EMPTY, lim)) {
-              ok = false;
-              break;
-            }
-            uint8_t* stg = s_ring + s * STG_BYTES;
-            mbar_arrive_expect_tx(&s_full[s], STG_BYTES);
+            for (int half = 0; half < BK / C::STG_ROWS; ++half, ++ks) {
+              const int s = static_cast<int>(ks % SS);
+              if (!dwait(&s_empty[s], ((ks / SS) & 1u) ^ 1u, abort_flag, p.status, WAIT_OP_EMPTY, lim)) {
+                ok = false;
+                break;
+              }
+              uint8_t* stg = s_ring + s * STG_BYTES;
+              mbar_arrive_expect_tx(&s_full[s], STG_BYTES);
 #pragma unroll
-            for (int bb = 0; bb < 4; ++bb) tma_load_2d(stg + bb * 8192, &p.tm_w, &s_full[s], tn * BN + bb * 32, kb * BK);
+              for (int bb = 0; bb < 4; ++bb)
+                tma_load_2d(stg + bb * 8192, &p.tm_w, &s_full[s], tn * BN + bb * 32, kb * BK + half * C::STG_ROWS);
+            }
+            if (!ok) break;
           } else {
             const int s = static_cast<int>(k % SB);
             if (!dwait(&b_empty[s], ((k / SB) & 1u) ^ 1u, abort_flag, p.status, WAIT_OP_EMPTY, lim)) {
@@ -189,7 +196,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dgrad_tc_kernel(const __grid_c
         }
       }
       if (!ok) {
-        if constexpr (F32W) ddrain(s_full, SS, k, p.status);
+        if constexpr (F32W) ddrain(s_full, SS, ks, p.status);
         else ddrain(b_full, SB, k, p.status);
       }
     }
@@ -311,43 +318,49 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dgrad_tc_kernel(const __grid_c
     // MN-major swizzled operand. Consecutive threads take consecutive K
     // rows, so both the reads and the writes are bank-conflict free.
     const int ct = threadIdx.x - 256;
-    uint32_t k = 0;
+    uint32_t k = 0, ks = 0;
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
       for (int kb = 0; kb < p.num_kb; ++kb, ++k) {
-        const int ss = static_cast<int>(k % SS), sb = static_cast<int>(k % SB);
-        ok = dwait(&s_full[ss], (k / SS) & 1u, abort_flag, p.status, WAIT_OP_FULL, lim) &&
-             dwait(&b_empty[sb], ((k / SB) & 1u) ^ 1u, abort_flag, p.status, WAIT_OP_EMPTY, lim);
-        ok = __all_sync(0xFFFFFFFFu, ok);
-        if (!ok) break;
+        const int sb = static_cast<int>(k % SB);
         uint8_t* b = b_ring + sb * B_BYTES;
-        const uint8_t* stg = s_ring + ss * STG_BYTES;
-        uint4 o[4];
-        int dst[4];
+        // A stage's BK rows arrive as BK / 64 staging slots of 64 rows.
+        for (int half = 0; half < BK / C::STG_ROWS; ++half, ++ks) {
+          const int ss = static_cast<int>(ks % SS);
+          ok = dwait(&s_full[ss], (ks / SS) & 1u, abort_flag, p.status, WAIT_OP_FULL, lim) &&
+               (half > 0 || dwait(&b_empty[sb], ((k / SB) & 1u) ^ 1u, abort_flag, p.status, WAIT_OP_EMPTY, lim));
+          ok = __all_sync(0xFFFFFFFFu, ok);
+          if (!ok) break;
+          const uint8_t* stg = s_ring + ss * STG_BYTES;
+          uint4 o[4];
+          int dst[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int i = ct + CONV_THREADS * j;
-          const int kr = i & 63;             // K row
-          const int hh = (i >> 6) & 3;       // 8-column group within the 32-column box
-          const int bb = i >> 8;             // box (32 columns)
-          const uint8_t* src = stg + bb * 8192 + kr * 128;
-          const float4 u0 = *reinterpret_cast<const float4*>(src + (((2 * hh) ^ (kr & 7)) << 4));
-          const float4 u1 = *reinterpret_cast<const float4*>(src + (((2 * hh + 1) ^ (kr & 7)) << 4));
-          o[j].x = pack_bf16x2_rn(u0.x, u0.y);
-          o[j].y = pack_bf16x2_rn(u0.z, u0.w);
-          o[j].z = pack_bf16x2_rn(u1.x, u1.y);
-          o[j].w = pack_bf16x2_rn(u1.z, u1.w);
-          const int n = bb * 32 + hh * 8;    // column within the 128-wide tile
-          dst[j] = (n >> 6) * 8192 + kr * 128 + ((((n & 63) >> 3) ^ (kr & 7)) << 4);
+          for (int j = 0; j < 4; ++j) {
+            const int i = ct + CONV_THREADS * j;
+            const int kr = i & 63;             // row within the staging slot
+            const int hh = (i >> 6) & 3;       // 8-column group within the 32-column box
+            const int bb = i >> 8;             // box (32 columns)
+            const uint8_t* src = stg + bb * 8192 + kr * 128;
+            const float4 u0 = *reinterpret_cast<const float4*>(src + (((2 * hh) ^ (kr & 7)) << 4));
+            const float4 u1 = *reinterpret_cast<const float4*>(src + (((2 * hh + 1) ^ (kr & 7)) << 4));
+            o[j].x = pack_bf16x2_rn(u0.x, u0.y);
+            o[j].y = pack_bf16x2_rn(u0.z, u0.w);
+            o[j].z = pack_bf16x2_rn(u1.x, u1.y);
+            o[j].w = pack_bf16x2_rn(u1.z, u1.w);
+            const int n = bb * 32 + hh * 8;    // column within the 128-wide tile
+            const int row = half * C::STG_ROWS + kr;  // K row of the stage (row % 8 == kr % 8)
+            dst[j] = (n >> 6) * C::ATOM + row * 128 + ((((n & 63) >> 3) ^ (kr & 7)) << 4);
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j) *reinterpret_cast<uint4*>(b + dst[j]) = o[j];
+          fence_proxy_async_smem();
+          // Release the staging slot only now: the stores above consume every
+          // value loaded from it, so those loads have returned before the next
+          // TMA fill may overwrite the slot.
+          mbar_arrive(&s_empty[ss]);
         }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) *reinterpret_cast<uint4*>(b + dst[j]) = o[j];
-        fence_proxy_async_smem();
+        if (!ok) break;
         mbar_arrive(&b_full[sb]);
-        // Release the staging slot only now: the stores above consume every
-        // value loaded from it, so those loads have returned before the next
-        // TMA fill may overwrite the slot.
-        mbar_arrive(&s_empty[ss]);
       }
     }
   }
@@ -363,6 +376,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dgrad_tc_kernel(const __grid_c
 
 template <bool F32W, int BN>
 cudaError_t launch_d(const DgradParams& p, int grid, cudaStream_t stream) {
+  // The stage depth the host encoded the tensor maps and num_kb for must be
+  // the kernel's: a mismatch would overfill the shared-memory rings.
+  if (p.bk != DCfg<F32W, BN>::BK || (p.w_f32 != nullptr) != F32W) return cudaErrorInvalidValue;
   auto kern = dgrad_tc_kernel<F32W, BN>;
   static unsigned long long attr_mask = 0ull;
   int dev = 0;

@@ -762,18 +762,6 @@ forge_status dgrad_impl(const forge_tensor* dY, const forge_tensor* W_old, forge
   if ((st = encode_2d(&p.tm_dy, dY, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, "dY")) !=
       FORGE_OK)
     return st;
-  if (W_old->dtype == FORGE_BF16) {
-    if ((st = encode_2d(&p.tm_w, W_old, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B,
-                        "W")) != FORGE_OK)
-      return st;
-    p.w_f32 = nullptr;
-  } else {
-    if ((st = encode_2d(&p.tm_w, W_old, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 32, 64, CU_TENSOR_MAP_SWIZZLE_128B,
-                        "W")) != FORGE_OK)
-      return st;
-    p.w_f32 = static_cast<const float*>(W_old->data);
-    p.ld_w32 = W_old->ld;
-  }
   p.dX = dX->data;
   p.ld_dx = dX->ld;
   p.dx_bf16 = dX->dtype == FORGE_BF16 ? 1 : 0;
@@ -787,12 +775,24 @@ forge_status dgrad_impl(const forge_tensor* dY, const forge_tensor* W_old, forge
   p.bn = (W_old->dtype == FORGE_BF16 && p.tiles_m * ((d_in + 255) / 256) >= dev->sms) ? 256 : 128;
   p.tiles_n = static_cast<int>((d_in + p.bn - 1) / p.bn);
   p.num_tiles = p.tiles_m * p.tiles_n;
-  // Rows of D_out per stage: 128 for bf16 weights on 128-column tiles, else 64.
-  const int64_t rows_per_stage = (W_old->dtype == FORGE_BF16 && p.bn == 128) ? 128 : 64;
-  if (rows_per_stage == 128 &&
-      (st = encode_2d(&p.tm_w, W_old, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B,
-                      "W")) != FORGE_OK)
-    return st;
+  // Rows of D_out per stage: 128 on 128-column tiles, 64 on 128 x 256 tiles.
+  // The W boxes must match what the kernel expects per load: bf16 weights
+  // one box of 64 columns x rows_per_stage; fp32 weights 32-column x 64-row
+  // boxes (staged in 64-row slots, two per 128-row stage).
+  const int64_t rows_per_stage = p.bn == 128 ? 128 : 64;
+  if (W_old->dtype == FORGE_BF16) {
+    if ((st = encode_2d(&p.tm_w, W_old, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64,
+                        static_cast<uint32_t>(rows_per_stage), CU_TENSOR_MAP_SWIZZLE_128B, "W")) != FORGE_OK)
+      return st;
+    p.w_f32 = nullptr;
+  } else {
+    if ((st = encode_2d(&p.tm_w, W_old, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 32, 64, CU_TENSOR_MAP_SWIZZLE_128B,
+                        "W")) != FORGE_OK)
+      return st;
+    p.w_f32 = static_cast<const float*>(W_old->data);
+    p.ld_w32 = W_old->ld;
+  }
+  p.bk = static_cast<int>(rows_per_stage);
   p.num_kb = static_cast<int>((d_out + rows_per_stage - 1) / rows_per_stage);
   p.group_m = 8;
   p.timeout_ns = kTimeoutNs;

@@ -93,7 +93,7 @@ struct WgradSimtParams {
 // Input gradient dX = dY W (tensor cores).
 struct alignas(128) DgradParams {
   CUtensorMap tm_dy;  // dY [BT][D_out] bf16, box 64 (K) x 128 (M rows), 128-byte swizzle
-  CUtensorMap tm_w;   // W bf16 [D_out][D_in], box 64 (N) x 64 (K), 128-byte swizzle
+  CUtensorMap tm_w;   // W [D_out][D_in]: bf16, box 64 (N) x bk (K); or fp32, box 32 (N) x 64 (K); 128-byte swizzle
   const float* w_f32; // W fp32 (staged and rounded to bf16 by the kernel) or null
   int64_t ld_w32;
   void* dX;           // [BT][D_in]
@@ -104,6 +104,7 @@ struct alignas(128) DgradParams {
   int tiles_m, tiles_n, num_tiles, num_kb;
   int group_m;
   int bn;             // tile width (input features): 128, or 256 for bf16 W
+  int bk;             // rows of D_out per stage (128, or 64 with bn 256); must match the kernel's
   uint32_t flags;
   uint64_t timeout_ns;
 };
