@@ -3,7 +3,7 @@
 //
 // One persistent CTA per SM walks a grouped raster of 128 x BN gradient
 // tiles G_ij = sum_k dY_k,i^T X_k,j (Eq. 5), BN = 64, 128 or 256. Warp
-// roles (640 threads):
+// roles (640 threads; 768 or 800 with the fused input gradient, below):
 //
 //   warp 0      operand producer: TMA loads of the BK-token slabs of dY and
 //               X (BK = 64, or 128 with the fused input gradient) into a
