@@ -1,8 +1,10 @@
 """Full-size parity at the Llama-3.1-8B up-projection shape (W 14336 x 4096,
 BT = 512 and the BT sweep), in the launch configuration the benchmark
-times: the whole layer runs on the GPU; the oracle recomputes a sample of
-rows (every column of each sampled row, so every column tile and every
-8-bit block of those rows is covered) from the same inputs."""
+times (forge_backward_step with its workspace: the fused input-gradient
+pass at BT 512): the whole layer runs on the GPU; the oracle recomputes a
+sample of rows (every column of each sampled row, so every column tile and
+every 8-bit block of those rows is covered) and a sample of dX rows (the
+full contraction over D_out) from the same inputs."""
 
 import numpy as np
 import pytest
@@ -38,13 +40,21 @@ def _row_problem(prob, rows):
 
 
 def _gpu_full(prob, *, sr_w, t=1):
+    """The layer's backward pass as the benchmark launches it. fp32 / bf16
+    state: one forge_backward_step with a workspace of workspace_bytes() and
+    no path flag (the fused input-gradient pass at BT 512; dgrad + step past
+    768 tokens). 8-bit state: forge_dgrad, then the step."""
     dev = "cuda:0"
     X, dY, W, m, v = (prob.X.to(dev), prob.dY.to(dev), prob.W.to(dev), prob.m.to(dev), prob.v.to(dev))
     ms = prob.m_scale.to(dev) if prob.m_scale is not None else None
     vs = prob.v_scale.to(dev) if prob.v_scale is not None else None
     dX = torch.empty((X.shape[0], D_IN), dtype=torch.bfloat16, device=dev)
-    F.dgrad(dY, W, dX)
-    F.wgrad_step_adamw(X, dY, W, m, v, m_scale=ms, v_scale=vs, step=t, seed=1234, sr_w=sr_w, **HYPER["adamw"])
+    if ms is None:
+        ws = torch.empty(max(16, F.workspace_bytes(D_OUT, D_IN, X.shape[0])), dtype=torch.uint8, device=dev)
+        F.backward_step("adamw", X, dY, W, m, v, dX, step=t, seed=1234, sr_w=sr_w, workspace=ws, **HYPER["adamw"])
+    else:
+        F.dgrad(dY, W, dX)
+        F.wgrad_step_adamw(X, dY, W, m, v, m_scale=ms, v_scale=vs, step=t, seed=1234, sr_w=sr_w, **HYPER["adamw"])
     F.sync_status()
     return W, m, v, ms, vs, dX
 
@@ -93,3 +103,43 @@ def test_up_proj_full_size_sampled_rows(w, st, bt):
     assert np.all(np.abs(gx - ref) <= tol)
     if rep is not None:
         print(w, st, bt, rep)
+
+
+def test_up_proj_accumulation_window_full_size():
+    # The accumulation benchmark's window at full size: three micro-batches
+    # through forge_backward_accumulate (dX and G_acc in one pass), the last
+    # through forge_dgrad + forge_wgrad_step_accumulated. The sampled rows of
+    # the new state must match one AdamW step on the concatenated batch, and
+    # every micro-batch's sampled dX rows the product with the window's W.
+    dev, nmb, bt = "cuda:0", 4, 512
+    prob = S.linear_problem(D_OUT, D_IN, bt, seed=7, x_dtype="bf16", w_dtype="f32", state="f32")
+    mbs = [(S.normal((bt, D_IN), 1.0, 70 + i, S.STREAM_X, "bf16"), S.normal((bt, D_OUT), 1.0, 70 + i, S.STREAM_DY, "bf16"))
+           for i in range(nmb)]
+    W, m, v = prob.W.to(dev), prob.m.to(dev), prob.v.to(dev)
+    G = torch.empty_like(W)
+    ws = torch.empty(F.workspace_bytes(D_OUT, D_IN, bt), dtype=torch.uint8, device=dev)
+    dxs = []
+    for i, (X, dY) in enumerate(mbs):
+        Xd, dYd = X.to(dev), dY.to(dev)
+        dX = torch.empty((bt, D_IN), dtype=torch.bfloat16, device=dev)
+        if i < nmb - 1:
+            F.backward_accumulate(Xd, dYd, W, G, dX, overwrite=(i == 0), workspace=ws, flags=F.FLAG_BACKWARD_FUSED)
+        else:
+            F.dgrad(dYd, W, dX)
+            F.wgrad_step_accumulated("adamw", Xd, dYd, G, W, m, v, step=1, **HYPER["adamw"])
+        dxs.append(dX)
+    F.sync_status()
+    rows = _sample_rows(D_OUT, 24, 5)
+    idx = torch.from_numpy(rows).cuda()
+    got = O.State(W=to_np(W[idx]), m=to_np(m[idx]), v=to_np(v[idx]))
+    cat = S.LinearProblem(**{**prob.__dict__, "X": torch.cat([x for x, _ in mbs]),
+                             "dY": torch.cat([d for _, d in mbs])})
+    print("accumulation window", check_tolerance("adamw", _row_problem(cat, rows), "f32", "f32", 1, got))
+    w16 = O.bf16_bits_to_f32(O.f32_to_bf16_rne(prob.W.float().numpy())).astype(np.float64)
+    toks = _sample_rows(bt, 8, 6)
+    for (_, dY), dX in zip(mbs, dxs):
+        dYt = dY[torch.from_numpy(toks)].float().numpy().astype(np.float64)
+        ref = dYt @ w16
+        tol = 1e-5 * (np.abs(dYt) @ np.abs(w16)) + np.abs(ref) * 2 ** -8      # bf16 output rounding
+        gx = dX[torch.from_numpy(toks).cuda()].float().cpu().numpy()
+        assert np.all(np.abs(gx - ref) <= tol)
