@@ -374,8 +374,9 @@ const char* forge_last_error(void);
 const char* forge_version(void);
 
 /*
- * forge_workspace_bytes -- device scratch that forge_backward_step's fused
- * path needs for a layer of this shape on the current device: one fp32
+ * forge_workspace_bytes -- device scratch that the fused paths of
+ * forge_backward_step and forge_backward_accumulate need for a layer of
+ * this shape on the current device: one fp32
  * slab of ceil(BT/128)*128 x 64 dX partial sums per (CTA, tile column)
  * pair. 0 when the fused path does not apply (BT = 0 or BT > 768) or the
  * device cannot be queried. The forge_wgrad_step_* calls and forge_dgrad
