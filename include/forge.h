@@ -95,8 +95,9 @@ typedef struct {
  * step returns without touching W or its moments; forge_sync_status() then
  * reports FORGE_ERR_TIMEOUT. */
 #define FORGE_FLAG_TEST_FORCE_TIMEOUT 0x100u
-/* forge_backward_step only: force the fused input gradient (an error if
- * this layer or workspace cannot take it), or force dgrad + step. */
+/* forge_backward_step (in forge_hyper.flags) and forge_backward_accumulate
+ * (its flags argument) only: force the fused input gradient (an error if
+ * this layer or workspace cannot take it), or force the two-kernel path. */
 #define FORGE_FLAG_BACKWARD_FUSED 0x200u
 #define FORGE_FLAG_BACKWARD_SPLIT 0x400u
 
