@@ -149,3 +149,46 @@ def test_accumulation_window_equals_one_step_on_the_whole_batch(rule):
     assert torch.equal(acc.state0, one.state0)
     if acc.state1 is not None:
         assert torch.equal(acc.state1, one.state1)
+
+
+@pytest.mark.gpu
+def test_backward_allocates_no_weight_gradient():
+    # Proposition 3: the weight gradient never exists in HBM. Through the
+    # layer: no W.grad, and the backward pass allocates only dX (4 MB here),
+    # far below one fp32 gradient (64 MB). Through the C ABI with caller
+    # buffers: the call allocates nothing, from torch or from the driver.
+    dev = "cuda:0"
+    d_in, d_out, bt = 4096, 4096, 512
+    layer = ForgeLinear(d_in, d_out, device=dev)
+    mgr = ForgeStepManager(layer)
+    mgr.pre_step(lr=1e-3)
+    x = torch.randn(bt, d_in, device=dev).bfloat16().requires_grad_(True)
+    g = torch.randn(bt, d_out, device=dev).bfloat16()
+    layer(x).backward(g)                              # first call creates the shared workspace
+    mgr.pre_step()
+    x.grad = None
+    y = layer(x)
+    torch.cuda.synchronize()
+    torch.cuda.reset_peak_memory_stats()
+    base = torch.cuda.memory_allocated()
+    y.backward(g)
+    torch.cuda.synchronize()
+    F.sync_status()
+    assert layer.weight.grad is None
+    assert torch.cuda.max_memory_allocated() - base < (d_out * d_in * 4) // 8
+
+    X, dY = x.detach(), g
+    W = layer.weight.detach()
+    m, v = layer.state0, layer.state1
+    dX = torch.empty((bt, d_in), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(F.workspace_bytes(d_out, d_in, bt), dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    torch.cuda.reset_peak_memory_stats()
+    base = torch.cuda.memory_allocated()
+    for flags in (F.FLAG_BACKWARD_FUSED, F.FLAG_BACKWARD_SPLIT):
+        F.backward_step("adamw", X, dY, W, m, v, dX, lr=1e-3, step=3, workspace=ws, flags=flags)
+    torch.cuda.synchronize()
+    F.sync_status()
+    assert torch.cuda.max_memory_allocated() == base
+    assert torch.cuda.mem_get_info()[0] > free0 - 8 * 2 ** 20     # no driver-level allocation either
