@@ -57,6 +57,7 @@ struct DCfg {
   static constexpr int TMEM_COLS = 2 * BN;
   static constexpr uint32_t IDESC = make_idesc_bf16(BM, BN, 0, 1);
   static_assert(!F32W || BN == 128, "fp32 weight staging is sized for 128-column tiles");
+  static_assert(F32W || SA == SB, "bf16 weights: one empty barrier per stage serves both rings");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 };
 
@@ -182,8 +183,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dgrad_tc_kernel(const __grid_c
             }
             if (!ok) break;
           } else {
+            // bf16 weights: both rings have the same depth and one commit
+            // per stage releases the dY and W slots together (a_empty).
             const int s = static_cast<int>(k % SB);
-            if (!dwait(&b_empty[s], ((k / SB) & 1u) ^ 1u, abort_flag, p.status, WAIT_OP_EMPTY, lim)) {
+            if (!dwait(&a_empty[s], ((k / SB) & 1u) ^ 1u, abort_flag, p.status, WAIT_OP_EMPTY, lim)) {
               ok = false;
               break;
             }
@@ -240,7 +243,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dgrad_tc_kernel(const __grid_c
             umma_f16(d, ad0 + astep, bd0 + bstep, IDESC, (kb > 0 || kk > 0) ? 1u : 0u);
           }
           umma_commit(&a_empty[sa]);
-          umma_commit(&b_empty[sb]);
+          if constexpr (F32W) umma_commit(&b_empty[sb]);  // bf16: a_empty releases both slots
         }
         if (!ok) break;
         umma_commit(&tm_full[buf]);
