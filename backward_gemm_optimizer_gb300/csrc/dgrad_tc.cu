@@ -27,12 +27,13 @@ constexpr int BM = 128;
 constexpr int NUM_THREADS = 512;
 constexpr int CONV_THREADS = 256;          // warps 8-15
 
-// Three rings, each released by its own consumer, so that a load is never
-// held back by an unrelated stage: dY tiles (released by the MMA), fp32
-// staging tiles (released by the converters once read) and bf16 W tiles
-// (filled by TMA or by the converters, released by the MMA). Tiles are 128
-// tokens x BN input features: 128, or 256 for bf16 weights when the wider
-// tiles still fill the GPU (half the operand traffic of dY per output).
+// Rings: dY tiles and bf16 W tiles (filled by TMA, or by the converters
+// from the fp32 staging ring), of the same depth and released together by
+// one MMA commit per stage (a commit is not free: 68 -> 66 us with one
+// instead of two), and the fp32 staging tiles (released by the converters
+// once read). Tiles are 128 tokens x BN input features: 128, or 256 for
+// bf16 weights when the wider tiles still fill the GPU (half the operand
+// traffic of dY per output).
 template <bool F32W, int BN_>
 struct DCfg {
   static constexpr int BN = BN_;
@@ -57,7 +58,7 @@ struct DCfg {
   static constexpr int TMEM_COLS = 2 * BN;
   static constexpr uint32_t IDESC = make_idesc_bf16(BM, BN, 0, 1);
   static_assert(!F32W || BN == 128, "fp32 weight staging is sized for 128-column tiles");
-  static_assert(F32W || SA == SB, "bf16 weights: one empty barrier per stage serves both rings");
+  static_assert(SA == SB, "one empty barrier per stage serves the dY and the bf16 W ring");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 };
 
@@ -107,7 +108,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dgrad_tc_kernel(const __grid_c
   constexpr uint32_t IDESC = C::IDESC;
   constexpr int SA = C::SA, SB = C::SB, SS = C::SS > 0 ? C::SS : 1;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t a_full[SA], a_empty[SA], b_full[SB], b_empty[SB], s_full[SS], s_empty[SS];
+  __shared__ __align__(8) uint64_t a_full[SA], a_empty[SA], b_full[SB], s_full[SS], s_empty[SS];
   __shared__ __align__(8) uint64_t tm_full[2], tm_empty[2], drain_bar;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
@@ -122,7 +123,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dgrad_tc_kernel(const __grid_c
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < SA; ++s) { mbar_init(&a_full[s], 1); mbar_init(&a_empty[s], 1); }
-    for (int s = 0; s < SB; ++s) { mbar_init(&b_full[s], F32W ? CONV_THREADS : 1); mbar_init(&b_empty[s], 1); }
+    for (int s = 0; s < SB; ++s) mbar_init(&b_full[s], F32W ? CONV_THREADS : 1);
     for (int s = 0; s < SS; ++s) { mbar_init(&s_full[s], 1); mbar_init(&s_empty[s], CONV_THREADS); }
     for (int b = 0; b < 2; ++b) { mbar_init(&tm_full[b], 1); mbar_init(&tm_empty[b], 4); }
     mbar_init(&drain_bar, 1);
@@ -183,8 +184,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dgrad_tc_kernel(const __grid_c
             }
             if (!ok) break;
           } else {
-            // bf16 weights: both rings have the same depth and one commit
-            // per stage releases the dY and W slots together (a_empty).
+            // Both rings have the same depth and one commit per stage
+            // releases the dY and W slots together (a_empty).
             const int s = static_cast<int>(k % SB);
             if (!dwait(&a_empty[s], ((k / SB) & 1u) ^ 1u, abort_flag, p.status, WAIT_OP_EMPTY, lim)) {
               ok = false;
@@ -242,8 +243,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dgrad_tc_kernel(const __grid_c
             const uint64_t bstep = static_cast<uint64_t>((kk * 2048) >> 4);
             umma_f16(d, ad0 + astep, bd0 + bstep, IDESC, (kb > 0 || kk > 0) ? 1u : 0u);
           }
-          umma_commit(&a_empty[sa]);
-          if constexpr (F32W) umma_commit(&b_empty[sb]);  // bf16: a_empty releases both slots
+          umma_commit(&a_empty[sa]);  // releases the stage's dY slot and its bf16 W slot
         }
         if (!ok) break;
         umma_commit(&tm_full[buf]);
@@ -331,7 +331,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dgrad_tc_kernel(const __grid_c
         for (int half = 0; half < BK / C::STG_ROWS; ++half, ++ks) {
           const int ss = static_cast<int>(ks % SS);
           ok = dwait(&s_full[ss], (ks / SS) & 1u, abort_flag, p.status, WAIT_OP_FULL, lim) &&
-               (half > 0 || dwait(&b_empty[sb], ((k / SB) & 1u) ^ 1u, abort_flag, p.status, WAIT_OP_EMPTY, lim));
+               (half > 0 || dwait(&a_empty[sb], ((k / SB) & 1u) ^ 1u, abort_flag, p.status, WAIT_OP_EMPTY, lim));
           ok = __all_sync(0xFFFFFFFFu, ok);
           if (!ok) break;
           const uint8_t* stg = s_ring + ss * STG_BYTES;
