@@ -328,3 +328,20 @@ def test_backward_accumulate_rejects_what_it_cannot_do():
         F.backward_accumulate(X, dY, W, G, dX, workspace=small, flags=F.FLAG_BACKWARD_FUSED)
     assert ei.value.status == 1
     F.sync_status()
+
+
+def test_backward_accumulate_with_no_tokens():
+    # An empty micro-batch: the first of a window sets G_acc to zero, a later
+    # one leaves it as it is; dX is empty.
+    d_out, d_in = 256, 384
+    W = torch.zeros((d_out, d_in), device=DEV)
+    G = torch.full((d_out, d_in), 3.0, device=DEV)
+    X = torch.empty((0, d_in), dtype=torch.bfloat16, device=DEV)
+    dY = torch.empty((0, d_out), dtype=torch.bfloat16, device=DEV)
+    dX = torch.empty((0, d_in), dtype=torch.bfloat16, device=DEV)
+    F.backward_accumulate(X, dY, W, G, dX, overwrite=False)
+    F.sync_status()
+    assert torch.all(G == 3.0)
+    F.backward_accumulate(X, dY, W, G, dX, overwrite=True)
+    F.sync_status()
+    assert torch.all(G == 0.0)
