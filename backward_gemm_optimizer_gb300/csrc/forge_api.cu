@@ -473,7 +473,11 @@ forge_status wgrad_step(int opt, const forge_tensor* X, const forge_tensor* dY, 
   p.tiles_n = tiles_n;
   p.num_tiles = tiles_m * tiles_n;
   p.num_kb = static_cast<int>((bt + box_tokens - 1) / box_tokens);
-  p.group_m = 8;
+  // Grouped raster: tile rows per group. With 128 x 256 tiles (long token
+  // axes, operands far larger than L2) 16 rows keep fewer X column blocks
+  // live per window of in-flight tiles (BT 8192 up-projection: 791 -> 775 us
+  // with bf16 state); 8 elsewhere.
+  p.group_m = bn == 256 ? 16 : 8;
   p.step = static_cast<uint32_t>(step);
   p.seed_lo = static_cast<uint32_t>(seed);
   p.seed_hi = static_cast<uint32_t>(seed >> 32);
