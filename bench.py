@@ -677,6 +677,7 @@ def run_stack(args, rank, world, local_rank):
         eb = 4 if stname == "f32state" else 2
         sb = 2 * eb * (3 if two else 2)     # W and each moment read + written once
         ab = a["d_out"] * a["d_in"] * sb + 2 * bt * (a["d_out"] + 2 * a["d_in"])   # + X, dY read, dX written
+        a["backward_algorithmic_bytes"] = ab
         a["backward_GBps"] = round(ab / (a["backward_us"] * 1e-6) / 1e9, 1)
         a["backward_frac_of_hbm"] = round(a["backward_GBps"] / hbm, 4)
 
@@ -720,6 +721,12 @@ def run_stack(args, rank, world, local_rank):
     if rank != 0:
         return
     params = sum(a["d_out"] * a["d_in"] * a["n"] for a in per_shape.values())
+    # The whole stack against the measured HBM peak: every linear's state read
+    # and written once, X and dY read, dX written (the CUDA-graph time where
+    # it was taken, else the eager one).
+    stack_bytes = sum(a["backward_algorithmic_bytes"] * a["n"] for a in per_shape.values())
+    best_ms = graph_ms if graph_ms is not None else eager_ms
+    achieved = stack_bytes / (best_ms * 1e-3) / 1e9
     line = {
         "metric": METRIC, "value": round(eager_ms * 1000.0, 1), "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(eager_ms, 3), "higher_is_better": False, "scaling": "weak",
@@ -729,6 +736,9 @@ def run_stack(args, rank, world, local_rank):
                    "l2": "state 84 GB (fp32) / 42 GB (bf16) >> L2"},
         "graph_ms_per_step": round(graph_ms, 3) if graph_ms is not None else None,
         "split_ms_per_step": round(split_ms, 3),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(achieved / hbm, 4), "traffic": None, "algorithmic_bytes": stack_bytes,
+                     "timed": "CUDA graph" if graph_ms is not None else "eager"},
         "per_shape": per_shape, "gpu_launches": 2 * n_lin * K, "clocks": clocks,
     }
     print(json.dumps(line), flush=True)
