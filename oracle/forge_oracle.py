@@ -50,9 +50,9 @@ design notes of this library):
   a nonzero m never gets code 0 (it gets sign(m)); second moment:
   u = sqrt(v), s = absmax(u) / 255, code = clamp(rint(u / s), 1, 255)
   for v != 0 and 0 for v == 0; an all-zero block has scale 0. The stored
-  scale is s. Dequantisation: m = code * s, v = (code * s)^2. The code
-  decisions are taken in float32, the kernel's precision, with x / s
-  evaluated as x * fl(1/s) (one correctly rounded reciprocal per block);
+  scale is s. Dequantisation: m = code * s, v = (code * s)^2. Each code
+  is round(x / s) of the stored float32 x and s, rounded exactly (ties to
+  even), the paper's q(x) = s * round(x / s);
 * a NaN stored as bf16 with round-to-nearest-even becomes 0x7FFF.
 """
 
@@ -523,28 +523,48 @@ def _blocks(a: np.ndarray) -> np.ndarray:
     return a.reshape(rows, cols // QBLOCK, QBLOCK)
 
 
-def _inv(s: np.ndarray) -> np.ndarray:
-    """1/s correctly rounded in float32 (1 where s == 0; those blocks are all zero)."""
-    safe = np.where(s > 0, s, F32(1.0)).astype(np.float32)
-    return (F32(1.0) / safe).astype(np.float32)
+def round_quotient(x, s) -> np.ndarray:
+    """round(x / s) with ties to even, for float32 x and float32 s > 0.
+
+    This is the rounding of the paper's quantiser q(x) = s * round(x / s)
+    (Section 2.3; Appendix B, Proposition 4), decided on the exact quotient
+    of the two float32 numbers. The quotient is formed in float64, which
+    decides that rounding exactly for float32 operands with |x / s| < 2^9:
+
+    * an exact tie x / s = k + 1/2 is representable, so the correctly
+      rounded float64 quotient is that tie and ``rint`` sends it to the
+      even neighbour;
+    * otherwise 2x - (2k + 1) s is a nonzero multiple of the last-bit
+      value of the smaller-exponent operand, which puts x / s at least
+      2^-27 away from k + 1/2, far more than the float64 division's
+      error of at most 2^9 * 2^-53.
+
+    The brute-force check of this against exact rational arithmetic is in
+    the oracle's pin tests.
+    """
+    x64 = np.asarray(x, np.float32).astype(np.float64)
+    s64 = np.asarray(s, np.float32).astype(np.float64)
+    return np.rint(x64 / s64)
 
 
 def quant_m(m1) -> Tuple[np.ndarray, np.ndarray]:
     """First moment -> (int8 codes [rows, cols], scales [cols/128, rows]).
 
-    s = absmax / 127 (float32 division); code = clamp(rint(m * (1/s)), -127, 127)
-    with the float32 reciprocal 1/s taken once per block; a nonzero m whose
-    code rounds to 0 gets sign(m); all-zero block: s = 0.
+    s = absmax / 127 (float32 division); code = clamp(round(m / s), -127, 127)
+    with round the exact ties-to-even rounding of ``round_quotient``; a
+    nonzero m whose code rounds to 0 gets sign(m); a block whose scale is 0
+    (all zero) gets codes 0.
     """
     m1 = _f32(m1)
     b = _blocks(m1)
     amax = np.max(np.abs(b), axis=2)                    # [rows, nb] f32
     s = (amax / F32(127.0)).astype(np.float32)
-    q = np.rint((b * _inv(s)[:, :, None]).astype(np.float32))
+    pos = (s > 0)[:, :, None]
+    q = round_quotient(b, np.where(pos, s[:, :, None], F32(1.0)))
     q = np.clip(q, -127, 127)
     bump = (b != 0) & (q == 0)
     q = np.where(bump, np.sign(b), q)
-    q = np.where((s > 0)[:, :, None], q, 0)
+    q = np.where(pos, q, 0)
     codes = q.astype(np.int8).reshape(m1.shape)
     return codes, np.ascontiguousarray(s.T)
 
@@ -553,17 +573,19 @@ def quant_v(v1) -> Tuple[np.ndarray, np.ndarray]:
     """Second moment -> (uint8 codes of sqrt(v), scales [cols/128, rows]).
 
     u = sqrt(v) (float32); s = absmax(u) / 255; code = 0 for v == 0 and
-    clamp(rint(u * (1/s)), 1, 255) otherwise (zero code only for exact zero,
-    which floors a nonzero v away from zero).
+    clamp(round(u / s), 1, 255) otherwise, with the exact ties-to-even
+    rounding of ``round_quotient`` (zero code only for exact zero, which
+    floors a nonzero v away from zero).
     """
     v1 = _f32(v1)
     u = np.sqrt(v1)
     b = _blocks(u)
     amax = np.max(b, axis=2)
     s = (amax / F32(255.0)).astype(np.float32)
-    q = np.clip(np.rint((b * _inv(s)[:, :, None]).astype(np.float32)), 1, 255)
+    pos = (s > 0)[:, :, None]
+    q = np.clip(round_quotient(b, np.where(pos, s[:, :, None], F32(1.0))), 1, 255)
     q = np.where(_blocks(v1) == 0, 0, q)
-    q = np.where((s > 0)[:, :, None], q, 0)
+    q = np.where(pos, q, 0)
     codes = q.astype(np.uint8).reshape(v1.shape)
     return codes, np.ascontiguousarray(s.T)
 
@@ -776,3 +798,15 @@ def accumulated_step(opt: str, micro_batches, st: "State", h: Hyper, t: int, **k
 def dgrad_f64(dY, W) -> np.ndarray:
     """dX = dY W in float64 (Remark 1, Appendix A). dY: [BT, D_out], W: [D_out, D_in]."""
     return np.asarray(dY, np.float64) @ np.asarray(W, np.float64)
+
+
+def backward_step(opt: str, X, dY, st: "State", h: Hyper, t: int, **kw):
+    """The layer's whole backward pass: (dX, new stored state).
+
+    Remark 1 (Appendix A): the input gradient must be formed from the
+    weights the forward pass used, so dX = dY W_old is taken from the
+    stored W before the fused step overwrites it. Keyword arguments as for
+    ``step``.
+    """
+    dX = dgrad_f64(dY, load_w(st))
+    return dX, step(opt, X, dY, st, h, t, **kw)

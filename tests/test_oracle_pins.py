@@ -442,6 +442,140 @@ def test_q8_roundtrip_bounds_and_zero_codes():
     assert np.all(np.abs(ub - u)[floor] <= srow[floor] * (1 + 1e-5))
 
 
+def _exact_round_half_even(x, s):
+    """round(x / s), ties to even, in exact rational arithmetic."""
+    from fractions import Fraction
+    return round(Fraction(float(x)) / Fraction(float(s)))
+
+
+def _near_tie_pairs(rs, n, kmax):
+    """(x, s) float32 pairs whose quotient lies on or within a few float32
+    steps of a half-integer k + 1/2, |k| < kmax, plus exact ties."""
+    xs, ss = [], []
+    for _ in range(n):
+        s = np.float32(rs.uniform(0.5, 1.0) * 2.0 ** rs.randint(-40, 10))
+        k = rs.randint(-kmax, kmax)
+        x0 = np.float32((k + 0.5) * float(s))
+        x = x0
+        for d in range(-3, 4):
+            xs.append(x); ss.append(s)
+            x = np.nextafter(x, np.float32(np.inf)) if d >= 0 else x
+        xd = x0
+        for _ in range(3):
+            xd = np.nextafter(xd, np.float32(-np.inf))
+            xs.append(xd); ss.append(s)
+    # exact ties: s = 2^e * (odd / 2^j) with few bits, so (k + 1/2) s is a float32
+    for k in range(-kmax, kmax):
+        for e in (-30, -3, 0, 7):
+            s = np.float32(2.0 ** e * 3.0)
+            xs.append(np.float32((k + 0.5) * float(s))); ss.append(s)
+    return np.array(xs, np.float32), np.array(ss, np.float32)
+
+
+def test_q8_round_quotient_is_exact_on_near_ties():
+    # q(x) = s * round(x / s) (Section 2.3; Appendix B, Proposition 4): the
+    # oracle's rounding of x / s against exact rational arithmetic, on
+    # quotients on and next to half-integers and on random pairs.
+    rs = np.random.RandomState(41)
+    x, s = _near_tie_pairs(rs, 400, 256)
+    xr = (rs.randn(3000) * 1e-3).astype(np.float32)
+    sr = (np.abs(rs.randn(3000)) * 1e-5 + 1e-7).astype(np.float32)
+    keep = np.abs(xr.astype(np.float64) / sr) < 500
+    x = np.concatenate([x, xr[keep]]); s = np.concatenate([s, sr[keep]])
+    got = O.round_quotient(x, s)
+    want = np.array([_exact_round_half_even(a, b) for a, b in zip(x, s)], np.float64)
+    assert np.array_equal(got, want), np.argwhere(got != want)[:5]
+    # the set really holds exact ties and near misses on both sides
+    exact_tie = np.array([(2 * float(a)) / float(b) % 2 == 1 for a, b in zip(x, s)])
+    assert exact_tie.sum() > 100
+
+
+def _codes_by_rationals(x, which):
+    """The paper's block quantiser written out element by element with exact
+    rationals: scale s = fl32(absmax / 127) (m) or fl32(absmax(sqrt v) / 255)
+    (v), code = clamp(round(x / s)), ties to even, reserved zero code."""
+    rows, cols = x.shape
+    codes = np.zeros((rows, cols), np.int64)
+    for r in range(rows):
+        for b in range(cols // 128):
+            blk = x[r, b * 128:(b + 1) * 128]
+            if which == "m":
+                s = np.float32(np.float32(np.max(np.abs(blk))) / np.float32(127.0))
+                for j, e in enumerate(blk):
+                    if s == 0:
+                        c = 0
+                    else:
+                        c = max(-127, min(127, _exact_round_half_even(e, s)))
+                        if c == 0 and e != 0:
+                            c = 1 if e > 0 else -1
+                    codes[r, b * 128 + j] = c
+            else:
+                u = np.sqrt(blk.astype(np.float32))
+                s = np.float32(np.float32(np.max(u)) / np.float32(255.0))
+                for j, (e, ue) in enumerate(zip(blk, u)):
+                    c = 0 if (s == 0 or e == 0) else max(1, min(255, _exact_round_half_even(ue, s)))
+                    codes[r, b * 128 + j] = c
+    return codes
+
+
+def _planted_tie_block(rs, rows, which):
+    """Rows of 128-element blocks whose values sit on and next to code
+    boundaries of their own block scale (the largest element fixes s)."""
+    out = np.zeros((rows, 256), np.float32)
+    for r in range(rows):
+        for b in range(2):
+            top = np.float32(rs.uniform(0.5, 1.0) * 1e-3)
+            lim = 127 if which == "m" else 255
+            s = np.float32(top / np.float32(lim)) if which == "m" else np.float32(np.sqrt(top) / np.float32(lim))
+            vals = [top if which == "m" else top]
+            while len(vals) < 128:
+                k = rs.randint(-126 if which == "m" else 0, lim - 1)
+                t = np.float32((k + 0.5) * float(s))
+                for _ in range(rs.randint(0, 3)):
+                    t = np.nextafter(t, np.float32(np.inf if rs.rand() < 0.5 else -np.inf))
+                vals.append(t if which == "m" else np.float32(t) * np.float32(t))
+            blk = np.array(vals[:128], np.float32)
+            if which == "v":
+                blk = np.abs(blk)
+                blk[rs.randint(1, 128)] = 0.0
+            out[r, b * 128:(b + 1) * 128] = rs.permutation(blk)
+    return out
+
+
+def test_q8_codes_equal_the_exact_rule_elementwise():
+    rs = np.random.RandomState(42)
+    m = _planted_tie_block(rs, 6, "m")
+    m[0, :3] = 0.0
+    m[1, 128:] = 0.0
+    codes, s = O.quant_m(m)
+    assert np.array_equal(codes.astype(np.int64), _codes_by_rationals(m, "m"))
+    v = _planted_tie_block(rs, 6, "v")
+    vc, vs = O.quant_v(v)
+    assert np.array_equal(vc.astype(np.int64), _codes_by_rationals(v, "v"))
+
+
+def test_planted_reciprocal_quantiser_is_caught(monkeypatch):
+    # x * fl(1/s) rounded in float32 (a cheaper sequence) moves codes next to
+    # half-integers: the exact-rule pins must fail with it.
+    def recip(x, s):
+        x = np.asarray(x, np.float32); s = np.asarray(s, np.float32)
+        return np.rint((x * (np.float32(1.0) / s)).astype(np.float32)).astype(np.float64)
+    monkeypatch.setattr(O, "round_quotient", recip)
+    with pytest.raises(AssertionError):
+        test_q8_round_quotient_is_exact_on_near_ties()
+    with pytest.raises(AssertionError):
+        test_q8_codes_equal_the_exact_rule_elementwise()
+
+
+def test_planted_half_away_rounding_is_caught(monkeypatch):
+    def away(x, s):
+        q = np.asarray(x, np.float32).astype(np.float64) / np.asarray(s, np.float32).astype(np.float64)
+        return np.sign(q) * np.floor(np.abs(q) + 0.5)
+    monkeypatch.setattr(O, "round_quotient", away)
+    with pytest.raises(AssertionError):
+        test_q8_round_quotient_is_exact_on_near_ties()
+
+
 def test_q8_first_moment_drift_bound_prop4():
     # The stored 8-bit first moment stays within sum_k beta^(t-k) * e_k of the
     # fp32-state moment, with |e_k| <= s_k (s_k / 2 for round-to-nearest,
@@ -489,6 +623,62 @@ def test_q8_zero_rows_keep_zero_state_and_decay_only():
         else:                  # exact product, rounded once
             expect = ((1.0 - 1e-3 * 0.01) * W[2].astype(np.float64)).astype(np.float32)
         assert np.array_equal(out.W[2], expect)
+
+
+# ---------------------------------------------------------------------------
+# The input gradient (Appendix A, Remark 1): dX = dY W_old
+# ---------------------------------------------------------------------------
+
+def test_dgrad_brute_force_triple_loop():
+    rs = np.random.RandomState(51)
+    for (bt, d_out, d_in) in [(1, 1, 1), (2, 3, 5), (4, 2, 3), (6, 5, 7)]:
+        dY = rs.randn(bt, d_out)
+        W = rs.randn(d_out, d_in)
+        dX = O.dgrad_f64(dY, W)
+        assert dX.shape == (bt, d_in)
+        for t in range(bt):
+            for q in range(d_in):
+                acc = 0.0
+                for p in range(d_out):
+                    acc += dY[t, p] * W[p, q]
+                assert abs(dX[t, q] - acc) <= 1e-12 * (1 + abs(acc))
+
+
+def test_dgrad_hand_2x2():
+    # dY = [[1, 2], [3, 4]], W = [[5, 6], [7, 8]]: dX = dY W = [[19, 22], [43, 50]]
+    # (dY W^T would be [[17, 23], [39, 53]]).
+    dX = O.dgrad_f64(np.array([[1.0, 2.0], [3.0, 4.0]]), np.array([[5.0, 6.0], [7.0, 8.0]]))
+    assert np.array_equal(dX, np.array([[19.0, 22.0], [43.0, 50.0]]))
+
+
+def test_planted_transposed_weight_in_dgrad_is_caught(monkeypatch):
+    monkeypatch.setattr(O, "dgrad_f64", lambda dY, W: np.asarray(dY, float) @ np.asarray(W, float).T)
+    with pytest.raises(AssertionError):
+        test_dgrad_hand_2x2()
+
+
+@pytest.mark.parametrize("opt", ["adamw", "sgdm", "lion"])
+def test_backward_reads_the_weights_before_the_step(opt):
+    # Remark 1: dX comes from W_old. With lr != 0 the step moves W, so dY W_old
+    # and dY W_new differ; the oracle's backward pass must give the former.
+    rs = np.random.RandomState(52)
+    d_out, d_in, bt = 6, 5, 4
+    X = rs.randint(-3, 4, size=(bt, d_in)).astype(np.float32)
+    dY = rs.randint(-3, 4, size=(bt, d_out)).astype(np.float32)
+    W = rs.randint(-3, 4, size=(d_out, d_in)).astype(np.float32) * np.float32(0.25)
+    st = O.State(W=W.copy(), m=np.zeros((d_out, d_in), np.float32),
+                 v=np.zeros((d_out, d_in), np.float32) if opt == "adamw" else None)
+    h = O.Hyper(lr=0.5, beta1=0.9, beta2=0.99, eps=1e-8, weight_decay=0.1)
+    dX, new = O.backward_step(opt, X, dY, st, h, 1)
+    old = np.zeros((bt, d_in))
+    for t in range(bt):
+        for q in range(d_in):
+            old[t, q] = sum(float(dY[t, p]) * float(W[p, q]) for p in range(d_out))
+    assert np.array_equal(dX, old)
+    assert not np.array_equal(dX, dY.astype(np.float64) @ new.W.astype(np.float64))
+    # and the state is the plain step
+    ref = O.step(opt, X, dY, st, h, 1)
+    assert np.array_equal(new.W, ref.W)
 
 
 # ---------------------------------------------------------------------------
