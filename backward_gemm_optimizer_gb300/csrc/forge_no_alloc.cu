@@ -29,7 +29,11 @@ std::mutex g_scratch_mu;
 
 // Device address of the array on the current device. In host code the
 // array's name is only a host-side stand-in, so the address is asked of the
-// runtime, once per device, with that device current.
+// runtime, once per device, with that device current. Under lazy module
+// loading this first lookup is when the driver loads the module on the device
+// and reserves the array, so it is the call that can run out of memory. The
+// cached address belongs to the device's current context: a cudaDeviceReset
+// leaves it stale (the header tells callers not to reset and call again).
 forge_status scratch_address(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);

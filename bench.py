@@ -209,7 +209,7 @@ def run_reference(args, rank, world):
         "impl": "reference", "metric": METRIC, "value": round(v, 1), "unit": UNIT, "n_gpus": world,
         "steps": len(vals), "warmup": args.warmup, "ms_per_step": round(v / 1000, 3), "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": args.workload, "d_out": d_out, "d_in": d_in, "bt": bt, "w": w, "state": st},
+        "config": layer_config(args.workload, world),
         "cpu_baseline": {"value": round(v, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": f"rows 0..{rows} of W ({rows}/{d_out} of the layer), dgrad share + step, "
                                    f"float64 numpy, extrapolated x{d_out / rows:.2f}"},
@@ -219,6 +219,17 @@ def run_reference(args, rank, world):
 
 
 # --------------------------------------------------------------------------- ranks (replicas)
+
+
+def layer_config(workload: str, world: int) -> dict:
+    """The ``config`` of a single-layer workload's line (both arms print the same)."""
+    d_out, d_in, bt, w, st = WORKLOADS[workload]
+    return {"workload": workload, "d_out": d_out, "d_in": d_in, "bt": bt, "w_storage": w,
+            "moment_storage": st, "optimizer": "adamw",
+            "step": "forge_backward_step, fused input gradient (one pass over W)" if fused_path(bt, st) else
+                    "forge_dgrad + forge_wgrad_step_adamw",
+            "l2": "flushed between steps (256 MB write) and state 1.4 GB > L2",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
 
 
 def replica_seed(rank: int) -> int:
@@ -415,12 +426,7 @@ def run_gpu(args, rank, world, local_rank):
         "metric": METRIC, "value": round(us, 2), "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(us / 1000.0, 4), "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": args.workload, "d_out": d_out, "d_in": d_in, "bt": bt, "w_storage": w,
-                   "moment_storage": st, "optimizer": "adamw",
-                   "step": "forge_backward_step, fused input gradient (one pass over W)" if fused else
-                           "forge_dgrad + forge_wgrad_step_adamw",
-                   "l2": "flushed between steps (256 MB write) and state 1.4 GB > L2",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "config": layer_config(args.workload, world),
         "step_median_us": round(med_us, 2),
         "roofline_us": round(t_roof, 2), "frac_of_roofline": round(t_roof / kern_us, 4),
         "GBps": round(achieved, 1), "TFLOPs": round(tfl, 1),

@@ -349,6 +349,13 @@ forge_status forge_wgrad_step_accumulated(forge_rule rule, const forge_tensor* X
  *
  * The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * With CUDA's lazy module loading that first call is also when the driver
+ * loads this part of the library on the device and reserves the 64 MiB, so
+ * it can fail (FORGE_ERR_CUDA) if the device is already full: make it at
+ * start-up, before a framework allocator takes the device's memory. The
+ * address is kept per device for the life of the process; after a
+ * cudaDeviceReset it no longer points at the array, so do not call this
+ * entry point again in a process that has reset the device.
  * All calls share the one array and it keeps what the last call left
  * there; nothing in it needs to start at zero, since every partial sum is
  * written before it is read. Calls whose kernels overlap on the GPU (on

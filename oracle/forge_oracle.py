@@ -644,28 +644,36 @@ def load_v(st: State) -> np.ndarray:
     return bf16_bits_to_f32(st.v) if st.state == "bf16" else _f32(st.v)
 
 
-def _store_w(W1, st: State, mode: str, sr: bool, seed: int, t: int):
+def row_draws(seed: int, t: int, site: int, shape, rows=None) -> np.ndarray:
+    """The stochastic-rounding draws of a [r, c] array of whole rows: rows
+    0 .. r-1 of the tensor, or the global rows ``rows`` of a tensor whose
+    rows have c elements (a sample of rows of a larger layer)."""
+    r, c = shape
+    if rows is None:
+        return sr_draws(seed, t, site, r, c)
+    return np.stack([sr_draws(seed, t, site, 1, c, row0=int(p), total_cols=c)[0] for p in rows])
+
+
+def _store_w(W1, st: State, mode: str, sr: bool, seed: int, t: int, rows=None):
     if st.w_dtype == "f32":
         return np.asarray(W1).astype(np.float32)
     if sr:
         w32 = np.asarray(W1).astype(np.float32)
-        rows, cols = w32.shape
-        return f32_to_bf16_sr(w32, sr_draws(seed, t, SITE_W, rows, cols))
+        return f32_to_bf16_sr(w32, row_draws(seed, t, SITE_W, w32.shape, rows))
     if mode == "f64":
         return f64_to_bf16_rne(W1)
     return f32_to_bf16_rne(W1)
 
 
-def _store_moment(x1, which: str, st: State, mode: str, sr: bool, seed: int, t: int):
+def _store_moment(x1, which: str, st: State, mode: str, sr: bool, seed: int, t: int, rows=None):
     """Returns (stored array, scale or None)."""
     if st.state == "f32":
         return np.asarray(x1).astype(np.float32), None
     if st.state == "bf16":
         if sr:
             x32 = np.asarray(x1).astype(np.float32)
-            rows, cols = x32.shape
             site = SITE_M if which == "m" else SITE_V
-            return f32_to_bf16_sr(x32, sr_draws(seed, t, site, rows, cols)), None
+            return f32_to_bf16_sr(x32, row_draws(seed, t, site, x32.shape, rows)), None
         if mode == "f64":
             return f64_to_bf16_rne(x1), None
         return f32_to_bf16_rne(x1), None
@@ -677,7 +685,7 @@ def _store_moment(x1, which: str, st: State, mode: str, sr: bool, seed: int, t: 
 
 def step(opt: str, X, dY, st: State, h: Hyper, t: int, *, seed: int = 0,
          sr_w: bool = False, sr_moments: bool = False, mode: str = "f64",
-         G: Optional[np.ndarray] = None) -> State:
+         G: Optional[np.ndarray] = None, rows: Optional[np.ndarray] = None) -> State:
     """One fused step of ``opt`` ("adamw", "sgdm", "lion"); returns the new stored state.
 
     mode "f64": Phase 2 in float64 from the exactly upcast stored state,
@@ -685,6 +693,9 @@ def step(opt: str, X, dY, st: State, h: Hyper, t: int, *, seed: int = 0,
     mode "f32emu": G rounded to float32, Phase 2 as the float32 op
     sequence of ``adamw_f32`` / ``sgdm_f32`` / ``lion_f32``.
     ``G`` may be given to skip Phase 1 (it must equal dY^T X).
+    ``rows``: when the state holds a sample of whole rows of a larger layer,
+    their global row indices (the stochastic-rounding streams are keyed on
+    the element's index in the whole layer).
     """
     if G is None:
         G = wgrad_f64(dY, X)
@@ -736,12 +747,12 @@ def step(opt: str, X, dY, st: State, h: Hyper, t: int, *, seed: int = 0,
     else:
         raise ValueError(mode)
 
-    Wn = _store_w(W1, st, mode, sr_w, seed, t)
+    Wn = _store_w(W1, st, mode, sr_w, seed, t, rows)
     mn = msn = vn = vsn = None
     if m1 is not None:
-        mn, msn = _store_moment(m1, "m", st, mode, sr_moments, seed, t)
+        mn, msn = _store_moment(m1, "m", st, mode, sr_moments, seed, t, rows)
     if v1 is not None:
-        vn, vsn = _store_moment(v1, "v", st, mode, sr_moments, seed, t)
+        vn, vsn = _store_moment(v1, "v", st, mode, sr_moments, seed, t, rows)
     return State(W=Wn, m=mn, v=vn, m_scale=msn, v_scale=vsn, w_dtype=st.w_dtype, state=st.state)
 
 

@@ -127,16 +127,50 @@ def _vals(x, kind):
     return np.asarray(x, np.float64)
 
 
+# Parity bounds for stored bf16 values (the oracle's reading of Appendix C,
+# Proposition 5, and of the storage rules): the GPU's stored value must be the
+# storage rounding (round-to-nearest-even, or stochastic rounding with the
+# element's own draw) of some value within the fp32 tolerance of the exact
+# result. Both roundings are monotone, so that set is the interval between
+# the roundings of (exact - tol) and (exact + tol): where the tolerance is far
+# below an ulp this means "equal", and a difference is allowed only where the
+# tolerance window straddles a rounding boundary. Stochastically rounded
+# weights besides differ from the oracle's in at most BF16_SR_MISMATCH_MAX of
+# the elements. 8-bit codes differ by at most one step, in at most
+# CODE_MISMATCH_MAX of the elements (random inputs), and not at all when the
+# quantiser sees the same fp32 inputs (exact gradients: bit-exact tests).
+BF16_SR_MISMATCH_MAX = 1e-4
+CODE_MISMATCH_MAX = 1e-4
+
+
+def bf16_window(x64, tol, r16=None):
+    """(lo, hi) bf16 values: the storage rounding of x64 -/+ tol.
+
+    The GPU rounds an fp32 value y with |y - x64| <= tol; rounding to fp32
+    and then to bf16 are both monotone, so its stored value lies between the
+    roundings of fp32(x64 - tol) and fp32(x64 + tol)."""
+    a = (np.asarray(x64, np.float64) - tol).astype(np.float32)
+    b = (np.asarray(x64, np.float64) + tol).astype(np.float32)
+    if r16 is None:
+        lo, hi = O.f32_to_bf16_rne(a), O.f32_to_bf16_rne(b)
+    else:
+        lo, hi = O.f32_to_bf16_sr(a, r16), O.f32_to_bf16_sr(b, r16)
+    return O.bf16_bits_to_f32(lo).astype(np.float64), O.bf16_bits_to_f32(hi).astype(np.float64)
+
+
 def check_tolerance(opt, prob, w_dtype, state, t, got: O.State, *, seed=0, sr_w=False, sr_moments=False,
-                    hyper=None, rtol=1e-5):
-    """Compare a random-input GPU step with the float64 oracle; returns a report dict."""
+                    hyper=None, rtol=1e-5, rows=None):
+    """Compare a random-input GPU step with the float64 oracle; returns a report dict.
+
+    ``rows``: the global row indices when ``prob`` holds a sample of rows of a
+    larger layer (the stochastic-rounding streams are keyed on them)."""
     hp = dict(HYPER[opt] if hyper is None else hyper)
     h = O.Hyper(**hp)
     st = oracle_state(prob, w_dtype, state, opt)
     Xn = prob.X.float().numpy(); dYn = prob.dY.float().numpy()
     G = O.wgrad_f64(dYn, Xn)
     A = O.abs_wgrad_f64(dYn, Xn)
-    ref = O.step(opt, None, None, st, h, t, seed=seed, sr_w=sr_w, sr_moments=sr_moments, G=G)
+    ref = O.step(opt, None, None, st, h, t, seed=seed, sr_w=sr_w, sr_moments=sr_moments, G=G, rows=rows)
     W0 = O.load_w(st)
     m0 = O.load_m(st) if NSTATE[opt] >= 1 else None
     if opt == "adamw":
@@ -149,43 +183,46 @@ def check_tolerance(opt, prob, w_dtype, state, t, got: O.State, *, seed=0, sr_w=
         v0 = O.load_v(st) if NSTATE[opt] == 2 else None
         tw, tm, tv = T.generic_tol(opt, W0, m0, v0, G, A, h, t, rtol)
     rep = {}
+    exact = O.step_values(opt, None, None, st, h, t, G=G)
 
-    def cmp(name, g, r, tol, kind):
+    def cmp(name, g, r, tol, kind, site=None, sr=False):
         if kind == "f32":
             rep[name] = T.rel_violation(g, r, tol)
             assert rep[name] <= 1.0, f"{name}: {rep[name]:.3f} of the tolerance"
         elif kind == "bf16":
-            # The stored bf16 value is the fp32 result rounded once: within the
-            # fp32 tolerance plus one bf16 ulp (where there is no cancellation
-            # the tolerance is far below an ulp, so that is "within 1 ulp").
+            x64 = exact[{"W": 0, "m": 1, "v": 2}[name]]
+            r16 = O.row_draws(seed, t, site, np.shape(g), rows) if sr else None
+            lo, hi = bf16_window(x64, tol, r16)
             gv = O.bf16_bits_to_f32(g).astype(np.float64)
-            rv = O.bf16_bits_to_f32(r).astype(np.float64)
-            ulp = np.maximum(T.bf16_ulp(g), T.bf16_ulp(r))
-            rep[name] = T.rel_violation(gv, rv, tol + ulp)
+            outside = (gv < lo) | (gv > hi)
             d = T.bf16_ulp_distance(g, r)
+            rep[name + "_outside_window"] = int(outside.sum())
             rep[name + "_max_ulp"] = int(d.max()) if d.size else 0
             rep[name + "_mismatch"] = float(np.mean(d != 0)) if d.size else 0.0
-            rep[name + "_beyond_1ulp"] = float(np.mean(d > 1)) if d.size else 0.0
-            assert rep[name] <= 1.0, f"{name}: {rep[name]:.3f} of (tolerance + 1 ulp)"
-            assert rep[name + "_beyond_1ulp"] <= 1e-3, rep
-            assert rep[name + "_mismatch"] <= 1e-2, rep
+            assert rep[name + "_outside_window"] == 0, (name, np.argwhere(outside)[:3].tolist(), rep)
+            if sr and name == "W" and np.shape(prob.X)[0] <= 2048:
+                # The share bound presumes the GPU's pre-rounding value is a few
+                # fp32 ulps from the oracle's. Past ~2048 tokens the fp32 sum of
+                # G (in another order) moves it further (BT 8192 measured
+                # 1.2e-4), and only the window above applies.
+                assert rep[name + "_mismatch"] <= BF16_SR_MISMATCH_MAX, rep
 
-    cmp("W", got.W, ref.W, tw, w_dtype)
+    cmp("W", got.W, ref.W, tw, w_dtype, O.SITE_W, sr_w)
     if state in ("f32", "bf16"):
         if ref.m is not None:
-            cmp("m", got.m, ref.m, tm, state)
+            cmp("m", got.m, ref.m, tm, state, O.SITE_M, sr_moments)
         if ref.v is not None:
-            cmp("v", got.v, ref.v, tv, state)
+            cmp("v", got.v, ref.v, tv, state, O.SITE_V, sr_moments)
     else:
         # 8-bit: codes within one step of the oracle's, rare differences.
         dm = np.abs(got.m.astype(np.int32) - ref.m.astype(np.int32))
         rep["m_code_max"] = int(dm.max()); rep["m_code_mismatch"] = float(np.mean(dm != 0))
-        assert rep["m_code_max"] <= 1 and rep["m_code_mismatch"] <= 1e-2, rep
+        assert rep["m_code_max"] <= 1 and rep["m_code_mismatch"] <= CODE_MISMATCH_MAX, rep
         np.testing.assert_allclose(got.m_scale, ref.m_scale, rtol=1e-4, atol=1e-30)
         if opt == "adamw":
             dv = np.abs(got.v.astype(np.int32) - ref.v.astype(np.int32))
             rep["v_code_max"] = int(dv.max()); rep["v_code_mismatch"] = float(np.mean(dv != 0))
-            assert rep["v_code_max"] <= 1 and rep["v_code_mismatch"] <= 1e-2, rep
+            assert rep["v_code_max"] <= 1 and rep["v_code_mismatch"] <= CODE_MISMATCH_MAX, rep
             np.testing.assert_allclose(got.v_scale, ref.v_scale, rtol=1e-4, atol=1e-30)
             # the reserved zero code: exactly the zero moments
             assert np.array_equal(got.v == 0, ref.v == 0)

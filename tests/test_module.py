@@ -192,3 +192,62 @@ def test_backward_allocates_no_weight_gradient():
     F.sync_status()
     assert torch.cuda.max_memory_allocated() == base
     assert torch.cuda.mem_get_info()[0] > free0 - 8 * 2 ** 20     # no driver-level allocation either
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("rule,wdt,sdt", [("adamw", torch.float32, torch.float32),
+                                          ("lion", torch.bfloat16, torch.bfloat16),
+                                          ("sgdm", torch.float32, torch.float32)],
+                         ids=["adamw-f32", "lion-bf16-sr", "sgdm-f32"])
+def test_layer_matches_oracle_over_steps_with_changing_lr(rule, wdt, sdt):
+    # The user-facing layer (ForgeLinear + ForgeStepManager.pre_step(lr=...))
+    # against the CPU oracle: three backward passes with a different learning
+    # rate each, fresh seeded inputs each step. After every step the layer's
+    # W and moments are one oracle step (at the manager's 1-based step count
+    # and lr) from the state before it, and dX is dY W_old (Appendix A,
+    # Remark 1). A wrong step counter, a stale lr or a dX from the updated
+    # weights fails the comparison.
+    import numpy as np
+    import oracle.forge_oracle as O
+    from backward_gemm_optimizer_gb300 import synthetic as S
+    from forge_cases import HYPER, check_tolerance, to_np
+
+    dev = "cuda:0"
+    d_in, d_out, bt = 384, 256, 200
+    torch.manual_seed(3)
+    layer = ForgeLinear(d_in, d_out, rule=rule, weight_dtype=wdt, state_dtype=sdt, device=dev)
+    hp = dict(HYPER[rule])
+    mgr = ForgeStepManager(layer)
+    c = mgr.config
+    c.beta1, c.beta2, c.eps, c.weight_decay = hp["beta1"], hp["beta2"], hp["eps"], hp["weight_decay"]
+    c.sr_w, c.seed = wdt == torch.bfloat16, 99
+    w_kind = "bf16" if wdt == torch.bfloat16 else "f32"
+    s_kind = "bf16" if sdt == torch.bfloat16 else "f32"
+    with torch.no_grad():   # non-zero moments from the start, so the bias corrections matter
+        layer.state0.copy_(S.normal((d_out, d_in), 1e-3, 5, S.STREAM_M, s_kind).to(dev))
+        if layer.state1 is not None:
+            layer.state1.copy_(S.abs_normal((d_out, d_in), 1e-6, 5, S.STREAM_V, s_kind).to(dev))
+    lrs = [hp["lr"], hp["lr"] * 0.5, hp["lr"] * 0.2]
+    for t, lr in enumerate(lrs, start=1):
+        X, dY = S.step_inputs(d_out, d_in, bt, 11, t, "bf16")
+        prob = S.LinearProblem(X=X, dY=dY, W=layer.weight.detach().cpu().clone(),
+                               m=layer.state0.detach().cpu().clone(),
+                               v=None if layer.state1 is None else layer.state1.detach().cpu().clone())
+        mgr.pre_step(lr=lr)
+        assert c.step == t and c.lr == lr
+        x = X.to(dev).requires_grad_(True)
+        y = layer(x)
+        y.backward(dY.to(dev))
+        torch.cuda.synchronize()
+        F.sync_status()
+        assert layer.weight.grad is None
+        got = O.State(W=to_np(layer.weight), m=to_np(layer.state0),
+                      v=None if layer.state1 is None else to_np(layer.state1))
+        rep = check_tolerance(rule, prob, w_kind, s_kind, t, got, seed=99, sr_w=c.sr_w,
+                              hyper={**hp, "lr": lr})
+        w16 = O.bf16_bits_to_f32(O.f32_to_bf16_rne(prob.W.float().numpy())).astype(np.float64)
+        ref = O.dgrad_f64(dY.float().numpy(), w16)
+        tol = 1e-5 * (np.abs(dY.float().numpy()).astype(np.float64) @ np.abs(w16)) + np.abs(ref) * 2 ** -8
+        viol = float(np.max(np.abs(x.grad.float().cpu().numpy() - ref) / np.maximum(tol, 1e-300)))
+        assert viol <= 1.0, (t, viol)
+        print(rule, "step", t, "lr", lr, rep, "dX", viol)

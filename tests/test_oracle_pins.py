@@ -396,6 +396,8 @@ def test_sr_draw_stream_mapping():
     sub = O.sr_draws(seed, t, site, 2, 5, row0=1, col0=9, total_cols=cols)
     assert np.array_equal(sub, r[1:3, 9:14])
     # different step / site / seed give different streams
+    # a sample of whole rows draws what those rows of the whole tensor draw
+    assert np.array_equal(O.row_draws(seed, t, site, (2, cols), rows=[0, 2]), r[[0, 2]])
     assert not np.array_equal(r, O.sr_draws(seed, t + 1, site, rows, cols))
     assert not np.array_equal(r, O.sr_draws(seed, t, site + 1, rows, cols))
     assert not np.array_equal(r, O.sr_draws(seed + 1, t, site, rows, cols))

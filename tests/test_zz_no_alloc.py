@@ -42,8 +42,18 @@ def test_no_alloc_matches_backward_step_on_two_calls(shape):
         dx_got = torch.full((bt, d_in), float("nan"), dtype=torch.float32, device=DEV)
         F.backward_step("adamw", X, dY, ref[0], ref[1], ref[2], dx_ref, step=t, workspace=ws,
                         flags=F.FLAG_BACKWARD_FUSED, **HP)
+        torch.cuda.synchronize()
+        torch.cuda.reset_peak_memory_stats(DEV)
+        base = torch.cuda.max_memory_allocated(DEV)
+        free0 = torch.cuda.mem_get_info(DEV)[0]
         F.backward_step_no_alloc("adamw", X, dY, got[0], got[1], got[2], dx_got, step=t, **HP)
         F.sync_status()
+        if t == 2:
+            # The defining property: once the array is loaded (first call), a
+            # call allocates nothing, neither from torch's allocator nor from
+            # the driver.
+            assert torch.cuda.max_memory_allocated(DEV) == base
+            assert torch.cuda.mem_get_info(DEV)[0] > free0 - (8 << 20)
         # Same kernels, same inputs, fixed summation order: identical bits.
         for a, b, name in zip(got + [dx_got], ref + [dx_ref], ("W", "m", "v", "dX")):
             assert np.array_equal(_bits(a), _bits(b)), f"call {t}: {name} differs"
