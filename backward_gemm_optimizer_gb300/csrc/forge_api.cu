@@ -248,6 +248,8 @@ const char* opt_name(int opt) {
 int mkind(int dt) { return dt == FORGE_F32 ? M_F32 : dt == FORGE_BF16 ? M_BF16 : M_Q8; }
 
 constexpr uint64_t kTimeoutNs = 4000000000ull;  // 4 s: far beyond any healthy wait
+constexpr int64_t kOperandHintBytes = int64_t(48) << 20;  // X + dY up to 48 MB: well inside L2
+constexpr size_t kDxL2SlabBytes = size_t(16) << 20;        // dX partial slabs kept in L2 up to 16 MB
 
 // ------------------------------------------------------------------ fused input gradient: geometry
 
@@ -485,6 +487,24 @@ forge_status wgrad_step(int opt, const forge_tensor* X, const forge_tensor* dY, 
   p.sr_m = h->sr_moments ? 1 : 0;
   p.flags = h->flags;
   p.timeout_ns = kTimeoutNs;
+  // Operands that fit comfortably in L2 are loaded evict-last: every tile of
+  // a row (column) of tiles re-reads the same dY (X) slabs while the state
+  // streams through L2 once and would otherwise push them out (up-projection
+  // BT 512: fused backward 68 MB fewer DRAM reads, 290 -> 283 us; split step
+  // 262 -> 239 us). Not for the fused pass with bf16 weights, where it
+  // measured 235 -> 239 us.
+  const int64_t op_bytes = 2 * bt * (d_in + d_out);
+  if (bt > 0 && op_bytes <= kOperandHintBytes && !(dx != nullptr && wk == W_BF16)) {
+    p.op_hint = 1;
+    const forge_tensor* ops[2] = {X, dY};
+    for (int i = 0; i < 2; ++i) {
+      const uintptr_t a = reinterpret_cast<uintptr_t>(ops[i]->data);
+      const uintptr_t e = a + static_cast<uintptr_t>((ops[i]->rows - 1) * ops[i]->ld + ops[i]->cols) * 2u;
+      p.op_lo[i] = reinterpret_cast<const uint8_t*>((a + 127u) & ~uintptr_t(127));   // whole lines only
+      p.op_hi[i] = reinterpret_cast<const uint8_t*>(e & ~uintptr_t(127));
+      if (p.op_hi[i] < p.op_lo[i]) p.op_hi[i] = p.op_lo[i];
+    }
+  }
 
   TcLaunch l{};
   l.opt = opt; l.wk = wk; l.mk = mk; l.bn = bn; l.deep = deep; l.dx = dx != nullptr ? 1 : 0;
@@ -507,6 +527,9 @@ forge_status wgrad_step(int opt, const forge_tensor* X, const forge_tensor* dY, 
     p.dx_ws = static_cast<float*>(dx->ws);
     p.dx_runs = g.runs;
     p.dx_slab = g.slab;
+    // Small slab sets stay in L2 until the reduction reads and drops them
+    // (whole lines only: a 128-byte aligned workspace).
+    p.dx_l2 = (g.bytes <= kDxL2SlabBytes && reinterpret_cast<uintptr_t>(dx->ws) % 128 == 0) ? 1 : 0;
   }
   cudaError_t e;
   switch (opt) {
@@ -534,6 +557,7 @@ forge_status wgrad_step(int opt, const forge_tensor* X, const forge_tensor* dY, 
     r.grid = g.grid;
     r.runs = g.runs;
     r.slab = g.slab;
+    r.discard = p.dx_l2;
     e = launch_dx_reduce(r, dev->sms, s);
     if (e != cudaSuccess) return fail(FORGE_ERR_CUDA, "%s: dX reduction launch: %s", oname, cudaGetErrorString(e));
   }

@@ -55,12 +55,20 @@ struct alignas(128) WgradTcParams {
   int sr_w, sr_m;
   uint32_t flags;
   uint64_t timeout_ns;
+  // Operand residency: with op_hint the X / dY loads carry an L2 evict-last
+  // policy (every tile of a column / row re-reads them, while the state
+  // streams through L2 once); at the end each CTA returns its share of the
+  // operands' whole 128-byte lines, [op_lo[i], op_hi[i]), to normal priority.
+  int op_hint;
+  const uint8_t* op_lo[2];
+  const uint8_t* op_hi[2];
   // Fused input gradient (DX kernels only).
   void* w_ptr;        // W_old, read by the converters
   int64_t ld_w;
   float* dx_ws;       // workspace: [grid][dx_runs] slabs of dx_slab floats
   int dx_runs;        // column runs per CTA (slab slots)
   int64_t dx_slab;    // floats per slab: num_kb * 128 * 64
+  int dx_l2;          // 1: slabs are stored evict-last (the reduction reads them from L2 and drops them)
 };
 
 // Deterministic reduction of the dX partial slabs into dX.
@@ -72,6 +80,7 @@ struct DxReduceParams {
   int bt, d_in;
   int tiles_m, num_tiles, grid, runs;
   int64_t slab;
+  int discard;        // 1: drop each slab line from L2 once read (the slabs are dead scratch)
 };
 
 // fp32 fused step (fp32 X / dY), plain CUDA cores.

@@ -68,6 +68,42 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
+// The same load with an L2 cache policy (a createpolicy operand).
+__device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* map, uint64_t* bar, int32_t x,
+                                                 int32_t y, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "l"(policy)
+      : "memory");
+}
+
+// L2 policy: keep the lines in L2 ahead of lines of normal priority.
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// 16-byte global store with an L2 cache policy.
+__device__ __forceinline__ void st_global_v4_hint(float* dst, float a, float b, float c, float d, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(dst), "f"(a), "f"(b), "f"(c),
+               "f"(d), "l"(policy)
+               : "memory");
+}
+
+// Drops the 128-byte L2 line at `line` (128-byte aligned) without writing it
+// back: its contents become undefined. For scratch data that is dead.
+__device__ __forceinline__ void l2_discard_line(const void* line) {
+  asm volatile("discard.global.L2 [%0], 128;" ::"l"(reinterpret_cast<uint64_t>(line)) : "memory");
+}
+
+// Returns the 128-byte L2 line at `line` to normal eviction priority.
+__device__ __forceinline__ void l2_demote_line(const void* line) {
+  asm volatile("applypriority.global.L2::evict_normal [%0], 128;" ::"l"(reinterpret_cast<uint64_t>(line))
+               : "memory");
+}
+
 // 2-D tiled store shared -> global (elements outside the tensor are clipped).
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int32_t x, int32_t y) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(

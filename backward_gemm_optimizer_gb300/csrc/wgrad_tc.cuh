@@ -260,21 +260,29 @@ __device__ __forceinline__ void walk_coords(const WgradTcParams& p, int tile, in
 // memory to its workspace slab: the warp with TMEM lane quadrant q writes
 // tokens 32q .. 32q + 31 of every 128-token block, one token row per
 // thread. Runs once per tile column of the CTA.
+// With l2 the slab is stored evict-last, and the reduction that follows this
+// kernel reads it from L2 and drops it, so that it need not reach DRAM.
 template <int BN>
-__device__ __forceinline__ void write_dx_partial(float* slab, uint32_t tmem_dx, int q, int lane, int num_kb) {
+__device__ __forceinline__ void write_dx_partial(float* slab, uint32_t tmem_dx, int q, int lane, int num_kb,
+                                                 bool l2) {
+  const uint64_t pol = l2_policy_evict_last();
   for (int b = 0; b < num_kb; ++b) {
     const int tok = b * 128 + q * 32 + lane;
     const uint32_t ta = tmem_dx + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(b * BN);
-    float4* dst = reinterpret_cast<float4*>(slab + static_cast<int64_t>(tok) * BN);
+    float* dst = slab + static_cast<int64_t>(tok) * BN;
 #pragma unroll 1
     for (int c16 = 0; c16 < BN / 16; ++c16) {
       uint32_t d[16];
       tmem_ld_32x32b_x16(ta + c16 * 16, d);
       tmem_ld_wait();
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        dst[c16 * 4 + j] = make_float4(__uint_as_float(d[4 * j]), __uint_as_float(d[4 * j + 1]),
-                                       __uint_as_float(d[4 * j + 2]), __uint_as_float(d[4 * j + 3]));
+      for (int j = 0; j < 4; ++j) {
+        float* o = dst + c16 * 16 + 4 * j;
+        const float a = __uint_as_float(d[4 * j]), bb = __uint_as_float(d[4 * j + 1]);
+        const float c = __uint_as_float(d[4 * j + 2]), e = __uint_as_float(d[4 * j + 3]);
+        if (l2) st_global_v4_hint(o, a, bb, c, e, pol);
+        else *reinterpret_cast<float4*>(o) = make_float4(a, bb, c, e);
+      }
     }
   }
 }
@@ -445,14 +453,37 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, N
           uint8_t* a = op_base + s * C::STAGE_BYTES;
           uint8_t* b = a + C::A_BYTES;
           mbar_arrive_expect_tx(&op_full[s], C::STAGE_BYTES);
-          tma_load_2d(a, &p.tm_dy, &op_full[s], tm * C::BM, kb * C::BK);
-          tma_load_2d(a + C::BOX, &p.tm_dy, &op_full[s], tm * C::BM + 64, kb * C::BK);
+          if (p.op_hint) {
+            const uint64_t pol = l2_policy_evict_last();
+            tma_load_2d_hint(a, &p.tm_dy, &op_full[s], tm * C::BM, kb * C::BK, pol);
+            tma_load_2d_hint(a + C::BOX, &p.tm_dy, &op_full[s], tm * C::BM + 64, kb * C::BK, pol);
 #pragma unroll
-          for (int bb = 0; bb < BN / 64; ++bb)
-            tma_load_2d(b + bb * C::BOX, &p.tm_x, &op_full[s], tn * BN + bb * 64, kb * C::BK);
+            for (int bb = 0; bb < BN / 64; ++bb)
+              tma_load_2d_hint(b + bb * C::BOX, &p.tm_x, &op_full[s], tn * BN + bb * 64, kb * C::BK, pol);
+          } else {
+            tma_load_2d(a, &p.tm_dy, &op_full[s], tm * C::BM, kb * C::BK);
+            tma_load_2d(a + C::BOX, &p.tm_dy, &op_full[s], tm * C::BM + 64, kb * C::BK);
+#pragma unroll
+            for (int bb = 0; bb < BN / 64; ++bb)
+              tma_load_2d(b + bb * C::BOX, &p.tm_x, &op_full[s], tn * BN + bb * 64, kb * C::BK);
+          }
         }
       }
       if (!ok) drain_ring(op_full, STAGES, kseq, p.status);
+    }
+    if (p.op_hint) {
+      // This CTA's share of the operands' lines back to normal priority, so
+      // that evict-last lines do not pile up in L2 across calls.
+      __syncwarp();
+#pragma unroll 1
+      for (int i = 0; i < 2; ++i) {
+        // fewer than 2^19 lines (the host takes operands of at most 48 MB)
+        const uint32_t lines = static_cast<uint32_t>((p.op_hi[i] - p.op_lo[i]) >> 7);
+        const uint32_t l1 = lines * (blockIdx.x + 1) / gridDim.x;
+        const uint8_t* base = p.op_lo[i];
+#pragma unroll 1
+        for (uint32_t l = lines * blockIdx.x / gridDim.x + lane; l < l1; l += 32) l2_demote_line(base + (l << 7));
+      }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (weight gradient)
@@ -752,8 +783,8 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, N
           au = fmaxf(au, red_sh[it & 1][1][k][r]);
         }
         // sqrt is monotonic and correctly rounded: max sqrt(v') = sqrt(max v').
-        const float sm_new = __fdiv_rn(am, 127.0f);
-        const float sv_new = __fdiv_rn(__fsqrt_rn(au), 255.0f);
+        const float sm_new = div_rn(am, 127.0f);
+        const float sv_new = div_rn(sqrt_rn(au), 255.0f);
         const float im_new = block_inv(sm_new), iv_new = block_inv(sv_new);
         if (h == 0 && row < p.d_out) {
           p.m_scale[static_cast<int64_t>(jb) * p.d_out + row] = sm_new;
@@ -772,6 +803,7 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, N
           uint32_t cm[8], cv[8];
           float w[8];
           ld8<WK == W_F32 ? 0 : 1>(sw, r, h, w);
+          bool near = false;  // a product within 1e-4 of a half-integer: decide those codes exactly
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const float m1 = __uint_as_float(k0[j]);
@@ -779,15 +811,26 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, N
             if constexpr (OPT == OPT_ADAMW) {
               const float v1 = __uint_as_float(k1[j]);
               float sq1;
-              adamw_apply(w[j], m1, v1, sc, w1, sq1);
-              cv[j] = quant_v_byte(v1, sq1, sv_new, iv_new);
+              adamw_apply_zg(w[j], m1, v1, sc, w1, sq1);
+              cv[j] = quant_v_byte_fast(v1, sq1, sv_new, iv_new, near);
             } else if constexpr (OPT == OPT_SGDM) {
               w1 = sgdm_apply(w[j], m1, sc);
             } else {
               w1 = lion_apply(w[j], __uint_as_float(k1[j]), sc);
             }
             w[j] = w1;
-            cm[j] = quant_m_byte(m1, sm_new, im_new);
+            cm[j] = quant_m_byte_fast(m1, sm_new, im_new, near);
+          }
+          if (near) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const float m1 = __uint_as_float(k0[j]);
+              cm[j] = quant_m_byte(m1, sm_new, im_new);
+              if constexpr (OPT == OPT_ADAMW) {
+                const float v1 = __uint_as_float(k1[j]);
+                cv[j] = quant_v_byte(v1, sqrt_rn(v1), sv_new, iv_new);
+              }
+            }
           }
           if constexpr (WK == W_F32) {
             st8_f32(sw, r, h, w);
@@ -881,7 +924,7 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, N
           tc_fence_after_sync();
           const int run = tn - tw.first / p.tiles_m;
           float* slab = p.dx_ws + (static_cast<int64_t>(blockIdx.x) * p.dx_runs + run) * p.dx_slab;
-          write_dx_partial<BN>(slab, tmem_base + static_cast<uint32_t>(C::DX_COL), q, lane, p.num_kb);
+          write_dx_partial<BN>(slab, tmem_base + static_cast<uint32_t>(C::DX_COL), q, lane, p.num_kb, p.dx_l2 != 0);
           tc_fence_before_sync();
           __syncwarp();
           if (lane == 0) mbar_arrive(&dx_empty);

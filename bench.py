@@ -165,6 +165,124 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# --------------------------------------------------------------------------- the other configurations
+
+
+CONFIG_LAYERS = {
+    # name: (D_out, D_in, BT, W storage, moment storage, zero-gradient row share)
+    "up_proj_bt512_bf16state_sr": (14336, 4096, 512, "bf16", "bf16", 0.0),
+    "up_proj_bt2048_bf16state_sr": (14336, 4096, 2048, "bf16", "bf16", 0.0),
+    "up_proj_bt8192_bf16state_sr": (14336, 4096, 8192, "bf16", "bf16", 0.0),
+    "up_proj_bt512_q8state_zero30": (14336, 4096, 512, "f32", "q8", 0.3),
+}
+
+
+def device_layer(d_out, d_in, bt, w, st, dev, seed, zero_frac=0.0):
+    """One layer's backward-pass inputs and state, drawn on the device (the
+    distributions of the host generator: X, dY ~ N(0, 1), W ~ N(0, 0.02),
+    m ~ N(0, 1e-3), v = |N(0, 1e-6)|; 8-bit state as codes with one scale per
+    block; zero rows get zero dY columns and zero state)."""
+    import torch
+    from backward_gemm_optimizer_gb300 import synthetic as S
+    f = lambda shape, dt, std, sid, absolute=False: S.device_normal_(  # noqa: E731
+        torch.empty(shape, dtype=dt, device=dev), std, seed, sid, absolute)
+    wdt = torch.float32 if w == "f32" else torch.bfloat16
+    s = {"X": f((bt, d_in), torch.bfloat16, 1.0, S.STREAM_X), "dY": f((bt, d_out), torch.bfloat16, 1.0, S.STREAM_DY),
+         "W": f((d_out, d_in), wdt, 0.02, S.STREAM_W),
+         "dX": torch.empty((bt, d_in), dtype=torch.bfloat16, device=dev)}
+    if st == "q8":
+        g = torch.Generator(device=dev)
+        g.manual_seed(seed * 1000003 + S.STREAM_M_CODES)
+        s["m"] = torch.randn((d_out, d_in), device=dev, generator=g).mul_(42.0).round_().clamp_(-127, 127).to(torch.int8)
+        s["v"] = torch.randint(1, 256, (d_out, d_in), device=dev, generator=g, dtype=torch.int32).to(torch.uint8)
+        s["m_scale"] = torch.full((d_in // 128, d_out), 3e-3 / 127.0, dtype=torch.float32, device=dev)
+        s["v_scale"] = torch.full((d_in // 128, d_out), 2e-3 / 255.0, dtype=torch.float32, device=dev)
+    else:
+        mdt = torch.float32 if st == "f32" else torch.bfloat16
+        s["m"] = f((d_out, d_in), mdt, 1e-3, S.STREAM_M)
+        s["v"] = f((d_out, d_in), mdt, 1e-6, S.STREAM_V, True)
+    if zero_frac > 0.0:
+        zr = torch.from_numpy(S.zero_row_mask(d_out, zero_frac, seed)).to(dev)
+        s["dY"][:, zr] = 0
+        s["m"][zr] = 0
+        s["v"][zr] = 0
+        if st == "q8":
+            s["m_scale"][:, zr] = 0
+            s["v_scale"][:, zr] = 0
+    return s
+
+
+def measure_configs(F, dev, K, warm, hbm, tflops):
+    """Time the other configurations the benchmark is quoted on, each as one
+    backward pass per step through the public API (library path policy, L2
+    flushed between steps), and the 224-linear stack per rule and state as a
+    replayed CUDA graph. Returns a compact record per configuration."""
+    import torch
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    out = {}
+    for name, (d_out, d_in, bt, w, st, zf) in CONFIG_LAYERS.items():
+        s = device_layer(d_out, d_in, bt, w, st, dev, seed=5, zero_frac=zf)
+        ws = torch.empty(max(16, F.workspace_bytes(d_out, d_in, bt)), dtype=torch.uint8, device=dev)
+        t = 1
+        for _ in range(warm):
+            one_step(F, s, w, st, t, stream, ws, 0); t += 1
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+        for i in range(K):
+            flush.fill_(float(i))
+            ev[i][0].record(stream)
+            one_step(F, s, w, st, t, stream, ws, 0); t += 1
+            ev[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        F.sync_status(stream)
+        us = statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev) * 1000.0
+        ab = backward_algorithmic_bytes(d_out, d_in, bt, w, st)
+        flops = 2.0 * 2.0 * bt * d_out * d_in          # weight gradient + input gradient
+        t_roof = max(ab / (hbm * 1e9), flops / (tflops * 1e12)) * 1e6
+        out[name] = {"us": round(us, 2), "GBps": round(ab / (us * 1e-6) / 1e9, 1),
+                     "TFLOPs": round(flops / (us * 1e-6) / 1e12, 1),
+                     "bound": "hbm" if ab / (hbm * 1e9) >= flops / (tflops * 1e12) else "tensor",
+                     "frac": round(t_roof / us, 4), "algorithmic_bytes": ab,
+                     "path": "fused input gradient" if fused_path(bt, st) else "forge_dgrad + fused step"}
+        del s, ws
+    for opt in ("adamw", "lion", "sgdm"):
+        for stname in ("f32state", "bf16state"):
+            st = build_stack(opt, stname, dev, seed=7)
+            layers, order = st["layers"], st["order"]
+
+            def stack_step(t, stream_):
+                for layer in reversed(range(len(layers))):
+                    for lname, _, _ in order:
+                        stack_backward(F, st, layers[layer][lname], t, stream_)
+
+            for t in range(1, warm + 1):
+                stack_step(t, stream)
+            torch.cuda.synchronize(dev)
+            g = torch.cuda.CUDAGraph()
+            side = torch.cuda.Stream(dev)
+            side.wait_stream(stream)
+            with torch.cuda.graph(g, stream=side):
+                stack_step(warm + 1, torch.cuda.current_stream(dev))
+            g.replay(); torch.cuda.synchronize(dev)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ks = max(2, min(K, 5))
+            e0.record(stream)
+            for _ in range(ks):
+                g.replay()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            F.sync_status(stream)
+            ms = e0.elapsed_time(e1) / ks
+            ab = stack_algorithmic_bytes(st)
+            out[f"stack_{opt}_{stname}"] = {"ms": round(ms, 3), "GBps": round(ab / (ms * 1e-3) / 1e9, 1),
+                                            "bound": "hbm", "frac": round(ab / (ms * 1e-3) / 1e9 / hbm, 4),
+                                            "algorithmic_bytes": ab, "timed": f"CUDA graph, {ks} replays"}
+            del g, st, layers
+            torch.cuda.synchronize(dev)
+            torch.cuda.empty_cache()
+    return out
+
+
 # --------------------------------------------------------------------------- CPU oracle arm
 
 
@@ -450,6 +568,12 @@ def run_gpu(args, rank, world, local_rank):
         "clocks": clocks,
         "wall_s_timed": round(wall, 3),
     }
+    if not args.no_configs and world == 1:
+        del s, host, bufs, ws
+        torch.cuda.empty_cache()
+        cfg_t0 = time.perf_counter()
+        line["configs"] = measure_configs(F, dev, max(3, min(K, 20)), 3, hbm, tflops)
+        line["configs"]["wall_s"] = round(time.perf_counter() - cfg_t0, 1)
     if not args.no_cpu_baseline:
         try:
             rows = min(args.cpu_rows, d_out)
@@ -584,22 +708,17 @@ def run_accum(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
-def run_stack(args, rank, world, local_rank):
-    """One step = backward over the 224 linears of Llama-3.1-8B (layer 31 .. 0,
-    down, up, gate, o, v, k, q): one forge_backward_step per linear, on the
-    path the library picks for each shape (the split path is timed too)."""
+def build_stack(opt, stname, dev, seed, bt=512):
+    """The 224 linears of Llama-3.1-8B (32 layers x down, up, gate, o, v, k, q)
+    with their state, inputs and one shared dX buffer per D_in and workspace,
+    drawn on the device."""
     import torch
     import backward_gemm_optimizer_gb300 as F
     from backward_gemm_optimizer_gb300 import synthetic as S
 
-    opt, stname = STACKS[args.workload]
     wdt = torch.float32 if stname == "f32state" else torch.bfloat16
     mdt = wdt
     two = opt == "adamw"
-    bt = 512
-    dev = torch.device(f"cuda:{local_rank}")
-    torch.cuda.set_device(dev)
-    hp = STACK_HYPER[opt]
     order = [x for x in reversed(S.LLAMA31_8B_LINEARS)]
     layers = []
     sid = 0
@@ -608,38 +727,67 @@ def run_stack(args, rank, world, local_rank):
         for name, d_out, d_in in order:
             sid += 1
             L = {"name": name, "d_out": d_out, "d_in": d_in}
-            L["W"] = S.device_normal_(torch.empty((d_out, d_in), dtype=wdt, device=dev), 0.02, replica_seed(rank), 16 * sid)
-            L["m"] = S.device_normal_(torch.empty((d_out, d_in), dtype=mdt, device=dev), 1e-3, replica_seed(rank), 16 * sid + 1)
+            L["W"] = S.device_normal_(torch.empty((d_out, d_in), dtype=wdt, device=dev), 0.02, seed, 16 * sid)
+            L["m"] = S.device_normal_(torch.empty((d_out, d_in), dtype=mdt, device=dev), 1e-3, seed, 16 * sid + 1)
             if two:
-                L["v"] = S.device_normal_(torch.empty((d_out, d_in), dtype=mdt, device=dev), 1e-6, replica_seed(rank),
+                L["v"] = S.device_normal_(torch.empty((d_out, d_in), dtype=mdt, device=dev), 1e-6, seed,
                                           16 * sid + 2, absolute=True)
-            L["X"] = S.device_normal_(torch.empty((bt, d_in), dtype=torch.bfloat16, device=dev), 1.0, replica_seed(rank),
+            L["X"] = S.device_normal_(torch.empty((bt, d_in), dtype=torch.bfloat16, device=dev), 1.0, seed,
                                       16 * sid + 3)
-            L["dY"] = S.device_normal_(torch.empty((bt, d_out), dtype=torch.bfloat16, device=dev), 1.0,
-                                       replica_seed(rank), 16 * sid + 4)
+            L["dY"] = S.device_normal_(torch.empty((bt, d_out), dtype=torch.bfloat16, device=dev), 1.0, seed,
+                                       16 * sid + 4)
             lin[name] = L
         layers.append(lin)
     dX = {d_in: torch.empty((bt, d_in), dtype=torch.bfloat16, device=dev) for _, _, d_in in order}
-    stream = torch.cuda.current_stream(dev)
-    sr = stname == "bf16state"
-
     # One workspace serves every linear: the calls run one after another on one stream.
     ws_bytes = max(F.workspace_bytes(d_out, d_in, bt) for _, d_out, d_in in order)
     ws = torch.empty(max(16, ws_bytes), dtype=torch.uint8, device=dev)
+    return {"opt": opt, "stname": stname, "layers": layers, "order": order, "dX": dX, "ws": ws, "bt": bt,
+            "hp": STACK_HYPER[opt], "sr": stname == "bf16state", "two": two}
+
+
+def stack_backward(F, st, L, t, stream_, flags=0):
+    """One linear's backward pass (dX and the fused step) through the public API."""
+    opt, hp, sr, ws = st["opt"], st["hp"], st["sr"], st["ws"]
+    dxb = st["dX"][L["d_in"]]
+    if opt == "adamw":
+        F.backward_step("adamw", L["X"], L["dY"], L["W"], L["m"], L["v"], dxb, step=t, seed=1234, sr_w=sr,
+                        workspace=ws, flags=flags, stream=stream_, **hp)
+    elif opt == "lion":
+        F.backward_step("lion", L["X"], L["dY"], L["W"], L["m"], None, dxb, lr=hp["lr"], beta1=hp["beta1"],
+                        beta2=hp["beta2"], weight_decay=hp["weight_decay"], step=t, seed=1234, sr_w=sr,
+                        workspace=ws, flags=flags, stream=stream_)
+    else:
+        F.backward_step("sgdm", L["X"], L["dY"], L["W"], L["m"], None, dxb, lr=hp["lr"], momentum=hp["beta1"],
+                        weight_decay=hp["weight_decay"], step=t, seed=1234, sr_w=sr, workspace=ws, flags=flags,
+                        stream=stream_)
+
+
+def stack_algorithmic_bytes(st):
+    """Every linear's state read and written once, X and dY read, dX written."""
+    eb = 4 if st["stname"] == "f32state" else 2
+    sb = 2 * eb * (3 if st["two"] else 2)
+    bt = st["bt"]
+    return sum(len(st["layers"]) * (d_out * d_in * sb + 2 * bt * (d_out + 2 * d_in))
+               for _, d_out, d_in in st["order"])
+
+
+def run_stack(args, rank, world, local_rank):
+    """One step = backward over the 224 linears of Llama-3.1-8B (layer 31 .. 0,
+    down, up, gate, o, v, k, q): one forge_backward_step per linear, on the
+    path the library picks for each shape (the split path is timed too)."""
+    import torch
+    import backward_gemm_optimizer_gb300 as F
+
+    opt, stname = STACKS[args.workload]
+    dev = torch.device(f"cuda:{local_rank}")
+    torch.cuda.set_device(dev)
+    st = build_stack(opt, stname, dev, replica_seed(rank))
+    layers, order, bt, two = st["layers"], st["order"], st["bt"], st["two"]
+    stream = torch.cuda.current_stream(dev)
 
     def backward(L, t, stream_, flags=0):
-        dxb = dX[L["d_in"]]
-        if opt == "adamw":
-            F.backward_step("adamw", L["X"], L["dY"], L["W"], L["m"], L["v"], dxb, step=t, seed=1234, sr_w=sr,
-                            workspace=ws, flags=flags, stream=stream_, **hp)
-        elif opt == "lion":
-            F.backward_step("lion", L["X"], L["dY"], L["W"], L["m"], None, dxb, lr=hp["lr"], beta1=hp["beta1"],
-                            beta2=hp["beta2"], weight_decay=hp["weight_decay"], step=t, seed=1234, sr_w=sr,
-                            workspace=ws, flags=flags, stream=stream_)
-        else:
-            F.backward_step("sgdm", L["X"], L["dY"], L["W"], L["m"], None, dxb, lr=hp["lr"], momentum=hp["beta1"],
-                            weight_decay=hp["weight_decay"], step=t, seed=1234, sr_w=sr, workspace=ws, flags=flags,
-                            stream=stream_)
+        stack_backward(F, st, L, t, stream_, flags)
 
     def stack_step(t, events=None, flags=0, stream_=None):
         stream_ = stream if stream_ is None else stream_
@@ -764,6 +912,8 @@ def main():
     ap.add_argument("--cpu-min-s", type=float, default=10.0)
     ap.add_argument("--cpu-budget-s", type=float, default=120.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other configurations' compact record (BT sweep, 8-bit, 224-linear stacks)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
