@@ -207,11 +207,10 @@ __device__ __forceinline__ void st8_codes(uint8_t* base, int r, int h, const uin
 __device__ __forceinline__ void to_bf16x8(const float (&x)[8], bool sr, uint64_t idx8, uint32_t site,
                                           const WgradTcParams& p, uint4& o) {
   if (sr) {
+    // Lanes 2i and 2i + 1 take the low and high half of Philox word i.
     const U4 rr = sr_block(idx8, p.step, site, p.seed_lo, p.seed_hi);
-    uint32_t b[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) b[j] = f32_to_bf16_sr(x[j], sr_lane(rr, j));
-    o = make_uint4(b[0] | (b[1] << 16), b[2] | (b[3] << 16), b[4] | (b[5] << 16), b[6] | (b[7] << 16));
+    o = make_uint4(sr_bf16x2(x[0], x[1], rr.x & 0xFFFFu, rr.x >> 16), sr_bf16x2(x[2], x[3], rr.y & 0xFFFFu, rr.y >> 16),
+                   sr_bf16x2(x[4], x[5], rr.z & 0xFFFFu, rr.z >> 16), sr_bf16x2(x[6], x[7], rr.w & 0xFFFFu, rr.w >> 16));
   } else {
     o = make_uint4(pack_bf16x2_rn(x[0], x[1]), pack_bf16x2_rn(x[2], x[3]), pack_bf16x2_rn(x[4], x[5]),
                    pack_bf16x2_rn(x[6], x[7]));
@@ -821,14 +820,23 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, N
             w[j] = w1;
             cm[j] = quant_m_byte_fast(m1, sm_new, im_new, near);
           }
-          if (near) {
+          // Rare (a product within 1e-4 of a half-integer): decide this
+          // thread's 8 codes exactly. The new moments are read again from
+          // tensor memory (a warp-wide load, hence the warp-uniform branch)
+          // rather than kept in registers across the loop above.
+          if (__any_sync(0xFFFFFFFFu, near)) {
+            uint32_t r0[8], r1[8];
+            tmem_ld_32x32b_x8(t_keep + c * C::CW + h * 8, r0);
+            if constexpr (OPT == OPT_ADAMW) tmem_ld_32x32b_x8(t_keep + BN + c * C::CW + h * 8, r1);
+            tmem_ld_wait();
+            if (near) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const float m1 = __uint_as_float(k0[j]);
-              cm[j] = quant_m_byte(m1, sm_new, im_new);
-              if constexpr (OPT == OPT_ADAMW) {
-                const float v1 = __uint_as_float(k1[j]);
-                cv[j] = quant_v_byte(v1, sqrt_rn(v1), sv_new, iv_new);
+              for (int j = 0; j < 8; ++j) {
+                cm[j] = quant_m_byte(__uint_as_float(r0[j]), sm_new, im_new);
+                if constexpr (OPT == OPT_ADAMW) {
+                  const float v1 = __uint_as_float(r1[j]);
+                  cv[j] = quant_v_byte(v1, sqrt_rn(v1), sv_new, iv_new);
+                }
               }
             }
           }
