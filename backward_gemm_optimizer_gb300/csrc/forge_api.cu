@@ -422,7 +422,12 @@ forge_status wgrad_step(int opt, const forge_tensor* X, const forge_tensor* dY, 
   // Deep operand ring for long token axes, and for the accumulation rules at
   // any length: their slots hold only the fp32 accumulator, so shared memory
   // has room for four operand stages, and their tile time is the mainloop's.
-  const bool deep128 = dx == nullptr && G_acc == nullptr && bn == 128 && (bt >= 1024 || accum);
+  // Measured on the up-projection (step alone): bf16 W + bf16 moments at
+  // BT 512 181 -> 178 us, BT 768 211 -> 180 us; 8-bit moments at BT 512
+  // 227.5 -> 220 us; fp32 state at BT 768 277 -> 268 us but at BT 512
+  // 240 -> 262 us (its state ring loses slots).
+  const bool deep128 = dx == nullptr && G_acc == nullptr && bn == 128 &&
+                       (bt >= 768 || accum || (bt >= 512 && ((wk == W_BF16 && mk == M_BF16) || mk == M_Q8)));
   // 256-column tiles always use the deep ring; the fused input gradient takes
   // a third operand stage past 512 tokens (its mainloop then sets the pace).
   // The fused input gradient takes a third operand stage past 512 tokens, and
