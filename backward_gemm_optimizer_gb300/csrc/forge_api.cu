@@ -447,11 +447,13 @@ forge_status wgrad_step(int opt, const forge_tensor* X, const forge_tensor* dY, 
       return st;
   }
   // State chunk width: 16 columns for the fused input gradient with fp32 W
-  // and two fp32 moments at BT <= 256 (measured: the deeper state ring wins
-  // when the mainloop is short; at BT 512 the extra chunk turns cost more)
-  // and past 512 tokens (the narrow slots leave room for a third operand
-  // stage: 398 -> 351 us at BT 768 on the up-projection).
-  const bool narrow = dx != nullptr && wk == W_F32 && mk == M_F32 && nst == 2 && (bt <= 256 || bt > 512);
+  // and two fp32 moments (four 24 KB state slots instead of two 48 KB
+  // ones): up-projection at BT 256 282 -> 259 us, at BT 512 283.7 -> 269.3 us
+  // (with the evict-last operand loads; before them the extra chunk turns
+  // cost more than the deeper ring gained at BT 512), and past 512 tokens
+  // the narrow slots leave room for a third operand stage (398 -> 351 us at
+  // BT 768).
+  const bool narrow = dx != nullptr && wk == W_F32 && mk == M_F32 && nst == 2;
   const int cw = narrow ? 16 : 32;
   if ((st = encode_state(&p.tm_w, W, "W", cw)) != FORGE_OK) return st;
   if (nst >= 1) {
