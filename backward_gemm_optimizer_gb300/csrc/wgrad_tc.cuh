@@ -81,7 +81,7 @@ struct TcCfg {
   static constexpr int BK = DX ? 128 : 64;  // tokens per operand stage
   static constexpr int BOX = BK * 128; // bytes of one 64-column operand box (BK rows of 128 bytes)
   // State chunk width (columns): 32, or 16 (NARROW) for the fused-input-
-  // gradient kernel with fp32 W and two fp32 moments -- its shared memory
+  // gradient kernel with fp32 W and fp32 moments -- its shared memory
   // holds two 48 KB slots of 32 columns or four of 16: on short token axes
   // the deeper state ring pays for the extra chunk turns, and on long ones
   // the narrow slots leave room for a third operand stage.
@@ -361,7 +361,8 @@ template <int OPT, int WK, int MK, int BN, int STAGES, int NBUF, bool DX, bool G
 __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, NARROW>::NUM_THREADS, 1)
     wgrad_step_tc_kernel(const __grid_constant__ WgradTcParams p) {
   using C = TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, NARROW>;
-  static_assert(!NARROW || (DX && WK == W_F32 && MK == M_F32 && C::TWO), "16-column chunks: fp32 fused kernel");
+  static_assert(!NARROW || (DX && WK == W_F32 && MK == M_F32 && C::NST >= 1 && !C::ACC),
+                "16-column chunks: fused kernel with fp32 W and fp32 state");
   static_assert(!GA || (!DX && !C::Q8), "accumulated-gradient step: split path, fp32 / bf16 state");
   static_assert(!C::ACC || ((WK == W_F32 || DX) && !GA), "fp32 gradient accumulator");
   static_assert(BN == 64 || BN == 128 || BN == 256, "tile width");
@@ -648,7 +649,7 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, N
           if constexpr (Q == 4) {  // fp32 W and moments (the 16-column chunks)
             ld4_f32(sw, r, h, w);
             ld4_f32(sm, r, h, m);
-            ld4_f32(sv, r, h, v);
+            if constexpr (C::TWO) ld4_f32(sv, r, h, v);
           } else {
             if constexpr (C::LOAD_W) ld8<C::SLOT_F32 ? 0 : 1>(sw, r, h, w);
             if constexpr (C::NST >= 1) ld8<MK == M_F32 ? 0 : 1>(sm, r, h, m);
@@ -668,7 +669,7 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, N
           if constexpr (Q == 4) {
             st4_f32(sw, r, h, w);
             st4_f32(sm, r, h, m);
-            st4_f32(sv, r, h, v);
+            if constexpr (C::TWO) st4_f32(sv, r, h, v);
             fence_proxy_async_smem();
             mbar_arrive(&st_written[s]);
             continue;

@@ -73,7 +73,7 @@ cudaError_t launch_mk(const WgradTcParams& p, const TcLaunch& l) {
     if constexpr (MK == M_Q8) return cudaErrorInvalidValue;
     else {
       if (l.bn != 64) return cudaErrorInvalidValue;
-      if constexpr (WK == W_F32 && MK == M_F32 && opt_nstate(OPT) == 2)
+      if constexpr (WK == W_F32 && MK == M_F32 && opt_nstate(OPT) >= 1)
         if (l.narrow)
           return l.deep ? launch_dx<OPT, WK, MK, true, true>(p, l.grid, l.stream)
                         : launch_dx<OPT, WK, MK, true, false>(p, l.grid, l.stream);

@@ -98,10 +98,12 @@ def _check_dx(got, prob, dx_dtype, exact):
 
 @pytest.mark.parametrize("rule", RULES)
 @pytest.mark.parametrize("variant", VARIANTS, ids=lambda v: f"W{v[0]}-m{v[1]}")
-@pytest.mark.parametrize("shape", SHAPES[:2] + [(264, 384, 600)], ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("shape", SHAPES[:2] + [(264, 384, 512), (264, 384, 600)], ids=lambda s: "x".join(map(str, s)))
 def test_fused_backward_exact(rule, variant, shape):
     # BT 200 / 70: short token axes (16-column state chunks for fp32 W and
-    # two fp32 moments); BT 600: three operand stages where they fit.
+    # two fp32 moments); BT 512: 16-column chunks for one-state fp32 rules
+    # too, three operand stages with bf16 weights; BT 600: three operand
+    # stages where they fit.
     w, st = variant
     prob = _prob(shape, 21, w, st, exact=True)
     sr, srm = w == "bf16", st == "bf16" and NSTATE[rule] > 0
