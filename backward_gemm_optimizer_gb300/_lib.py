@@ -234,14 +234,16 @@ def dgrad(dY, W_old, dX, *, stream=None):
 
 def backward_step(rule, X, dY, W, s0, s1, dX, *, lr, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0,
                   momentum_decay=4e-3, momentum=None, alpha=None, step, seed=0, sr_w=False, sr_moments=False,
-                  workspace=None, flags=0, stream=None):
+                  workspace=None, flags=0, stream=None, m_scale=None, v_scale=None):
     """dX = dY W_old and the fused step of `rule` on W and its state (forge_backward_step).
 
     s0 / s1 are the rule's state tensors as the wgrad_step_<rule> call takes
-    them (None where the rule has fewer). `momentum` (SGD-momentum) and
-    `alpha` (RMSprop) are aliases of beta1 / beta2. `workspace`: a device
-    tensor of at least workspace_bytes(D_out, D_in, BT) bytes enables the
-    fused input-gradient path; without it dgrad and the step run apart.
+    them (None where the rule has fewer); m_scale / v_scale are their block
+    scales for 8-bit state. `momentum` (SGD-momentum) and `alpha` (RMSprop)
+    are aliases of beta1 / beta2. `workspace`: a device tensor of at least
+    workspace_bytes(D_out, D_in, BT) bytes enables the fused input-gradient
+    path, and on the split path (dgrad, then the step) lets the input
+    gradient spread over all SMs.
     """
     if rule not in RULES:
         raise ValueError(f"unknown rule {rule!r}; one of {tuple(RULES)}")
@@ -250,8 +252,8 @@ def backward_step(rule, X, dY, W, s0, s1, dX, *, lr, beta1=0.9, beta2=0.999, eps
     if alpha is not None:
         beta2 = alpha
     tX, tdY, tW, tdX = tensor_desc(X), tensor_desc(dY), tensor_desc(W), tensor_desc(dX)
-    t0 = tensor_desc(s0) if s0 is not None else None
-    t1 = tensor_desc(s1) if s1 is not None else None
+    t0 = tensor_desc(s0, m_scale) if s0 is not None else None
+    t1 = tensor_desc(s1, v_scale) if s1 is not None else None
     h = _hyper(lr, beta1, beta2, eps, weight_decay, sr_w, sr_moments, flags, momentum_decay)
     ws_ptr = ctypes.c_void_p(workspace.data_ptr() if workspace is not None and workspace.numel() else 0)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0

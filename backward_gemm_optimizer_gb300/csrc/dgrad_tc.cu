@@ -10,6 +10,11 @@
 // warps round them to bf16 (round-to-nearest-even) into the swizzled
 // operand layout before the MMA consumes them.
 //
+// With a workspace, layers with at most half as many tiles as SMs split the
+// contraction over D_out into S equal parts run by S CTAs each (one wave);
+// the parts' fp32 partial sums are added in a fixed order by a fix-up
+// kernel, so more SMs work on a skinny dX.
+//
 // Warp roles (512 threads): 0 dY producer, 1 MMA issuer + TMEM owner,
 // 2 W producer, 4-7 epilogue (TMEM lane quadrant = warp % 4, thread =
 // token row), 8-15 converters (fp32 weights only). All waits are bounded.
@@ -100,6 +105,40 @@ __device__ __forceinline__ void dtile(int tile, int tiles_m, int tiles_n, int gr
   tn = in_g / gsize;
 }
 
+// The (tile, stage range) segments a CTA processes, in order: whole tiles
+// blockIdx.x, blockIdx.x + gridDim.x, ... or, with the contraction split in
+// S = splitk parts (grid = num_tiles * S, one wave), the single segment
+// (tile c % num_tiles, stages [s num_kb / S, (s + 1) num_kb / S)) with
+// s = c / num_tiles: the token tiles that share a column of W read the same
+// rows of it at the same time, so W comes from DRAM once. Every role walks
+// the same sequence.
+struct SegWalk {
+  int64_t pos, end;
+  int stride;
+};
+
+__device__ __forceinline__ SegWalk seg_walk(const DgradParams& p) {
+  if (p.splitk) return SegWalk{0, 1, 0};
+  return SegWalk{static_cast<int64_t>(blockIdx.x), static_cast<int64_t>(p.num_tiles), static_cast<int>(gridDim.x)};
+}
+
+__device__ __forceinline__ bool seg_next(const DgradParams& p, SegWalk& w, int& tile, int& kb0, int& kb1) {
+  if (w.pos >= w.end) return false;
+  if (p.splitk) {
+    const int part = static_cast<int>(blockIdx.x) / p.num_tiles;
+    tile = static_cast<int>(blockIdx.x) % p.num_tiles;
+    kb0 = static_cast<int>(static_cast<int64_t>(part) * p.num_kb / p.splitk);
+    kb1 = static_cast<int>(static_cast<int64_t>(part + 1) * p.num_kb / p.splitk);
+    w.pos = 1;
+  } else {
+    tile = static_cast<int>(w.pos);
+    kb0 = 0;
+    kb1 = p.num_kb;
+    w.pos += w.stride;
+  }
+  return true;
+}
+
 template <bool F32W, int BN>
 __global__ void __launch_bounds__(NUM_THREADS, 1) dgrad_tc_kernel(const __grid_constant__ DgradParams p) {
   using C = DCfg<F32W, BN>;
@@ -142,10 +181,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dgrad_tc_kernel(const __grid_c
     if (lane == 0) {
       uint32_t k = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+      SegWalk w = seg_walk(p);
+      int tile, kb0, kb1;
+      while (ok && seg_next(p, w, tile, kb0, kb1)) {
         int tm, tn;
         dtile(tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
-        for (int kb = 0; kb < p.num_kb; ++kb, ++k) {
+        for (int kb = kb0; kb < kb1; ++kb, ++k) {
           const int s = static_cast<int>(k % SA);
           if (!dwait(&a_empty[s], ((k / SA) & 1u) ^ 1u, abort_flag, p.status, WAIT_OP_EMPTY, lim)) {
             ok = false;
@@ -165,10 +206,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dgrad_tc_kernel(const __grid_c
       uint32_t k = 0;
       uint32_t ks = 0;  // fp32 staging slots filled
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+      SegWalk w = seg_walk(p);
+      int tile, kb0, kb1;
+      while (ok && seg_next(p, w, tile, kb0, kb1)) {
         int tm, tn;
         dtile(tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
-        for (int kb = 0; kb < p.num_kb; ++kb, ++k) {
+        for (int kb = kb0; kb < kb1; ++kb, ++k) {
           if constexpr (F32W) {
             for (int half = 0; half < BK / C::STG_ROWS; ++half, ++ks) {
               const int s = static_cast<int>(ks % SS);
@@ -210,7 +253,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dgrad_tc_kernel(const __grid_c
       uint32_t k = 0;
       bool ok = true;
       int it = 0;
-      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++it) {
+      SegWalk w = seg_walk(p);
+      int tile, kb0, kb1;
+      for (; ok && seg_next(p, w, tile, kb0, kb1); ++it) {
         const int buf = it & 1;
         if (!dwait(&tm_empty[buf], ((it >> 1) & 1) ^ 1u, abort_flag, p.status, WAIT_TMEM_EMPTY, lim)) {
           ok = false;
@@ -218,7 +263,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dgrad_tc_kernel(const __grid_c
         }
         tc_fence_after_sync();
         const uint32_t d = tmem_base + static_cast<uint32_t>(buf * BN);
-        for (int kb = 0; kb < p.num_kb; ++kb, ++k) {
+        for (int kb = kb0; kb < kb1; ++kb, ++k) {
           const int sa = static_cast<int>(k % SA), sb = static_cast<int>(k % SB);
           if (!dwait(&a_full[sa], (k / SA) & 1u, abort_flag, p.status, WAIT_OP_FULL, lim) ||
               !dwait(&b_full[sb], (k / SB) & 1u, abort_flag, p.status, WAIT_OP_FULL, lim)) {
@@ -241,7 +286,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dgrad_tc_kernel(const __grid_c
             // box (boxes 16 KB apart); B's advances 16 rows = 2048 bytes.
             const uint64_t astep = static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
             const uint64_t bstep = static_cast<uint64_t>((kk * 2048) >> 4);
-            umma_f16(d, ad0 + astep, bd0 + bstep, IDESC, (kb > 0 || kk > 0) ? 1u : 0u);
+            umma_f16(d, ad0 + astep, bd0 + bstep, IDESC, (kb > kb0 || kk > 0) ? 1u : 0u);
           }
           umma_commit(&a_empty[sa]);  // releases the stage's dY slot and its bf16 W slot
         }
@@ -261,7 +306,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dgrad_tc_kernel(const __grid_c
     const int r = q * 32 + lane;
     int it = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++it) {
+    SegWalk w = seg_walk(p);
+    int tile, kb0, kb1;
+    for (; ok && seg_next(p, w, tile, kb0, kb1); ++it) {
       int tm, tn;
       dtile(tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
       const int buf = it & 1;
@@ -271,6 +318,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dgrad_tc_kernel(const __grid_c
       tc_fence_after_sync();
       const int row = tm * BM + r;
       const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * BN);
+      // A split contraction: this CTA's fp32 partial sum goes to its slot
+      // (row r of a 128 x BN slab), for the fix-up kernel to add in order.
+      const bool partial = p.splitk != 0;
+      float* slot = partial ? p.part + (static_cast<int64_t>(blockIdx.x) * BM + r) * BN : nullptr;
 #pragma unroll 1
       for (int c = 0; c < BN / 16; ++c) {
         uint32_t acc[16];
@@ -280,6 +331,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dgrad_tc_kernel(const __grid_c
         } else {
 #pragma unroll
           for (int j = 0; j < 16; ++j) acc[j] = 0u;
+        }
+        if (partial) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            reinterpret_cast<float4*>(slot + c * 16)[j] =
+                make_float4(__uint_as_float(acc[4 * j]), __uint_as_float(acc[4 * j + 1]),
+                            __uint_as_float(acc[4 * j + 2]), __uint_as_float(acc[4 * j + 3]));
+          continue;
         }
         const int col0 = tn * BN + c * 16;
         if (row >= p.bt || col0 >= p.d_in) continue;
@@ -323,8 +382,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dgrad_tc_kernel(const __grid_c
     const int ct = threadIdx.x - 256;
     uint32_t k = 0, ks = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-      for (int kb = 0; kb < p.num_kb; ++kb, ++k) {
+    SegWalk w = seg_walk(p);
+    int tile, kb0, kb1;
+    while (ok && seg_next(p, w, tile, kb0, kb1)) {
+      for (int kb = kb0; kb < kb1; ++kb, ++k) {
         const int sb = static_cast<int>(k % SB);
         uint8_t* b = b_ring + sb * B_BYTES;
         // A stage's BK rows arrive as BK / 64 staging slots of 64 rows.
@@ -377,6 +438,46 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dgrad_tc_kernel(const __grid_c
   }
 }
 
+// The second half of a split dgrad: for each tile, adds the partial sums of
+// its S parts in increasing part order -- the order of the contraction, and
+// a fixed one, so dX is bit-reproducible -- and stores dX. Part s of tile t
+// is CTA t + s * num_tiles's slot. One block per (tile, 16 token rows).
+__global__ void __launch_bounds__(256) dgrad_fixup_kernel(const DgradFixupParams p) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int tile = blockIdx.x;
+  int tm, tn;
+  dtile(tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+  const int nq = p.bn / 4;  // 16-byte pieces per row
+  for (int idx = threadIdx.x; idx < 16 * nq; idx += blockDim.x) {
+    const int rr = static_cast<int>(blockIdx.y) * 16 + idx / nq;
+    const int col = (idx % nq) * 4;
+    const int t = tm * BM + rr, i = tn * p.bn + col;
+    if (t >= p.bt || i >= p.d_in) continue;  // D_in % 8 == 0: 4 columns all in or all out
+    float4 v[4];
+#pragma unroll
+    for (int s = 0; s < 4; ++s)
+      v[s] = s < p.parts ? __ldcg(reinterpret_cast<const float4*>(
+                               p.part + ((static_cast<int64_t>(s) * p.num_tiles + tile) * BM + rr) * p.bn + col))
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 0; s < p.parts; ++s) {
+      const float4 u = s < 4 ? v[s]
+                             : __ldcg(reinterpret_cast<const float4*>(
+                                   p.part + ((static_cast<int64_t>(s) * p.num_tiles + tile) * BM + rr) * p.bn + col));
+      acc.x = __fadd_rn(acc.x, u.x);
+      acc.y = __fadd_rn(acc.y, u.y);
+      acc.z = __fadd_rn(acc.z, u.z);
+      acc.w = __fadd_rn(acc.w, u.w);
+    }
+    if (p.dx_bf16) {
+      *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.dX) + static_cast<int64_t>(t) * p.ld_dx + i) =
+          make_uint2(pack_bf16x2_rn(acc.x, acc.y), pack_bf16x2_rn(acc.z, acc.w));
+    } else {
+      *reinterpret_cast<float4*>(static_cast<float*>(p.dX) + static_cast<int64_t>(t) * p.ld_dx + i) = acc;
+    }
+  }
+}
+
 template <bool F32W, int BN>
 cudaError_t launch_d(const DgradParams& p, int grid, cudaStream_t stream) {
   // The stage depth the host encoded the tensor maps and num_kb for must be
@@ -398,6 +499,20 @@ cudaError_t launch_d(const DgradParams& p, int grid, cudaStream_t stream) {
 }
 
 }  // namespace
+
+cudaError_t launch_dgrad_fixup(const DgradFixupParams& p, cudaStream_t stream) {
+  if (p.bt == 0 || p.d_in == 0 || p.num_tiles == 0) return cudaSuccess;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.num_tiles), static_cast<unsigned>(BM / 16));
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, dgrad_fixup_kernel, p);
+}
 
 cudaError_t launch_dgrad_tc(const DgradParams& p, int grid, cudaStream_t stream) {
   if (p.w_f32) return p.bn == 128 ? launch_d<true, 128>(p, grid, stream) : cudaErrorInvalidValue;

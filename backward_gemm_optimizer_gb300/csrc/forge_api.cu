@@ -285,6 +285,42 @@ DxGeometry dx_geometry(int64_t d_out, int64_t d_in, int64_t bt, int sms) {
   return g;
 }
 
+// The split contraction of the input gradient (dgrad with a workspace): a
+// layer whose 128 x 128 tiles would leave at least half the SMs idle runs
+// S = SMs / tiles parts of each tile's contraction on S CTAs (one wave),
+// S <= 4, each part at least 32 stages long; the fix-up kernel adds the
+// parts' fp32 sums in order. bf16 weights use 128 x 256 tiles there (twice
+// the work per MMA instruction, which one thread issues). Measured (Lion,
+// bf16 state, split path): up-projection BT 256 176.6 -> 159 us; where the
+// tiles already fill half the GPU, or the contraction is short, the split
+// lost (BT 512: q/o 72 -> 83 us, k/v 34 -> 46 us, up-projection even).
+struct DgradSplit {
+  int bn = 0, tiles_m = 0, tiles_n = 0, num_tiles = 0, num_kb = 0, parts = 0;
+  size_t bytes = 0;  // one 128 x bn fp32 partial sum per CTA
+  bool worthwhile = false;
+};
+
+DgradSplit dgrad_split(int64_t d_out, int64_t d_in, int64_t bt, bool w_bf16, int sms) {
+  DgradSplit g;
+  if (bt < 1 || d_out < 1 || d_in < 1 || sms < 1) return g;
+  g.bn = w_bf16 ? 256 : 128;
+  const int64_t rows_per_stage = g.bn == 128 ? 128 : 64;
+  g.tiles_m = static_cast<int>((bt + 127) / 128);
+  g.tiles_n = static_cast<int>((d_in + g.bn - 1) / g.bn);
+  g.num_tiles = g.tiles_m * g.tiles_n;
+  g.num_kb = static_cast<int>((d_out + rows_per_stage - 1) / rows_per_stage);
+  const int64_t tiles128 = static_cast<int64_t>(g.tiles_m) * ((d_in + 127) / 128);
+  int parts = sms / g.num_tiles;
+  if (parts > 4) parts = 4;
+  while (parts >= 2 && g.num_kb * (rows_per_stage / 64) < 32 * parts) --parts;
+  g.parts = parts;
+  // ... and only where it puts more SMs to work than whole 128 x 128 tiles
+  // would (q/o at BT 256: 2 x 32 tiles either way, 64.1 -> 70.7 us split).
+  g.worthwhile = parts >= 2 && 2 * tiles128 <= sms && 2 * g.num_tiles * parts >= 3 * tiles128;
+  g.bytes = g.worthwhile ? static_cast<size_t>(g.num_tiles) * parts * 128 * g.bn * sizeof(float) : 0;
+  return g;
+}
+
 // Extra arguments of the fused backward pass (dX and its workspace). W_dx:
 // the weights dX is formed from when they are not the step's first tensor
 // (the accumulation rules, whose first tensor is G_acc); null otherwise.
@@ -592,7 +628,8 @@ bool dx_worthwhile(const DxGeometry& g, int64_t d_out, int64_t d_in, int w_bytes
   return saved >= partial;
 }
 
-forge_status dgrad_impl(const forge_tensor* dY, const forge_tensor* W_old, forge_tensor* dX, forge_stream_t stream);
+forge_status dgrad_impl(const forge_tensor* dY, const forge_tensor* W_old, forge_tensor* dX, forge_stream_t stream,
+                        void* ws = nullptr, size_t ws_bytes = 0);
 
 forge_status backward_step(int opt, const forge_tensor* X, const forge_tensor* dY, forge_tensor* W, forge_tensor* s0,
                            forge_tensor* s1, forge_tensor* dX, const forge_hyper* h, int64_t step, uint64_t seed,
@@ -635,7 +672,7 @@ forge_status backward_step(int opt, const forge_tensor* X, const forge_tensor* d
   if (X->dtype != FORGE_BF16)
     return fail(FORGE_ERR_UNSUPPORTED, "backward_step(%s): dX needs bf16 dY (the fp32-input step has no dgrad)",
                 oname);
-  if ((st = dgrad_impl(dY, W, dX, stream)) != FORGE_OK) return st;
+  if ((st = dgrad_impl(dY, W, dX, stream, ws, ws_bytes)) != FORGE_OK) return st;
   forge_hyper h2 = *h;
   h2.flags &= ~(FORGE_FLAG_BACKWARD_FUSED | FORGE_FLAG_BACKWARD_SPLIT);
   return wgrad_step(opt, X, dY, W, s0, s1, &h2, step, seed, stream);
@@ -683,7 +720,7 @@ forge_status backward_accumulate(const forge_tensor* X, const forge_tensor* dY, 
   }
   if (X->dtype != FORGE_BF16)
     return fail(FORGE_ERR_UNSUPPORTED, "backward_accumulate: gradient accumulation needs bf16 X, dY");
-  if ((st = dgrad_impl(dY, W, dX, stream)) != FORGE_OK) return st;
+  if ((st = dgrad_impl(dY, W, dX, stream, ws, ws_bytes)) != FORGE_OK) return st;
   return wgrad_step(opt, X, dY, G_acc, nullptr, nullptr, &h, 1, 0, stream);
 }
 
@@ -776,7 +813,8 @@ forge_status forge_wgrad_step_accumulated(forge_rule rule, const forge_tensor* X
 
 namespace {
 
-forge_status dgrad_impl(const forge_tensor* dY, const forge_tensor* W_old, forge_tensor* dX, forge_stream_t stream) {
+forge_status dgrad_impl(const forge_tensor* dY, const forge_tensor* W_old, forge_tensor* dX, forge_stream_t stream,
+                        void* ws, size_t ws_bytes) {
   if (dY == nullptr || W_old == nullptr || dX == nullptr) return fail(FORGE_ERR_INVALID_ARG, "dgrad: null argument");
   const int64_t bt = dY->rows, d_out = dY->cols, d_in = W_old->cols;
   if (bt < 0 || d_out < 0 || d_in < 0) return fail(FORGE_ERR_INVALID_ARG, "dgrad: negative size");
@@ -812,8 +850,13 @@ forge_status dgrad_impl(const forge_tensor* dY, const forge_tensor* W_old, forge
   p.d_in = static_cast<int>(d_in);
   p.tiles_m = static_cast<int>((bt + 127) / 128);
   // 128 x 256 tiles for bf16 weights when they still fill the GPU (long
-  // token axes): half the dY operand traffic per output of 128 x 128.
-  p.bn = (W_old->dtype == FORGE_BF16 && p.tiles_m * ((d_in + 255) / 256) >= dev->sms) ? 256 : 128;
+  // token axes): half the dY operand traffic per output of 128 x 128. With
+  // a workspace large enough, layers with few tiles split the contraction
+  // over D_out (dgrad_split).
+  const DgradSplit sp = dgrad_split(d_out, d_in, bt, W_old->dtype == FORGE_BF16, dev->sms);
+  const bool split = sp.worthwhile && ws != nullptr && ws_bytes >= sp.bytes &&
+                     reinterpret_cast<uintptr_t>(ws) % 16 == 0;
+  p.bn = split ? sp.bn : (W_old->dtype == FORGE_BF16 && p.tiles_m * ((d_in + 255) / 256) >= dev->sms) ? 256 : 128;
   p.tiles_n = static_cast<int>((d_in + p.bn - 1) / p.bn);
   p.num_tiles = p.tiles_m * p.tiles_n;
   // Rows of D_out per stage: 128 on 128-column tiles, 64 on 128 x 256 tiles.
@@ -837,9 +880,33 @@ forge_status dgrad_impl(const forge_tensor* dY, const forge_tensor* W_old, forge
   p.num_kb = static_cast<int>((d_out + rows_per_stage - 1) / rows_per_stage);
   p.group_m = 8;
   p.timeout_ns = kTimeoutNs;
-  const int grid = p.num_tiles < dev->sms ? p.num_tiles : dev->sms;
+  int grid = p.num_tiles < dev->sms ? p.num_tiles : dev->sms;
+  if (split) {
+    if (sp.num_tiles != p.num_tiles || sp.num_kb != p.num_kb)
+      return fail(FORGE_ERR_INVALID_ARG, "dgrad: internal geometry mismatch");
+    p.splitk = sp.parts;
+    p.part = static_cast<float*>(ws);
+    grid = sp.num_tiles * sp.parts;
+  }
   cudaError_t e = launch_dgrad_tc(p, grid, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(FORGE_ERR_CUDA, "dgrad launch: %s", cudaGetErrorString(e));
+  if (split) {
+    DgradFixupParams f{};
+    f.part = p.part;
+    f.dX = p.dX;
+    f.ld_dx = p.ld_dx;
+    f.dx_bf16 = p.dx_bf16;
+    f.bt = p.bt;
+    f.d_in = p.d_in;
+    f.bn = p.bn;
+    f.tiles_m = p.tiles_m;
+    f.tiles_n = p.tiles_n;
+    f.group_m = p.group_m;
+    f.num_tiles = p.num_tiles;
+    f.parts = sp.parts;
+    e = launch_dgrad_fixup(f, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(FORGE_ERR_CUDA, "dgrad fix-up launch: %s", cudaGetErrorString(e));
+  }
   return ok();
 }
 
@@ -888,7 +955,13 @@ const char* forge_version(void) { return "0.3.0"; }
 size_t forge_workspace_bytes(int64_t d_out, int64_t d_in, int64_t bt) {
   DeviceInfo* dev = nullptr;
   if (device_info(&dev) != FORGE_OK) return 0;
-  return dx_geometry(d_out, d_in, bt, dev->sms).bytes;
+  const size_t fused = dx_geometry(d_out, d_in, bt, dev->sms).bytes;
+  size_t split = 0;
+  for (const bool w_bf16 : {false, true}) {
+    const DgradSplit g = dgrad_split(d_out, d_in, bt, w_bf16, dev->sms);
+    if (g.worthwhile && g.bytes > split) split = g.bytes;
+  }
+  return fused > split ? fused : split;
 }
 
 }  // extern "C"

@@ -116,6 +116,22 @@ struct alignas(128) DgradParams {
   int bk;             // rows of D_out per stage (128, or 64 with bn 256); must match the kernel's
   uint32_t flags;
   uint64_t timeout_ns;
+  // Split contraction (splitk = S >= 2; grid = num_tiles * S): CTA c runs
+  // stages [s num_kb / S, (s + 1) num_kb / S) of tile c % num_tiles,
+  // s = c / num_tiles, and stores its fp32 partial sum to part + c * 128 * bn
+  // (128 x bn, row-major); dgrad_fixup_kernel adds a tile's parts in order.
+  int splitk;
+  float* part;
+};
+
+// Sum of the partial tiles of a split dgrad (see DgradParams::splitk).
+struct DgradFixupParams {
+  const float* part;
+  void* dX;
+  int64_t ld_dx;
+  int dx_bf16;
+  int bt, d_in;
+  int bn, tiles_m, tiles_n, group_m, num_tiles, parts;
 };
 
 struct TcLaunch {
@@ -141,6 +157,7 @@ cudaError_t launch_wgrad_tc_radam(const WgradTcParams& p, const TcLaunch& l);
 cudaError_t launch_wgrad_tc_accum(const WgradTcParams& p, const TcLaunch& l);
 cudaError_t launch_wgrad_simt(const WgradSimtParams& p, int opt, int wk, int mk, cudaStream_t stream);
 cudaError_t launch_dgrad_tc(const DgradParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_dgrad_fixup(const DgradFixupParams& p, cudaStream_t stream);
 cudaError_t launch_dx_reduce(const DxReduceParams& p, int sms, cudaStream_t stream);
 
 // Whether a (opt, wk, mk, bn, deep) variant has a tensor-core kernel.

@@ -386,14 +386,11 @@ def make_state(d_out, d_in, bt, w, st, dev, seed=0):
 
 
 def one_step(F, s, w, st, t, stream, ws, flags):
-    """One backward pass of the layer through the public API."""
-    if st == "q8":  # 8-bit state descriptors carry their scales: dgrad, then the rule's call
-        F.dgrad(s["dY"], s["W"], s["dX"], stream=stream)
-        F.wgrad_step_adamw(s["X"], s["dY"], s["W"], s["m"], s["v"], m_scale=s.get("m_scale"),
-                           v_scale=s.get("v_scale"), step=t, seed=1234, sr_w=(w == "bf16"), stream=stream, **HYPER)
-    else:
-        F.backward_step("adamw", s["X"], s["dY"], s["W"], s["m"], s["v"], s["dX"], step=t, seed=1234,
-                        sr_w=(w == "bf16"), workspace=ws, flags=flags, stream=stream, **HYPER)
+    """One backward pass of the layer through the public API (8-bit state:
+    the descriptors carry their block scales)."""
+    F.backward_step("adamw", s["X"], s["dY"], s["W"], s["m"], s["v"], s["dX"], step=t, seed=1234,
+                    sr_w=(w == "bf16"), workspace=ws, flags=flags, stream=stream, m_scale=s.get("m_scale"),
+                    v_scale=s.get("v_scale"), **HYPER)
 
 
 def split_step(F, s, w, t, stream, events=None):
@@ -421,7 +418,8 @@ def run_gpu(args, rank, world, local_rank):
 
     fused = fused_path(bt, st)
     flags = F.FLAG_BACKWARD_FUSED if fused else F.FLAG_BACKWARD_SPLIT
-    ws = torch.empty(max(16, F.workspace_bytes(d_out, d_in, bt)), dtype=torch.uint8, device=dev) if fused else None
+    # the fused pass's dX slabs, or on the split path the balanced dgrad's partial sums
+    ws = torch.empty(max(16, F.workspace_bytes(d_out, d_in, bt)), dtype=torch.uint8, device=dev)
     t = 1
     for _ in range(args.warmup):
         one_step(F, s, w, st, t, stream, ws, flags); t += 1

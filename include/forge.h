@@ -263,7 +263,11 @@ forge_status forge_dgrad(const forge_tensor* dY, const forge_tensor* W_old, forg
  * 1 <= BT <= 768, and `workspace` of forge_workspace_bytes(D_out, D_in, BT)
  * bytes (device memory, 16-byte aligned, owned by the caller, contents
  * need not be initialised; it must not be shared by calls in flight at the
- * same time). The split path enqueues forge_dgrad and then the step.
+ * same time). The split path enqueues the input gradient (forge_dgrad's
+ * kernel; given that workspace and few tiles, its contraction is split
+ * over several SMs and a second kernel adds the partial sums in a fixed
+ * order) and then the step. 8-bit state takes the split
+ * path.
  * With no FORGE_FLAG_BACKWARD_* flag the library takes the fused path when
  * it applies, the workspace is large enough, and it saves more traffic
  * than its partial sums cost; FORGE_FLAG_BACKWARD_FUSED /
@@ -382,14 +386,22 @@ const char* forge_last_error(void);
 const char* forge_version(void);
 
 /*
- * forge_workspace_bytes -- device scratch that the fused paths of
- * forge_backward_step and forge_backward_accumulate need for a layer of
- * this shape on the current device: one fp32
- * slab of ceil(BT/128)*128 x 64 dX partial sums per (CTA, tile column)
- * pair. 0 when the fused path does not apply (BT = 0 or BT > 768) or the
- * device cannot be queried. The forge_wgrad_step_* calls and forge_dgrad
- * need no scratch: their schedulers keep their state on chip and the
- * gradient never leaves the tensor-memory accumulators.
+ * forge_workspace_bytes -- device scratch for a layer of this shape on the
+ * current device, the larger of:
+ *   - the fused paths of forge_backward_step and forge_backward_accumulate:
+ *     one fp32 slab of ceil(BT/128)*128 x 64 dX partial sums per (CTA, tile
+ *     column) pair (1 <= BT <= 768);
+ *   - the split path's input gradient, for layers whose 128 x 128 dX tiles
+ *     would leave at least half the SMs idle (short token axes): the
+ *     contraction over D_out is split in S = min(4, SMs / tiles) parts of
+ *     at least 2048 rows, run side by side (128 x 256 tiles for bf16 W)
+ *     where that occupies at least 1.5 times as many SMs as the tiles, one
+ *     fp32 partial sum per part, which a second kernel adds in a fixed order
+ *     (dX stays bit-reproducible).
+ * 0 when neither applies or the device cannot be queried. Passing less only
+ * forgoes these paths (forced fused paths then fail). The forge_wgrad_step_*
+ * calls and forge_dgrad need no scratch: their schedulers keep their state on
+ * chip and the gradient never leaves the tensor-memory accumulators.
  */
 size_t forge_workspace_bytes(int64_t d_out, int64_t d_in, int64_t bt);
 

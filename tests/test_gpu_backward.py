@@ -173,7 +173,8 @@ def test_fused_backward_one_token():
 def test_workspace_bytes_geometry():
     sms = torch.cuda.get_device_properties(0).multi_processor_count
 
-    def expect(d_out, d_in, bt):
+    def fused(d_out, d_in, bt):
+        # one fp32 slab of ceil(BT/128)*128 x 64 per (CTA, tile column) of the fused pass
         if bt < 1 or bt > 768:
             return 0
         tm, tn = -(-d_out // 128), -(-d_in // 64)
@@ -182,10 +183,29 @@ def test_workspace_bytes_geometry():
         runs = max((((c + 1) * T // G) - 1) // tm - (c * T // G) // tm + 1 for c in range(G))
         return G * runs * (-(-bt // 128) * 128 * 64) * 4
 
-    for shape in [(14336, 4096, 512), (4096, 14336, 512), (1024, 4096, 512), (136, 200, 70), (8, 8, 1)]:
-        assert F.workspace_bytes(*shape) == expect(*shape), shape
+    def split(d_out, d_in, bt):
+        # the split input gradient, where 128 x 128 tiles would leave half the
+        # SMs idle: S = min(4, SMs // tiles) parts per tile, each at least 2048
+        # rows of D_out, one 128 x bn fp32 partial sum per part (bn 128 with
+        # fp32 W, 256 with bf16 W)
+        if bt < 1 or 2 * (-(-bt // 128) * -(-d_in // 128)) > sms:
+            return 0
+        best = 0
+        for bn, rows in ((128, 128), (256, 64)):
+            tiles = -(-bt // 128) * -(-d_in // bn)
+            kb = -(-d_out // rows)
+            parts = min(4, sms // tiles)
+            while parts >= 2 and kb * rows < 2048 * parts:
+                parts -= 1
+            if parts >= 2 and 2 * tiles * parts >= 3 * (-(-bt // 128) * -(-d_in // 128)):
+                best = max(best, tiles * parts * 128 * bn * 4)
+        return best
+
+    for shape in [(14336, 4096, 512), (4096, 14336, 512), (1024, 4096, 512), (136, 200, 70), (8, 8, 1),
+                  (14336, 4096, 2048), (14336, 4096, 8192), (4096, 4096, 769), (14336, 4096, 256),
+                  (14336, 4096, 128), (4096, 4096, 256)]:
+        assert F.workspace_bytes(*shape) == max(fused(*shape), split(*shape)), shape
     assert F.workspace_bytes(4096, 4096, 0) == 0
-    assert F.workspace_bytes(4096, 4096, 769) == 0
 
 
 def test_forced_fused_without_workspace_is_an_error():
@@ -246,3 +266,31 @@ def test_fused_forced_timeout_reports_and_leaves_state():
                     **_hyper_kw("adamw"))
     F.sync_status()
     assert not torch.equal(W.cpu(), prob.W)
+
+
+@pytest.mark.parametrize("w", ["f32", "bf16"])
+@pytest.mark.parametrize("shape", [(8192, 520, 200), (6144, 1024, 128)], ids=lambda s: "x".join(map(str, s)))
+def test_split_path_input_gradient_split_contraction(w, shape):
+    # Short token axes, long contraction: on the split path the input
+    # gradient runs its contraction over D_out in parts on several SMs and a
+    # second kernel adds the parts in a fixed order. Exact inputs: dX and the
+    # state bit-exact; random inputs: within tolerance, run-to-run identical,
+    # and equal to the one-kernel dgrad (forge_dgrad) up to summation order.
+    d_out, d_in, bt = shape
+    assert F.workspace_bytes(d_out, d_in, bt) > 0
+    prob = _prob(shape, 29, w, w, exact=True)
+    got, dx = run_backward("adamw", prob, 2, path="split", sr_w=w == "bf16", seed=3)
+    ref = oracle_step("adamw", prob, w, w, 2, seed=3, sr_w=w == "bf16", mode="f32emu")
+    assert_bit_exact(got, ref, "adamw")
+    _check_dx(dx, prob, "bf16", exact=True)
+    prob = _prob(shape, 30, w, w, exact=False)
+    _, dx1 = run_backward("adamw", prob, 1, dx_dtype="f32", path="split", sr_w=w == "bf16")
+    _, dx2 = run_backward("adamw", prob, 1, dx_dtype="f32", path="split", sr_w=w == "bf16")
+    assert np.array_equal(dx1.view(np.uint32), dx2.view(np.uint32))
+    _check_dx(dx1, prob, "f32", exact=False)
+    dY, W = prob.dY.to(DEV), prob.W.to(DEV)
+    dx3 = torch.empty((bt, d_in), dtype=torch.float32, device=DEV)
+    F.dgrad(dY, W, dx3)
+    F.sync_status()
+    _, A = _dx_ref(prob)
+    assert np.all(np.abs(dx1.astype(np.float64) - dx3.cpu().numpy()) <= 2e-5 * A)
