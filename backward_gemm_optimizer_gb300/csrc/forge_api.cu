@@ -248,7 +248,9 @@ const char* opt_name(int opt) {
 int mkind(int dt) { return dt == FORGE_F32 ? M_F32 : dt == FORGE_BF16 ? M_BF16 : M_Q8; }
 
 constexpr uint64_t kTimeoutNs = 4000000000ull;  // 4 s: far beyond any healthy wait
-constexpr int64_t kOperandHintBytes = int64_t(48) << 20;  // X + dY up to 48 MB: well inside L2
+// X + dY up to 96 MB: the up-projection at BT 2048 (75 MB) gains too (fp32
+// state step 391 -> 380 us); at BT 8192 (302 MB) the policy lost (762 -> 772).
+constexpr int64_t kOperandHintBytes = int64_t(96) << 20;
 constexpr size_t kDxL2SlabBytes = size_t(16) << 20;        // dX partial slabs kept in L2 up to 16 MB
 
 // ------------------------------------------------------------------ fused input gradient: geometry
@@ -536,7 +538,7 @@ forge_status wgrad_step(int opt, const forge_tensor* X, const forge_tensor* dY, 
   p.sr_m = h->sr_moments ? 1 : 0;
   p.flags = h->flags;
   p.timeout_ns = kTimeoutNs;
-  // Operands that fit comfortably in L2 are loaded evict-last: every tile of
+  // Operands that fit in L2 are loaded evict-last: every tile of
   // a row (column) of tiles re-reads the same dY (X) slabs while the state
   // streams through L2 once and would otherwise push them out (up-projection
   // BT 512: fused backward 68 MB fewer DRAM reads, 290 -> 283 us; split step

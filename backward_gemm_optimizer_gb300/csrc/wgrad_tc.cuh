@@ -477,7 +477,7 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, N
       __syncwarp();
 #pragma unroll 1
       for (int i = 0; i < 2; ++i) {
-        // fewer than 2^19 lines (the host takes operands of at most 48 MB)
+        // fewer than 2^20 lines (the host takes operands of at most 96 MB)
         const uint32_t lines = static_cast<uint32_t>((p.op_hi[i] - p.op_lo[i]) >> 7);
         const uint32_t l1 = lines * (blockIdx.x + 1) / gridDim.x;
         const uint8_t* base = p.op_lo[i];
