@@ -112,26 +112,29 @@ __device__ __forceinline__ void dtile(int tile, int tiles_m, int tiles_n, int gr
 // s = c / num_tiles: the token tiles that share a column of W read the same
 // rows of it at the same time, so W comes from DRAM once. Every role walks
 // the same sequence.
+// (The split is a template parameter: the one-kernel walk compiles to the
+// plain tile loop -- a runtime walk cost the one-kernel dgrad 4-6 %.)
 struct SegWalk {
-  int64_t pos, end;
-  int stride;
+  int pos, end, stride;
 };
 
+template <bool SPLIT>
 __device__ __forceinline__ SegWalk seg_walk(const DgradParams& p) {
-  if (p.splitk) return SegWalk{0, 1, 0};
-  return SegWalk{static_cast<int64_t>(blockIdx.x), static_cast<int64_t>(p.num_tiles), static_cast<int>(gridDim.x)};
+  if constexpr (SPLIT) return SegWalk{0, 1, 0};
+  else return SegWalk{static_cast<int>(blockIdx.x), p.num_tiles, static_cast<int>(gridDim.x)};
 }
 
+template <bool SPLIT>
 __device__ __forceinline__ bool seg_next(const DgradParams& p, SegWalk& w, int& tile, int& kb0, int& kb1) {
   if (w.pos >= w.end) return false;
-  if (p.splitk) {
+  if constexpr (SPLIT) {
     const int part = static_cast<int>(blockIdx.x) / p.num_tiles;
     tile = static_cast<int>(blockIdx.x) % p.num_tiles;
     kb0 = static_cast<int>(static_cast<int64_t>(part) * p.num_kb / p.splitk);
     kb1 = static_cast<int>(static_cast<int64_t>(part + 1) * p.num_kb / p.splitk);
     w.pos = 1;
   } else {
-    tile = static_cast<int>(w.pos);
+    tile = w.pos;
     kb0 = 0;
     kb1 = p.num_kb;
     w.pos += w.stride;
@@ -139,7 +142,7 @@ __device__ __forceinline__ bool seg_next(const DgradParams& p, SegWalk& w, int& 
   return true;
 }
 
-template <bool F32W, int BN>
+template <bool F32W, int BN, bool SPLIT>
 __global__ void __launch_bounds__(NUM_THREADS, 1) dgrad_tc_kernel(const __grid_constant__ DgradParams p) {
   using C = DCfg<F32W, BN>;
   constexpr int A_BYTES = C::A_BYTES, B_BYTES = C::B_BYTES, STG_BYTES = C::STG_BYTES, TMEM_COLS = C::TMEM_COLS;
@@ -181,9 +184,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dgrad_tc_kernel(const __grid_c
     if (lane == 0) {
       uint32_t k = 0;
       bool ok = true;
-      SegWalk w = seg_walk(p);
+      SegWalk w = seg_walk<SPLIT>(p);
       int tile, kb0, kb1;
-      while (ok && seg_next(p, w, tile, kb0, kb1)) {
+      while (ok && seg_next<SPLIT>(p, w, tile, kb0, kb1)) {
         int tm, tn;
         dtile(tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
         for (int kb = kb0; kb < kb1; ++kb, ++k) {
@@ -206,9 +209,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dgrad_tc_kernel(const __grid_c
       uint32_t k = 0;
       uint32_t ks = 0;  // fp32 staging slots filled
       bool ok = true;
-      SegWalk w = seg_walk(p);
+      SegWalk w = seg_walk<SPLIT>(p);
       int tile, kb0, kb1;
-      while (ok && seg_next(p, w, tile, kb0, kb1)) {
+      while (ok && seg_next<SPLIT>(p, w, tile, kb0, kb1)) {
         int tm, tn;
         dtile(tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
         for (int kb = kb0; kb < kb1; ++kb, ++k) {
@@ -253,9 +256,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dgrad_tc_kernel(const __grid_c
       uint32_t k = 0;
       bool ok = true;
       int it = 0;
-      SegWalk w = seg_walk(p);
+      SegWalk w = seg_walk<SPLIT>(p);
       int tile, kb0, kb1;
-      for (; ok && seg_next(p, w, tile, kb0, kb1); ++it) {
+      for (; ok && seg_next<SPLIT>(p, w, tile, kb0, kb1); ++it) {
         const int buf = it & 1;
         if (!dwait(&tm_empty[buf], ((it >> 1) & 1) ^ 1u, abort_flag, p.status, WAIT_TMEM_EMPTY, lim)) {
           ok = false;
@@ -306,9 +309,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dgrad_tc_kernel(const __grid_c
     const int r = q * 32 + lane;
     int it = 0;
     bool ok = true;
-    SegWalk w = seg_walk(p);
+    SegWalk w = seg_walk<SPLIT>(p);
     int tile, kb0, kb1;
-    for (; ok && seg_next(p, w, tile, kb0, kb1); ++it) {
+    for (; ok && seg_next<SPLIT>(p, w, tile, kb0, kb1); ++it) {
       int tm, tn;
       dtile(tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
       const int buf = it & 1;
@@ -320,7 +323,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dgrad_tc_kernel(const __grid_c
       const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * BN);
       // A split contraction: this CTA's fp32 partial sum goes to its slot
       // (row r of a 128 x BN slab), for the fix-up kernel to add in order.
-      const bool partial = p.splitk != 0;
+      constexpr bool partial = SPLIT;
       float* slot = partial ? p.part + (static_cast<int64_t>(blockIdx.x) * BM + r) * BN : nullptr;
 #pragma unroll 1
       for (int c = 0; c < BN / 16; ++c) {
@@ -382,9 +385,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dgrad_tc_kernel(const __grid_c
     const int ct = threadIdx.x - 256;
     uint32_t k = 0, ks = 0;
     bool ok = true;
-    SegWalk w = seg_walk(p);
+    SegWalk w = seg_walk<SPLIT>(p);
     int tile, kb0, kb1;
-    while (ok && seg_next(p, w, tile, kb0, kb1)) {
+    while (ok && seg_next<SPLIT>(p, w, tile, kb0, kb1)) {
       for (int kb = kb0; kb < kb1; ++kb, ++k) {
         const int sb = static_cast<int>(k % SB);
         uint8_t* b = b_ring + sb * B_BYTES;
@@ -478,12 +481,13 @@ __global__ void __launch_bounds__(256) dgrad_fixup_kernel(const DgradFixupParams
   }
 }
 
-template <bool F32W, int BN>
+template <bool F32W, int BN, bool SPLIT>
 cudaError_t launch_d(const DgradParams& p, int grid, cudaStream_t stream) {
   // The stage depth the host encoded the tensor maps and num_kb for must be
   // the kernel's: a mismatch would overfill the shared-memory rings.
-  if (p.bk != DCfg<F32W, BN>::BK || (p.w_f32 != nullptr) != F32W) return cudaErrorInvalidValue;
-  auto kern = dgrad_tc_kernel<F32W, BN>;
+  if (p.bk != DCfg<F32W, BN>::BK || (p.w_f32 != nullptr) != F32W || (p.splitk != 0) != SPLIT)
+    return cudaErrorInvalidValue;
+  auto kern = dgrad_tc_kernel<F32W, BN, SPLIT>;
   static unsigned long long attr_mask = 0ull;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -515,8 +519,12 @@ cudaError_t launch_dgrad_fixup(const DgradFixupParams& p, cudaStream_t stream) {
 }
 
 cudaError_t launch_dgrad_tc(const DgradParams& p, int grid, cudaStream_t stream) {
-  if (p.w_f32) return p.bn == 128 ? launch_d<true, 128>(p, grid, stream) : cudaErrorInvalidValue;
-  return p.bn == 256 ? launch_d<false, 256>(p, grid, stream) : launch_d<false, 128>(p, grid, stream);
+  if (p.splitk) {
+    if (p.w_f32) return p.bn == 128 ? launch_d<true, 128, true>(p, grid, stream) : cudaErrorInvalidValue;
+    return p.bn == 256 ? launch_d<false, 256, true>(p, grid, stream) : cudaErrorInvalidValue;
+  }
+  if (p.w_f32) return p.bn == 128 ? launch_d<true, 128, false>(p, grid, stream) : cudaErrorInvalidValue;
+  return p.bn == 256 ? launch_d<false, 256, false>(p, grid, stream) : launch_d<false, 128, false>(p, grid, stream);
 }
 
 }  // namespace forge
