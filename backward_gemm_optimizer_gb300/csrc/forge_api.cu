@@ -498,7 +498,15 @@ forge_status wgrad_step(int opt, const forge_tensor* X, const forge_tensor* dY, 
   // Lion up-projection 225.3 -> 220.6 us, SGD-momentum unchanged, both a
   // little slower at 256.
   const bool narrow = dx != nullptr && wk == W_F32 && mk == M_F32 && (nst == 2 || (nst == 1 && bt >= 512));
-  const int cw = narrow ? 16 : 32;
+  // 64-column chunks for the plain step with bf16 W and bf16 moments on
+  // 128-column tiles below 768 tokens: half as many slot hand-overs for the
+  // same bytes in flight (up-projection, AdamW: BT 256 176.4 -> 168.2 us,
+  // BT 512 178.0 -> 175.5 us). From 768 tokens the 48 KB slots cost the ring
+  // its fourth operand stage (181 -> 184 us), and on 256-column tiles its
+  // third (BT 2048: 253 -> 319 us).
+  const bool wide = dx == nullptr && G_acc == nullptr && !accum && wk == W_BF16 && mk == M_BF16 && nst >= 1 &&
+                    bn == 128 && bt < 768;
+  const int cw = narrow ? 16 : (wide ? 64 : 32);
   if ((st = encode_state(&p.tm_w, W, "W", cw)) != FORGE_OK) return st;
   if (nst >= 1) {
     if ((st = encode_state(&p.tm_m, m, "m", cw)) != FORGE_OK) return st;
@@ -561,6 +569,7 @@ forge_status wgrad_step(int opt, const forge_tensor* X, const forge_tensor* dY, 
   l.opt = opt; l.wk = wk; l.mk = mk; l.bn = bn; l.deep = deep; l.dx = dx != nullptr ? 1 : 0;
   l.ga = G_acc != nullptr ? 1 : 0;
   l.narrow = narrow ? 1 : 0;
+  l.wide = wide ? 1 : 0;
   l.grid = p.num_tiles < dev->sms ? p.num_tiles : dev->sms;
   l.stream = s;
   DxGeometry g;

@@ -141,6 +141,7 @@ struct TcLaunch {
   int dx;       // 1: fused input gradient (64-column tiles, fp32 / bf16 state)
   int ga;       // 1: add the accumulated gradient G_acc (tm_g) to each tile
   int narrow;   // 1: 16-column state chunks (fused kernel, fp32 W and moments, short token axes)
+  int wide;     // 1: 64-column state chunks (plain step, bf16 W and bf16 moments)
   int grid;
   cudaStream_t stream;
 };

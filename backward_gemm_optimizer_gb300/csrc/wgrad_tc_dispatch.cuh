@@ -11,9 +11,10 @@ namespace forge {
 // shared memory (barriers + the 8 KB absmax exchange) is accounted for.
 constexpr int kDynSmemBudget = 227 * 1024 - 9 * 1024;
 
-template <int OPT, int WK, int MK, int BN, int STAGES, bool DX = false, bool GA = false, bool NARROW = false>
+template <int OPT, int WK, int MK, int BN, int STAGES, bool DX = false, bool GA = false, bool NARROW = false,
+          bool WIDE = false>
 constexpr int slots_that_fit() {
-  using C = TcCfg<OPT, WK, MK, BN, STAGES, 2, DX, GA, NARROW>;
+  using C = TcCfg<OPT, WK, MK, BN, STAGES, 2, DX, GA, NARROW, WIDE>;
   const int avail = kDynSmemBudget - 1024 - STAGES * C::STAGE_BYTES - C::WB_BYTES;
   const int n = avail / C::SLOT_BYTES;
   return n > 8 ? 8 : n;
@@ -22,21 +23,21 @@ constexpr int slots_that_fit() {
 // Operand stages: 2 for short token axes (the step is bound by the state
 // stream); for long ones as many as leave room for the state ring (4, else
 // 3, else 2).
-template <int OPT, int WK, int MK, int BN, int DEEP>
+template <int OPT, int WK, int MK, int BN, int DEEP, bool WIDE = false>
 constexpr int pick_stages() {
   if (!DEEP) return 2;
   constexpr int need = (MK == M_Q8) ? 4 : 2;
-  if (slots_that_fit<OPT, WK, MK, BN, 4>() >= need) return 4;
-  if (slots_that_fit<OPT, WK, MK, BN, 3>() >= need) return 3;
+  if (slots_that_fit<OPT, WK, MK, BN, 4, false, false, false, WIDE>() >= need) return 4;
+  if (slots_that_fit<OPT, WK, MK, BN, 3, false, false, false, WIDE>() >= need) return 3;
   return 2;
 }
 
-template <int OPT, int WK, int MK, int BN, int DEEP>
+template <int OPT, int WK, int MK, int BN, int DEEP, bool WIDE = false>
 cudaError_t launch_one(const WgradTcParams& p, int grid, cudaStream_t stream) {
-  constexpr int S = pick_stages<OPT, WK, MK, BN, DEEP>();
-  constexpr int N = slots_that_fit<OPT, WK, MK, BN, S>();
+  constexpr int S = pick_stages<OPT, WK, MK, BN, DEEP, WIDE>();
+  constexpr int N = slots_that_fit<OPT, WK, MK, BN, S, false, false, false, WIDE>();
   static_assert(N >= ((MK == M_Q8) ? 4 : 2), "state ring does not fit");
-  return launch_tc_variant<OPT, WK, MK, BN, S, N, false>(p, grid, stream);
+  return launch_tc_variant<OPT, WK, MK, BN, S, N, false, false, false, WIDE>(p, grid, stream);
 }
 
 // Step with an accumulated gradient (the last micro-batch): two operand
@@ -88,9 +89,18 @@ cudaError_t launch_mk(const WgradTcParams& p, const TcLaunch& l) {
                   : launch_one<OPT, WK, MK, 128, 0>(p, l.grid, l.stream);
   } else {
     if (l.bn == 64) {
-      if (l.deep) return cudaErrorInvalidValue;
+      if (l.deep || l.wide) return cudaErrorInvalidValue;
       return launch_one<OPT, WK, MK, 64, 0>(p, l.grid, l.stream);
     }
+    if constexpr (WK == W_BF16 && MK == M_BF16 && opt_nstate(OPT) >= 1) {
+      // 64-column state chunks (128-column tiles only).
+      if (l.wide) {
+        if (l.bn != 128) return cudaErrorInvalidValue;
+        return l.deep ? launch_one<OPT, WK, MK, 128, 1, true>(p, l.grid, l.stream)
+                      : launch_one<OPT, WK, MK, 128, 0, true>(p, l.grid, l.stream);
+      }
+    }
+    if (l.wide) return cudaErrorInvalidValue;
     if (l.bn == 256) {
       // 128 x 256 tiles for long token axes: a quarter less operand traffic
       // per gradient element than 128 x 128, half the MMA instructions.

@@ -388,6 +388,21 @@ def test_wide_tiles_exact(opt, variant, shape):
     assert_bit_exact(got, ref, opt)
 
 
+@pytest.mark.parametrize("opt", ["adamw", "lion", "sgdm", "nadam"])
+@pytest.mark.parametrize("shape", [(264, 520, 300), (136, 200, 600), (384, 1024, 1100)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_bf16_state_64_column_chunks_exact(opt, shape):
+    # bf16 W + bf16 moments on 128-column tiles below 768 tokens stream the
+    # state in 64-column chunks (two- and three-stage operand rings at 300
+    # and 600 tokens), elsewhere in 32-column ones; ragged D_in leaves a
+    # chunk partly or wholly past the edge.
+    prob = _prob(shape, 23, "bf16", "bf16", "bf16", exact=True)
+    for flag in (F.FLAG_TILE_N_128, F.FLAG_TILE_N_256):
+        got = gpu_step(opt, prob, 2, seed=9, sr_w=True, sr_moments=True, flags=flag)
+        ref = oracle_step(opt, prob, "bf16", "bf16", 2, seed=9, sr_w=True, sr_moments=True, mode="f32emu")
+        assert_bit_exact(got, ref, opt)
+
+
 @pytest.mark.parametrize("exact", [True, False])
 def test_tile_width_invariance_wide(exact):
     prob = _prob((512, 768, 1088), 18, "bf16", "f32", "f32", exact=exact)
@@ -400,3 +415,41 @@ def test_wide_tiles_random_within_tolerance():
     prob = _prob((640, 1024, 2048), 19, "bf16", "f32", "f32", exact=False)
     got = gpu_step("adamw", prob, 3, flags=F.FLAG_TILE_N_256)
     check_tolerance("adamw", prob, "f32", "f32", 3, got)
+
+
+# ---------------------------------------------------------------------------
+# Non-finite weights through the stochastic-rounding store
+# ---------------------------------------------------------------------------
+
+def _bf16_is_nan(b):
+    b = np.asarray(b, np.uint16)
+    return (b & 0x7FFF) > 0x7F80
+
+
+@pytest.mark.parametrize("flag", ["n128", "n64"])
+def test_sr_store_non_finite_weights(flag):
+    # NaN and +-Inf weights (bf16 W, stochastic rounding): a NaN stays a NaN
+    # (its payload is the arithmetic's, which differs between the GPU and the
+    # host), an infinity stays that infinity, and every finite neighbour in
+    # the same group of eight -- the kernel tests a group for NaN at once --
+    # takes the oracle's draws bit for bit. Both chunk widths of the bf16
+    # store (64 columns on 128-column tiles, 32 on 64-column ones).
+    prob = _prob((256, 512, 200), 29, "bf16", "bf16", "bf16", exact=True)
+    bits = prob.W.view(torch.int16).numpy().view(np.uint16)
+    planted = {(0, 0): 0x7FC0, (0, 3): 0xFFC1, (5, 9): 0x7F81, (7, 16): 0x7F80, (7, 17): 0xFF80,
+               (100, 200): 0x7F80, (130, 64): 0x7FC0, (255, 511): 0xFF80, (200, 130): 0xFFFF}
+    for (i, j), b in planted.items():
+        bits[i, j] = b
+    flags = F.FLAG_TILE_N_128 if flag == "n128" else F.FLAG_TILE_N_64
+    got = gpu_step("adamw", prob, 2, seed=9, sr_w=True, sr_moments=True, flags=flags)
+    with np.errstate(invalid="ignore"):
+        ref = oracle_step("adamw", prob, "bf16", "bf16", 2, seed=9, sr_w=True, sr_moments=True, mode="f32emu")
+    nan_ref = _bf16_is_nan(ref.W)
+    assert np.array_equal(_bf16_is_nan(got.W), nan_ref)
+    assert int(nan_ref.sum()) == 5
+    fin = ~nan_ref
+    assert np.array_equal(np.asarray(got.W)[fin], np.asarray(ref.W)[fin])
+    for (i, j), b in planted.items():
+        if b in (0x7F80, 0xFF80):
+            assert int(got.W[i, j]) == b
+    assert_bit_exact(O.State(W=ref.W, m=got.m, v=got.v), ref, "adamw")
