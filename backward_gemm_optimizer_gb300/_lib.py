@@ -21,6 +21,7 @@ F32, BF16, I8B128 = 0, 1, 2
 FLAG_TILE_N_AUTO, FLAG_TILE_N_128, FLAG_TILE_N_64, FLAG_TILE_N_256 = 0, 1, 2, 3
 FLAG_TEST_FORCE_TIMEOUT = 0x100
 FLAG_BACKWARD_FUSED, FLAG_BACKWARD_SPLIT = 0x200, 0x400
+FLAG_DGRAD_TOKENS_128, FLAG_DGRAD_ALL_TOKENS = 0x800, 0x1000
 RULES = {"adamw": 0, "sgdm": 1, "lion": 2, "sgd": 3, "rmsprop": 4, "adagrad": 5, "nadam": 6, "radam": 7}
 
 STATUS_NAMES = {0: "FORGE_OK", 1: "FORGE_ERR_INVALID_ARG", 2: "FORGE_ERR_UNSUPPORTED",

@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -296,31 +297,106 @@ DxGeometry dx_geometry(int64_t d_out, int64_t d_in, int64_t bt, int sms) {
 // bf16 state, split path): up-projection BT 256 176.6 -> 159 us; where the
 // tiles already fill half the GPU, or the contraction is short, the split
 // lost (BT 512: q/o 72 -> 83 us, k/v 34 -> 46 us, up-projection even).
-struct DgradSplit {
-  int bn = 0, tiles_m = 0, tiles_n = 0, num_tiles = 0, num_kb = 0, parts = 0;
-  size_t bytes = 0;  // one 128 x bn fp32 partial sum per CTA
-  bool worthwhile = false;
+// How the input gradient is tiled, and whether its contraction over D_out
+// is split over several CTAs (parts >= 2; needs `bytes` of workspace for
+// the fp32 partial sums, which dgrad_fixup_kernel adds in a fixed order).
+struct DgradPlan {
+  int mb = 1;         // 128-token blocks per tile (2 / 4: all tokens of BT <= 256 / 512)
+  int bn = 128;       // tile width (input features)
+  int bk = 128;       // rows of D_out per stage
+  int stg_rows = 64;  // fp32 W: rows per staging slot
+  int tiles_m = 0, tiles_n = 0, num_tiles = 0, num_kb = 0;
+  int parts = 0;
+  size_t bytes = 0;
+  double cost = 0.0;  // bytes through the busiest SM's shared memory (dgrad_cost)
 };
 
-DgradSplit dgrad_split(int64_t d_out, int64_t d_in, int64_t bt, bool w_bf16, int sms) {
-  DgradSplit g;
-  if (bt < 1 || d_out < 1 || d_in < 1 || sms < 1) return g;
-  g.bn = w_bf16 ? 256 : 128;
-  const int64_t rows_per_stage = g.bn == 128 ? 128 : 64;
-  g.tiles_m = static_cast<int>((bt + 127) / 128);
-  g.tiles_n = static_cast<int>((d_in + g.bn - 1) / g.bn);
-  g.num_tiles = g.tiles_m * g.tiles_n;
-  g.num_kb = static_cast<int>((d_out + rows_per_stage - 1) / rows_per_stage);
-  const int64_t tiles128 = static_cast<int64_t>(g.tiles_m) * ((d_in + 127) / 128);
-  int parts = sms / g.num_tiles;
-  if (parts > 4) parts = 4;
-  while (parts >= 2 && g.num_kb * (rows_per_stage / 64) < 32 * parts) --parts;
-  g.parts = parts;
-  // ... and only where it puts more SMs to work than whole 128 x 128 tiles
-  // would (q/o at BT 256: 2 x 32 tiles either way, 64.1 -> 70.7 us split).
-  g.worthwhile = parts >= 2 && 2 * tiles128 <= sms && 2 * g.num_tiles * parts >= 3 * tiles128;
-  g.bytes = g.worthwhile ? static_cast<size_t>(g.num_tiles) * parts * 128 * g.bn * sizeof(float) : 0;
-  return g;
+// The kernel is bound by shared-memory bandwidth (about 128 bytes per
+// clock per SM): the TMA writes of dY and W, the fp32-to-bf16 converters'
+// reads and writes, and the tensor cores' operand reads. Per multiply-add,
+// with tiles of MB blocks of 128 tokens x BN features:
+//   dY written 2/BN + W written (and converted) (wb + 6 [fp32]) / (128 MB)
+//   + operands read 2/BN + 1/64 bytes.
+// This model gives the measured times within 0.7-1.0 (128 x 128 tiles,
+// fp32 weights: 29.4 MB through shared memory per CTA, 117 us). A plan's
+// cost is waves x that per CTA (token blocks padded to 128), plus, for a
+// split, 740 KB for the fix-up launch (3 us).
+double dgrad_cost(const DgradPlan& g, int64_t d_out, int wbytes, bool f32w, int sms) {
+  const int parts = g.parts >= 2 ? g.parts : 1;
+  const int64_t ctas = static_cast<int64_t>(g.num_tiles) * parts;
+  const double waves = static_cast<double>((ctas + sms - 1) / sms);
+  const double per_mac = 4.0 / g.bn + (wbytes + (f32w ? 6.0 : 0.0)) / (128.0 * g.mb) + 1.0 / 64.0;
+  const double macs = 128.0 * g.mb * g.bn * (static_cast<double>(d_out) / parts);
+  double c = waves * macs * per_mac;
+  if (g.parts >= 2) c += 740e3;
+  return c;
+}
+
+// force: 0 the cheapest plan, 1 128-token tiles only, 2 all-token tiles only
+// (an empty plan, num_tiles == 0, where they do not apply).
+DgradPlan dgrad_plan(int64_t d_out, int64_t d_in, int64_t bt, bool w_bf16, int sms, bool may_split, int force = 0) {
+  DgradPlan best;
+  if (bt < 1 || d_out < 1 || d_in < 1 || sms < 1) return best;
+  const int wbytes = w_bf16 ? 2 : 4;
+  auto finish = [&](DgradPlan g) {
+    g.tiles_n = static_cast<int>((d_in + g.bn - 1) / g.bn);
+    g.num_tiles = g.tiles_m * g.tiles_n;
+    g.num_kb = static_cast<int>((d_out + g.bk - 1) / g.bk);
+    g.cost = dgrad_cost(g, d_out, wbytes, !w_bf16, sms);
+    g.bytes = g.parts >= 2 ? static_cast<size_t>(g.num_tiles) * g.parts * 128 * g.mb * g.bn * sizeof(float) : 0;
+    return g;
+  };
+  // 1. 128-token tiles, 128 x 256 for bf16 weights when those still fill
+  //    the GPU (half the dY traffic per output of 128 x 128).
+  {
+    DgradPlan g;
+    g.tiles_m = static_cast<int>((bt + 127) / 128);
+    g.bn = (w_bf16 && g.tiles_m * ((d_in + 255) / 256) >= sms) ? 256 : 128;
+    g.bk = g.bn == 128 ? 128 : 64;
+    best = finish(g);
+    if (force == 2) best = DgradPlan{};
+  }
+  // 2. The same tiles with the contraction split in S = min(4, SMs / tiles)
+  //    parts of >= 2048 rows, where that puts >= 1.5x as many SMs to work
+  //    as whole 128 x 128 tiles would (bf16 weights on 128 x 256 tiles).
+  if (may_split && force != 2) {
+    DgradPlan g;
+    g.tiles_m = static_cast<int>((bt + 127) / 128);
+    g.bn = w_bf16 ? 256 : 128;
+    g.bk = g.bn == 128 ? 128 : 64;
+    g = finish(g);
+    const int64_t tiles128 = static_cast<int64_t>(g.tiles_m) * ((d_in + 127) / 128);
+    int parts = sms / g.num_tiles;
+    if (parts > 4) parts = 4;
+    while (parts >= 2 && g.num_kb * (g.bk / 64) < 32 * parts) --parts;
+    if (parts >= 2 && 2 * tiles128 <= sms && 2 * g.num_tiles * parts >= 3 * tiles128) {
+      g.parts = parts;
+      g = finish(g);
+      if (g.cost < best.cost) best = g;
+    }
+  }
+  // 3. All-token tiles on short token axes: 2 or 4 blocks of 128 tokens x
+  //    128 columns (one weight read and conversion per tile instead of one
+  //    per 128 tokens) in 64-row stages, the contraction split in
+  //    S = min(4, SMs / tiles) parts of >= 256 rows where a workspace allows.
+  if (bt > 128 && bt <= 512 && force != 1) {
+    DgradPlan g;
+    g.mb = bt <= 256 ? 2 : 4;
+    g.tiles_m = 1;
+    g.bn = 128;
+    g.bk = 64;
+    g.stg_rows = 32;
+    g = finish(g);
+    if (may_split) {
+      int parts = sms / g.num_tiles;
+      if (parts > 4) parts = 4;
+      while (parts >= 2 && g.num_kb * g.bk < 256 * parts) --parts;
+      if (parts >= 2) g.parts = parts;
+      g = finish(g);
+    }
+    if (force == 2 || g.cost < best.cost) best = g;
+  }
+  return best;
 }
 
 // Extra arguments of the fused backward pass (dX and its workspace). W_dx:
@@ -640,7 +716,11 @@ bool dx_worthwhile(const DxGeometry& g, int64_t d_out, int64_t d_in, int w_bytes
 }
 
 forge_status dgrad_impl(const forge_tensor* dY, const forge_tensor* W_old, forge_tensor* dX, forge_stream_t stream,
-                        void* ws = nullptr, size_t ws_bytes = 0);
+                        void* ws = nullptr, size_t ws_bytes = 0, uint32_t flags = 0);
+
+// forge_backward_step's own flags, taken off before the step.
+constexpr uint32_t kBackwardOnlyFlags =
+    FORGE_FLAG_BACKWARD_FUSED | FORGE_FLAG_BACKWARD_SPLIT | FORGE_FLAG_DGRAD_TOKENS_128 | FORGE_FLAG_DGRAD_ALL_TOKENS;
 
 forge_status backward_step(int opt, const forge_tensor* X, const forge_tensor* dY, forge_tensor* W, forge_tensor* s0,
                            forge_tensor* s1, forge_tensor* dX, const forge_hyper* h, int64_t step, uint64_t seed,
@@ -649,9 +729,14 @@ forge_status backward_step(int opt, const forge_tensor* X, const forge_tensor* d
   if (X == nullptr || dY == nullptr || W == nullptr || dX == nullptr || h == nullptr)
     return fail(FORGE_ERR_INVALID_ARG, "backward_step(%s): null argument", oname);
   const bool want_fused = (h->flags & FORGE_FLAG_BACKWARD_FUSED) != 0;
-  const bool want_split = (h->flags & FORGE_FLAG_BACKWARD_SPLIT) != 0;
-  if (want_fused && want_split)
+  const bool dgrad_tiles = (h->flags & (FORGE_FLAG_DGRAD_TOKENS_128 | FORGE_FLAG_DGRAD_ALL_TOKENS)) != 0;
+  const bool want_split = (h->flags & FORGE_FLAG_BACKWARD_SPLIT) != 0 || dgrad_tiles;
+  if (want_fused && (h->flags & FORGE_FLAG_BACKWARD_SPLIT))
     return fail(FORGE_ERR_INVALID_ARG, "backward_step(%s): both BACKWARD_FUSED and BACKWARD_SPLIT set", oname);
+  if (want_fused && dgrad_tiles)
+    return fail(FORGE_ERR_INVALID_ARG, "backward_step(%s): DGRAD_* tile flags apply to the split path only", oname);
+  if ((h->flags & FORGE_FLAG_DGRAD_TOKENS_128) && (h->flags & FORGE_FLAG_DGRAD_ALL_TOKENS))
+    return fail(FORGE_ERR_INVALID_ARG, "backward_step(%s): both DGRAD_TOKENS_128 and DGRAD_ALL_TOKENS set", oname);
   const int64_t bt = X->rows, d_in = X->cols, d_out = dY->cols;
   if (dX->dtype != FORGE_BF16 && dX->dtype != FORGE_F32)
     return fail(FORGE_ERR_UNSUPPORTED, "backward_step(%s): dX must be bf16 or f32", oname);
@@ -683,9 +768,9 @@ forge_status backward_step(int opt, const forge_tensor* X, const forge_tensor* d
   if (X->dtype != FORGE_BF16)
     return fail(FORGE_ERR_UNSUPPORTED, "backward_step(%s): dX needs bf16 dY (the fp32-input step has no dgrad)",
                 oname);
-  if ((st = dgrad_impl(dY, W, dX, stream, ws, ws_bytes)) != FORGE_OK) return st;
+  if ((st = dgrad_impl(dY, W, dX, stream, ws, ws_bytes, h->flags)) != FORGE_OK) return st;
   forge_hyper h2 = *h;
-  h2.flags &= ~(FORGE_FLAG_BACKWARD_FUSED | FORGE_FLAG_BACKWARD_SPLIT);
+  h2.flags &= ~kBackwardOnlyFlags;
   return wgrad_step(opt, X, dY, W, s0, s1, &h2, step, seed, stream);
 }
 
@@ -825,7 +910,7 @@ forge_status forge_wgrad_step_accumulated(forge_rule rule, const forge_tensor* X
 namespace {
 
 forge_status dgrad_impl(const forge_tensor* dY, const forge_tensor* W_old, forge_tensor* dX, forge_stream_t stream,
-                        void* ws, size_t ws_bytes) {
+                        void* ws, size_t ws_bytes, uint32_t flags) {
   if (dY == nullptr || W_old == nullptr || dX == nullptr) return fail(FORGE_ERR_INVALID_ARG, "dgrad: null argument");
   const int64_t bt = dY->rows, d_out = dY->cols, d_in = W_old->cols;
   if (bt < 0 || d_out < 0 || d_in < 0) return fail(FORGE_ERR_INVALID_ARG, "dgrad: negative size");
@@ -849,9 +934,6 @@ forge_status dgrad_impl(const forge_tensor* dY, const forge_tensor* W_old, forge
   if ((st = device_info(&dev)) != FORGE_OK) return st;
   DgradParams p;
   std::memset(&p, 0, sizeof(p));
-  if ((st = encode_2d(&p.tm_dy, dY, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, "dY")) !=
-      FORGE_OK)
-    return st;
   p.dX = dX->data;
   p.ld_dx = dX->ld;
   p.dx_bf16 = dX->dtype == FORGE_BF16 ? 1 : 0;
@@ -859,45 +941,54 @@ forge_status dgrad_impl(const forge_tensor* dY, const forge_tensor* W_old, forge
   p.bt = static_cast<int>(bt);
   p.d_out = static_cast<int>(d_out);
   p.d_in = static_cast<int>(d_in);
-  p.tiles_m = static_cast<int>((bt + 127) / 128);
-  // 128 x 256 tiles for bf16 weights when they still fill the GPU (long
-  // token axes): half the dY operand traffic per output of 128 x 128. With
-  // a workspace large enough, layers with few tiles split the contraction
-  // over D_out (dgrad_split).
-  const DgradSplit sp = dgrad_split(d_out, d_in, bt, W_old->dtype == FORGE_BF16, dev->sms);
-  const bool split = sp.worthwhile && ws != nullptr && ws_bytes >= sp.bytes &&
-                     reinterpret_cast<uintptr_t>(ws) % 16 == 0;
-  p.bn = split ? sp.bn : (W_old->dtype == FORGE_BF16 && p.tiles_m * ((d_in + 255) / 256) >= dev->sms) ? 256 : 128;
-  p.tiles_n = static_cast<int>((d_in + p.bn - 1) / p.bn);
-  p.num_tiles = p.tiles_m * p.tiles_n;
-  // Rows of D_out per stage: 128 on 128-column tiles, 64 on 128 x 256 tiles.
+  // The plan (dgrad_plan): tile shape, and a split contraction where the
+  // caller's workspace holds its partial sums.
+  const bool w_bf16 = W_old->dtype == FORGE_BF16;
+  const bool ws_ok = ws != nullptr && reinterpret_cast<uintptr_t>(ws) % 16 == 0;
+  const int force = (flags & FORGE_FLAG_DGRAD_ALL_TOKENS) ? 2 : (flags & FORGE_FLAG_DGRAD_TOKENS_128) ? 1 : 0;
+  DgradPlan g = dgrad_plan(d_out, d_in, bt, w_bf16, dev->sms, ws_ok, force);
+  if (g.parts >= 2 && ws_bytes < g.bytes) g = dgrad_plan(d_out, d_in, bt, w_bf16, dev->sms, false, force);
+  if (g.num_tiles == 0)
+    return fail(FORGE_ERR_UNSUPPORTED, "dgrad: all-token tiles need 128 < BT <= 512 (BT = %lld)", (long long)bt);
+  const bool split = g.parts >= 2;
+  // dY boxes: 64 K columns x 128 token rows, 128-byte swizzle.
+  if ((st = encode_2d(&p.tm_dy, dY, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, "dY")) !=
+      FORGE_OK)
+    return st;
+  p.mb = g.mb;
+  p.bn = g.bn;
+  p.bk = g.bk;
+  p.stg_rows = g.stg_rows;
+  // All-token tiles start their stage walks at evenly spaced stages, so that
+  // the tiles (which all read the same dY rows) spread over L2 (down-
+  // projection, bf16 weights, BT 512: 86 -> 76 us; 128-token tiles: no gain).
+  p.k_rotate = g.mb > 1 ? 1 : 0;
+  p.tiles_m = g.tiles_m;
+  p.tiles_n = g.tiles_n;
+  p.num_tiles = g.num_tiles;
+  p.num_kb = g.num_kb;
   // The W boxes must match what the kernel expects per load: bf16 weights
-  // one box of 64 columns x rows_per_stage; fp32 weights 32-column x 64-row
-  // boxes (staged in 64-row slots, two per 128-row stage).
-  const int64_t rows_per_stage = p.bn == 128 ? 128 : 64;
-  if (W_old->dtype == FORGE_BF16) {
-    if ((st = encode_2d(&p.tm_w, W_old, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64,
-                        static_cast<uint32_t>(rows_per_stage), CU_TENSOR_MAP_SWIZZLE_128B, "W")) != FORGE_OK)
+  // one box of 64 columns x bk rows; fp32 weights 32-column x stg_rows
+  // boxes (staged in slots of stg_rows rows, bk / stg_rows per stage).
+  if (w_bf16) {
+    if ((st = encode_2d(&p.tm_w, W_old, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, static_cast<uint32_t>(g.bk),
+                        CU_TENSOR_MAP_SWIZZLE_128B, "W")) != FORGE_OK)
       return st;
     p.w_f32 = nullptr;
   } else {
-    if ((st = encode_2d(&p.tm_w, W_old, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 32, 64, CU_TENSOR_MAP_SWIZZLE_128B,
-                        "W")) != FORGE_OK)
+    if ((st = encode_2d(&p.tm_w, W_old, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 32, static_cast<uint32_t>(g.stg_rows),
+                        CU_TENSOR_MAP_SWIZZLE_128B, "W")) != FORGE_OK)
       return st;
     p.w_f32 = static_cast<const float*>(W_old->data);
     p.ld_w32 = W_old->ld;
   }
-  p.bk = static_cast<int>(rows_per_stage);
-  p.num_kb = static_cast<int>((d_out + rows_per_stage - 1) / rows_per_stage);
   p.group_m = 8;
   p.timeout_ns = kTimeoutNs;
   int grid = p.num_tiles < dev->sms ? p.num_tiles : dev->sms;
   if (split) {
-    if (sp.num_tiles != p.num_tiles || sp.num_kb != p.num_kb)
-      return fail(FORGE_ERR_INVALID_ARG, "dgrad: internal geometry mismatch");
-    p.splitk = sp.parts;
+    p.splitk = g.parts;
     p.part = static_cast<float*>(ws);
-    grid = sp.num_tiles * sp.parts;
+    grid = g.num_tiles * g.parts;
   }
   cudaError_t e = launch_dgrad_tc(p, grid, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(FORGE_ERR_CUDA, "dgrad launch: %s", cudaGetErrorString(e));
@@ -914,7 +1005,8 @@ forge_status dgrad_impl(const forge_tensor* dY, const forge_tensor* W_old, forge
     f.tiles_n = p.tiles_n;
     f.group_m = p.group_m;
     f.num_tiles = p.num_tiles;
-    f.parts = sp.parts;
+    f.parts = g.parts;
+    f.rows = 128 * g.mb;
     e = launch_dgrad_fixup(f, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail(FORGE_ERR_CUDA, "dgrad fix-up launch: %s", cudaGetErrorString(e));
   }
@@ -969,8 +1061,8 @@ size_t forge_workspace_bytes(int64_t d_out, int64_t d_in, int64_t bt) {
   const size_t fused = dx_geometry(d_out, d_in, bt, dev->sms).bytes;
   size_t split = 0;
   for (const bool w_bf16 : {false, true}) {
-    const DgradSplit g = dgrad_split(d_out, d_in, bt, w_bf16, dev->sms);
-    if (g.worthwhile && g.bytes > split) split = g.bytes;
+    const DgradPlan g = dgrad_plan(d_out, d_in, bt, w_bf16, dev->sms, true);
+    if (g.bytes > split) split = g.bytes;
   }
   return fused > split ? fused : split;
 }

@@ -102,7 +102,7 @@ struct WgradSimtParams {
 // Input gradient dX = dY W (tensor cores).
 struct alignas(128) DgradParams {
   CUtensorMap tm_dy;  // dY [BT][D_out] bf16, box 64 (K) x 128 (M rows), 128-byte swizzle
-  CUtensorMap tm_w;   // W [D_out][D_in]: bf16, box 64 (N) x bk (K); or fp32, box 32 (N) x 64 (K); 128-byte swizzle
+  CUtensorMap tm_w;   // W [D_out][D_in]: bf16, box 64 (N) x bk (K); or fp32, box 32 (N) x stg_rows (K); 128-byte swizzle
   const float* w_f32; // W fp32 (staged and rounded to bf16 by the kernel) or null
   int64_t ld_w32;
   void* dX;           // [BT][D_in]
@@ -113,13 +113,17 @@ struct alignas(128) DgradParams {
   int tiles_m, tiles_n, num_tiles, num_kb;
   int group_m;
   int bn;             // tile width (input features): 128, or 256 for bf16 W
-  int bk;             // rows of D_out per stage (128, or 64 with bn 256); must match the kernel's
+  int bk;             // rows of D_out per stage (128, or 64 with bn 256 or mb > 1); must match the kernel's
+  int mb;             // 128-token blocks per tile: 1, or 2 / 4 (all tokens of BT <= 256 / 512; tiles_m = 1)
+  int stg_rows;       // fp32 W: rows per staging slot (64, or 32 with mb > 1); must match the kernel's
+  int k_rotate;       // 1: tiles of a row start their stage walks at evenly spaced stages
   uint32_t flags;
   uint64_t timeout_ns;
   // Split contraction (splitk = S >= 2; grid = num_tiles * S): CTA c runs
   // stages [s num_kb / S, (s + 1) num_kb / S) of tile c % num_tiles,
-  // s = c / num_tiles, and stores its fp32 partial sum to part + c * 128 * bn
-  // (128 x bn, row-major); dgrad_fixup_kernel adds a tile's parts in order.
+  // s = c / num_tiles, and stores its fp32 partial sum to
+  // part + c * mb * 128 * bn (mb * 128 x bn, row-major); dgrad_fixup_kernel
+  // adds a tile's parts in order.
   int splitk;
   float* part;
 };
@@ -132,6 +136,7 @@ struct DgradFixupParams {
   int dx_bf16;
   int bt, d_in;
   int bn, tiles_m, tiles_n, group_m, num_tiles, parts;
+  int rows;  // token rows per tile (mb * 128)
 };
 
 struct TcLaunch {

@@ -100,6 +100,13 @@ typedef struct {
  * this layer or workspace cannot take it), or force the two-kernel path. */
 #define FORGE_FLAG_BACKWARD_FUSED 0x200u
 #define FORGE_FLAG_BACKWARD_SPLIT 0x400u
+/* forge_backward_step only, split path (either flag implies it): the tiles
+ * of the input gradient dX = dY W_old -- 128 tokens each, or all the tokens
+ * (2 or 4 blocks of 128, for 128 < BT <= 512; FORGE_ERR_UNSUPPORTED
+ * otherwise). Without either, the library costs both and takes the
+ * cheaper. dX differs between them only in the fp32 summation order. */
+#define FORGE_FLAG_DGRAD_TOKENS_128 0x800u
+#define FORGE_FLAG_DGRAD_ALL_TOKENS 0x1000u
 
 /* Optimizer rule of forge_backward_step. */
 typedef enum {
@@ -391,13 +398,14 @@ const char* forge_version(void);
  *   - the fused paths of forge_backward_step and forge_backward_accumulate:
  *     one fp32 slab of ceil(BT/128)*128 x 64 dX partial sums per (CTA, tile
  *     column) pair (1 <= BT <= 768);
- *   - the split path's input gradient, for layers whose 128 x 128 dX tiles
- *     would leave at least half the SMs idle (short token axes): the
- *     contraction over D_out is split in S = min(4, SMs / tiles) parts of
- *     at least 2048 rows, run side by side (128 x 256 tiles for bf16 W)
- *     where that occupies at least 1.5 times as many SMs as the tiles, one
- *     fp32 partial sum per part, which a second kernel adds in a fixed order
- *     (dX stays bit-reproducible).
+ *   - the split path's input gradient where its plan splits the
+ *     contraction over D_out: one fp32 partial sum per part (S = min(4,
+ *     SMs / tiles) parts run side by side), which a second kernel adds in a
+ *     fixed order (dX stays bit-reproducible). Tiles of 128 tokens split in
+ *     parts of at least 2048 rows where 128 x 128 tiles would leave at least
+ *     half the SMs idle (128 x 256 tiles for bf16 W); tiles of all the
+ *     tokens (128 < BT <= 512) in parts of at least 256 rows. The plan with
+ *     the least shared-memory traffic per SM is taken.
  * 0 when neither applies or the device cannot be queried. Passing less only
  * forgoes these paths (forced fused paths then fail). The forge_wgrad_step_*
  * calls and forge_dgrad need no scratch: their schedulers keep their state on

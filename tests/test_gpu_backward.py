@@ -183,27 +183,57 @@ def test_workspace_bytes_geometry():
         runs = max((((c + 1) * T // G) - 1) // tm - (c * T // G) // tm + 1 for c in range(G))
         return G * runs * (-(-bt // 128) * 128 * 64) * 4
 
-    def split(d_out, d_in, bt):
-        # the split input gradient, where 128 x 128 tiles would leave half the
-        # SMs idle: S = min(4, SMs // tiles) parts per tile, each at least 2048
-        # rows of D_out, one 128 x bn fp32 partial sum per part (bn 128 with
-        # fp32 W, 256 with bf16 W)
-        if bt < 1 or 2 * (-(-bt // 128) * -(-d_in // 128)) > sms:
-            return 0
-        best = 0
-        for bn, rows in ((128, 128), (256, 64)):
-            tiles = -(-bt // 128) * -(-d_in // bn)
-            kb = -(-d_out // rows)
-            parts = min(4, sms // tiles)
-            while parts >= 2 and kb * rows < 2048 * parts:
+    def plan(d_out, d_in, bt, wbytes):
+        # The input gradient's plan, costed by the bytes through the busiest
+        # SM's shared memory: waves x multiply-adds per CTA (token blocks
+        # padded to 128) x (4 / BN + (W bytes + 6 for fp32 W) / (128 MB)
+        # + 1 / 64), plus 740 KB for a split's fix-up. Candidates: 128-token
+        # tiles (128 x 256 for bf16 W when those fill the GPU); the same split
+        # in S = min(4, SMs // tiles) parts of >= 2048 rows where that puts
+        # >= 1.5x as many SMs to work as 128 x 128 tiles (bf16 W on 128 x 256
+        # tiles); all-token tiles (2 / 4 blocks of 128 tokens x 128 columns,
+        # BT in (128, 512], 64-row stages) split in parts of >= 256 rows.
+        def cost(mb, bn, bk, tiles_m, parts):
+            tiles_n = -(-d_in // bn)
+            P = parts if parts >= 2 else 1
+            waves = -(-(tiles_m * tiles_n * P) // sms)
+            per_mac = 4.0 / bn + (wbytes + (6.0 if wbytes == 4 else 0.0)) / (128.0 * mb) + 1.0 / 64.0
+            c = waves * (128.0 * mb * bn * (d_out / P)) * per_mac
+            if parts >= 2:
+                c += 740e3
+            nbytes = tiles_m * tiles_n * parts * 128 * mb * bn * 4 if parts >= 2 else 0
+            return c, nbytes
+
+        tm = -(-bt // 128)
+        bn = 256 if wbytes == 2 and tm * -(-d_in // 256) >= sms else 128
+        best = cost(1, bn, 128 if bn == 128 else 64, tm, 0)
+        bn = 256 if wbytes == 2 else 128
+        bk = 128 if bn == 128 else 64
+        tiles, kb, tiles128 = tm * -(-d_in // bn), -(-d_out // bk), tm * -(-d_in // 128)
+        parts = min(4, sms // tiles)
+        while parts >= 2 and kb * (bk // 64) < 32 * parts:
+            parts -= 1
+        if parts >= 2 and 2 * tiles128 <= sms and 2 * tiles * parts >= 3 * tiles128:
+            c = cost(1, bn, bk, tm, parts)
+            if c[0] < best[0]:
+                best = c
+        if 128 < bt <= 512:
+            mb, tiles_n, kb = (2 if bt <= 256 else 4), -(-d_in // 128), -(-d_out // 64)
+            parts = min(4, sms // tiles_n)
+            while parts >= 2 and kb * 64 < 256 * parts:
                 parts -= 1
-            if parts >= 2 and 2 * tiles * parts >= 3 * (-(-bt // 128) * -(-d_in // 128)):
-                best = max(best, tiles * parts * 128 * bn * 4)
-        return best
+            c = cost(mb, 128, 64, 1, parts if parts >= 2 else 0)
+            if c[0] < best[0]:
+                best = c
+        return best[1]
+
+    def split(d_out, d_in, bt):
+        return max(plan(d_out, d_in, bt, 4), plan(d_out, d_in, bt, 2)) if bt >= 1 else 0
 
     for shape in [(14336, 4096, 512), (4096, 14336, 512), (1024, 4096, 512), (136, 200, 70), (8, 8, 1),
                   (14336, 4096, 2048), (14336, 4096, 8192), (4096, 4096, 769), (14336, 4096, 256),
-                  (14336, 4096, 128), (4096, 4096, 256)]:
+                  (14336, 4096, 128), (4096, 4096, 256), (8192, 2600, 512), (8192, 2600, 200), (8192, 520, 200),
+                  (4096, 4096, 300), (14336, 4096, 129)]:
         assert F.workspace_bytes(*shape) == max(fused(*shape), split(*shape)), shape
     assert F.workspace_bytes(4096, 4096, 0) == 0
 
@@ -294,3 +324,44 @@ def test_split_path_input_gradient_split_contraction(w, shape):
     F.sync_status()
     _, A = _dx_ref(prob)
     assert np.all(np.abs(dx1.astype(np.float64) - dx3.cpu().numpy()) <= 2e-5 * A)
+
+
+@pytest.mark.parametrize("w", ["f32", "bf16"])
+@pytest.mark.parametrize("shape", [(4096, 2600, 512), (4096, 2600, 300), (2048, 1000, 200), (1000, 520, 129)],
+                         ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("workspace", [True, False], ids=["split", "whole"])
+def test_split_path_all_token_input_gradient(w, shape, workspace):
+    # The input gradient on all-token tiles (FORGE_FLAG_DGRAD_ALL_TOKENS):
+    # 4 blocks of 128 tokens (BT 512; BT 300: the last block empty, the third
+    # ragged) or 2 (BT 200, 129), 128 features, ragged last column of tiles
+    # and last stage (D_out 1000); with a workspace the contraction is split
+    # in parts added by the fix-up kernel, without one each tile runs whole.
+    # Exact inputs: state and dX bit-exact; random inputs: dX within
+    # tolerance, run-to-run identical, and equal to the 128-token tiles'
+    # dX up to summation order.
+    d_out, d_in, bt = shape
+    prob = _prob(shape, 31, w, w, exact=True)
+    fl = F.FLAG_DGRAD_ALL_TOKENS
+    got, dx = run_backward("adamw", prob, 2, path="split", sr_w=w == "bf16", seed=3, workspace=workspace, flags=fl)
+    ref = oracle_step("adamw", prob, w, w, 2, seed=3, sr_w=w == "bf16", mode="f32emu")
+    assert_bit_exact(got, ref, "adamw")
+    _check_dx(dx, prob, "bf16", exact=True)
+    prob = _prob(shape, 32, w, w, exact=False)
+    kw = dict(dx_dtype="f32", path="split", sr_w=w == "bf16", workspace=workspace)
+    _, dx1 = run_backward("adamw", prob, 1, flags=fl, **kw)
+    _, dx2 = run_backward("adamw", prob, 1, flags=fl, **kw)
+    assert np.array_equal(dx1.view(np.uint32), dx2.view(np.uint32))
+    _check_dx(dx1, prob, "f32", exact=False)
+    _, dx3 = run_backward("adamw", prob, 1, flags=F.FLAG_DGRAD_TOKENS_128, **kw)
+    _, A = _dx_ref(prob)
+    assert np.all(np.abs(dx1.astype(np.float64) - dx3) <= 2e-5 * A)
+
+
+def test_all_token_input_gradient_needs_a_short_token_axis():
+    prob = _prob((256, 256, 600), 33, "f32", "f32", exact=False)
+    with pytest.raises(F.ForgeError) as ei:
+        run_backward("adamw", prob, 1, path="split", flags=F.FLAG_DGRAD_ALL_TOKENS)
+    assert ei.value.status == 2 and "all-token" in str(ei.value)
+    with pytest.raises(F.ForgeError) as ei:
+        run_backward("adamw", prob, 1, path="fused", flags=F.FLAG_DGRAD_TOKENS_128)
+    assert ei.value.status == 1

@@ -277,10 +277,13 @@ def test_forced_device_timeout_reports_and_leaves_state():
 @pytest.mark.parametrize("w_dtype", ["bf16", "f32"])
 @pytest.mark.parametrize("dx_dtype", ["bf16", "f32"])
 @pytest.mark.parametrize("shape", [(256, 384, 200), (136, 200, 70), (1024, 512, 512), (2048, 1024, 64),
-                                   (1024, 512, 640), (1024, 4000, 1300)])
+                                   (1024, 512, 640), (1024, 4000, 1300), (256, 10000, 200), (1000, 10000, 512)])
 def test_dgrad_exact(w_dtype, dx_dtype, shape):
     # (1024, 4000, 1300): with bf16 weights, 128 x 256 tiles with ragged
-    # token and feature tails.
+    # token and feature tails. D_in 10000 on short token axes: the policy
+    # takes all-token tiles for fp32 weights (2 / 4 blocks of 128 tokens, 79
+    # columns of tiles, the last one ragged; D_out 1000: a ragged last
+    # stage).
     d_out, d_in, bt = shape
     dev = "cuda:0"
     dY = S.small_integers((bt, d_out), -3, 3, 1, S.STREAM_DY, "bf16")
@@ -314,20 +317,37 @@ def test_dgrad_random_reads_pre_update_weights():
 
 
 @pytest.mark.parametrize("shape", [(4096, 512, 256), (14336, 4096, 512), (2048, 4096, 512), (4096, 14336, 512)])
-def test_dgrad_f32_and_bf16_weights_agree_bit_for_bit(shape):
+@pytest.mark.parametrize("tiles", ["auto", "tokens128", "all_tokens"])
+def test_dgrad_f32_and_bf16_weights_agree_bit_for_bit(shape, tiles):
     # fp32 master weights that are bf16-representable must give exactly the
-    # dX of the same weights stored as bf16 (the staging conversion is exact),
-    # on every repetition (no stale staging data).
+    # dX of the same weights stored as bf16 (the staging conversion is exact)
+    # on the same tiles, on every repetition (no stale staging data). "auto":
+    # forge_dgrad's own choice where both dtypes take the same tiles (the
+    # 128-token tiles at these shapes, except the down-projection, where fp32
+    # weights take all-token tiles); otherwise forced through
+    # forge_backward_step's split path without a workspace (SGD with lr = 0:
+    # W unchanged).
     d_out, d_in, bt = shape
     dev = "cuda:0"
     W16 = S.normal((d_out, d_in), 0.02, 2, S.STREAM_W, "bf16").to(dev)
     W32 = W16.float()
     dY = S.normal((bt, d_out), 1.0, 2, S.STREAM_DY, "bf16").to(dev)
+    X = S.normal((bt, d_in), 1.0, 2, S.STREAM_X, "bf16").to(dev)
+
+    def run(W, out):
+        if tiles == "auto":
+            F.dgrad(dY, W, out)
+        else:
+            fl = F.FLAG_DGRAD_TOKENS_128 if tiles == "tokens128" else F.FLAG_DGRAD_ALL_TOKENS
+            F.backward_step("sgd", X, dY, W, None, None, out, lr=0.0, step=1, flags=fl | F.FLAG_BACKWARD_SPLIT)
+
+    if tiles == "auto" and d_in == 14336:
+        pytest.skip("fp32 and bf16 weights take different tiles here")
     ref = torch.empty((bt, d_in), dtype=torch.float32, device=dev)
-    F.dgrad(dY, W16, ref)
+    run(W16, ref)
     for _ in range(4):
         out = torch.empty_like(ref)
-        F.dgrad(dY, W32, out)
+        run(W32, out)
         F.sync_status()
         assert torch.equal(out, ref), int((out != ref).sum())
 
