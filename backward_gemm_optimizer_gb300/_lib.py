@@ -30,7 +30,8 @@ STATUS_NAMES = {0: "FORGE_OK", 1: "FORGE_ERR_INVALID_ARG", 2: "FORGE_ERR_UNSUPPO
 EXPORTED = ("forge_wgrad_step_adamw", "forge_wgrad_step_sgdm", "forge_wgrad_step_lion",
             "forge_wgrad_step_sgd", "forge_wgrad_step_rmsprop", "forge_wgrad_step_adagrad",
             "forge_wgrad_step_nadam", "forge_wgrad_step_radam",
-            "forge_dgrad", "forge_backward_step", "forge_backward_step_no_alloc", "forge_wgrad_accumulate",
+            "forge_dgrad", "forge_dgrad_ws", "forge_backward_step", "forge_backward_step_no_alloc",
+            "forge_wgrad_accumulate",
             "forge_backward_accumulate", "forge_wgrad_step_accumulated", "forge_sync_status", "forge_last_error", "forge_version",
             "forge_workspace_bytes")
 
@@ -71,6 +72,7 @@ def _load() -> ctypes.CDLL:
     lib.forge_wgrad_step_nadam.argtypes = [P(T), P(T), P(T), P(T), P(T), P(H), i64, u64, vp]
     lib.forge_wgrad_step_radam.argtypes = [P(T), P(T), P(T), P(T), P(T), P(H), i64, u64, vp]
     lib.forge_dgrad.argtypes = [P(T), P(T), P(T), vp]
+    lib.forge_dgrad_ws.argtypes = [P(T), P(T), P(T), vp, ctypes.c_size_t, vp]
     lib.forge_backward_step.argtypes = [ctypes.c_int, P(T), P(T), P(T), P(T), P(T), P(T), P(H), i64, u64, vp,
                                         ctypes.c_size_t, vp]
     lib.forge_backward_step_no_alloc.argtypes = [ctypes.c_int, P(T), P(T), P(T), P(T), P(T), P(T), P(H), i64,
@@ -83,7 +85,7 @@ def _load() -> ctypes.CDLL:
     lib.forge_sync_status.argtypes = [vp]
     for f in ("forge_wgrad_step_adamw", "forge_wgrad_step_sgdm", "forge_wgrad_step_lion",
               "forge_wgrad_step_sgd", "forge_wgrad_step_rmsprop", "forge_wgrad_step_adagrad",
-              "forge_wgrad_step_nadam", "forge_wgrad_step_radam", "forge_dgrad", "forge_backward_step",
+              "forge_wgrad_step_nadam", "forge_wgrad_step_radam", "forge_dgrad", "forge_dgrad_ws", "forge_backward_step",
               "forge_backward_step_no_alloc", "forge_wgrad_accumulate", "forge_backward_accumulate",
               "forge_wgrad_step_accumulated",
               "forge_sync_status"):
@@ -227,10 +229,17 @@ def wgrad_step_radam(X, dY, W, m, v, *, lr, beta1=0.9, beta2=0.999, eps=1e-8, we
                                         ctypes.byref(tv), ctypes.byref(h), int(step), _seed(seed), _stream(stream)))
 
 
-def dgrad(dY, W_old, dX, *, stream=None):
-    """dX = dY W_old (forge_dgrad); enqueue before the step that overwrites W."""
+def dgrad(dY, W_old, dX, *, workspace=None, stream=None):
+    """dX = dY W_old (forge_dgrad, or forge_dgrad_ws given a `workspace` device tensor of
+    workspace_bytes(D_out, D_in, BT) bytes); enqueue before the step that overwrites W."""
     tdY, tW, tdX = tensor_desc(dY), tensor_desc(W_old), tensor_desc(dX)
-    _check(lib().forge_dgrad(ctypes.byref(tdY), ctypes.byref(tW), ctypes.byref(tdX), _stream(stream)))
+    if workspace is None:
+        _check(lib().forge_dgrad(ctypes.byref(tdY), ctypes.byref(tW), ctypes.byref(tdX), _stream(stream)))
+    else:
+        ws_bytes = workspace.numel() * workspace.element_size()
+        _check(lib().forge_dgrad_ws(ctypes.byref(tdY), ctypes.byref(tW), ctypes.byref(tdX),
+                                    ctypes.c_void_p(workspace.data_ptr() if ws_bytes else 0), ws_bytes,
+                                    _stream(stream)))
 
 
 def backward_step(rule, X, dY, W, s0, s1, dX, *, lr, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0,

@@ -881,6 +881,11 @@ forge_status forge_dgrad(const forge_tensor* dY, const forge_tensor* W_old, forg
   return dgrad_impl(dY, W_old, dX, stream);
 }
 
+forge_status forge_dgrad_ws(const forge_tensor* dY, const forge_tensor* W_old, forge_tensor* dX, void* workspace,
+                            size_t workspace_bytes, forge_stream_t stream) {
+  return dgrad_impl(dY, W_old, dX, stream, workspace, workspace_bytes);
+}
+
 forge_status forge_wgrad_accumulate(const forge_tensor* X, const forge_tensor* dY, forge_tensor* G_acc, int overwrite,
                                     forge_stream_t stream) {
   if (G_acc == nullptr) return fail(FORGE_ERR_INVALID_ARG, "accumulate: null G_acc");

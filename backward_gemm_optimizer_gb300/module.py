@@ -170,8 +170,9 @@ class ForgeLinear(torch.nn.Module):
                 F.backward_accumulate(x2d, dy2d, self.weight, self.grad_acc, dx, overwrite=(c.micro == 0),
                                       workspace=ws, flags=c.backward_flags & _PATH_FLAGS)
         else:
-            if dx is not None:
-                F.dgrad(dy2d, self.weight, dx)             # from W before the step (Remark 1)
+            if dx is not None:                             # from W before the step (Remark 1)
+                ws = _workspace(x2d.device, F.workspace_bytes(self.out_features, self.in_features, x2d.shape[0]))
+                F.dgrad(dy2d, self.weight, dx, workspace=ws)
             F.wgrad_step_accumulated(c.rule, x2d, dy2d, self.grad_acc, self.weight, self.state0, self.state1,
                                      lr=c.lr, beta1=c.beta1, beta2=c.beta2, eps=c.eps,
                                      weight_decay=c.weight_decay, momentum_decay=c.momentum_decay, step=c.step,

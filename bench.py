@@ -6,8 +6,8 @@ W 14336 x 4096 fp32 master weights with fp32 AdamW moments, BT = 512
 tokens of bf16 activations X and upstream gradients dY. One step = one
 forge_backward_step call: the input gradient dX = dY W_old and the fused
 weight-gradient / AdamW step, in one pass over W where the layer allows it
-(BT <= 768, fp32 / bf16 state), else forge_dgrad followed by
-forge_wgrad_step_adamw. The state (1.4 GB) is far larger than L2 and L2 is
+(BT <= 768, fp32 / bf16 state), else its split path: the input gradient
+(forge_dgrad_ws's kernel, given the workspace) followed by the step. The state (1.4 GB) is far larger than L2 and L2 is
 also flushed between timed steps. The two-kernel split path is timed as
 well and reported beside the headline (split_* keys).
 
@@ -243,7 +243,7 @@ def measure_configs(F, dev, K, warm, hbm, tflops):
                      "TFLOPs": round(flops / (us * 1e-6) / 1e12, 1),
                      "bound": "hbm" if ab / (hbm * 1e9) >= flops / (tflops * 1e12) else "tensor",
                      "frac": round(t_roof / us, 4), "algorithmic_bytes": ab,
-                     "path": "fused input gradient" if fused_path(bt, st) else "forge_dgrad + fused step"}
+                     "path": "fused input gradient" if fused_path(bt, st) else "split path: dgrad + fused step"}
         del s, ws
     for opt in ("adamw", "lion", "sgdm"):
         for stname in ("f32state", "bf16state"):
@@ -345,7 +345,7 @@ def layer_config(workload: str, world: int) -> dict:
     return {"workload": workload, "d_out": d_out, "d_in": d_in, "bt": bt, "w_storage": w,
             "moment_storage": st, "optimizer": "adamw",
             "step": "forge_backward_step, fused input gradient (one pass over W)" if fused_path(bt, st) else
-                    "forge_dgrad + forge_wgrad_step_adamw",
+                    "forge_backward_step, split path (dgrad with workspace, then the fused step)",
             "l2": "flushed between steps (256 MB write) and state 1.4 GB > L2",
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
 
@@ -393,10 +393,10 @@ def one_step(F, s, w, st, t, stream, ws, flags):
                     v_scale=s.get("v_scale"), **HYPER)
 
 
-def split_step(F, s, w, t, stream, events=None):
+def split_step(F, s, w, t, stream, ws, events=None):
     if events is not None:
         events[0].record(stream)
-    F.dgrad(s["dY"], s["W"], s["dX"], stream=stream)
+    F.dgrad(s["dY"], s["W"], s["dX"], workspace=ws, stream=stream)   # the split path's input gradient
     if events is not None:
         events[1].record(stream)
     F.wgrad_step_adamw(s["X"], s["dY"], s["W"], s["m"], s["v"], m_scale=s.get("m_scale"),
@@ -448,14 +448,14 @@ def run_gpu(args, rank, world, local_rank):
     step_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
     total_ms = max_over_ranks(sum(step_ms), world, dev)
 
-    # ---- the split path (forge_dgrad, then the fused step), for comparison
+    # ---- the split path (forge_dgrad_ws, then the fused step), for comparison
     KS = max(1, min(K, args.split_steps))
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(KS)]
     for _ in range(3):
-        split_step(F, s, w, t, stream); t += 1
+        split_step(F, s, w, t, stream, ws); t += 1
     for i in range(KS):
         flush.fill_(float(i))
-        split_step(F, s, w, t, stream, evs[i]); t += 1
+        split_step(F, s, w, t, stream, ws, evs[i]); t += 1
     torch.cuda.synchronize(dev)
     F.sync_status(stream)
     split_ms = [evs[i][0].elapsed_time(evs[i][2]) for i in range(KS)]
@@ -529,7 +529,7 @@ def run_gpu(args, rank, world, local_rank):
     else:
         abytes = algorithmic_bytes(d_out, d_in, bt, w, st)
         kern_us = statistics.mean(wstep_ms) * 1000.0
-        kernel = "wgrad_step_tc_kernel (split path: the step after forge_dgrad)"
+        kernel = "wgrad_step_tc_kernel (split path: the step after forge_dgrad_ws)"
     achieved = abytes / (kern_us * 1e-6) / 1e9
     tfl = flops / (kern_us * 1e-6) / 1e12
     t_roof = max(abytes / (hbm * 1e9), flops / (tflops * 1e12)) * 1e6
@@ -594,8 +594,8 @@ def run_accum(args, rank, world, local_rank):
     """One step = one accumulation window on the up-projection (fp32 W, m, v):
     every micro-batch but the last runs forge_backward_accumulate (dX and the
     accumulation into G_acc in one pass; the first overwrites G_acc), the last
-    forge_dgrad and forge_wgrad_step_accumulated. The same window with
-    forge_dgrad + forge_wgrad_accumulate per micro-batch is timed after it
+    forge_dgrad_ws and forge_wgrad_step_accumulated. The same window with
+    forge_dgrad_ws + forge_wgrad_accumulate per micro-batch is timed after it
     (split_* keys)."""
     import torch
     import backward_gemm_optimizer_gb300 as F
@@ -624,7 +624,7 @@ def run_accum(args, rank, world, local_rank):
             if ev is not None:
                 ev[k][0].record(stream)
             if last or split:
-                F.dgrad(dY, W, dX, stream=stream)
+                F.dgrad(dY, W, dX, workspace=ws, stream=stream)
             if ev is not None:
                 ev[k][1].record(stream)
             if last:
@@ -687,7 +687,7 @@ def run_accum(args, rank, world, local_rank):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": args.workload, "d_out": d_out, "d_in": d_in, "micro_batches": nmb, "bt": bt,
                    "effective_batch": nmb * bt, "optimizer": "adamw", "state": "fp32 W, m, v; fp32 G_acc",
-                   "step": f"{nmb - 1} x forge_backward_accumulate (fused), 1 x forge_dgrad + "
+                   "step": f"{nmb - 1} x forge_backward_accumulate (fused), 1 x forge_dgrad_ws + "
                            "forge_wgrad_step_accumulated",
                    "l2": "flushed between windows"},
         "backward_accumulate_first_us": round(fa_first, 2),

@@ -252,6 +252,19 @@ forge_status forge_dgrad(const forge_tensor* dY, const forge_tensor* W_old, forg
                          forge_stream_t stream);
 
 /*
+ * forge_dgrad_ws -- the same product with a device workspace (16-byte
+ * aligned, caller-owned, not shared by calls in flight; contents need not
+ * be initialised): given forge_workspace_bytes(D_out, D_in, BT) bytes, a
+ * layer with few dX tiles splits its contraction over D_out across the SMs
+ * and a second kernel adds the parts in a fixed order (dX bit-reproducible;
+ * it differs from forge_dgrad's only in the fp32 summation order). Less
+ * workspace (or NULL) gives forge_dgrad's plan. This is the input gradient
+ * of forge_backward_step's split path.
+ */
+forge_status forge_dgrad_ws(const forge_tensor* dY, const forge_tensor* W_old, forge_tensor* dX, void* workspace,
+                            size_t workspace_bytes, forge_stream_t stream);
+
+/*
  * forge_backward_step -- the whole backward pass of one linear layer with
  * its optimizer step: dX = dY W_old (Remark 1, Appendix A) and the fused
  * weight-gradient step of `rule` (Algorithm 1 for AdamW; Appendix N (i)
@@ -297,7 +310,7 @@ forge_status forge_backward_step(forge_rule rule, const forge_tensor* X, const f
  * G_acc: FORGE_F32, D_out x D_in, caller-owned; it is the one
  * gradient-shaped buffer of this mode and lives for the accumulation
  * window. X, dY: FORGE_BF16. The micro-batch's input gradient is a
- * separate forge_dgrad call, or use forge_backward_accumulate for both.
+ * separate forge_dgrad (or forge_dgrad_ws) call, or use forge_backward_accumulate for both.
  */
 forge_status forge_wgrad_accumulate(const forge_tensor* X, const forge_tensor* dY, forge_tensor* G_acc, int overwrite,
                                     forge_stream_t stream);

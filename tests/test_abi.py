@@ -84,6 +84,8 @@ def test_null_arguments():
     assert r == INVALID
     r = lib.forge_dgrad(None, None, None, None)
     assert r == INVALID
+    r = lib.forge_dgrad_ws(None, None, None, None, 0, None)
+    assert r == INVALID
 
 
 def test_shape_mismatch():
@@ -147,9 +149,11 @@ def test_dgrad_validation():
     dY, W, dX = _t(rows=16, cols=32), _t(dtype=0, rows=32, cols=64), _t(dtype=1, rows=16, cols=64)
     dY.dtype = 0
     assert lib.forge_dgrad(ctypes.byref(dY), ctypes.byref(W), ctypes.byref(dX), None) == UNSUPPORTED
+    assert lib.forge_dgrad_ws(ctypes.byref(dY), ctypes.byref(W), ctypes.byref(dX), None, 0, None) == UNSUPPORTED
     dY.dtype = 1
     W.rows = 31
     assert lib.forge_dgrad(ctypes.byref(dY), ctypes.byref(W), ctypes.byref(dX), None) == INVALID
+    assert lib.forge_dgrad_ws(ctypes.byref(dY), ctypes.byref(W), ctypes.byref(dX), None, 0, None) == INVALID
 
 
 def test_backward_step_host_checks():

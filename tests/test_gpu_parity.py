@@ -298,6 +298,30 @@ def test_dgrad_exact(w_dtype, dx_dtype, shape):
     assert np.array_equal(got, ref.astype(np.float32))
 
 
+@pytest.mark.parametrize("w_dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("shape", [(8192, 2600, 512), (8192, 520, 200), (4096, 1000, 300), (136, 200, 70)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_dgrad_with_workspace_exact(w_dtype, shape):
+    # forge_dgrad_ws: with the workspace the contraction is split over D_out
+    # where the plan says so (all-token tiles at 2600 x 512, 128-token tiles
+    # at 520 x 200), else the same kernel as forge_dgrad; exact inputs, so
+    # dX is exact either way, and a second call gives the same bits.
+    d_out, d_in, bt = shape
+    dev = "cuda:0"
+    dY = S.small_integers((bt, d_out), -3, 3, 7, S.STREAM_DY, "bf16")
+    W = S.small_integers((d_out, d_in), -3, 3, 7, S.STREAM_W, w_dtype)
+    ws = torch.empty(max(16, F.workspace_bytes(d_out, d_in, bt)), dtype=torch.uint8, device=dev)
+    outs = []
+    for _ in range(2):
+        dX = torch.full((bt, d_in), float("nan"), dtype=torch.float32, device=dev)
+        F.dgrad(dY.to(dev), W.to(dev), dX, workspace=ws)
+        F.sync_status()
+        outs.append(dX.cpu().numpy())
+    ref = O.dgrad_f64(dY.float().numpy(), W.float().numpy())
+    assert np.array_equal(outs[0], ref.astype(np.float32))
+    assert np.array_equal(outs[0].view(np.uint32), outs[1].view(np.uint32))
+
+
 def test_dgrad_random_reads_pre_update_weights():
     d_out, d_in, bt = 1024, 512, 256
     dev = "cuda:0"
