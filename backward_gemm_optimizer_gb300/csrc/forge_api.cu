@@ -701,18 +701,22 @@ forge_status wgrad_step(int opt, const forge_tensor* X, const forge_tensor* dY, 
 }
 
 // Whether the fused backward pass beats dgrad + step for this layer: it
-// saves the dgrad kernel's read of W and its launch, and costs writing and
-// re-reading one fp32 dX partial slab per (CTA, column) pair. With bf16 W
-// and fewer than two state tensors the step is bound by its per-element
-// arithmetic (stochastic rounding of W) rather than by the bytes, and the
-// fused kernel's 64-column tiles lose to the split path's 128-column ones
-// (measured on the Llama-3.1-8B projections: Lion 270 vs 260 us, SGD-momentum
-// 257 vs 251 us), so those take the split path.
-bool dx_worthwhile(const DxGeometry& g, int64_t d_out, int64_t d_in, int w_bytes, int nst) {
-  if (w_bytes < 4 && nst < 2) return false;
-  const double saved = static_cast<double>(d_out) * static_cast<double>(d_in) * w_bytes;
-  const double partial = 2.0 * static_cast<double>(g.grid + g.tiles_n) * static_cast<double>(g.slab) * 4.0;
-  return saved >= partial;
+// saves the split path's dgrad (its read of W, its launches) and costs
+// writing and re-reading one fp32 dX partial slab per (CTA, column) pair,
+// with 64-column instead of 128-column step tiles. Measured at BT 512 on the
+// Llama-3.1-8B projections (forge_backward_step fused / split, us):
+//   fp32 W, fp32 state: fused everywhere -- up 269 / 318 (AdamW),
+//     220 / 271 (Lion); down 290 / 322; q/o 102 / 118; k/v 50 / 58.
+//   bf16 W, two bf16 moments: fused where D_in <= D_out -- up 227 / 246,
+//     q/o 88 / 99; split where it is wider -- down 247 / 238, k/v 44 / 38.
+//   bf16 W, one or no state tensor: split -- the step is bound by its
+//     per-element arithmetic (stochastic rounding of W) and the fused
+//     pass's slabs and narrower tiles do not pay: down Lion 226 / 197,
+//     k/v 42 / 33, up 206 / 203, q/o 82 / 84 (within 2 %).
+bool dx_worthwhile(const DxGeometry&, int64_t d_out, int64_t d_in, int w_bytes, int nst) {
+  if (w_bytes == 4) return true;
+  if (nst < 2) return false;
+  return d_in <= d_out;
 }
 
 forge_status dgrad_impl(const forge_tensor* dY, const forge_tensor* W_old, forge_tensor* dX, forge_stream_t stream,
