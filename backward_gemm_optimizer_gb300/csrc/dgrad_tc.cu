@@ -91,9 +91,19 @@ struct DCfg {
   // one is drained) where they fit in the 512 columns, else one.
   static constexpr int NBUF = 2 * MB * BN <= 512 ? 2 : 1;
   static constexpr int TMEM_COLS = NBUF * MB * BN;
-  static constexpr uint32_t IDESC = make_idesc_bf16(BM, BN, 0, 1);
+  // 128-token tiles: A = dY (M = 128 tokens, K-major), B = W (N = BN
+  // features, MN-major). All-token tiles swap the operands: A = W (M = 128
+  // features, MN-major), B = dY (N = 256 tokens, K-major) -- one product per
+  // 256 tokens instead of one per 128, a third fewer operand bytes read from
+  // shared memory per multiply-add; the accumulator is then dX transposed
+  // (tensor-memory lane = feature, column = token).
+  static constexpr bool SWAP = MB > 1;
+  static constexpr int DRAIN_WARPS = SWAP ? 12 : 4;   // warps that drain the accumulator
+  static constexpr int NT = 256;                  // tokens per product (swapped)
+  static constexpr uint32_t IDESC = SWAP ? make_idesc_bf16(BM, NT, 1, 0) : make_idesc_bf16(BM, BN, 0, 1);
   static_assert(!F32W || BN == 128, "fp32 weight staging is sized for 128-column tiles");
   static_assert(MB == 1 || (BN == 128 && (MB == 2 || MB == 4)), "all-token tiles: 2 or 4 blocks x 128 columns");
+  static_assert(!SWAP || (MB * BM) % NT == 0, "whole 256-token products");
   static_assert(BK % A_BOX_K == 0 && (!F32W || BK % STG_ROWS == 0), "stage rows");
   static_assert(SA == SB, "one empty barrier per stage serves the dY and the bf16 W ring");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
@@ -215,7 +225,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dgrad_tc_kernel(const __grid_c
     for (int s = 0; s < SA; ++s) { mbar_init(&a_full[s], 1); mbar_init(&a_empty[s], 1); }
     for (int s = 0; s < SB; ++s) mbar_init(&b_full[s], F32W ? CONV_THREADS : 1);
     for (int s = 0; s < SS; ++s) { mbar_init(&s_full[s], 1); mbar_init(&s_empty[s], CONV_THREADS); }
-    for (int b = 0; b < NBUF; ++b) { mbar_init(&tm_full[b], 1); mbar_init(&tm_empty[b], 4); }
+    for (int b = 0; b < NBUF; ++b) { mbar_init(&tm_full[b], 1); mbar_init(&tm_empty[b], C::DRAIN_WARPS); }
     mbar_init(&drain_bar, 1);
     abort_sh = 0;
     fence_mbar_init();
@@ -339,6 +349,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dgrad_tc_kernel(const __grid_c
           // below 2^18 bytes, so it never carries).
           const uint64_t ad0 = make_smem_desc(a0, 16, 8 * C::A_ROW, C::A_SWZ);
           const uint64_t bd0 = make_smem_desc(b0, C::ATOM, 1024, 2);
+          if constexpr (C::SWAP) {
+            // A = the W tile (descriptor bd0), B = 256 tokens of dY: token
+            // blocks 2 nb and 2 nb + 1, contiguous (ad0 + nb * 2 A_BLOCK).
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              const uint64_t wstep = static_cast<uint64_t>((kk * 2048) >> 4);
+              const uint64_t ystep = static_cast<uint64_t>(((kk % 4) * 32) >> 4);
+#pragma unroll
+              for (int nb = 0; nb < MB * BM / C::NT; ++nb)
+                umma_f16(d + static_cast<uint32_t>(nb * C::NT), bd0 + wstep,
+                         ad0 + static_cast<uint64_t>((nb * 2 * C::A_BLOCK) >> 4) + ystep, IDESC,
+                         (i > 0 || kk > 0) ? 1u : 0u);
+            }
+          } else {
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             // A K step of 16 elements advances 32 bytes within a box (boxes
@@ -353,6 +377,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dgrad_tc_kernel(const __grid_c
               umma_f16(d + static_cast<uint32_t>(b * BN), ad0 + static_cast<uint64_t>((b * C::A_BLOCK) >> 4) + astep,
                        bd0 + bstep, IDESC, (i > 0 || kk > 0) ? 1u : 0u);
           }
+          }
           umma_commit(&a_empty[sa]);  // releases the stage's dY slot and its bf16 W slot
         }
         if (!ok) break;
@@ -365,141 +390,185 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dgrad_tc_kernel(const __grid_c
           if (globaltimer_ns() - t0 > 200000000ull) { atomicCAS(p.status, 0u, WAIT_MMA_DRAIN); break; }
       }
     }
-  } else if (warp >= 4 && warp < 8) {
-    // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;
-    const int r = q * 32 + lane;
-    int it = 0;
-    bool ok = true;
-    SegWalk w = seg_walk<SPLIT>(p);
-    int tile, kb0, kb1, rot;
-    for (; ok && seg_next<SPLIT>(p, w, tile, kb0, kb1, rot); ++it) {
-      int tm, tn;
-      dtile(tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
-      const int buf = it % NBUF;
-      ok = dwait(&tm_full[buf], (it / NBUF) & 1, abort_flag, p.status, WAIT_TMEM_FULL, lim);
-      ok = __all_sync(0xFFFFFFFFu, ok);
-      if (!ok) break;
-      tc_fence_after_sync();
-#pragma unroll 1
-      for (int blk = 0; blk < MB; ++blk) {
-        const int row = (tm * MB + blk) * BM + r;
-        const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                                static_cast<uint32_t>((buf * MB + blk) * BN);
-        // A split contraction: this CTA's fp32 partial sum goes to its slot
-        // (row blk * 128 + r of an MB * 128 x BN slab), for the fix-up kernel
-        // to add in order.
-        constexpr bool partial = SPLIT;
-        float* slot = partial ? p.part + ((static_cast<int64_t>(blockIdx.x) * MB + blk) * BM + r) * BN : nullptr;
-#pragma unroll 1
-        for (int c = 0; c < BN / 16; ++c) {
-          uint32_t acc[16];
-          if (p.num_kb > 0) {
-            tmem_ld_32x32b_x16(t_lane + c * 16, acc);
-            tmem_ld_wait();
-          } else {
+  } else if (warp >= 4) {
+    if (warp >= 8 && F32W) {
+      // ------------------------------------------------------------ fp32 -> bf16 converters
+      // The fp32 rows landed by TMA as four [STG_ROWS rows][32 columns] boxes
+      // with the 128-byte swizzle. Work item = (box, K row, 8-column group): read
+      // two 16-byte chunks, round to bf16, write one 16-byte chunk of the
+      // MN-major swizzled operand. Consecutive threads take consecutive K
+      // rows, so both the reads and the writes are bank-conflict free.
+      const int ct = threadIdx.x - 256;
+      uint32_t k = 0, ks = 0;
+      bool ok = true;
+      SegWalk w = seg_walk<SPLIT>(p);
+      int tile, kb0, kb1, rot;
+      while (ok && seg_next<SPLIT>(p, w, tile, kb0, kb1, rot)) {
+        for (int i = 0; i < kb1 - kb0; ++i, ++k) {
+          const int kb = stage_at(kb0, kb1, rot, i);
+          const int sb = static_cast<int>(k % SB);
+          uint8_t* b = b_ring + sb * B_BYTES;
+          // A stage's BK rows arrive as BK / 64 staging slots of 64 rows.
+          for (int half = 0; half < BK / C::STG_ROWS; ++half, ++ks) {
+            const int ss = static_cast<int>(ks % SS);
+            ok = dwait(&s_full[ss], (ks / SS) & 1u, abort_flag, p.status, WAIT_OP_FULL, lim) &&
+                 (half > 0 || dwait(&a_empty[sb], ((k / SB) & 1u) ^ 1u, abort_flag, p.status, WAIT_OP_EMPTY, lim));
+            ok = __all_sync(0xFFFFFFFFu, ok);
+            if (!ok) break;
+            const uint8_t* stg = s_ring + ss * STG_BYTES;
+            // Work items of the slot: 4 boxes x STG_ROWS rows x 4 groups of 8
+            // columns, STG_ROWS / 16 per thread.
+            constexpr int NJ = C::STG_ROWS / 16;
+            uint4 o[NJ];
+            int dst[NJ];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) acc[j] = 0u;
-          }
-          if (partial) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              reinterpret_cast<float4*>(slot + c * 16)[j] =
-                  make_float4(__uint_as_float(acc[4 * j]), __uint_as_float(acc[4 * j + 1]),
-                              __uint_as_float(acc[4 * j + 2]), __uint_as_float(acc[4 * j + 3]));
-            continue;
-          }
-          const int col0 = tn * BN + c * 16;
-          if (row >= p.bt || col0 >= p.d_in) continue;
-          const bool full_chunk = col0 + 16 <= p.d_in;
-          if (p.dx_bf16) {
-            uint16_t* out = static_cast<uint16_t*>(p.dX) + static_cast<int64_t>(row) * p.ld_dx + col0;
-            if (full_chunk) {
-              uint32_t b[8];
-#pragma unroll
-              for (int j = 0; j < 8; ++j)
-                b[j] = pack_bf16x2_rn(__uint_as_float(acc[2 * j]), __uint_as_float(acc[2 * j + 1]));
-              reinterpret_cast<uint4*>(out)[0] = make_uint4(b[0], b[1], b[2], b[3]);
-              reinterpret_cast<uint4*>(out)[1] = make_uint4(b[4], b[5], b[6], b[7]);
-            } else {
-              for (int j = 0; j < 16 && col0 + j < p.d_in; ++j)
-                out[j] = static_cast<uint16_t>(f32_to_bf16_rne(__uint_as_float(acc[j])));
+            for (int j = 0; j < NJ; ++j) {
+              const int i = ct + CONV_THREADS * j;
+              const int kr = i % C::STG_ROWS;                // row within the staging slot
+              const int hh = (i / C::STG_ROWS) & 3;          // 8-column group within the 32-column box
+              const int bb = i / (4 * C::STG_ROWS);          // box (32 columns)
+              const uint8_t* src = stg + bb * (C::STG_ROWS * 128) + kr * 128;
+              const float4 u0 = *reinterpret_cast<const float4*>(src + (((2 * hh) ^ (kr & 7)) << 4));
+              const float4 u1 = *reinterpret_cast<const float4*>(src + (((2 * hh + 1) ^ (kr & 7)) << 4));
+              o[j].x = pack_bf16x2_rn(u0.x, u0.y);
+              o[j].y = pack_bf16x2_rn(u0.z, u0.w);
+              o[j].z = pack_bf16x2_rn(u1.x, u1.y);
+              o[j].w = pack_bf16x2_rn(u1.z, u1.w);
+              const int n = bb * 32 + hh * 8;    // column within the 128-wide tile
+              const int row = half * C::STG_ROWS + kr;  // K row of the stage (row % 8 == kr % 8)
+              dst[j] = (n >> 6) * C::ATOM + row * 128 + ((((n & 63) >> 3) ^ (kr & 7)) << 4);
             }
-          } else {
-            float* out = static_cast<float*>(p.dX) + static_cast<int64_t>(row) * p.ld_dx + col0;
-            if (full_chunk) {
 #pragma unroll
-              for (int j = 0; j < 4; ++j)
-                reinterpret_cast<float4*>(out)[j] =
-                    make_float4(__uint_as_float(acc[4 * j]), __uint_as_float(acc[4 * j + 1]),
-                                __uint_as_float(acc[4 * j + 2]), __uint_as_float(acc[4 * j + 3]));
-            } else {
-              for (int j = 0; j < 16 && col0 + j < p.d_in; ++j) out[j] = __uint_as_float(acc[j]);
-            }
+            for (int j = 0; j < NJ; ++j) *reinterpret_cast<uint4*>(b + dst[j]) = o[j];
+            fence_proxy_async_smem();
+            // Release the staging slot only now: the stores above consume every
+            // value loaded from it, so those loads have returned before the next
+            // TMA fill may overwrite the slot.
+            mbar_arrive(&s_empty[ss]);
           }
+          if (!ok) break;
+          mbar_arrive(&b_full[sb]);
         }
       }
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tm_empty[buf]);
     }
-  } else if (warp >= 8 && F32W) {
-    // ------------------------------------------------------------ fp32 -> bf16 converters
-    // The fp32 rows landed by TMA as four [STG_ROWS rows][32 columns] boxes
-    // with the 128-byte swizzle. Work item = (box, K row, 8-column group): read
-    // two 16-byte chunks, round to bf16, write one 16-byte chunk of the
-    // MN-major swizzled operand. Consecutive threads take consecutive K
-    // rows, so both the reads and the writes are bank-conflict free.
-    const int ct = threadIdx.x - 256;
-    uint32_t k = 0, ks = 0;
-    bool ok = true;
-    SegWalk w = seg_walk<SPLIT>(p);
-    int tile, kb0, kb1, rot;
-    while (ok && seg_next<SPLIT>(p, w, tile, kb0, kb1, rot)) {
-      for (int i = 0; i < kb1 - kb0; ++i, ++k) {
-        const int kb = stage_at(kb0, kb1, rot, i);
-        const int sb = static_cast<int>(k % SB);
-        uint8_t* b = b_ring + sb * B_BYTES;
-        // A stage's BK rows arrive as BK / 64 staging slots of 64 rows.
-        for (int half = 0; half < BK / C::STG_ROWS; ++half, ++ks) {
-          const int ss = static_cast<int>(ks % SS);
-          ok = dwait(&s_full[ss], (ks / SS) & 1u, abort_flag, p.status, WAIT_OP_FULL, lim) &&
-               (half > 0 || dwait(&a_empty[sb], ((k / SB) & 1u) ^ 1u, abort_flag, p.status, WAIT_OP_EMPTY, lim));
-          ok = __all_sync(0xFFFFFFFFu, ok);
-          if (!ok) break;
-          const uint8_t* stg = s_ring + ss * STG_BYTES;
-          // Work items of the slot: 4 boxes x STG_ROWS rows x 4 groups of 8
-          // columns, STG_ROWS / 16 per thread.
-          constexpr int NJ = C::STG_ROWS / 16;
-          uint4 o[NJ];
-          int dst[NJ];
-#pragma unroll
-          for (int j = 0; j < NJ; ++j) {
-            const int i = ct + CONV_THREADS * j;
-            const int kr = i % C::STG_ROWS;                // row within the staging slot
-            const int hh = (i / C::STG_ROWS) & 3;          // 8-column group within the 32-column box
-            const int bb = i / (4 * C::STG_ROWS);          // box (32 columns)
-            const uint8_t* src = stg + bb * (C::STG_ROWS * 128) + kr * 128;
-            const float4 u0 = *reinterpret_cast<const float4*>(src + (((2 * hh) ^ (kr & 7)) << 4));
-            const float4 u1 = *reinterpret_cast<const float4*>(src + (((2 * hh + 1) ^ (kr & 7)) << 4));
-            o[j].x = pack_bf16x2_rn(u0.x, u0.y);
-            o[j].y = pack_bf16x2_rn(u0.z, u0.w);
-            o[j].z = pack_bf16x2_rn(u1.x, u1.y);
-            o[j].w = pack_bf16x2_rn(u1.z, u1.w);
-            const int n = bb * 32 + hh * 8;    // column within the 128-wide tile
-            const int row = half * C::STG_ROWS + kr;  // K row of the stage (row % 8 == kr % 8)
-            dst[j] = (n >> 6) * C::ATOM + row * 128 + ((((n & 63) >> 3) ^ (kr & 7)) << 4);
-          }
-#pragma unroll
-          for (int j = 0; j < NJ; ++j) *reinterpret_cast<uint4*>(b + dst[j]) = o[j];
-          fence_proxy_async_smem();
-          // Release the staging slot only now: the stores above consume every
-          // value loaded from it, so those loads have returned before the next
-          // TMA fill may overwrite the slot.
-          mbar_arrive(&s_empty[ss]);
-        }
+    // All-token tiles drain their transposed accumulator with warps 4-15
+    // (three groups of four, one warp per lane quadrant in each); the
+    // converters join once their last stage is written.
+    if (warp < 8 || C::SWAP) {
+      // ------------------------------------------------------------ epilogue
+      const int q = warp & 3;
+      const int r = q * 32 + lane;
+      int it = 0;
+      bool ok = true;
+      SegWalk w = seg_walk<SPLIT>(p);
+      int tile, kb0, kb1, rot;
+      for (; ok && seg_next<SPLIT>(p, w, tile, kb0, kb1, rot); ++it) {
+        int tm, tn;
+        dtile(tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+        const int buf = it % NBUF;
+        ok = dwait(&tm_full[buf], (it / NBUF) & 1, abort_flag, p.status, WAIT_TMEM_FULL, lim);
+        ok = __all_sync(0xFFFFFFFFu, ok);
         if (!ok) break;
-        mbar_arrive(&b_full[sb]);
+        tc_fence_after_sync();
+        if constexpr (C::SWAP) {
+          // Transposed accumulator: this thread's lane is feature r of the
+          // tile, its columns the tokens. Each load brings 16 tokens; a warp's
+          // store of one token covers 32 consecutive features.
+          const int col = tn * BN + r;
+          const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * MB * BN);
+          float* slot = SPLIT ? p.part + static_cast<int64_t>(blockIdx.x) * MB * BM * BN + r : nullptr;
+          const int group = (warp - 4) >> 2;   // 0..2: token chunks group, group + 3, ...
+#pragma unroll 1
+          for (int c = group; c < MB * BM / 16; c += 3) {
+            uint32_t acc[16];
+            if (p.num_kb > 0) {
+              tmem_ld_32x32b_x16(t_lane + c * 16, acc);
+              tmem_ld_wait();
+            } else {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) acc[j] = 0u;
+            }
+            const int t0 = tm * MB * BM + c * 16;
+            if constexpr (SPLIT) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) slot[static_cast<int64_t>(c * 16 + j) * BN] = __uint_as_float(acc[j]);
+              continue;
+            }
+            if (col >= p.d_in) continue;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int t = t0 + j;
+              if (t >= p.bt) break;
+              if (p.dx_bf16)
+                static_cast<uint16_t*>(p.dX)[static_cast<int64_t>(t) * p.ld_dx + col] =
+                    static_cast<uint16_t>(f32_to_bf16_rne(__uint_as_float(acc[j])));
+              else
+                static_cast<float*>(p.dX)[static_cast<int64_t>(t) * p.ld_dx + col] = __uint_as_float(acc[j]);
+            }
+          }
+        } else {
+#pragma unroll 1
+        for (int blk = 0; blk < MB; ++blk) {
+          const int row = (tm * MB + blk) * BM + r;
+          const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                  static_cast<uint32_t>((buf * MB + blk) * BN);
+          // A split contraction: this CTA's fp32 partial sum goes to its slot
+          // (row blk * 128 + r of an MB * 128 x BN slab), for the fix-up kernel
+          // to add in order.
+          constexpr bool partial = SPLIT;
+          float* slot = partial ? p.part + ((static_cast<int64_t>(blockIdx.x) * MB + blk) * BM + r) * BN : nullptr;
+#pragma unroll 1
+          for (int c = 0; c < BN / 16; ++c) {
+            uint32_t acc[16];
+            if (p.num_kb > 0) {
+              tmem_ld_32x32b_x16(t_lane + c * 16, acc);
+              tmem_ld_wait();
+            } else {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) acc[j] = 0u;
+            }
+            if (partial) {
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                reinterpret_cast<float4*>(slot + c * 16)[j] =
+                    make_float4(__uint_as_float(acc[4 * j]), __uint_as_float(acc[4 * j + 1]),
+                                __uint_as_float(acc[4 * j + 2]), __uint_as_float(acc[4 * j + 3]));
+              continue;
+            }
+            const int col0 = tn * BN + c * 16;
+            if (row >= p.bt || col0 >= p.d_in) continue;
+            const bool full_chunk = col0 + 16 <= p.d_in;
+            if (p.dx_bf16) {
+              uint16_t* out = static_cast<uint16_t*>(p.dX) + static_cast<int64_t>(row) * p.ld_dx + col0;
+              if (full_chunk) {
+                uint32_t b[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                  b[j] = pack_bf16x2_rn(__uint_as_float(acc[2 * j]), __uint_as_float(acc[2 * j + 1]));
+                reinterpret_cast<uint4*>(out)[0] = make_uint4(b[0], b[1], b[2], b[3]);
+                reinterpret_cast<uint4*>(out)[1] = make_uint4(b[4], b[5], b[6], b[7]);
+              } else {
+                for (int j = 0; j < 16 && col0 + j < p.d_in; ++j)
+                  out[j] = static_cast<uint16_t>(f32_to_bf16_rne(__uint_as_float(acc[j])));
+              }
+            } else {
+              float* out = static_cast<float*>(p.dX) + static_cast<int64_t>(row) * p.ld_dx + col0;
+              if (full_chunk) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                  reinterpret_cast<float4*>(out)[j] =
+                      make_float4(__uint_as_float(acc[4 * j]), __uint_as_float(acc[4 * j + 1]),
+                                  __uint_as_float(acc[4 * j + 2]), __uint_as_float(acc[4 * j + 3]));
+              } else {
+                for (int j = 0; j < 16 && col0 + j < p.d_in; ++j) out[j] = __uint_as_float(acc[j]);
+              }
+            }
+          }
+        }
+        }
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tm_empty[buf]);
       }
     }
   }

@@ -316,18 +316,24 @@ struct DgradPlan {
 // reads and writes, and the tensor cores' operand reads. Per multiply-add,
 // with tiles of MB blocks of 128 tokens x BN features:
 //   dY written 2/BN + W written (and converted) (wb + 6 [fp32]) / (128 MB)
-//   + operands read 2/BN + 1/64 bytes.
+//   + operands read 2/N + 2/M bytes for M x N products (128 tokens x BN
+//   features; all-token tiles: 128 features x 256 tokens).
 // This model gives the measured times within 0.7-1.0 (128 x 128 tiles,
 // fp32 weights: 29.4 MB through shared memory per CTA, 117 us). A plan's
-// cost is waves x that per CTA (token blocks padded to 128), plus, for a
-// split, 740 KB for the fix-up launch (3 us).
+// cost is waves x that per CTA (token blocks padded to 128), x 1.2 for
+// all-token tiles (their two-stage rings and transposed drain: on the
+// down-projection with bf16 weights they take 73 us where the model puts
+// them 9 % below the 68 us of 128 x 256 tiles), plus, for a split, 740 KB
+// for the fix-up launch (3 us).
 double dgrad_cost(const DgradPlan& g, int64_t d_out, int wbytes, bool f32w, int sms) {
   const int parts = g.parts >= 2 ? g.parts : 1;
   const int64_t ctas = static_cast<int64_t>(g.num_tiles) * parts;
   const double waves = static_cast<double>((ctas + sms - 1) / sms);
-  const double per_mac = 4.0 / g.bn + (wbytes + (f32w ? 6.0 : 0.0)) / (128.0 * g.mb) + 1.0 / 64.0;
+  const double operands = g.mb > 1 ? 2.0 / 256.0 + 2.0 / 128.0 : 2.0 / g.bn + 2.0 / 128.0;
+  const double per_mac = 2.0 / g.bn + (wbytes + (f32w ? 6.0 : 0.0)) / (128.0 * g.mb) + operands;
   const double macs = 128.0 * g.mb * g.bn * (static_cast<double>(d_out) / parts);
   double c = waves * macs * per_mac;
+  if (g.mb > 1) c *= 1.2;
   if (g.parts >= 2) c += 740e3;
   return c;
 }

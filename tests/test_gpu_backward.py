@@ -186,8 +186,10 @@ def test_workspace_bytes_geometry():
     def plan(d_out, d_in, bt, wbytes):
         # The input gradient's plan, costed by the bytes through the busiest
         # SM's shared memory: waves x multiply-adds per CTA (token blocks
-        # padded to 128) x (4 / BN + (W bytes + 6 for fp32 W) / (128 MB)
-        # + 1 / 64), plus 740 KB for a split's fix-up. Candidates: 128-token
+        # padded to 128) x (2 / BN + (W bytes + 6 for fp32 W) / (128 MB)
+        # + 2 / N + 2 / M for M x N products: 128 x BN, or 128 x 256 on
+        # all-token tiles), x 1.2 for all-token tiles, plus 740 KB for a
+        # split's fix-up. Candidates: 128-token
         # tiles (128 x 256 for bf16 W when those fill the GPU); the same split
         # in S = min(4, SMs // tiles) parts of >= 2048 rows where that puts
         # >= 1.5x as many SMs to work as 128 x 128 tiles (bf16 W on 128 x 256
@@ -197,8 +199,11 @@ def test_workspace_bytes_geometry():
             tiles_n = -(-d_in // bn)
             P = parts if parts >= 2 else 1
             waves = -(-(tiles_m * tiles_n * P) // sms)
-            per_mac = 4.0 / bn + (wbytes + (6.0 if wbytes == 4 else 0.0)) / (128.0 * mb) + 1.0 / 64.0
+            operands = 2.0 / 256.0 + 2.0 / 128.0 if mb > 1 else 2.0 / bn + 2.0 / 128.0
+            per_mac = 2.0 / bn + (wbytes + (6.0 if wbytes == 4 else 0.0)) / (128.0 * mb) + operands
             c = waves * (128.0 * mb * bn * (d_out / P)) * per_mac
+            if mb > 1:
+                c *= 1.2
             if parts >= 2:
                 c += 740e3
             nbytes = tiles_m * tiles_n * parts * 128 * mb * bn * 4 if parts >= 2 else 0
