@@ -523,6 +523,8 @@ forge_status wgrad_step(int opt, const forge_tensor* X, const forge_tensor* dY, 
 
   // ---- tensor-core path: tile-shape / scheduler policy
   const int tiles_m = static_cast<int>((d_out + 127) / 128);
+  // W and state bytes per parameter (read once; written once).
+  const int state_bytes = (wk == W_F32 ? 4 : 2) + nst * (mk == M_F32 ? 4 : mk == M_BF16 ? 2 : 1);
   int bn = 128;
   const uint32_t force = h->flags & FORGE_FLAG_TILE_N_MASK;
   if (dx != nullptr) bn = kDxBN;  // the fused input gradient fixes the tile width
@@ -531,8 +533,15 @@ forge_status wgrad_step(int opt, const forge_tensor* X, const forge_tensor* dY, 
   else if (force == FORGE_FLAG_TILE_N_256) bn = 256;
   else if (force != FORGE_FLAG_TILE_N_AUTO) return fail(FORGE_ERR_INVALID_ARG, "%s: bad tile flag", oname);
   else if (mk != M_Q8 && tiles_m * ((d_in + 127) / 128) < dev->sms) bn = 64;  // too few tiles for one wave
-  else if (mk != M_Q8 && !accum && G_acc == nullptr && bt >= 1024 && tiles_m * ((d_in + 255) / 256) >= dev->sms)
-    bn = 256;  // long token axes: the GEMM dominates, wider tiles cut its operand traffic
+  else if (mk != M_Q8 && !accum && G_acc == nullptr && tiles_m * ((d_in + 255) / 256) >= dev->sms &&
+           (bt >= 1024 || (bt >= 512 && state_bytes <= 4)))
+    // Long token axes (the GEMM dominates) and, from 512 tokens, light state
+    // (<= 4 bytes per parameter): wider tiles cut the operand pipeline's
+    // share (up-projection, BT 512, step alone: SGD bf16 W 108 -> 75 us,
+    // SGD fp32 W 129 -> 92, Lion bf16 129 -> 110, SGD-momentum bf16
+    // 117 -> 104.5; Lion fp32 188 -> 202, AdamW fp32 238 -> 267, AdamW
+    // bf16 173 either way; BT 256: 128 columns everywhere).
+    bn = 256;
   if (mk == M_Q8 && bn != 128)
     return fail(FORGE_ERR_UNSUPPORTED, "%s: 8-bit block moments need 128-column tiles", oname);
   if (bn == 256 && (accum || G_acc != nullptr))
@@ -546,8 +555,11 @@ forge_status wgrad_step(int opt, const forge_tensor* X, const forge_tensor* dY, 
   // BT 512 181 -> 178 us, BT 768 211 -> 180 us; 8-bit moments at BT 512
   // 227.5 -> 220 us; fp32 state at BT 768 277 -> 268 us but at BT 512
   // 240 -> 262 us (its state ring loses slots).
+  // The stateless rule (SGD) takes it from 256 tokens (BT 256: bf16 W
+  // 69 -> 60 us, fp32 W 86.5 -> 84 us).
   const bool deep128 = dx == nullptr && G_acc == nullptr && bn == 128 &&
-                       (bt >= 768 || accum || (bt >= 512 && ((wk == W_BF16 && mk == M_BF16) || mk == M_Q8)));
+                       (bt >= 768 || accum || (bt >= 256 && nst == 0) ||
+                        (bt >= 512 && ((wk == W_BF16 && mk == M_BF16) || mk == M_Q8)));
   // 256-column tiles always use the deep ring; the fused input gradient takes
   // a third operand stage past 512 tokens (its mainloop then sets the pace).
   // The fused input gradient takes a third operand stage past 512 tokens, and
