@@ -61,13 +61,10 @@ struct DCfg {
   // and twice the ring depth, measured slower: 81 -> 86 us on the
   // down-projection with fp32 weights, 46 -> 61 us at BT 256 with bf16).
   static constexpr int BK = MB > 1 ? 64 : (BN == 256 ? 64 : 128);
-  // dY boxes: 64 K columns (128-byte rows, 128-byte swizzle), or 32 for
-  // 32-row stages (64-byte rows, 64-byte swizzle).
-  static constexpr int A_ROW = BK < 64 ? 2 * BK : 128;  // bytes per row of a dY box
-  static constexpr int A_BOX_K = A_ROW / 2;           // K columns per box
-  static constexpr int A_BOX = BM * A_ROW;            // bytes per box (128 token rows)
-  static constexpr int A_SWZ = A_ROW == 128 ? 2 : 4;  // descriptor swizzle code: 128-byte / 64-byte
-  static constexpr int A_BLOCK = BM * BK * 2;    // one token block of dY, K-major: BK / A_BOX_K boxes, A_BOX apart
+  // dY boxes: 64 K columns x 128 token rows (128-byte rows, 128-byte swizzle).
+  static constexpr int A_BOX_K = 64;              // K columns per box
+  static constexpr int A_BOX = BM * 128;          // bytes per box
+  static constexpr int A_BLOCK = BM * BK * 2;    // one token block of dY, K-major: BK / 64 boxes, A_BOX apart
   static constexpr int A_BYTES = MB * A_BLOCK;   // the stage's token blocks, A_BLOCK apart
   static constexpr int B_BYTES = BK * BN * 2;    // bf16 W tile, MN-major, 64-column atoms BK * 128 bytes apart
   static constexpr int ATOM = BK * 128;          // bytes of one 64-column atom (box) of the bf16 W tile
@@ -341,13 +338,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dgrad_tc_kernel(const __grid_c
           tc_fence_after_sync();
           const uint32_t a0 = smem_u32(a_ring + sa * A_BYTES);
           const uint32_t b0 = smem_u32(b_ring + sb * B_BYTES);
-          // A: K-major, rows of A_ROW bytes with the matching swizzle, 8-row
-          // groups 8 * A_ROW bytes apart. B: MN-major, 64-column atoms
-          // C::ATOM bytes apart, 8-row K groups of 1024 bytes. Both
-          // descriptors are built once per stage; a K step only moves the
-          // 14-bit start-address field (16-byte units; shared addresses stay
-          // below 2^18 bytes, so it never carries).
-          const uint64_t ad0 = make_smem_desc(a0, 16, 8 * C::A_ROW, C::A_SWZ);
+          // dY: K-major, 128-byte swizzle, 8-row groups 1024 bytes apart.
+          // W: MN-major, 64-column atoms C::ATOM bytes apart, 8-row K groups
+          // of 1024 bytes. Both descriptors are built once per stage; a K
+          // step only moves the 14-bit start-address field (16-byte units;
+          // shared addresses stay below 2^18 bytes, so it never carries).
+          const uint64_t ad0 = make_smem_desc(a0, 16, 1024, 2);
           const uint64_t bd0 = make_smem_desc(b0, C::ATOM, 1024, 2);
           if constexpr (C::SWAP) {
             // A = the W tile (descriptor bd0), B = 256 tokens of dY: token
