@@ -10,4 +10,4 @@ from ._lib import (  # noqa: F401
     FLAG_TILE_N_128, FLAG_TILE_N_256, FLAG_TILE_N_AUTO, I8B128, LIB_PATH, RULES, ForgeError, backward_step,
     backward_accumulate, backward_step_no_alloc, dgrad, lib, sync_status, tensor_desc, version, wgrad_accumulate,
     wgrad_step_accumulated, wgrad_step_adamw, wgrad_step_adagrad, wgrad_step_lion, wgrad_step_nadam,
-    wgrad_step_radam, wgrad_step_rmsprop, wgrad_step_sgd, wgrad_step_sgdm, workspace_bytes)
+    wgrad_step_radam, wgrad_step_rmsprop, wgrad_step_sgd, wgrad_step_sgdm, workspace_bytes, selftest_math)

@@ -33,7 +33,7 @@ EXPORTED = ("forge_wgrad_step_adamw", "forge_wgrad_step_sgdm", "forge_wgrad_step
             "forge_dgrad", "forge_dgrad_ws", "forge_backward_step", "forge_backward_step_no_alloc",
             "forge_wgrad_accumulate",
             "forge_backward_accumulate", "forge_wgrad_step_accumulated", "forge_sync_status", "forge_last_error", "forge_version",
-            "forge_workspace_bytes")
+            "forge_workspace_bytes", "forge_selftest_math")
 
 
 class ForgeTensor(ctypes.Structure):
@@ -94,6 +94,8 @@ def _load() -> ctypes.CDLL:
     lib.forge_version.restype = ctypes.c_char_p
     lib.forge_workspace_bytes.argtypes = [i64, i64, i64]
     lib.forge_workspace_bytes.restype = ctypes.c_size_t
+    lib.forge_selftest_math.argtypes = [ctypes.c_int, u64, u64, P(u64), P(u64)]
+    lib.forge_selftest_math.restype = ctypes.c_int
     return lib
 
 
@@ -345,3 +347,10 @@ def version() -> str:
 
 def workspace_bytes(d_out: int, d_in: int, bt: int) -> int:
     return int(lib().forge_workspace_bytes(d_out, d_in, bt))
+
+
+def selftest_math(which: int, first: int, count: int):
+    """(mismatches, declined) of forge_selftest_math (test hook)."""
+    mism, decl = ctypes.c_uint64(0), ctypes.c_uint64(0)
+    _check(lib().forge_selftest_math(int(which), int(first), int(count), ctypes.byref(mism), ctypes.byref(decl)))
+    return mism.value, decl.value

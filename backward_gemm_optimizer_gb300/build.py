@@ -22,6 +22,7 @@ LIB = os.path.join(HERE, "libforge.so")
 
 SOURCES = [
     "forge_api.cu",
+    "forge_selftest.cu",
     "wgrad_tc_adamw.cu",
     "wgrad_tc_sgdm.cu",
     "wgrad_tc_lion.cu",

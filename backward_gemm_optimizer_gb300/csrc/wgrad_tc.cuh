@@ -102,6 +102,13 @@ struct TcCfg {
   // the weights the converter warps read for dX.
   static constexpr bool ACC = (OPT == OPT_ACCUM || OPT == OPT_ACCSET);
   static constexpr bool SLOT_F32 = (WK == W_F32) || ACC;  // fp32 values in the slot's first tensor
+  // AdamW with bf16 or 8-bit moments in the plain step: the branch-free
+  // divide and square root (forge_math.cuh, adamw_group_fast; up-projection,
+  // BT 512: bf16 state 172.4 -> 161.2 us, 8-bit 221 -> 210 us with 30 % zero
+  // rows, 201 us without). Not in the fused input-gradient kernel (bf16
+  // state 226 -> 227 us, with spills around the out-of-line guarded path)
+  // nor with fp32 state (no faster; fused pass 269.5 -> 274.8 us).
+  static constexpr bool FASTDIV = OPT == OPT_ADAMW && (MK == M_BF16 || MK == M_Q8) && !DX;
   static constexpr int WE = SLOT_F32 ? 4 : 2;
   static constexpr int ME = (MK == M_F32) ? 4 : (MK == M_BF16 ? 2 : 1);
   static constexpr int A_BYTES = BM * BK * 2;
@@ -693,8 +700,12 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, N
               if constexpr (C::TWO) ld8_bf16_w(slot + C::W_CH + C::M_CH, r, hq, v);
 #pragma unroll
               for (int j = 0; j < 8; ++j) g[j] = __uint_as_float(gr[j]);
+              if constexpr (C::FASTDIV) {
+                adamw_group_fast(g, w, m, v, sc);
+              } else {
 #pragma unroll
-              for (int j = 0; j < 8; ++j) step_elem<OPT>(g[j], w[j], m[j], v[j], sc);
+                for (int j = 0; j < 8; ++j) step_elem<OPT>(g[j], w[j], m[j], v[j], sc);
+              }
               const uint64_t idx8 =
                   (static_cast<uint64_t>(row) * static_cast<uint64_t>(p.d_in) + (tn * BN + c * C::CW + col)) >> 3;
               uint4 b;
@@ -745,8 +756,12 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, N
 #pragma unroll
             for (int j = 0; j < 8; ++j) g[j] = __fadd_rn(ga[j], g[j]);
           }
+          if constexpr (C::FASTDIV) {
+            adamw_group_fast(g, w, m, v, sc);
+          } else {
 #pragma unroll
-          for (int j = 0; j < Q; ++j) step_elem<OPT>(g[j], w[j], m[j], v[j], sc);
+            for (int j = 0; j < Q; ++j) step_elem<OPT>(g[j], w[j], m[j], v[j], sc);
+          }
           if constexpr (Q == 4) {
             st4_f32(sw, r, h, w);
             st4_f32(sm, r, h, m);
@@ -886,15 +901,44 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, N
           float w[8];
           ld8<WK == W_F32 ? 0 : 1>(sw, r, h, w);
           bool near = false;  // a product within 1e-4 of a half-integer: decide those codes exactly
+          // AdamW: the weight update and sqrt(v') of the 8 values with the
+          // branch-free divide and square root, recomputed with the guarded
+          // correctly rounded ones if an operand is outside their ranges.
+          // A row whose new moments are all zero (its block maxima am, au are
+          // 0) takes u = m' (0 / d, signed) and sqrt(v') = v' directly.
+          float wn[8], sq[8];
+          if constexpr (OPT == OPT_ADAMW) {
+            if (am == 0.0f && au == 0.0f) {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                wn[j] = __fsub_rn(__fmul_rn(sc.decay, w[j]), __fmul_rn(sc.step_size, __uint_as_float(k0[j])));
+                sq[j] = __uint_as_float(k1[j]);
+              }
+            } else {
+              bool bad = false;
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                adamw_apply_fast(w[j], __uint_as_float(k0[j]), __uint_as_float(k1[j]), sc, wn[j], sq[j], bad);
+              if (__builtin_expect(bad, 0)) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  const AdamWOut o = adamw_value_guarded(0.0f, w[j], __uint_as_float(k0[j]), __uint_as_float(k1[j]),
+                                                         sc.b1, sc.omb1, sc.b2, sc.omb2, sc.decay, sc.step_size,
+                                                         sc.inv_sqrt_bc2, sc.eps, 1);
+                  wn[j] = o.w;
+                  sq[j] = o.sq;
+                }
+              }
+            }
+          }
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const float m1 = __uint_as_float(k0[j]);
             float w1;
             if constexpr (OPT == OPT_ADAMW) {
               const float v1 = __uint_as_float(k1[j]);
-              float sq1;
-              adamw_apply_zg(w[j], m1, v1, sc, w1, sq1);
-              cv[j] = quant_v_byte_fast(v1, sq1, sv_new, iv_new, near);
+              w1 = wn[j];
+              cv[j] = quant_v_byte_fast(v1, sq[j], sv_new, iv_new, near);
             } else if constexpr (OPT == OPT_SGDM) {
               w1 = sgdm_apply(w[j], m1, sc);
             } else {

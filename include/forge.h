@@ -427,6 +427,24 @@ const char* forge_version(void);
  */
 size_t forge_workspace_bytes(int64_t d_out, int64_t d_in, int64_t bt);
 
+/*
+ * forge_selftest_math -- test hook: enumerates cases of the branch-free
+ * correctly rounded divide and square root the AdamW epilogues use with
+ * bf16 / 8-bit moments, on the current device, and counts disagreements
+ * with the hardware's correctly rounded operations. which = 0: the square
+ * root of every float whose bit pattern is in [first, first + count)
+ * (< 2^32); 1: the refined reciprocal of every such divisor in
+ * [2^-60, 2^60]; 2: the quotient n / d over pairs of significands, case i
+ * being n = 1 + floor(i / 2^23) 2^-23, d = 1 + (i mod 2^23) 2^-23
+ * (i < 2^46). *mismatches receives the disagreements, *declined the cases
+ * the fast path leaves to the guarded functions (outside its range).
+ * Synchronous (waits for the device); FORGE_ERR_INVALID_ARG for a bad
+ * `which`, range or null pointer, FORGE_ERR_CUDA if a CUDA call fails; sets
+ * no forge_last_error message.
+ */
+forge_status forge_selftest_math(int which, uint64_t first, uint64_t count, uint64_t* mismatches,
+                                 uint64_t* declined);
+
 #ifdef __cplusplus
 }
 #endif

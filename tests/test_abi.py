@@ -220,3 +220,14 @@ def test_backward_accumulate_host_checks():
     Xf, dYf = _t(dtype=0, rows=16, cols=64), _t(dtype=0, rows=16, cols=32)
     assert f(b(Xf), b(dYf), b(W), b(G), b(dX), 0, 0, None, 0, None) == UNSUPPORTED      # bf16 inputs only
     assert f(b(Xf), b(dYf), b(W), b(G), b(dX), 0, F.FLAG_BACKWARD_FUSED, None, 0, None) == UNSUPPORTED
+
+
+def test_selftest_math_argument_checks():
+    # Host-side checks only (no device work): a bad selector, range or
+    # null output pointer is FORGE_ERR_INVALID_ARG.
+    lib = F.lib()
+    out = ctypes.c_uint64(0)
+    assert lib.forge_selftest_math(3, 0, 1, ctypes.byref(out), ctypes.byref(out)) == INVALID
+    assert lib.forge_selftest_math(0, 0, 1, None, ctypes.byref(out)) == INVALID
+    assert lib.forge_selftest_math(0, 1 << 32, 1, ctypes.byref(out), ctypes.byref(out)) == INVALID
+    assert lib.forge_selftest_math(2, (1 << 46) - 1, 2, ctypes.byref(out), ctypes.byref(out)) == INVALID
