@@ -106,9 +106,10 @@ struct TcCfg {
   // divide and square root (forge_math.cuh, adamw_group_fast; up-projection,
   // BT 512: bf16 state 172.4 -> 161.2 us, 8-bit 221 -> 210 us with 30 % zero
   // rows, 201 us without). Not in the fused input-gradient kernel (bf16
-  // state 226 -> 227 us, with spills around the out-of-line guarded path)
-  // nor with fp32 state (no faster; fused pass 269.5 -> 274.8 us).
-  static constexpr bool FASTDIV = OPT == OPT_ADAMW && (MK == M_BF16 || MK == M_Q8) && !DX;
+  // state 226 -> 227 us, with spills around the out-of-line guarded path),
+  // on 128 x 256 tiles (BT 2048 250 -> 272 us, BT 8192 771 -> 793 us) nor
+  // with fp32 state (no faster; fused pass 269.5 -> 274.8 us).
+  static constexpr bool FASTDIV = OPT == OPT_ADAMW && (MK == M_BF16 || MK == M_Q8) && !DX && BN_ != 256;
   static constexpr int WE = SLOT_F32 ? 4 : 2;
   static constexpr int ME = (MK == M_F32) ? 4 : (MK == M_BF16 ? 2 : 1);
   static constexpr int A_BYTES = BM * BK * 2;
