@@ -323,8 +323,10 @@ struct DgradPlan {
 // cost is waves x that per CTA (token blocks padded to 128), x 1.2 for
 // all-token tiles (their two-stage rings and transposed drain: on the
 // down-projection with bf16 weights they take 73 us where the model puts
-// them 9 % below the 68 us of 128 x 256 tiles), plus, for a split, 740 KB
-// for the fix-up launch (3 us).
+// them 9 % below the 68 us of 128 x 256 tiles) and x 1.4 for four blocks
+// with bf16 weights (up-projection, BT 512, split path: 141 against
+// 135 us with 128-token tiles), plus, for a split, 740 KB for the fix-up
+// launch (3 us).
 double dgrad_cost(const DgradPlan& g, int64_t d_out, int wbytes, bool f32w, int sms) {
   const int parts = g.parts >= 2 ? g.parts : 1;
   const int64_t ctas = static_cast<int64_t>(g.num_tiles) * parts;
@@ -333,7 +335,7 @@ double dgrad_cost(const DgradPlan& g, int64_t d_out, int wbytes, bool f32w, int 
   const double per_mac = 2.0 / g.bn + (wbytes + (f32w ? 6.0 : 0.0)) / (128.0 * g.mb) + operands;
   const double macs = 128.0 * g.mb * g.bn * (static_cast<double>(d_out) / parts);
   double c = waves * macs * per_mac;
-  if (g.mb > 1) c *= 1.2;
+  if (g.mb > 1) c *= (g.mb == 4 && wbytes == 2) ? 1.4 : 1.2;
   if (g.parts >= 2) c += 740e3;
   return c;
 }

@@ -188,8 +188,8 @@ def test_workspace_bytes_geometry():
         # SM's shared memory: waves x multiply-adds per CTA (token blocks
         # padded to 128) x (2 / BN + (W bytes + 6 for fp32 W) / (128 MB)
         # + 2 / N + 2 / M for M x N products: 128 x BN, or 128 x 256 on
-        # all-token tiles), x 1.2 for all-token tiles, plus 740 KB for a
-        # split's fix-up. Candidates: 128-token
+        # all-token tiles), x 1.2 for all-token tiles (x 1.4 for four blocks
+        # with bf16 W), plus 740 KB for a split's fix-up. Candidates: 128-token
         # tiles (128 x 256 for bf16 W when those fill the GPU); the same split
         # in S = min(4, SMs // tiles) parts of >= 2048 rows where that puts
         # >= 1.5x as many SMs to work as 128 x 128 tiles (bf16 W on 128 x 256
@@ -203,7 +203,7 @@ def test_workspace_bytes_geometry():
             per_mac = 2.0 / bn + (wbytes + (6.0 if wbytes == 4 else 0.0)) / (128.0 * mb) + operands
             c = waves * (128.0 * mb * bn * (d_out / P)) * per_mac
             if mb > 1:
-                c *= 1.2
+                c *= 1.4 if (mb == 4 and wbytes == 2) else 1.2
             if parts >= 2:
                 c += 740e3
             nbytes = tiles_m * tiles_n * parts * 128 * mb * bn * 4 if parts >= 2 else 0
