@@ -497,3 +497,63 @@ def test_sr_store_non_finite_weights(flag):
         if b in (0x7F80, 0xFF80):
             assert int(got.W[i, j]) == b
     assert_bit_exact(O.State(W=ref.W, m=got.m, v=got.v), ref, "adamw")
+
+
+# ---------------------------------------------------------------------------
+# AdamW with bf16 / 8-bit moments: operands outside the branch-free divide
+# and square root's ranges take the guarded path
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("tiles", ["n128", "n64"])
+def test_adamw_bf16_state_out_of_range_operands_bit_exact(tiles):
+    # Zero rows (m' = v' = 0), second moments above 2^100 and below 2^-100,
+    # first moments below 2^-60 and above 2^60, planted among ordinary
+    # values: each group of eight that holds one is recomputed by the
+    # guarded correctly rounded functions, and every value must still equal
+    # the oracle's float32 op sequence bit for bit.
+    prob = _prob((256, 512, 200), 37, "bf16", "bf16", "bf16", exact=True, zero_rows=0.1)
+    m = prob.m.view(torch.int16).numpy().view(np.uint16)
+    v = prob.v.view(torch.int16).numpy().view(np.uint16)
+    plants = {(3, 5): ("v", 1e32), (3, 77): ("v", 3e35), (9, 8): ("v", 1e-33), (17, 100): ("m", 1e-25),
+              (17, 101): ("m", -4e-30), (30, 200): ("m", 5e20), (31, 300): ("m", -2e24), (40, 9): ("v", 0.0),
+              (40, 10): ("m", 0.0)}
+    zr = np.flatnonzero(prob.zero_rows)
+    for k, r in enumerate(zr[:4]):            # the same extremes on rows with no gradient
+        plants[(int(r), 8 * k + 1)] = ("m", 3e-24)
+        plants[(int(r), 8 * k + 40)] = ("v", 1e-34)
+    for (i, j), (which, x) in plants.items():
+        (m if which == "m" else v)[i, j] = int(O.f32_to_bf16_rne(np.array([x], np.float32))[0])
+    flags = F.FLAG_TILE_N_128 if tiles == "n128" else F.FLAG_TILE_N_64
+    for t in (1, 3):
+        got = gpu_step("adamw", prob, t, seed=13, sr_w=True, sr_moments=True, flags=flags)
+        ref = oracle_step("adamw", prob, "bf16", "bf16", t, seed=13, sr_w=True, sr_moments=True, mode="f32emu")
+        assert_bit_exact(got, ref, "adamw")
+
+
+def test_adamw_q8_state_out_of_range_operands_bit_exact():
+    # 8-bit moments whose block scales put the decoded moments outside the
+    # fast path's ranges: |m| above 2^60 (scale x 2^72) and v above 2^100
+    # (square-root-domain scale x 2^62) on rows with a gradient; |m| below
+    # 2^-60 (x 2^-55) and v below 2^-100 (x 2^-45) on rows with none, whose
+    # codes are copied from a row that has a gradient. Bit-exact against the
+    # float32 op sequence.
+    prob = _prob((256, 512, 192), 38, "bf16", "f32", "q8", exact=True, zero_rows=0.1)
+    m, v = prob.m.numpy(), prob.v.numpy()
+    ms, vs = prob.m_scale.numpy(), prob.v_scale.numpy()
+    zr = np.flatnonzero(prob.zero_rows)
+    live = np.flatnonzero(~prob.zero_rows)
+    ms[0, live[3]] *= np.float32(2.0 ** 72)
+    ms[2, live[50]] *= np.float32(2.0 ** 72)
+    vs[1, live[3]] *= np.float32(2.0 ** 62)
+    vs[3, live[99]] *= np.float32(2.0 ** 62)
+    for k, r in enumerate(zr[:3]):
+        src = live[k]
+        cols = slice(128 * k, 128 * (k + 1))
+        m[r, cols] = m[src, cols]
+        v[r, cols] = v[src, cols]
+        ms[k, r] = ms[k, src] * np.float32(2.0 ** -55)
+        vs[k, r] = vs[k, src] * np.float32(2.0 ** -45)
+    for t in (1, 2):
+        got = gpu_step("adamw", prob, t, seed=5, flags=F.FLAG_TILE_N_128)
+        ref = oracle_step("adamw", prob, "f32", "q8", t, seed=5, mode="f32emu")
+        assert_bit_exact(got, ref, "adamw")
