@@ -593,7 +593,16 @@ forge_status wgrad_step(int opt, const forge_tensor* X, const forge_tensor* dY, 
   // BT 768). One-state rules (fp32 W + fp32 m) take them from 512 tokens:
   // Lion up-projection 225.3 -> 220.6 us, SGD-momentum unchanged, both a
   // little slower at 256.
-  const bool narrow = dx != nullptr && wk == W_F32 && mk == M_F32 && (nst == 2 || (nst == 1 && bt >= 512));
+  // On the plain step's 128 x 256 tiles the narrow slots make room for a
+  // third operand stage beside three (two moments) or four (one) slots,
+  // where 32-column slots left two stages and two slots (up-projection, step
+  // alone: AdamW BT 2048 381 -> 314 us, BT 8192 1123 -> 824 us; Lion BT
+  // 8192 779 -> 771 us); on deep 128 x 128 tiles (768 tokens) a fourth
+  // operand stage (AdamW 268.8 -> 256 us, Lion 203 -> 164, SGD-momentum
+  // 197 -> 163).
+  const bool narrow = wk == W_F32 && mk == M_F32 && nst >= 1 &&
+                      ((dx != nullptr && (nst == 2 || bt >= 512)) ||
+                       (dx == nullptr && G_acc == nullptr && !accum && (bn == 256 || deep128)));
   // 64-column chunks for the plain step with bf16 W and bf16 moments on
   // 128-column tiles below 768 tokens: half as many slot hand-overs for the
   // same bytes in flight (up-projection, AdamW: BT 256 176.4 -> 168.2 us,

@@ -80,11 +80,11 @@ struct TcCfg {
   static constexpr int BN = BN_;       // tile columns (D_in)
   static constexpr int BK = DX ? 128 : 64;  // tokens per operand stage
   static constexpr int BOX = BK * 128; // bytes of one 64-column operand box (BK rows of 128 bytes)
-  // State chunk width (columns): 32, or 16 (NARROW) for the fused-input-
-  // gradient kernel with fp32 W and fp32 moments -- its shared memory
-  // holds two 48 KB slots of 32 columns or four of 16: on short token axes
-  // the deeper state ring pays for the extra chunk turns, and on long ones
-  // the narrow slots leave room for a third operand stage.
+  // State chunk width (columns): 32, or 16 (NARROW) with fp32 W and fp32
+  // state in the fused-input-gradient kernel and the deep-ring step --
+  // shared memory holds two 48 KB slots of 32 columns or four of 16: on
+  // short token axes the deeper state ring pays for the extra chunk turns,
+  // and on long ones the narrow slots leave room for a third operand stage.
   static constexpr bool NARROW = NARROW_;
   // 64 (WIDE) for the plain step with bf16 W and bf16 moments: 48 KB slots
   // instead of 24 KB ones, half the chunk turns per byte of state.
@@ -409,8 +409,8 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, N
   using C = TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, NARROW, WIDE>;
   static_assert(!WIDE || (WK == W_BF16 && MK == M_BF16 && !DX && !GA && !C::ACC),
                 "64-column chunks: plain step with bf16 W and bf16 moments");
-  static_assert(!NARROW || (DX && WK == W_F32 && MK == M_F32 && C::NST >= 1 && !C::ACC),
-                "16-column chunks: fused kernel with fp32 W and fp32 state");
+  static_assert(!NARROW || ((DX || BN >= 128) && WK == W_F32 && MK == M_F32 && C::NST >= 1 && !C::ACC && !GA),
+                "16-column chunks: fused kernel or deep step tiles with fp32 W and fp32 state");
   static_assert(!GA || (!DX && !C::Q8), "accumulated-gradient step: split path, fp32 / bf16 state");
   static_assert(!C::ACC || ((WK == W_F32 || DX) && !GA), "fp32 gradient accumulator");
   static_assert(BN == 64 || BN == 128 || BN == 256, "tile width");

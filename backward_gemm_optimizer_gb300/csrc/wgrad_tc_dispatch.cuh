@@ -23,21 +23,21 @@ constexpr int slots_that_fit() {
 // Operand stages: 2 for short token axes (the step is bound by the state
 // stream); for long ones as many as leave room for the state ring (4, else
 // 3, else 2).
-template <int OPT, int WK, int MK, int BN, int DEEP, bool WIDE = false>
+template <int OPT, int WK, int MK, int BN, int DEEP, bool WIDE = false, bool NARROW = false>
 constexpr int pick_stages() {
   if (!DEEP) return 2;
   constexpr int need = (MK == M_Q8) ? 4 : 2;
-  if (slots_that_fit<OPT, WK, MK, BN, 4, false, false, false, WIDE>() >= need) return 4;
-  if (slots_that_fit<OPT, WK, MK, BN, 3, false, false, false, WIDE>() >= need) return 3;
+  if (slots_that_fit<OPT, WK, MK, BN, 4, false, false, NARROW, WIDE>() >= need) return 4;
+  if (slots_that_fit<OPT, WK, MK, BN, 3, false, false, NARROW, WIDE>() >= need) return 3;
   return 2;
 }
 
-template <int OPT, int WK, int MK, int BN, int DEEP, bool WIDE = false>
+template <int OPT, int WK, int MK, int BN, int DEEP, bool WIDE = false, bool NARROW = false>
 cudaError_t launch_one(const WgradTcParams& p, int grid, cudaStream_t stream) {
-  constexpr int S = pick_stages<OPT, WK, MK, BN, DEEP, WIDE>();
-  constexpr int N = slots_that_fit<OPT, WK, MK, BN, S, false, false, false, WIDE>();
+  constexpr int S = pick_stages<OPT, WK, MK, BN, DEEP, WIDE, NARROW>();
+  constexpr int N = slots_that_fit<OPT, WK, MK, BN, S, false, false, NARROW, WIDE>();
   static_assert(N >= ((MK == M_Q8) ? 4 : 2), "state ring does not fit");
-  return launch_tc_variant<OPT, WK, MK, BN, S, N, false, false, false, WIDE>(p, grid, stream);
+  return launch_tc_variant<OPT, WK, MK, BN, S, N, false, false, NARROW, WIDE>(p, grid, stream);
 }
 
 // Step with an accumulated gradient (the last micro-batch): two operand
@@ -105,8 +105,14 @@ cudaError_t launch_mk(const WgradTcParams& p, const TcLaunch& l) {
       // 128 x 256 tiles for long token axes: a quarter less operand traffic
       // per gradient element than 128 x 128, half the MMA instructions.
       if (!l.deep) return cudaErrorInvalidValue;
+      if constexpr (WK == W_F32 && MK == M_F32 && opt_nstate(OPT) >= 1)
+        if (l.narrow) return launch_one<OPT, WK, MK, 256, 1, false, true>(p, l.grid, l.stream);
+      if (l.narrow) return cudaErrorInvalidValue;
       return launch_one<OPT, WK, MK, 256, 1>(p, l.grid, l.stream);
     }
+    if constexpr (WK == W_F32 && MK == M_F32 && opt_nstate(OPT) >= 1)
+      if (l.narrow && l.deep) return launch_one<OPT, WK, MK, 128, 1, false, true>(p, l.grid, l.stream);
+    if (l.narrow) return cudaErrorInvalidValue;
     return l.deep ? launch_one<OPT, WK, MK, 128, 1>(p, l.grid, l.stream)
                   : launch_one<OPT, WK, MK, 128, 0>(p, l.grid, l.stream);
   }

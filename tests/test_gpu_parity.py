@@ -419,11 +419,13 @@ def test_more_families_fp32_inputs_bit_exact(opt):
 # 128 x 256 tiles (long token axes)
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("opt", ["adamw", "lion", "nadam"])
+@pytest.mark.parametrize("opt", ["adamw", "lion", "sgdm", "nadam"])
 @pytest.mark.parametrize("variant", [("f32", "f32"), ("f32", "bf16"), ("bf16", "bf16"), ("bf16", "f32")],
                          ids=lambda v: f"W{v[0]}-m{v[1]}")
 @pytest.mark.parametrize("shape", [(384, 520, 1100), (136, 256, 70)], ids=lambda s: "x".join(map(str, s)))
 def test_wide_tiles_exact(opt, variant, shape):
+    # fp32 W + fp32 state streams 16-column chunks on these tiles (three
+    # operand stages), the other storages 32-column ones.
     w, st = variant
     prob = _prob(shape, 17, "bf16", w, st, exact=True)
     sr, srm = w == "bf16", st == "bf16"
@@ -445,6 +447,19 @@ def test_bf16_state_64_column_chunks_exact(opt, shape):
         got = gpu_step(opt, prob, 2, seed=9, sr_w=True, sr_moments=True, flags=flag)
         ref = oracle_step(opt, prob, "bf16", "bf16", 2, seed=9, sr_w=True, sr_moments=True, mode="f32emu")
         assert_bit_exact(got, ref, opt)
+
+
+@pytest.mark.parametrize("opt", ["adamw", "lion", "sgdm", "radam"])
+def test_deep_ring_fp32_state_16_column_chunks_exact(opt):
+    # fp32 W + fp32 state past 768 tokens on 128-column tiles: four operand
+    # stages beside a ring of 16-column state chunks; ragged D_in and a
+    # ragged token tail. Against the oracle and against 64-column tiles
+    # (two stages, 32-column chunks).
+    prob = _prob((264, 520, 800), 29, "bf16", "f32", "f32", exact=True)
+    got = gpu_step(opt, prob, 2, seed=3, flags=F.FLAG_TILE_N_128)
+    ref = oracle_step(opt, prob, "f32", "f32", 2, seed=3, mode="f32emu")
+    assert_bit_exact(got, ref, opt)
+    assert_bit_exact(gpu_step(opt, prob, 2, seed=3, flags=F.FLAG_TILE_N_64), ref, opt)
 
 
 @pytest.mark.parametrize("exact", [True, False])
