@@ -18,7 +18,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libforge.so")
 
 F32, BF16, I8B128 = 0, 1, 2
-FLAG_TILE_N_AUTO, FLAG_TILE_N_128, FLAG_TILE_N_64, FLAG_TILE_N_256 = 0, 1, 2, 3
+FLAG_TILE_N_AUTO, FLAG_TILE_N_128, FLAG_TILE_N_64, FLAG_TILE_N_256, FLAG_TILE_PAIR_256 = 0, 1, 2, 3, 4
 FLAG_TEST_FORCE_TIMEOUT = 0x100
 FLAG_BACKWARD_FUSED, FLAG_BACKWARD_SPLIT = 0x200, 0x400
 FLAG_DGRAD_TOKENS_128, FLAG_DGRAD_ALL_TOKENS = 0x800, 0x1000

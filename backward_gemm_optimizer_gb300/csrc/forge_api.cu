@@ -528,11 +528,13 @@ forge_status wgrad_step(int opt, const forge_tensor* X, const forge_tensor* dY, 
   // W and state bytes per parameter (read once; written once).
   const int state_bytes = (wk == W_F32 ? 4 : 2) + nst * (mk == M_F32 ? 4 : mk == M_BF16 ? 2 : 1);
   int bn = 128;
+  bool pair = false;  // CTA pairs on 256 x 256 tiles
   const uint32_t force = h->flags & FORGE_FLAG_TILE_N_MASK;
   if (dx != nullptr) bn = kDxBN;  // the fused input gradient fixes the tile width
   else if (force == FORGE_FLAG_TILE_N_64) bn = 64;
   else if (force == FORGE_FLAG_TILE_N_128) bn = 128;
   else if (force == FORGE_FLAG_TILE_N_256) bn = 256;
+  else if (force == FORGE_FLAG_TILE_PAIR_256) { bn = 256; pair = true; }
   else if (force != FORGE_FLAG_TILE_N_AUTO) return fail(FORGE_ERR_INVALID_ARG, "%s: bad tile flag", oname);
   else if (mk != M_Q8 && tiles_m * ((d_in + 127) / 128) < dev->sms) bn = 64;  // too few tiles for one wave
   else if (mk != M_Q8 && !accum && G_acc == nullptr && tiles_m * ((d_in + 255) / 256) >= dev->sms &&
@@ -544,10 +546,21 @@ forge_status wgrad_step(int opt, const forge_tensor* X, const forge_tensor* dY, 
     // 117 -> 104.5; Lion fp32 188 -> 202, AdamW fp32 238 -> 267, AdamW
     // bf16 173 either way; BT 256: 128 columns everywhere).
     bn = 256;
+  // From 2048 tokens the 256-column tiles are shared by CTA pairs (256 x 256
+  // tiles; per CTA a third fewer operand bytes per stage for the same MMA
+  // work, and a deeper operand ring). Up-projection, step alone, single CTA
+  // / pair: AdamW bf16 state BT 2048 250 / 225.5 us, 4096 426 / 358, 8192
+  // 775 / 624; fp32 state 314 / 293 (four pair stages), 487 / 404, 827 /
+  // 660; Lion bf16 BT 2048 227 / 207.5, fp32 258 / 220. Below 2048 tokens
+  // the pair lost (BT 1024 AdamW bf16 180 / 188.6 at best; light state at
+  // BT 512: Lion bf16 110.5 / 128.5).
+  if (force == FORGE_FLAG_TILE_N_AUTO && dx == nullptr && bn == 256 && bt >= 2048) pair = true;
   if (mk == M_Q8 && bn != 128)
     return fail(FORGE_ERR_UNSUPPORTED, "%s: 8-bit block moments need 128-column tiles", oname);
   if (bn == 256 && (accum || G_acc != nullptr))
     return fail(FORGE_ERR_UNSUPPORTED, "%s: 256-column tiles exist for the plain step only", oname);
+  if (pair && mk == M_Q8)
+    return fail(FORGE_ERR_UNSUPPORTED, "%s: CTA-pair tiles need fp32 or bf16 state", oname);
   if (mk == M_Q8 && G_acc != nullptr)
     return fail(FORGE_ERR_UNSUPPORTED, "%s: the accumulated-gradient step has no 8-bit state variant", oname);
   // Deep operand ring for long token axes, and for the accumulation rules at
@@ -635,15 +648,16 @@ forge_status wgrad_step(int opt, const forge_tensor* X, const forge_tensor* dY, 
   p.d_out = static_cast<int>(d_out);
   p.d_in = static_cast<int>(d_in);
   p.bt = static_cast<int>(bt);
-  p.tiles_m = tiles_m;
+  // CTA pairs walk 256-row tiles (each CTA steps one 128-row half).
+  p.tiles_m = pair ? static_cast<int>((d_out + 255) / 256) : tiles_m;
   p.tiles_n = tiles_n;
-  p.num_tiles = tiles_m * tiles_n;
+  p.num_tiles = p.tiles_m * tiles_n;
   p.num_kb = static_cast<int>((bt + box_tokens - 1) / box_tokens);
   // Grouped raster: tile rows per group. With 128 x 256 tiles (long token
   // axes, operands far larger than L2) 16 rows keep fewer X column blocks
   // live per window of in-flight tiles (BT 8192 up-projection: 791 -> 775 us
   // with bf16 state); 8 elsewhere.
-  p.group_m = bn == 256 ? 16 : 8;
+  p.group_m = pair ? 8 : (bn == 256 ? 16 : 8);   // 2048 rows either way on 256-column tiles
   p.step = static_cast<uint32_t>(step);
   p.seed_lo = static_cast<uint32_t>(seed);
   p.seed_hi = static_cast<uint32_t>(seed >> 32);
@@ -675,7 +689,12 @@ forge_status wgrad_step(int opt, const forge_tensor* X, const forge_tensor* dY, 
   l.ga = G_acc != nullptr ? 1 : 0;
   l.narrow = narrow ? 1 : 0;
   l.wide = wide ? 1 : 0;
-  l.grid = p.num_tiles < dev->sms ? p.num_tiles : dev->sms;
+  // The pair's operand stages: 5 beside two state slots, or 4 beside three
+  // for fp32 W with two fp32 moments below 4096 tokens (BT 2048: 333 us with
+  // five stages, 293 with four; from 4096 five win: 404 / 431 us).
+  l.pair = !pair ? 0 : ((wk == W_F32 && mk == M_F32 && nst == 2 && bt < 4096) ? 4 : 5);
+  l.grid = pair ? 2 * (p.num_tiles < dev->sms / 2 ? p.num_tiles : dev->sms / 2)
+                : (p.num_tiles < dev->sms ? p.num_tiles : dev->sms);
   l.stream = s;
   DxGeometry g;
   if (dx != nullptr) {

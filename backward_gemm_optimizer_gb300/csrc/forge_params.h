@@ -141,12 +141,13 @@ struct DgradFixupParams {
 
 struct TcLaunch {
   int opt, wk, mk;
-  int bn;       // tile width (64 or 128)
+  int bn;       // tile width (64, 128 or 256)
   int deep;     // 1: deeper operand pipeline for long token axes
   int dx;       // 1: fused input gradient (64-column tiles, fp32 / bf16 state)
   int ga;       // 1: add the accumulated gradient G_acc (tm_g) to each tile
   int narrow;   // 1: 16-column state chunks (fused kernel, fp32 W and moments, short token axes)
   int wide;     // 1: 64-column state chunks (plain step, bf16 W and bf16 moments)
+  int pair;     // CTA pairs on 256 x 256 tiles (plain step, bn 256; grid = 2 x pairs): 0, or their operand stages (4, 5)
   int grid;
   cudaStream_t stream;
 };

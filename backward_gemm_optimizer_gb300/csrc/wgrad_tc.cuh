@@ -52,6 +52,16 @@
 //     partial to a workspace slab, and a separate reduction sums a
 //     column's slabs in a fixed order (deterministic dX).
 //
+// With PAIR (long token axes) two CTAs of a cluster share 256 x 256 tiles:
+// each loads its own 128 rows of dY^T and half (128 columns) of X, one
+// thread of the pair's first CTA issues tcgen05.mma.cta_group::2 (M = 256,
+// N = 256) that reads both CTAs' shared memory, and each CTA's epilogue
+// steps its own 128 x 256 accumulator half. Both CTAs' operand bytes are
+// counted on the first CTA's stage barriers; its commits arrive on the
+// stage and accumulator barriers of both; both epilogues release the
+// accumulator on the first CTA's barrier. Per CTA, an operand stage holds
+// a third less than a 128 x 256 tile's, for the same MMA work.
+//
 // The accumulator never leaves TMEM / registers: no gradient tile is ever
 // written to global memory (Proposition 3). Both operands are token-major
 // in memory, so A = dY^T and B = X are fed to the tensor cores as MN-major
@@ -71,13 +81,16 @@
 namespace forge {
 
 template <int OPT, int WK, int MK, int BN_, int STAGES_, int NBUF_, bool DX_ = false, bool GA_ = false,
-          bool NARROW_ = false, bool WIDE_ = false>
+          bool NARROW_ = false, bool WIDE_ = false, bool PAIR_ = false>
 struct TcCfg {
   static constexpr bool DX = DX_;      // fused input gradient (see above)
   static constexpr bool GA = GA_;      // add an fp32 accumulated gradient G_acc to each tile
   static constexpr bool LOAD_W = OPT != OPT_ACCSET;  // the set-accumulator rule never reads its target
   static constexpr int BM = 128;       // tile rows (D_out), one per TMEM lane
   static constexpr int BN = BN_;       // tile columns (D_in)
+  // A CTA pair (see above): 256 x BN tiles, this CTA's rows and B columns.
+  static constexpr bool PAIR = PAIR_;
+  static constexpr int BN_CTA = PAIR ? BN / 2 : BN;   // columns of X one CTA loads
   static constexpr int BK = DX ? 128 : 64;  // tokens per operand stage
   static constexpr int BOX = BK * 128; // bytes of one 64-column operand box (BK rows of 128 bytes)
   // State chunk width (columns): 32, or 16 (NARROW) with fp32 W and fp32
@@ -113,7 +126,7 @@ struct TcCfg {
   static constexpr int WE = SLOT_F32 ? 4 : 2;
   static constexpr int ME = (MK == M_F32) ? 4 : (MK == M_BF16 ? 2 : 1);
   static constexpr int A_BYTES = BM * BK * 2;
-  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int B_BYTES = BN_CTA * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int W_CH = BM * CW * WE;
   static constexpr int M_CH = NST >= 1 ? BM * CW * ME : 0;
@@ -142,7 +155,7 @@ struct TcCfg {
   static constexpr bool DX_ISSUER = DX && !(WK == W_F32 && MK == M_F32 && NST == 2);
   static constexpr int DXMMA_WARP = 4 + EPI_WARPS + 4;
   static constexpr int NUM_THREADS = 128 + EPI_THREADS + CONV_THREADS + (DX_ISSUER ? 32 : 0);
-  static constexpr uint32_t IDESC = make_idesc_bf16(BM, BN, 1, 1);
+  static constexpr uint32_t IDESC = make_idesc_bf16(PAIR ? 2 * BM : BM, BN, 1, 1);
   // dX: A = dY (M = 128 tokens, K-major), B = Wb (N = BN, MN-major).
   static constexpr uint32_t IDESC_DX = make_idesc_bf16(128, BN, 0, 1);
 
@@ -280,23 +293,28 @@ struct TileWalk {
   int first, step, end;
 };
 
-template <bool DX>
+template <bool DX, bool PAIR>
 __device__ __forceinline__ TileWalk tile_walk(const WgradTcParams& p) {
   if constexpr (DX) {
     const int64_t T = p.num_tiles, G = gridDim.x, c = blockIdx.x;
     return TileWalk{static_cast<int>(c * T / G), 1, static_cast<int>((c + 1) * T / G)};
+  } else if constexpr (PAIR) {
+    // A pair (cluster) walks the raster of 256-row tiles.
+    return TileWalk{static_cast<int>(blockIdx.x >> 1), static_cast<int>(gridDim.x >> 1), p.num_tiles};
   } else {
     return TileWalk{static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), p.num_tiles};
   }
 }
 
-template <bool DX>
-__device__ __forceinline__ void walk_coords(const WgradTcParams& p, int tile, int& tm, int& tn) {
+// tm: this CTA's 128-row tile (PAIR: half `prank` of the pair's 256 rows).
+template <bool DX, bool PAIR>
+__device__ __forceinline__ void walk_coords(const WgradTcParams& p, int tile, int prank, int& tm, int& tn) {
   if constexpr (DX) {
     tm = tile % p.tiles_m;
     tn = tile / p.tiles_m;
   } else {
     tile_coords(tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+    if constexpr (PAIR) tm = 2 * tm + prank;
   }
 }
 
@@ -335,12 +353,15 @@ __device__ __forceinline__ void write_dx_partial(float* slab, uint32_t tmem_dx, 
 // (another role gave up) or if this wait exceeded `limit_ns`, in which case
 // it raises the abort flag and records `code` in the device status word.
 
+// CL: acquire at cluster scope (phases completed by the other CTA of a pair).
+template <bool CL = false>
 __device__ __forceinline__ bool bwait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                       unsigned int* status, uint32_t code, uint64_t limit_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
+  auto try_wait = [&]() { return CL ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
+  if (try_wait()) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t n = 1;; ++n) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (try_wait()) return true;
     if ((n & 7u) == 0u) {
       if (*abort_flag) return false;
       if (globaltimer_ns() - t0 > limit_ns) {
@@ -403,10 +424,11 @@ __device__ __forceinline__ bool dx_tile_ready(bool run_first, uint32_t runs_done
   return bwait(wb_full, it & 1, abort_flag, status, WAIT_WB_FULL, lim);
 }
 
-template <int OPT, int WK, int MK, int BN, int STAGES, int NBUF, bool DX, bool GA, bool NARROW, bool WIDE>
-__global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, NARROW, WIDE>::NUM_THREADS, 1)
+template <int OPT, int WK, int MK, int BN, int STAGES, int NBUF, bool DX, bool GA, bool NARROW, bool WIDE,
+          bool PAIR>
+__global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, NARROW, WIDE, PAIR>::NUM_THREADS, 1)
     wgrad_step_tc_kernel(const __grid_constant__ WgradTcParams p) {
-  using C = TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, NARROW, WIDE>;
+  using C = TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, NARROW, WIDE, PAIR>;
   static_assert(!WIDE || (WK == W_BF16 && MK == M_BF16 && !DX && !GA && !C::ACC),
                 "64-column chunks: plain step with bf16 W and bf16 moments");
   static_assert(!NARROW || ((DX || BN >= 128) && WK == W_F32 && MK == M_F32 && C::NST >= 1 && !C::ACC && !GA),
@@ -419,6 +441,7 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, N
   static_assert(!C::Q8 || BN == 128, "8-bit blocks span one 128-column tile row");
   static_assert(!C::Q8 || OPT == OPT_ADAMW || OPT == OPT_SGDM || OPT == OPT_LION, "8-bit state rules");
   static_assert(!C::Q8 || NBUF >= C::NCH, "8-bit moments hold a whole tile of slots");
+  static_assert(!PAIR || (BN == 256 && !DX && !GA && !C::Q8 && !C::ACC), "CTA pairs: 256-column plain-step tiles");
   static_assert(NBUF >= 2 && STAGES >= 2, "pipelines");
   static_assert(C::SMEM_BYTES <= 227 * 1024, "shared memory");
 
@@ -437,7 +460,9 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, N
   uint8_t* op_base = smem;
   uint8_t* wb_base = smem + STAGES * C::STAGE_BYTES;
   uint8_t* st_base = wb_base + C::WB_BYTES;
-  const TileWalk tw = tile_walk<DX>(p);
+  const TileWalk tw = tile_walk<DX, PAIR>(p);
+  // Rank in the CTA pair: 0 issues the pair's MMAs and owns the operand barriers.
+  const int prank = PAIR ? static_cast<int>(cluster_ctarank()) : 0;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -456,7 +481,7 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, N
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tm_full[b], 1);
-      mbar_init(&tm_empty[b], C::EPI_WARPS);
+      mbar_init(&tm_empty[b], PAIR ? 2 * C::EPI_WARPS : C::EPI_WARPS);  // both halves' epilogues
       mbar_init(&red_bar[b], C::EPI_THREADS);
     }
     mbar_init(&never_bar, 1);
@@ -477,11 +502,19 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, N
     if constexpr (C::TWO) prefetch_tmap(&p.tm_v);
   }
   if (warp == 1) {
-    tmem_alloc(&tmem_base_sh, C::TMEM_COLS);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(&tmem_base_sh, C::TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(&tmem_base_sh, C::TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before_sync();
   __syncthreads();
+  // The other CTA's barriers are initialised before any load or arrival
+  // reaches them.
+  if constexpr (PAIR) cluster_sync_all();
   tc_fence_after_sync();
   const uint32_t tmem_base = tmem_base_sh;
   const uint64_t lim = p.timeout_ns;
@@ -493,13 +526,34 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, N
       bool ok = true;
       for (int tile = tw.first; ok && tile < tw.end; tile += tw.step) {
         int tm, tn;
-        walk_coords<DX>(p, tile, tm, tn);
+        walk_coords<DX, PAIR>(p, tile, prank, tm, tn);
         for (int kb = 0; kb < p.num_kb; ++kb, ++kseq) {
           const int s = static_cast<int>(kseq % STAGES);
           const uint32_t ph = (kseq / STAGES) & 1u;
           if (!bwait(&op_empty[s], ph ^ 1u, abort_flag, p.status, WAIT_OP_EMPTY, lim)) { ok = false; break; }
           uint8_t* a = op_base + s * C::STAGE_BYTES;
           uint8_t* b = a + C::A_BYTES;
+          if constexpr (PAIR) {
+            // Both CTAs' bytes complete on the first CTA's stage barrier.
+            if (prank == 0) mbar_arrive_expect_tx(&op_full[s], 2 * C::STAGE_BYTES);
+            const uint32_t fb = cluster_map(smem_u32(&op_full[s]), 0u);
+            const int xb = tn * BN + prank * C::BN_CTA;
+            if (p.op_hint) {
+              const uint64_t pol = l2_policy_evict_last();
+              tma_load_2d_pair_hint(a, &p.tm_dy, fb, tm * C::BM, kb * C::BK, pol);
+              tma_load_2d_pair_hint(a + C::BOX, &p.tm_dy, fb, tm * C::BM + 64, kb * C::BK, pol);
+#pragma unroll
+              for (int bb = 0; bb < C::BN_CTA / 64; ++bb)
+                tma_load_2d_pair_hint(b + bb * C::BOX, &p.tm_x, fb, xb + bb * 64, kb * C::BK, pol);
+            } else {
+              tma_load_2d_pair(a, &p.tm_dy, fb, tm * C::BM, kb * C::BK);
+              tma_load_2d_pair(a + C::BOX, &p.tm_dy, fb, tm * C::BM + 64, kb * C::BK);
+#pragma unroll
+              for (int bb = 0; bb < C::BN_CTA / 64; ++bb)
+                tma_load_2d_pair(b + bb * C::BOX, &p.tm_x, fb, xb + bb * 64, kb * C::BK);
+            }
+            continue;
+          }
           mbar_arrive_expect_tx(&op_full[s], C::STAGE_BYTES);
           if (p.op_hint) {
             const uint64_t pol = l2_policy_evict_last();
@@ -517,7 +571,9 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, N
           }
         }
       }
-      if (!ok) drain_ring(op_full, STAGES, kseq, p.status);
+      // (PAIR: the second CTA's loads complete on the first CTA's barriers,
+      // which that CTA drains.)
+      if (!ok && prank == 0) drain_ring(op_full, STAGES, kseq, p.status);
     }
     if (p.op_hint) {
       // This CTA's share of the operands' lines back to normal priority, so
@@ -535,7 +591,8 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, N
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (weight gradient)
-    if (lane == 0) {
+    // (PAIR: the first CTA's thread issues for both.)
+    if (lane == 0 && prank == 0) {
       uint32_t kseq = 0;
       bool ok = true;
       int it = 0;
@@ -543,7 +600,7 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, N
       for (int tile = tw.first; ok && tile < tw.end; tile += tw.step, ++it) {
         const int buf = it & 1;
         const uint32_t eph = ((it >> 1) & 1) ^ 1u;
-        if (!bwait(&tm_empty[buf], eph, abort_flag, p.status, WAIT_TMEM_EMPTY, lim)) { ok = false; break; }
+        if (!bwait<PAIR>(&tm_empty[buf], eph, abort_flag, p.status, WAIT_TMEM_EMPTY, lim)) { ok = false; break; }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
         // dX issued here too (no dX issuer warp): the column's first tile
@@ -567,7 +624,8 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, N
           for (int kk = 0; kk < C::BK / 16; ++kk) {
             // 16 tokens = two 8-row K groups of 1024 bytes; MN atoms one box apart.
             const uint64_t step = static_cast<uint64_t>(kk * 2048 >> 4);
-            umma_f16(d_tmem, ad0 + step, bd0 + step, C::IDESC, (kb > 0 || kk > 0) ? 1u : 0u);
+            if constexpr (PAIR) umma_f16_pair(d_tmem, ad0 + step, bd0 + step, C::IDESC, (kb > 0 || kk > 0) ? 1u : 0u);
+            else umma_f16(d_tmem, ad0 + step, bd0 + step, C::IDESC, (kb > 0 || kk > 0) ? 1u : 0u);
           }
           if constexpr (DX_HERE) {
             if (kb == 0) {
@@ -579,7 +637,8 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, N
             }
             issue_dx_stage<C>(a0, smem_u32(wb_base), tmem_base, kb, run_first);
           }
-          umma_commit(&op_empty[s]);
+          if constexpr (PAIR) umma_commit_pair(&op_empty[s], 3);   // the stage in both CTAs
+          else umma_commit(&op_empty[s]);
         }
         if (!ok) break;
         if constexpr (DX_HERE) {
@@ -588,11 +647,13 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, N
             if (run_last) { umma_commit(&dx_full); ++runs_done; }
           }
         }
-        umma_commit(&tm_full[buf]);
+        if constexpr (PAIR) umma_commit_pair(&tm_full[buf], 3);   // both halves' epilogues
+        else umma_commit(&tm_full[buf]);
       }
       if (!ok) {
         // Let every MMA already issued finish before TMEM is released.
-        umma_commit(&mma_drain_bar);
+        if constexpr (PAIR) umma_commit_pair(&mma_drain_bar, 1);
+        else umma_commit(&mma_drain_bar);
         const uint64_t t0 = globaltimer_ns();
         while (!mbar_try_wait(&mma_drain_bar, 0)) {
           if (globaltimer_ns() - t0 > 200000000ull) { atomicCAS(p.status, 0u, WAIT_MMA_DRAIN); break; }
@@ -606,7 +667,7 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, N
       bool ok = true;
       for (int tile = tw.first; ok && tile < tw.end; tile += tw.step) {
         int tm, tn;
-        walk_coords<DX>(p, tile, tm, tn);
+        walk_coords<DX, PAIR>(p, tile, prank, tm, tn);
         for (int c = 0; c < C::NCH; ++c, ++cseq) {
           const int s = static_cast<int>(cseq % NBUF);
           const uint32_t ph = (cseq / NBUF) & 1u;
@@ -629,7 +690,7 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, N
       bool ok = true;
       for (int tile = tw.first; ok && tile < tw.end; tile += tw.step) {
         int tm, tn;
-        walk_coords<DX>(p, tile, tm, tn);
+        walk_coords<DX, PAIR>(p, tile, prank, tm, tn);
         for (int c = 0; c < C::NCH; ++c, ++cseq) {
           const int s = static_cast<int>(cseq % NBUF);
           const uint32_t ph = (cseq / NBUF) & 1u;
@@ -664,7 +725,7 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, N
 
     for (int tile = tw.first; ok && tile < tw.end; tile += tw.step, ++it) {
       int tm, tn;
-      walk_coords<DX>(p, tile, tm, tn);
+      walk_coords<DX, PAIR>(p, tile, prank, tm, tn);
       const int buf = it & 1;
       ok = bwait(&tm_full[buf], (it >> 1) & 1, abort_flag, p.status, WAIT_TMEM_FULL, lim);
       ok = __all_sync(0xFFFFFFFFu, ok);
@@ -986,7 +1047,11 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, N
       if constexpr (!C::Q8) {
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&tm_empty[buf]);
+        if constexpr (PAIR) {
+          if (lane == 0) mbar_arrive_cluster(cluster_map(smem_u32(&tm_empty[buf]), 0u));
+        } else {
+          if (lane == 0) mbar_arrive(&tm_empty[buf]);
+        }
       }
     }
   }
@@ -1005,7 +1070,7 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, N
       bool ok = p.num_kb > 0;
       for (int tile = tw.first; ok && tile < tw.end; tile += tw.step, ++it) {
         int tm, tn;
-        walk_coords<DX>(p, tile, tm, tn);
+        walk_coords<DX, PAIR>(p, tile, prank, tm, tn);
         uint4 o[8];
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
@@ -1116,18 +1181,22 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, N
   // ------------------------------------------------------------ teardown
   tc_fence_before_sync();
   __syncthreads();
+  // Neither CTA of a pair leaves (or frees tensor memory) while the other
+  // may still arrive on its barriers or read its accumulator half.
+  if constexpr (PAIR) cluster_sync_all();
   if (warp == 1) {
     __syncwarp();
     tc_fence_after_sync();
-    tmem_dealloc(tmem_base, C::TMEM_COLS);
+    if constexpr (PAIR) tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+    else tmem_dealloc(tmem_base, C::TMEM_COLS);
   }
 }
 
 template <int OPT, int WK, int MK, int BN, int STAGES, int NBUF, bool DX, bool GA = false, bool NARROW = false,
-          bool WIDE = false>
+          bool WIDE = false, bool PAIR = false>
 cudaError_t launch_tc_variant(const WgradTcParams& p, int grid, cudaStream_t stream) {
-  using C = TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, NARROW, WIDE>;
-  auto kern = wgrad_step_tc_kernel<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, NARROW, WIDE>;
+  using C = TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, NARROW, WIDE, PAIR>;
+  auto kern = wgrad_step_tc_kernel<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, NARROW, WIDE, PAIR>;
   // The opt-in shared-memory size is a per-device function attribute: set
   // it once per device (bit d of the mask) before the first launch there.
   static unsigned long long attr_mask = 0ull;
@@ -1140,8 +1209,38 @@ cudaError_t launch_tc_variant(const WgradTcParams& p, int grid, cudaStream_t str
     if (e != cudaSuccess) return e;
     __atomic_fetch_or(&attr_mask, bit, __ATOMIC_ACQ_REL);
   }
-  kern<<<grid, C::NUM_THREADS, C::SMEM_BYTES, stream>>>(p);
-  return cudaGetLastError();
+  if constexpr (PAIR) {
+    // Clusters of two; at most as many pairs as the device keeps resident
+    // at once (each pair walks its own share of the tiles).
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(C::NUM_THREADS);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    static int max_pairs[64] = {};
+    int mp = __atomic_load_n(&max_pairs[dev & 63], __ATOMIC_ACQUIRE);
+    if (mp == 0) {
+      cfg.gridDim = dim3(2);
+      e = cudaOccupancyMaxActiveClusters(&mp, kern, &cfg);
+      if (e != cudaSuccess) return e;
+      if (mp < 1) return cudaErrorInvalidConfiguration;
+      __atomic_store_n(&max_pairs[dev & 63], mp, __ATOMIC_RELEASE);
+    }
+    int pairs = grid / 2;
+    if (pairs > mp) pairs = mp;
+    if (pairs < 1) return cudaErrorInvalidValue;
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
+    return cudaLaunchKernelEx(&cfg, kern, p);
+  } else {
+    kern<<<grid, C::NUM_THREADS, C::SMEM_BYTES, stream>>>(p);
+    return cudaGetLastError();
+  }
 }
 
 }  // namespace forge

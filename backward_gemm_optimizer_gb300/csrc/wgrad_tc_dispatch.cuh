@@ -12,9 +12,9 @@ namespace forge {
 constexpr int kDynSmemBudget = 227 * 1024 - 9 * 1024;
 
 template <int OPT, int WK, int MK, int BN, int STAGES, bool DX = false, bool GA = false, bool NARROW = false,
-          bool WIDE = false>
+          bool WIDE = false, bool PAIR = false>
 constexpr int slots_that_fit() {
-  using C = TcCfg<OPT, WK, MK, BN, STAGES, 2, DX, GA, NARROW, WIDE>;
+  using C = TcCfg<OPT, WK, MK, BN, STAGES, 2, DX, GA, NARROW, WIDE, PAIR>;
   const int avail = kDynSmemBudget - 1024 - STAGES * C::STAGE_BYTES - C::WB_BYTES;
   const int n = avail / C::SLOT_BYTES;
   return n > 8 ? 8 : n;
@@ -22,22 +22,27 @@ constexpr int slots_that_fit() {
 
 // Operand stages: 2 for short token axes (the step is bound by the state
 // stream); for long ones as many as leave room for the state ring (4, else
-// 3, else 2).
-template <int OPT, int WK, int MK, int BN, int DEEP, bool WIDE = false, bool NARROW = false>
+// 3, else 2). CTA pairs, whose stages are a third smaller, take up to PS
+// (5, or 4 where the state stream is heavy) beside at least two slots.
+template <int OPT, int WK, int MK, int BN, int DEEP, bool WIDE = false, bool NARROW = false, bool PAIR = false,
+          int PS = 5>
 constexpr int pick_stages() {
   if (!DEEP) return 2;
   constexpr int need = (MK == M_Q8) ? 4 : 2;
-  if (slots_that_fit<OPT, WK, MK, BN, 4, false, false, NARROW, WIDE>() >= need) return 4;
-  if (slots_that_fit<OPT, WK, MK, BN, 3, false, false, NARROW, WIDE>() >= need) return 3;
+  if constexpr (PAIR)
+    if (PS >= 5 && slots_that_fit<OPT, WK, MK, BN, 5, false, false, NARROW, WIDE, PAIR>() >= need) return 5;
+  if (slots_that_fit<OPT, WK, MK, BN, 4, false, false, NARROW, WIDE, PAIR>() >= need) return 4;
+  if (slots_that_fit<OPT, WK, MK, BN, 3, false, false, NARROW, WIDE, PAIR>() >= need) return 3;
   return 2;
 }
 
-template <int OPT, int WK, int MK, int BN, int DEEP, bool WIDE = false, bool NARROW = false>
+template <int OPT, int WK, int MK, int BN, int DEEP, bool WIDE = false, bool NARROW = false, bool PAIR = false,
+          int PS = 5>
 cudaError_t launch_one(const WgradTcParams& p, int grid, cudaStream_t stream) {
-  constexpr int S = pick_stages<OPT, WK, MK, BN, DEEP, WIDE, NARROW>();
-  constexpr int N = slots_that_fit<OPT, WK, MK, BN, S, false, false, NARROW, WIDE>();
+  constexpr int S = pick_stages<OPT, WK, MK, BN, DEEP, WIDE, NARROW, PAIR, PS>();
+  constexpr int N = slots_that_fit<OPT, WK, MK, BN, S, false, false, NARROW, WIDE, PAIR>();
   static_assert(N >= ((MK == M_Q8) ? 4 : 2), "state ring does not fit");
-  return launch_tc_variant<OPT, WK, MK, BN, S, N, false, false, NARROW, WIDE>(p, grid, stream);
+  return launch_tc_variant<OPT, WK, MK, BN, S, N, false, false, NARROW, WIDE, PAIR>(p, grid, stream);
 }
 
 // Step with an accumulated gradient (the last micro-batch): two operand
@@ -62,6 +67,7 @@ cudaError_t launch_dx(const WgradTcParams& p, int grid, cudaStream_t stream) {
 
 template <int OPT, int WK, int MK>
 cudaError_t launch_mk(const WgradTcParams& p, const TcLaunch& l) {
+  if (l.pair && (l.ga || l.dx || l.wide || l.bn != 256 || MK == M_Q8)) return cudaErrorInvalidValue;
   if (l.ga) {
     if constexpr (MK == M_Q8) return cudaErrorInvalidValue;
     else {
@@ -105,14 +111,24 @@ cudaError_t launch_mk(const WgradTcParams& p, const TcLaunch& l) {
       // 128 x 256 tiles for long token axes: a quarter less operand traffic
       // per gradient element than 128 x 128, half the MMA instructions.
       if (!l.deep) return cudaErrorInvalidValue;
-      if constexpr (WK == W_F32 && MK == M_F32 && opt_nstate(OPT) >= 1)
-        if (l.narrow) return launch_one<OPT, WK, MK, 256, 1, false, true>(p, l.grid, l.stream);
-      if (l.narrow) return cudaErrorInvalidValue;
-      return launch_one<OPT, WK, MK, 256, 1>(p, l.grid, l.stream);
+      // l.pair: 0, or the CTA pair's operand stages (5; 4 for fp32 W with
+      // two fp32 moments below 4096 tokens).
+      if constexpr (WK == W_F32 && MK == M_F32 && opt_nstate(OPT) >= 1) {
+        if (l.narrow) {
+          if (l.pair == 0) return launch_one<OPT, WK, MK, 256, 1, false, true>(p, l.grid, l.stream);
+          if constexpr (opt_nstate(OPT) == 2)
+            if (l.pair == 4) return launch_one<OPT, WK, MK, 256, 1, false, true, true, 4>(p, l.grid, l.stream);
+          if (l.pair != 5) return cudaErrorInvalidValue;
+          return launch_one<OPT, WK, MK, 256, 1, false, true, true, 5>(p, l.grid, l.stream);
+        }
+      }
+      if (l.narrow || (l.pair != 0 && l.pair != 5)) return cudaErrorInvalidValue;
+      return l.pair ? launch_one<OPT, WK, MK, 256, 1, false, false, true, 5>(p, l.grid, l.stream)
+                    : launch_one<OPT, WK, MK, 256, 1>(p, l.grid, l.stream);
     }
     if constexpr (WK == W_F32 && MK == M_F32 && opt_nstate(OPT) >= 1)
       if (l.narrow && l.deep) return launch_one<OPT, WK, MK, 128, 1, false, true>(p, l.grid, l.stream);
-    if (l.narrow) return cudaErrorInvalidValue;
+    if (l.narrow || l.pair) return cudaErrorInvalidValue;
     return l.deep ? launch_one<OPT, WK, MK, 128, 1>(p, l.grid, l.stream)
                   : launch_one<OPT, WK, MK, 128, 0>(p, l.grid, l.stream);
   }

@@ -89,6 +89,9 @@ typedef struct {
 #define FORGE_FLAG_TILE_N_128 1u    /* force 128 x 128 gradient tiles */
 #define FORGE_FLAG_TILE_N_64 2u     /* force 128 x 64 gradient tiles */
 #define FORGE_FLAG_TILE_N_256 3u    /* force 128 x 256 gradient tiles (fp32 / bf16 state) */
+/* force 256 x 256 gradient tiles shared by a cluster of two CTAs (one
+ * 128-row half each; plain step, fp32 / bf16 state) */
+#define FORGE_FLAG_TILE_PAIR_256 4u
 #define FORGE_FLAG_TILE_N_MASK 7u
 /* Test hook for the device-side failure path: the epilogue waits on a
  * barrier that nothing signals, with a ~1 ms bound, gives up, and the

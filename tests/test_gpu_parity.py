@@ -449,6 +449,55 @@ def test_bf16_state_64_column_chunks_exact(opt, shape):
         assert_bit_exact(got, ref, opt)
 
 
+@pytest.mark.parametrize("opt", ["adamw", "lion", "sgdm", "nadam"])
+@pytest.mark.parametrize("variant", [("f32", "f32"), ("f32", "bf16"), ("bf16", "bf16"), ("bf16", "f32")],
+                         ids=lambda v: f"W{v[0]}-m{v[1]}")
+@pytest.mark.parametrize("shape", [(384, 520, 1100), (136, 256, 70), (640, 776, 300)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_cta_pair_tiles_exact(opt, variant, shape):
+    # 256 x 256 tiles shared by a cluster of two CTAs: ragged D_out leaves
+    # the second CTA's half of the last tile row partly (136 rows) or wholly
+    # (384 rows) past the edge; ragged D_in and token tails.
+    w, st = variant
+    prob = _prob(shape, 41, "bf16", w, st, exact=True)
+    sr, srm = w == "bf16", st == "bf16"
+    got = gpu_step(opt, prob, 2, seed=6, sr_w=sr, sr_moments=srm, flags=F.FLAG_TILE_PAIR_256)
+    ref = oracle_step(opt, prob, w, st, 2, seed=6, sr_w=sr, sr_moments=srm, mode="f32emu")
+    assert_bit_exact(got, ref, opt)
+
+
+@pytest.mark.parametrize("variant", [("f32", "f32"), ("bf16", "bf16")], ids=lambda v: f"W{v[0]}-m{v[1]}")
+@pytest.mark.parametrize("bt", [2048, 4160])
+def test_cta_pair_tiles_match_single_cta_tiles(variant, bt):
+    # Random inputs: the pair's M = 256 products give every gradient element
+    # the same value as one CTA's 128 x 256 and 128 x 128 tiles, bit for bit
+    # (fp32 state: four pair stages below 4096 tokens, five from there).
+    w, st = variant
+    prob = _prob((1024, 1280, bt), 43, "bf16", w, st, exact=False)
+    sr = w == "bf16"
+    a = gpu_step("adamw", prob, 1, seed=2, sr_w=sr, sr_moments=sr, flags=F.FLAG_TILE_PAIR_256)
+    b = gpu_step("adamw", prob, 1, seed=2, sr_w=sr, sr_moments=sr, flags=F.FLAG_TILE_N_256)
+    c = gpu_step("adamw", prob, 1, seed=2, sr_w=sr, sr_moments=sr, flags=F.FLAG_TILE_N_128)
+    assert_bit_exact(a, b, "adamw")
+    assert_bit_exact(a, c, "adamw")
+
+
+@pytest.mark.parametrize("opt", ["lion", "adamw"])
+def test_long_token_axis_automatic_tiles_exact(opt):
+    # 2048 tokens on a layer with >= 152 tiles of 256 columns: the automatic
+    # policy's tiles (CTA pairs) against the oracle's float32 sequence.
+    prob = _prob((4096, 2048, 2048), 45, "bf16", "bf16", "bf16", exact=True)
+    got = gpu_step(opt, prob, 3, seed=8, sr_w=True, sr_moments=True)
+    ref = oracle_step(opt, prob, "bf16", "bf16", 3, seed=8, sr_w=True, sr_moments=True, mode="f32emu")
+    assert_bit_exact(got, ref, opt)
+
+
+def test_cta_pair_tiles_reject_8bit_state():
+    prob = _prob((256, 512, 128), 44, "bf16", "f32", "q8", exact=False)
+    with pytest.raises(F.ForgeError):
+        gpu_step("adamw", prob, 1, flags=F.FLAG_TILE_PAIR_256)
+
+
 @pytest.mark.parametrize("opt", ["adamw", "lion", "sgdm", "radam"])
 def test_deep_ring_fp32_state_16_column_chunks_exact(opt):
     # fp32 W + fp32 state past 768 tokens on 128-column tiles: four operand
