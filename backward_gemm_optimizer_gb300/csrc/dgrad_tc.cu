@@ -233,6 +233,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dgrad_tc_kernel(const __grid_c
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = tmem_base_sh;
+  // A programmatic dependent (as the step kernel): the set-up above overlaps
+  // the previous kernel's tail; memory is touched after it completes.
+  griddep_launch_dependents();
+  griddep_wait();
 
   if (warp == 0) {
     // ------------------------------------------------------------ dY producer
@@ -585,6 +589,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dgrad_tc_kernel(const __grid_c
 // (tile, 16 token rows).
 __global__ void __launch_bounds__(256) dgrad_fixup_kernel(const DgradFixupParams p) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // the step may be scheduled
   const int tile = blockIdx.x;
   int tm, tn;
   dtile(tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
@@ -642,8 +647,17 @@ cudaError_t launch_d(const DgradParams& p, int grid, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     __atomic_fetch_or(&attr_mask, bit, __ATOMIC_ACQ_REL);
   }
-  kern<<<grid, NUM_THREADS, C::SMEM_BYTES, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 }  // namespace

@@ -38,6 +38,8 @@ __global__ void __launch_bounds__(256) dx_reduce_kernel(const DxReduceParams p) 
   // Launched as a programmatic dependent of the fused kernel: the blocks may
   // start while it finishes; its slab writes are visible after this wait.
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  // The next kernel may be scheduled once every block is running.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int q = blockIdx.x;
   const int64_t T = p.num_tiles, G = p.grid;
   const int64_t l0 = static_cast<int64_t>(q) * p.tiles_m;

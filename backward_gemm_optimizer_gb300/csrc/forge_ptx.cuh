@@ -19,6 +19,19 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+
+// Lets the next kernel in the stream (launched with programmatic stream
+// serialisation) be scheduled now; it still waits in griddep_wait() for
+// this grid's completion before touching memory.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Returns once the previous kernel in the stream has completed and its
+// memory operations are visible (at once if there is none to wait for).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {

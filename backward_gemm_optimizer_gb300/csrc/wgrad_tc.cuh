@@ -516,6 +516,12 @@ __global__ void __launch_bounds__(TcCfg<OPT, WK, MK, BN, STAGES, NBUF, DX, GA, N
   // reaches them.
   if constexpr (PAIR) cluster_sync_all();
   tc_fence_after_sync();
+  // Launched as a programmatic dependent: everything above (barriers, tensor
+  // memory, tensor-map prefetch) overlaps the previous kernel's tail; global
+  // memory is touched only after it has completed. The next kernel may be
+  // scheduled from here on (its CTAs take SMs as this grid's CTAs leave).
+  griddep_launch_dependents();
+  griddep_wait();
   const uint32_t tmem_base = tmem_base_sh;
   const uint64_t lim = p.timeout_ns;
 
@@ -1209,25 +1215,31 @@ cudaError_t launch_tc_variant(const WgradTcParams& p, int grid, cudaStream_t str
     if (e != cudaSuccess) return e;
     __atomic_fetch_or(&attr_mask, bit, __ATOMIC_ACQ_REL);
   }
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(C::NUM_THREADS);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see griddep_wait() in the kernel
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   if constexpr (PAIR) {
     // Clusters of two; at most as many pairs as the device keeps resident
     // at once (each pair walks its own share of the tiles).
-    cudaLaunchConfig_t cfg = {};
-    cfg.blockDim = dim3(C::NUM_THREADS);
-    cfg.dynamicSmemBytes = C::SMEM_BYTES;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 2;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
     static int max_pairs[64] = {};
     int mp = __atomic_load_n(&max_pairs[dev & 63], __ATOMIC_ACQUIRE);
     if (mp == 0) {
-      cfg.gridDim = dim3(2);
-      e = cudaOccupancyMaxActiveClusters(&mp, kern, &cfg);
+      cudaLaunchConfig_t q = cfg;
+      q.gridDim = dim3(2);
+      q.attrs = &attr[1];  // the cluster shape alone
+      q.numAttrs = 1;
+      e = cudaOccupancyMaxActiveClusters(&mp, kern, &q);
       if (e != cudaSuccess) return e;
       if (mp < 1) return cudaErrorInvalidConfiguration;
       __atomic_store_n(&max_pairs[dev & 63], mp, __ATOMIC_RELEASE);
@@ -1236,11 +1248,10 @@ cudaError_t launch_tc_variant(const WgradTcParams& p, int grid, cudaStream_t str
     if (pairs > mp) pairs = mp;
     if (pairs < 1) return cudaErrorInvalidValue;
     cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
-    return cudaLaunchKernelEx(&cfg, kern, p);
   } else {
-    kern<<<grid, C::NUM_THREADS, C::SMEM_BYTES, stream>>>(p);
-    return cudaGetLastError();
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
   }
+  return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 }  // namespace forge
