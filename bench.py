@@ -243,7 +243,9 @@ def measure_configs(F, dev, K, warm, hbm, tflops):
                      "TFLOPs": round(flops / (us * 1e-6) / 1e12, 1),
                      "bound": "hbm" if ab / (hbm * 1e9) >= flops / (tflops * 1e12) else "tensor",
                      "frac": round(t_roof / us, 4), "algorithmic_bytes": ab,
-                     "path": "fused input gradient" if fused_path(bt, st) else "split path: dgrad + fused step"}
+                     "path": ("fused input gradient" if fused_path(bt, st) else
+                              "split path: dgrad + fused step" +
+                              (" (256 x 256 step tiles on CTA pairs)" if bt >= 2048 else ""))}
         del s, ws
     for opt in ("adamw", "lion", "sgdm"):
         for stname in ("f32state", "bf16state"):
