@@ -27,8 +27,10 @@ DEV = "cuda:0"
 RULES = ["adamw", "sgdm", "lion", "sgd", "rmsprop", "adagrad", "nadam", "radam"]
 VARIANTS = [("f32", "f32"), ("f32", "bf16"), ("bf16", "bf16"), ("bf16", "f32")]
 # (D_out, D_in, BT): ragged D and tokens, one tile per CTA, several tiles per
-# CTA with runs that cross tile columns, and the largest token count.
-SHAPES = [(256, 384, 200), (136, 200, 70), (1000, 520, 300), (2048, 1024, 768)]
+# CTA with runs that cross tile columns, and the largest token count; the
+# last two take fewer CTAs than SMs (2 tiles each: within a column, and
+# across columns of 11 tiles).
+SHAPES = [(256, 384, 200), (136, 200, 70), (1000, 520, 300), (2048, 1024, 768), (1408, 1024, 300)]
 
 
 def _prob(shape, seed, w, st, exact):
@@ -180,6 +182,10 @@ def test_workspace_bytes_geometry():
         tm, tn = -(-d_out // 128), -(-d_in // 64)
         T = tm * tn
         G = min(T, sms)
+        # the fewest CTAs with the same most tiles per CTA, if that idles >= 10 % of them
+        per = -(-T // G)
+        if 10 * -(-T // per) <= 9 * G:
+            G = -(-T // per)
         runs = max((((c + 1) * T // G) - 1) // tm - (c * T // G) // tm + 1 for c in range(G))
         return G * runs * (-(-bt // 128) * 128 * 64) * 4
 
