@@ -765,8 +765,9 @@ forge_status wgrad_step(int opt, const forge_tensor* X, const forge_tensor* dY, 
 // Llama-3.1-8B projections (forge_backward_step fused / split, us):
 //   fp32 W, fp32 state: fused everywhere -- up 269 / 318 (AdamW),
 //     220 / 271 (Lion); down 290 / 322; q/o 102 / 118; k/v 50 / 58.
-//   bf16 W, two bf16 moments: fused where D_in <= D_out -- up 227 / 246,
-//     q/o 88 / 99; split where it is wider -- down 247 / 238, k/v 44 / 38.
+//   bf16 W, two bf16 moments: fused where D_in < D_out -- up 227 / 246;
+//     split where it is as wide or wider -- q/o 88.7 / 79.7 (with the
+//     branch-free divide in the split step), down 247 / 238, k/v 44 / 38.
 //   bf16 W, one or no state tensor: split -- the step is bound by its
 //     per-element arithmetic (stochastic rounding of W) and the fused
 //     pass's slabs and narrower tiles do not pay: down Lion 226 / 197,
@@ -774,7 +775,7 @@ forge_status wgrad_step(int opt, const forge_tensor* X, const forge_tensor* dY, 
 bool dx_worthwhile(const DxGeometry&, int64_t d_out, int64_t d_in, int w_bytes, int nst) {
   if (w_bytes == 4) return true;
   if (nst < 2) return false;
-  return d_in <= d_out;
+  return d_in < d_out;
 }
 
 forge_status dgrad_impl(const forge_tensor* dY, const forge_tensor* W_old, forge_tensor* dX, forge_stream_t stream,

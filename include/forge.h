@@ -293,7 +293,7 @@ forge_status forge_dgrad_ws(const forge_tensor* dY, const forge_tensor* W_old, f
  * path.
  * With no FORGE_FLAG_BACKWARD_* flag the library takes the fused path when
  * it applies, the workspace is large enough, and the layer is one where it
- * measured faster: fp32 W; bf16 W with two state tensors and D_in <= D_out
+ * measured faster: fp32 W; bf16 W with two state tensors and D_in < D_out
  * (otherwise the split path); FORGE_FLAG_BACKWARD_FUSED /
  * FORGE_FLAG_BACKWARD_SPLIT force a path. The fused path uses 128 x 64
  * gradient tiles (a FORGE_FLAG_TILE_N_128 request selects the split path).
