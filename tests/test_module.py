@@ -102,7 +102,7 @@ def test_small_model_trains_with_fused_layers():
         y = model(x)
         loss = ((y.float() - target.float()) ** 2).mean()
         loss.backward()
-        losses.append(float(loss))
+        losses.append(float(loss.detach()))
     F.sync_status()
     assert losses[-1] < 0.7 * losses[0], losses
     assert all(m.weight.grad is None for m in mgr.layers)
