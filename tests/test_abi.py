@@ -31,6 +31,18 @@ def test_header_declares_the_entry_points():
         assert n in names
 
 
+def test_binding_flags_match_the_header():
+    # Every FORGE_FLAG_* value the header defines (the tile-width mask
+    # aside) has a binding constant of the same value.
+    src = open(HEADER).read()
+    flags = dict(re.findall(r"#define FORGE_FLAG_([A-Z0-9_]+) (0x[0-9a-fA-F]+|[0-9]+)u", src))
+    assert "TILE_PAIR_256" in flags and "DGRAD_ALL_TOKENS" in flags
+    for name, val in flags.items():
+        if name == "TILE_N_MASK":
+            continue
+        assert getattr(F, "FLAG_" + name) == int(val, 0), name
+
+
 def test_library_exports_every_declared_symbol():
     lib = F.lib()
     for n in declared_functions():
