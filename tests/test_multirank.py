@@ -60,3 +60,31 @@ def test_reference_arm_other_ranks_do_no_work(capsys):
         cpu_budget_s = 1.0
     bench.run_reference(A(), rank=1, world=2)
     assert capsys.readouterr().out == ""
+
+
+def test_reference_arm_line_carries_the_contract_keys(capsys):
+    # Rank 0 of the reference arm (the oracle on the host cores) prints one
+    # JSON line with the keys of the GPU arm's line, the same `config`, and
+    # a cpu_baseline / e2e describing its own run (a small row sample here).
+    import json
+
+    import bench
+
+    class A:
+        workload = bench.DEFAULT
+        cpu_rows = 16
+        warmup = 0
+        steps = 1
+        cpu_budget_s = 30.0
+    bench.run_reference(A(), rank=0, world=1)
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    for k in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+              "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert k in line, k
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC and line["unit"] == bench.UNIT
+    assert line["higher_is_better"] is False and line["value"] > 0
+    assert line["config"] == bench.layer_config(bench.DEFAULT, 1)
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == line["value"] and cb["cores"] >= 1 and cb["sample"]
+    assert line["e2e"] == {"value": line["value"], "unit": bench.UNIT, "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
